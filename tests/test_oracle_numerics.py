@@ -1,0 +1,95 @@
+"""Pins for the fp64 oracle numerics (oracle/ref.c) against library routines evaluated in fp64 on
+the CPU (torch.matmul, torch.nn.grad.conv2d_weight) and against closed forms. Shapes are
+non-square and asymmetric so that a transposed operand, a swapped index or a dropped term fails."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import codec, numerics
+from workloads import gemm_operands, wgrad_operands, fp8_operands
+
+
+def _bits(t):
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("dtype,M,N,K", [("f16", 37, 53, 72), ("bf16", 64, 17, 136),
+                                         ("f16", 1, 129, 8)])
+def test_gemm_rcr_vs_torch_fp64(oracle_lib, dtype, M, N, K):
+    A, B = gemm_operands(M, N, K, dtype, "u11", seed_offset=11)
+    ref = A.double() @ B.double().T
+    out = numerics.gemm_rcr_rows(dtype, _bits(A), _bits(B))
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    ms = np.array([0, M - 1, M // 2]); ns = np.array([N - 1, 0, N // 3])
+    pts = numerics.gemm_rcr_points(dtype, _bits(A), _bits(B), ms, ns)
+    np.testing.assert_allclose(pts, ref.numpy()[ms, ns], rtol=1e-12, atol=1e-12)
+    part = numerics.gemm_rcr_rows(dtype, _bits(A), _bits(B), m0=M // 2, m1=M)
+    np.testing.assert_array_equal(part, out[M // 2:])
+
+
+def test_fp8_rowcol_vs_torch_fp64(oracle_lib):
+    M, N, K = 40, 24, 96
+    A, B, sa, sb = fp8_operands(M, N, K, seed_offset=3)
+    ref = (A.double() @ B.double().T) * sa.double()[:, None] * sb.double()[None, :]
+    out = numerics.fp8_rowcol_rows(_bits(A), _bits(B), sa.numpy(), sb.numpy())
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    ms = np.array([3, 39]); ns = np.array([23, 0])
+    pts = numerics.fp8_rowcol_points(_bits(A), _bits(B), sa.numpy(), sb.numpy(), ms, ns)
+    np.testing.assert_allclose(pts, ref.numpy()[ms, ns], rtol=1e-12, atol=1e-12)
+
+
+def _torch_wgrad(x, dy, R, S, stride, pad, groups):
+    xn = x.double().permute(0, 3, 1, 2)
+    dyn = dy.double().permute(0, 3, 1, 2)
+    K = dy.shape[3]
+    w = torch.nn.grad.conv2d_weight(xn, (K, x.shape[3] // groups, R, S), dyn, stride=stride,
+                                    padding=pad, groups=groups)
+    return w.permute(0, 2, 3, 1).numpy()          # KCRS -> KRSC
+
+
+@pytest.mark.parametrize("shape", [
+    dict(N=2, H=7, W=9, C=8, K=6, R=3, S=3, stride=(1, 1), pad=(1, 1), groups=1, dt="f16"),
+    dict(N=3, H=10, W=8, C=16, K=8, R=3, S=2, stride=(2, 2), pad=(1, 0), groups=2, dt="bf16"),
+    dict(N=1, H=9, W=11, C=12, K=12, R=1, S=3, stride=(2, 1), pad=(0, 2), groups=4, dt="f16"),
+    dict(N=2, H=5, W=5, C=4, K=4, R=5, S=5, stride=(3, 3), pad=(2, 2), groups=1, dt="bf16"),
+])
+def test_wgrad_vs_torch_conv2d_weight(oracle_lib, shape):
+    s = shape
+    x, dy = wgrad_operands(s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"], s["stride"],
+                           s["pad"], s["dt"], "u11", seed_offset=5)
+    ref = _torch_wgrad(x, dy, s["R"], s["S"], s["stride"], s["pad"], s["groups"])
+    out = numerics.wgrad_nhwc(s["dt"], _bits(x), _bits(dy), s["R"], s["S"], s["stride"], s["pad"],
+                              s["groups"])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    k0 = s["K"] // 2
+    part = numerics.wgrad_nhwc(s["dt"], _bits(x), _bits(dy), s["R"], s["S"], s["stride"], s["pad"],
+                               s["groups"], k0=k0)
+    np.testing.assert_array_equal(part, out[k0:])
+
+
+def test_wgrad_all_ones_closed_form(oracle_lib):
+    # x = dy = 1: dW[k,r,s,c] counts the (n, ho, wo) whose input tap (ho*sh-ph+r, wo*sw-pw+s)
+    # lies inside the image, which factors into N * rows(r) * cols(s).
+    N, H, W, C, K, R, S, sh, sw, ph, pw, G = 2, 6, 7, 4, 4, 3, 3, 2, 1, 1, 1, 2
+    Ho, Wo = (H + 2 * ph - R) // sh + 1, (W + 2 * pw - S) // sw + 1
+    one = 0x3C00
+    x = np.full((N, H, W, C), one, np.uint16)
+    dy = np.full((N, Ho, Wo, K), one, np.uint16)
+    out = numerics.wgrad_nhwc("f16", x, dy, R, S, (sh, sw), (ph, pw), G)
+    for r in range(R):
+        rows = sum(0 <= ho * sh - ph + r < H for ho in range(Ho))
+        for s_ in range(S):
+            cols = sum(0 <= wo * sw - pw + s_ < W for wo in range(Wo))
+            assert np.all(out[:, r, s_, :] == N * rows * cols)
+
+
+def test_round_output_and_tolerance():
+    ref = np.array([1.0 + 2.0 ** -12, -3.0, 0.1])
+    np.testing.assert_array_equal(numerics.round_output(ref, "f16"), codec.round_to(ref, "f16"))
+    assert numerics.round_output(ref, "f32")[2] == np.float64(np.float32(0.1))
+    # 2e-2*sqrt(K/4096)*max|ref|: K = 4096 -> 2e-2 * 3
+    assert numerics.tolerance(numerics.round_output(ref, "f32"), 4096) == pytest.approx(0.06)
+    assert numerics.tolerance(np.array([2.0]), 16384) == pytest.approx(0.08)
+    assert numerics.tolerance(np.array([2.0]), 10 ** 6, "fp8") == pytest.approx(0.04)

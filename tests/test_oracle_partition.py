@@ -1,0 +1,192 @@
+"""Pins for the partition replica: values printed on the pages (tests/golden), closed-form
+vectors worked by hand from the partition rule, a brute-force iteration assignment, the
+invariants the pages fix, and a forward-progress simulation of the linear/tree hand-off."""
+import itertools
+import os
+import random
+
+import pytest
+
+from oracle import partition as P
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "partition_page_points.txt")
+RED = {"linear": P.LINEAR, "tree": P.TREE, "atomic": P.ATOMIC, "workspace": P.WORKSPACE}
+MODE = {"off": P.OFF, "dp_sk": P.DP_SK, "persistent": P.PERSISTENT, "splitk": P.SPLITK}
+
+
+def plan(T, I, Pool, mode=P.DP_SK, red=P.LINEAR, tm=128, tn=128, tk=64):
+    # a 1 x T tile grid with kred = I*tk
+    return P.make_plan(tiles_m=1, tiles_n=T, groups=1, kred=I * tk, tm=tm, tn=tn, tk=tk,
+                       pool=Pool, mode=mode, reduction=red)
+
+
+def _kv(s):
+    return dict(x.split("=") for x in s.split())
+
+
+def test_golden_page_points():
+    n = 0
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, inp, exp = [x.strip() for x in line.split("|")]
+        i = _kv(inp)
+        if name.startswith("default_pool"):
+            got = P.default_pool(RED[i["reduction"]], int(i["num_sms"]), int(i["ctas_per_sm"]))
+            assert got == int(exp), name
+        else:
+            p = plan(int(i["T"]), int(i["I"]), int(i["P"]), MODE[i["mode"]])
+            for k, v in _kv(exp).items():
+                assert getattr(p, k) == int(v), (name, k)
+        n += 1
+    assert n == 8
+
+
+# Hand-worked vectors for 128x128 tiles (TK = 64 for 16-bit, 128 for fp8):
+#  T = tiles, I = ceil(Kred/TK), sk_tiles = T mod P, dp = T - sk_tiles, sk_iters = sk_tiles*I,
+#  ipc = sk_iters // P, extra = sk_iters mod P.
+VECTORS = [
+    # name, T, I, P, dp, sk_tiles, sk_iters, ipc, extra
+    ("gemm 256x256x4096 pool 3", 4, 64, 3, 3, 1, 64, 21, 1),
+    ("gemm 3840x4096x4096 pool 148", 960, 64, 148, 888, 72, 4608, 31, 20),
+    ("wgrad 32x56x56 c64 k64", 5, 1568, 148, 0, 5, 7840, 52, 144),
+    ("wgrad 64x28x28 g4 s2", 20, 196, 148, 0, 20, 3920, 26, 72),
+    ("fp8 8192^3 (TK=128)", 4096, 64, 148, 3996, 100, 6400, 43, 36),
+    ("gemm 512x512x65536 pool 148", 16, 1024, 148, 0, 16, 16384, 110, 104),
+]
+
+
+@pytest.mark.parametrize("v", VECTORS, ids=[v[0] for v in VECTORS])
+def test_worked_vectors(v):
+    _, T, I, Pool, dp, skt, ski, ipc, extra = v
+    p = plan(T, I, Pool)
+    assert (p.dp_tiles, p.sk_tiles, p.sk_iters, p.iters_per_sk_cta, p.extra) == \
+        (dp, skt, ski, ipc, extra)
+    assert p.sk_ctas == Pool and p.grid == Pool + dp
+    P.check_invariants(p)
+
+
+def test_gemm_pool3_ranges_and_tree_rounds():
+    p = plan(4, 64, 3, P.PERSISTENT)
+    assert [P.sk_range(p, c) for c in range(3)] == [(0, 22), (22, 43), (43, 64)]
+    assert P.contributors(p, 0) == [0, 1, 2]
+    assert p.max_contrib == 3 and p.rounds == 2
+    # tree of 3: index 0 takes 1 (round 0) then 2 (round 1); 1 and 2 only hand on
+    assert P.tree_senders(0, 3, 2) == [1, 2]
+    assert P.tree_senders(1, 3, 2) == [] and P.tree_senders(2, 3, 2) == []
+    # persistent: CTA c runs DP tile 1 + c, then its SK range over tile 0
+    segs = [P.cta_segments(p, c) for c in range(3)]
+    assert [s[0].tile for s in segs] == [1, 2, 3]
+    assert [(s[1].kind, s[1].k_begin, s[1].k_end) for s in segs] == \
+        [(P.SEG_OWNER, 0, 22), (P.SEG_PEER, 22, 43), (P.SEG_PEER, 43, 64)]
+
+
+def test_tree_senders_closed_form():
+    # n = 8: a binary tree; index 0 takes 1, 2, 4; 4 takes 5, 6; 6 takes 7; odd indices take none
+    assert P.tree_senders(0, 8, 3) == [1, 2, 4]
+    assert P.tree_senders(4, 8, 3) == [5, 6]
+    assert P.tree_senders(6, 8, 3) == [7]
+    assert all(P.tree_senders(j, 8, 3) == [] for j in (1, 3, 5, 7))
+    # every index but 0 hands on exactly once: sum of receives = n - 1
+    for n in range(1, 40):
+        r = max(0, (n - 1).bit_length())
+        assert sum(len(P.tree_senders(j, n, r)) for j in range(n)) == n - 1
+
+
+def test_brute_force_assignment_matches_closed_form():
+    rng = random.Random(3)
+    for _ in range(400):
+        T, I, Pool = rng.randint(1, 300), rng.randint(1, 200), rng.randint(1, 300)
+        p = plan(T, I, Pool)
+        if not p.sk_ctas:
+            continue
+        owner = P.brute_force_assignment(p)
+        assert all(P.cta_of_iter(p, i) == owner[i] for i in range(0, p.sk_iters, 7))
+
+
+SWEEP = [(T, I, Pool) for T, I, Pool in itertools.product(
+    [1, 2, 3, 4, 5, 7, 12, 13, 148, 149, 300], [1, 2, 3, 7, 64, 65], [1, 2, 3, 4, 5, 12, 148])]
+
+
+@pytest.mark.parametrize("mode", [P.OFF, P.DP_SK, P.PERSISTENT, P.SPLITK])
+def test_invariants_sweep(mode):
+    for T, I, Pool in SWEEP:
+        P.check_invariants(plan(T, I, Pool, mode))
+
+
+def test_all_dp_when_tiles_divide_pool():
+    for T, Pool in [(148, 148), (296, 148), (12, 3), (12, 4)]:
+        p = plan(T, 33, Pool)
+        assert p.sk_ctas == 0 and p.dp_tiles == T and p.iters_per_sk_cta == 1
+
+
+def test_splitk_comparator():
+    p = plan(16, 1024, 148, P.SPLITK)
+    assert p.splits == 9 and p.grid == 144
+    segs = P.cta_segments(p, 10)
+    assert segs[0].tile == 1 and (segs[0].k_begin, segs[0].k_end) == (113, 227)
+    assert plan(1, 3, 148, P.SPLITK).splits == 3          # never more slices than iterations
+    assert plan(300, 8, 148, P.SPLITK).splits == 1         # tiles fill the pool: no split
+
+
+def test_workspace_layout():
+    p = plan(4, 64, 3, P.PERSISTENT, P.LINEAR)
+    assert p.flag_bytes == 256 and p.partial_bytes == 3 * 128 * 128 * 4
+    assert p.ws_bytes == 256 + P.CONTROL_BYTES + 3 * 65536
+    w = plan(4, 64, 3, P.PERSISTENT, P.WORKSPACE)
+    assert w.partial_bytes == 0 and w.scratch_bytes == 1 * 65536
+    a = plan(4, 64, 3, P.PERSISTENT, P.ATOMIC)
+    assert a.ws_bytes == 256 + P.CONTROL_BYTES
+
+
+def test_forward_progress_simulation():
+    rng = random.Random(5)
+    cases = [(4, 64, 3), (5, 1568 // 16, 148 // 4), (7, 5, 6), (3, 40, 12)]
+    cases += [(rng.randint(1, 30), rng.randint(1, 40), rng.randint(2, 24)) for _ in range(60)]
+    for T, I, Pool in cases:
+        for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK):
+            for red in (P.LINEAR, P.TREE):
+                p = plan(T, I, Pool, mode, red)
+                # a blocked linear owner needs one more resident CTA to make progress; a tree
+                # blocks at most `rounds` CTAs at a time
+                need = 2 if red == P.LINEAR else p.rounds + 1
+                for slots in sorted({need, need + 1, max(need, p.grid // 2), max(need, p.grid)}):
+                    assert P.simulate_progress(p, slots, red), (T, I, Pool, mode, red, slots)
+
+
+# --- planted mistakes: each must be caught by the checks above -------------------------------
+
+def test_single_slot_linear_owner_blocks():
+    # with one resident CTA the owner of a shared tile waits for a CTA that never starts
+    assert not P.simulate_progress(plan(4, 64, 3, P.DP_SK, P.LINEAR), 1, P.LINEAR)
+
+
+def test_planted_extra_on_last_ctas_is_caught(monkeypatch):
+    orig = P.sk_range
+
+    def wrong(p, c):      # give the extra iteration to the LAST ctas instead of the first
+        b, e = orig(p, c)
+        if p.extra == 0:
+            return b, e
+        k = p.sk_ctas - p.extra
+        size = p.iters_per_sk_cta + (1 if c >= k else 0)
+        begin = c * p.iters_per_sk_cta + max(0, c - k)
+        return begin, begin + size
+    monkeypatch.setattr(P, "sk_range", wrong)
+    with pytest.raises(AssertionError):
+        P.check_invariants(plan(4, 64, 3))
+
+
+def test_planted_missing_all_dp_rule_is_caught():
+    p = plan(1, 1024, 1216)
+    assert p.sk_ctas == 0
+    q = plan(1, 1216, 1216)
+    assert q.sk_ctas == 1216
+
+
+def test_planted_wrong_tree_direction_is_caught(monkeypatch):
+    monkeypatch.setattr(P, "tree_senders",
+                        lambda j, n, r: [j - 1] if j % 2 == 1 else [])   # waits on a lower id
+    with pytest.raises(AssertionError):
+        P.check_invariants(plan(4, 64, 3, P.PERSISTENT, P.TREE))
