@@ -1,0 +1,669 @@
+// C ABI of libskgemm: argument validation (-2), the host planner, workspace layout, TMA
+// descriptors and the launch sequence on the caller's stream.
+//
+// The single-problem call shape and its return codes follow "feat(ck-tile): stream-K GEMM TE to
+// dispatcher bridge" (Design note / Changes: returns 0, -1 on a launch error, -2 for
+// unsupported arguments; the launch owns the reduction workspace). The knobs streamk /
+// reduction / ctas, the CTA-pool default and the validator's rejections follow rocm-libraries
+// PR #13151 (PR body: Technical Details, Constraints; commits "Resolve streamk_ctas=-1 from the
+// reduction" and "Address review feedback").
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "sk_kernels.h"
+#include "sk_plan.h"
+#include "skgemm.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(SK_ERR_LAUNCH, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+const char* mode_name(int m) {
+    switch (m) {
+        case SK_OFF: return "off";
+        case SK_DP_SK: return "dp_sk";
+        case SK_PERSISTENT: return "persistent";
+        case SK_SPLITK: return "splitk";
+        default: return "?";
+    }
+}
+const char* red_name(int r) {
+    switch (r) {
+        case SK_LINEAR: return "linear";
+        case SK_TREE: return "tree";
+        case SK_ATOMIC: return "atomic";
+        case SK_WORKSPACE: return "workspace";
+        default: return "?";
+    }
+}
+const char* dtype_name(int d) {
+    switch (d) {
+        case SK_F16: return "f16";
+        case SK_BF16: return "bf16";
+        case SK_F32: return "f32";
+        case SK_E4M3: return "e4m3";
+        default: return "?";
+    }
+}
+int dtype_size(int d) { return d == SK_F32 ? 4 : d == SK_E4M3 ? 1 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- device facts ---------------------------------------------------------------------------
+
+struct DevInfo {
+    bool ok = false;
+    int sms = 0, major = 0, minor = 0;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+int current_device_info(DevInfo& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SK_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SK_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].ok) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess)
+            return fail(SK_ERR_UNSUPPORTED, "cannot query device %d: %s", dev, cudaGetErrorString(e));
+        g_dev[dev].sms = prop.multiProcessorCount;
+        g_dev[dev].major = prop.major;
+        g_dev[dev].minor = prop.minor;
+        g_dev[dev].ok = true;
+    }
+    out = g_dev[dev];
+    return SK_OK;
+}
+
+// Make the device that owns `p` current (pointers from another runtime instance carry their
+// device in their attributes).
+int select_device_of(const void* p) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SK_ERR_UNSUPPORTED, "cannot query the output pointer: %s", cudaGetErrorString(e));
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+        return fail(SK_ERR_UNSUPPORTED, "output pointer is not device memory");
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != a.device) {
+        e = cudaSetDevice(a.device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    }
+    return SK_OK;
+}
+
+int check_arch(DevInfo& d) {
+    int rc = current_device_info(d);
+    if (rc != SK_OK) return rc;
+    if (!(d.major == 10 && d.minor == 3))
+        return fail(SK_ERR_UNSUPPORTED,
+                    "device is sm_%d%d; this library is built for sm_103a (GB300) only", d.major,
+                    d.minor);
+    return SK_OK;
+}
+
+// ---- planner --------------------------------------------------------------------------------
+
+int resolve_pool(int reduction, int ctas, int num_sms, int ctas_per_sm, int64_t& pool) {
+    if (ctas == 0 || ctas < -1)
+        return fail(SK_ERR_UNSUPPORTED, "streamk_ctas must be -1 (default) or >= 1, got %d", ctas);
+    if (ctas > 0) {
+        pool = ctas;
+        return SK_OK;
+    }
+    if (num_sms <= 0) return fail(SK_ERR_UNSUPPORTED, "default CTA pool needs the SM count");
+    if (reduction == SK_LINEAR || reduction == SK_TREE) {
+        pool = num_sms;   // every CTA may wait on a later one: one per SM
+    } else {
+        int per = ctas_per_sm < 1 ? 1 : ctas_per_sm;
+        pool = static_cast<int64_t>(num_sms) * (per < 4 ? per : 4);
+    }
+    return SK_OK;
+}
+
+struct View {          // GEMM view of a problem
+    int64_t gemm_m, gemm_n, kred, groups;
+    int op_kind;       // sk::OpKind
+};
+
+int problem_view(const sk_problem& p, View& v) {
+    switch (p.op) {
+        case SK_OP_GEMM:
+        case SK_OP_FP8_ROWCOL:
+            v.gemm_m = p.M;
+            v.gemm_n = p.N;
+            v.kred = p.K;
+            v.groups = 1;
+            v.op_kind = p.op == SK_OP_GEMM ? sk::kOpGemm16 : sk::kOpFp8;
+            return SK_OK;
+        case SK_OP_WGRAD: {
+            if (p.groups < 1) return fail(SK_ERR_UNSUPPORTED, "groups must be >= 1");
+            if (p.stride_h < 1 || p.stride_w < 1) return fail(SK_ERR_UNSUPPORTED, "stride must be >= 1");
+            const int64_t Ho = (p.h + 2 * p.pad_h - p.r) / p.stride_h + 1;
+            const int64_t Wo = (p.w + 2 * p.pad_w - p.s) / p.stride_w + 1;
+            if (p.h + 2 * p.pad_h < p.r || p.w + 2 * p.pad_w < p.s || Ho < 1 || Wo < 1)
+                return fail(SK_ERR_UNSUPPORTED, "filter larger than the padded image");
+            v.groups = p.groups;
+            v.gemm_m = p.k / p.groups;
+            v.gemm_n = p.r * p.s * (p.c / p.groups);
+            v.kred = p.n * Ho * Wo;
+            v.op_kind = sk::kOpWgrad16;
+            return SK_OK;
+        }
+        default:
+            return fail(SK_ERR_UNSUPPORTED, "unknown op %d", p.op);
+    }
+}
+
+int build_plan(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
+               int ctas_per_sm, sk_plan_t& p) {
+    if (mode < SK_OFF || mode > SK_SPLITK) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
+    if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
+        return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
+    View v;
+    int rc = problem_view(prob, v);
+    if (rc) return rc;
+    if (v.gemm_m < 1 || v.gemm_n < 1 || v.kred < 1 || v.groups < 1)
+        return fail(SK_ERR_UNSUPPORTED, "empty problem (M=%lld N=%lld K=%lld)", (long long)v.gemm_m,
+                    (long long)v.gemm_n, (long long)v.kred);
+    int64_t P = 0;
+    rc = resolve_pool(reduction, ctas, num_sms, ctas_per_sm, P);
+    if (rc) return rc;
+    memset(&p, 0, sizeof(p));
+    p.op = prob.op;
+    p.mode = mode;
+    p.reduction = reduction;
+    p.tm = sk::kTileM;
+    p.tn = 128;
+    p.tk = prob.op == SK_OP_FP8_ROWCOL ? 128 : 64;
+    p.gemm_m = v.gemm_m;
+    p.gemm_n = v.gemm_n;
+    p.kred = v.kred;
+    p.groups = v.groups;
+    p.tiles_m = sk::ceil_div(v.gemm_m, p.tm);
+    p.tiles_n = sk::ceil_div(v.gemm_n, p.tn);
+    p.tiles = v.groups * p.tiles_m * p.tiles_n;
+    p.iters_per_tile = sk::ceil_div(v.kred, p.tk);
+    p.pool = P;
+    p.iters_per_sk_cta = 1;
+    const int64_t T = p.tiles, I = p.iters_per_tile;
+    if (mode == SK_OFF) {
+        p.dp_tiles = T;
+        p.grid = T;
+    } else if (mode == SK_SPLITK) {
+        int64_t s = P / T;
+        if (s < 1) s = 1;
+        if (s > I) s = I;
+        p.splits = s;
+        p.dp_tiles = s == 1 ? T : 0;
+        p.grid = T * s;
+        p.publishers = s > 1 ? T * s : 0;
+    } else {
+        p.sk_tiles = T % P;
+        p.dp_tiles = T - p.sk_tiles;
+        p.sk_iters = p.sk_tiles * I;
+        if (p.sk_tiles == 0 || p.sk_iters < P) {   // too few iterations for the pool: all-DP
+            p.sk_tiles = 0;
+            p.dp_tiles = T;
+            p.sk_iters = 0;
+            p.sk_ctas = 0;
+        } else {
+            p.sk_ctas = P;
+            p.iters_per_sk_cta = sk::imax(1, p.sk_iters / p.sk_ctas);
+            p.extra_iters = p.sk_iters % p.sk_ctas;
+        }
+        p.grid = mode == SK_DP_SK ? p.sk_ctas + p.dp_tiles : P;
+        p.publishers = p.sk_ctas;
+    }
+    if (p.grid > 0x7fffffffLL) return fail(SK_ERR_UNSUPPORTED, "grid too large");
+    int64_t maxc = 1, shared = 0;
+    for (int64_t t = 0; t < sk::n_shared_candidates(p); ++t) {
+        int64_t first, n;
+        sk::tile_contributors(p, t, first, n);
+        if (n > maxc) maxc = n;
+        shared += n > 1;
+    }
+    p.max_contributors = maxc;
+    p.shared_tiles = shared;
+    while ((int64_t(1) << p.tree_rounds) < maxc) ++p.tree_rounds;
+    if (reduction == SK_TREE && p.tree_rounds > 32)
+        return fail(SK_ERR_UNSUPPORTED, "tree reduction supports at most 2^32 contributors");
+    const int64_t tile_bytes = p.tm * p.tn * 4;
+    p.flag_bytes = sk::round_up(4 * p.publishers, 256);
+    p.control_offset = p.flag_bytes;
+    p.partial_offset = p.control_offset + sk::kControlBytes;
+    p.partial_bytes = (reduction == SK_LINEAR || reduction == SK_TREE) ? p.publishers * tile_bytes : 0;
+    p.scratch_offset = p.partial_offset + p.partial_bytes;
+    p.scratch_bytes = reduction == SK_WORKSPACE ? sk::n_shared_candidates(p) * tile_bytes : 0;
+    p.ws_bytes = p.scratch_offset + p.scratch_bytes;
+    return SK_OK;
+}
+
+// ---- TMA descriptors ------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                   cuuint32_t, cuuint32_t, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+std::once_flag g_enc_once;
+EncodeTiledFn g_encode_tiled = nullptr;
+EncodeIm2colFn g_encode_im2col = nullptr;
+
+int load_encoders() {
+    std::call_once(g_enc_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<EncodeTiledFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(f);
+    });
+    if (!g_encode_tiled || !g_encode_im2col)
+        return fail(SK_ERR_LAUNCH, "cuTensorMapEncode* entry points unavailable");
+    return SK_OK;
+}
+
+// 2-D K-major (inner dimension first) tile map with 128-byte swizzle; box = {box_inner, box_outer}.
+int encode_2d(CUtensorMap* m, const void* base, int elem, uint64_t inner, uint64_t outer,
+              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                                2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return SK_OK;
+}
+
+uint64_t flag_timeout_ns() {
+    const char* s = getenv("SKGEMM_FLAG_TIMEOUT_MS");
+    long long ms = s ? atoll(s) : 1000;
+    if (ms < 1) ms = 1;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+// ---- launch sequence ------------------------------------------------------------------------
+
+int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelParams& kp,
+        void* out, size_t out_pitch_bytes, size_t out_rows, size_t out_row_bytes, void* ws,
+        size_t ws_bytes, cudaStream_t stream) {
+    DevInfo dev;
+    int rc = check_arch(dev);
+    if (rc) return rc;
+    View v;
+    problem_view(prob, v);
+    const int per_sm = sk::main_ctas_per_sm(v.op_kind, 128);
+    sk_plan_t plan;
+    rc = build_plan(prob, mode, reduction, ctas, dev.sms, per_sm, plan);
+    if (rc) return rc;
+    if (ws != nullptr) {
+        if (ws_bytes < static_cast<size_t>(plan.ws_bytes))
+            return fail(SK_ERR_UNSUPPORTED, "workspace too small: %zu < %lld bytes", ws_bytes,
+                        (long long)plan.ws_bytes);
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+            return fail(SK_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+    }
+    bool own_ws = false;
+    cudaError_t e;
+    if (ws == nullptr) {
+        e = cudaMallocAsync(&ws, static_cast<size_t>(plan.ws_bytes), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+        own_ws = true;
+    }
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    kp.plan = plan;
+    kp.flags = reinterpret_cast<uint32_t*>(w);
+    kp.control = reinterpret_cast<uint32_t*>(w + plan.control_offset);
+    kp.partials = reinterpret_cast<float*>(w + plan.partial_offset);
+    kp.scratch = reinterpret_cast<float*>(w + plan.scratch_offset);
+    kp.flag_timeout_ns = flag_timeout_ns();
+    kp.mbar_timeout_ns = 2000000000ull;
+
+    rc = SK_OK;
+    do {
+        e = cudaMemsetAsync(w, 0, static_cast<size_t>(plan.flag_bytes + sk::kControlBytes), stream);
+        if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags)"); break; }
+        if (plan.scratch_bytes > 0) {
+            e = cudaMemsetAsync(w + plan.scratch_offset, 0, static_cast<size_t>(plan.scratch_bytes), stream);
+            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
+        }
+        if (reduction == SK_ATOMIC && plan.shared_tiles > 0) {
+            e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
+            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
+        }
+        int le = sk::launch_main(kp, v.op_kind, 128, stream);
+        if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
+        if (reduction == SK_WORKSPACE && plan.shared_tiles > 0) {
+            sk::Stage2Params s2;
+            s2.plan = plan;
+            s2.c = kp.c;
+            s2.ldc = kp.ldc;
+            s2.sa = kp.sa;
+            s2.sb = kp.sb;
+            s2.scratch = kp.scratch;
+            s2.c_dtype = kp.c_dtype;
+            le = sk::launch_stage2(s2, stream);
+            if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
+        }
+    } while (false);
+    if (own_ws) {
+        e = cudaFreeAsync(ws, stream);
+        if (e != cudaSuccess && rc == SK_OK) rc = cuda_fail(e, "cudaFreeAsync(workspace)");
+    }
+    return rc;
+}
+
+int check_common(int mode, int reduction, int ctas, int c_dtype) {
+    if (mode < SK_OFF || mode > SK_SPLITK) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
+    if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
+        return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
+    if (ctas == 0 || ctas < -1)
+        return fail(SK_ERR_UNSUPPORTED, "streamk_ctas must be -1 (default) or >= 1, got %d", ctas);
+    if (reduction == SK_ATOMIC && c_dtype != SK_F32)
+        return fail(SK_ERR_UNSUPPORTED, "reduction 'atomic' needs an fp32 output, got %s",
+                    dtype_name(c_dtype));
+    return SK_OK;
+}
+
+}  // namespace
+
+// =============================================================================================
+// C ABI
+// =============================================================================================
+
+extern "C" {
+
+const char* sk_last_error(void) { return g_err; }
+
+int sk_version(void) { return 100; }
+
+int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out) {
+    if (!out) return fail(SK_ERR_UNSUPPORTED, "out is NULL");
+    if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
+        return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
+    int64_t pool = 0;
+    int rc = resolve_pool(reduction, -1, num_sms, ctas_per_sm, pool);
+    if (rc) return rc;
+    *out = static_cast<int>(pool);
+    return SK_OK;
+}
+
+int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_sms, sk_plan_t* out) {
+    if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
+    int per_sm = 1;
+    if (ctas == -1 && num_sms <= 0) {
+        DevInfo d;
+        int rc = current_device_info(d);
+        if (rc) return rc;
+        num_sms = d.sms;
+        View v;
+        if (problem_view(*p, v) == SK_OK) per_sm = sk::main_ctas_per_sm(v.op_kind, 128);
+    }
+    return build_plan(*p, streamk, reduction, ctas, num_sms, per_sm, *out);
+}
+
+int sk_plan_cta_work(const sk_plan_t* plan, int64_t cta, sk_segment_t* out, int max_out, int* n_out) {
+    if (!plan || !n_out || (max_out > 0 && !out)) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
+    if (cta < 0 || cta >= plan->grid) return fail(SK_ERR_UNSUPPORTED, "cta %lld outside the grid", (long long)cta);
+    sk::SegCursor c;
+    sk::seg_init(*plan, cta, c);
+    sk_segment_t s;
+    int n = 0;
+    while (sk::seg_next(*plan, cta, c, s)) {
+        if (n < max_out) out[n] = s;
+        ++n;
+    }
+    *n_out = n;
+    return SK_OK;
+}
+
+int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out) {
+    if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
+    sk_plan_t plan;
+    int rc = sk_plan(p, streamk, reduction, ctas, 0, &plan);
+    if (rc) return rc;
+    *out = static_cast<size_t>(plan.ws_bytes);
+    return SK_OK;
+}
+
+int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, const void* A,
+                int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int streamk,
+                int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    if (ab_dtype != SK_F16 && ab_dtype != SK_BF16)
+        return fail(SK_ERR_UNSUPPORTED, "GEMM inputs must be f16 or bf16, got %s", dtype_name(ab_dtype));
+    if (c_dtype != ab_dtype && c_dtype != SK_F32)
+        return fail(SK_ERR_UNSUPPORTED, "GEMM output must be %s or f32, got %s", dtype_name(ab_dtype),
+                    dtype_name(c_dtype));
+    int rc = check_common(streamk, reduction, ctas, c_dtype);
+    if (rc) return rc;
+    if (M < 0 || N < 0 || K < 0) return fail(SK_ERR_UNSUPPORTED, "negative size");
+    if (M == 0 || N == 0) return SK_OK;   // nothing to write
+    if (!C || (K > 0 && (!A || !B))) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    const int cs = dtype_size(c_dtype);
+    if (K % 8 != 0) return fail(SK_ERR_UNSUPPORTED, "K must be a multiple of 8 (16-byte rows), got %lld", (long long)K);
+    if (lda < K || ldb < K || ldc < N) return fail(SK_ERR_UNSUPPORTED, "leading dimension smaller than the row");
+    if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldc * cs) % 16)
+        return fail(SK_ERR_UNSUPPORTED, "lda, ldb and ldc rows must be multiples of 16 bytes");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+        return fail(SK_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned");
+    rc = select_device_of(C);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {   // empty reduction: C = 0
+        cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc * cs), 0,
+                                          static_cast<size_t>(N * cs), static_cast<size_t>(M), st);
+        return e == cudaSuccess ? SK_OK : cuda_fail(e, "cudaMemset2DAsync(C)");
+    }
+    rc = load_encoders();
+    if (rc) return rc;
+    sk_problem prob;
+    memset(&prob, 0, sizeof(prob));
+    prob.op = SK_OP_GEMM;
+    prob.ab_dtype = ab_dtype;
+    prob.c_dtype = c_dtype;
+    prob.M = M;
+    prob.N = N;
+    prob.K = K;
+    prob.groups = 1;
+    sk::KernelParams kp;
+    memset(&kp, 0, sizeof(kp));
+    rc = encode_2d(&kp.tmap_a, A, 2, K, M, lda * 2, 64, 128);
+    if (rc) return rc;
+    rc = encode_2d(&kp.tmap_b, B, 2, K, N, ldb * 2, 64, 128);
+    if (rc) return rc;
+    kp.c = C;
+    kp.ldc = ldc;
+    kp.c_dtype = c_dtype;
+    const uint32_t fmt = ab_dtype == SK_BF16 ? 1u : 0u;
+    kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, 128);
+    return run(prob, streamk, reduction, ctas, kp, C, ldc * cs, M, N * cs, ws, ws_bytes, st);
+}
+
+int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                       const float* sa, const float* sb, void* C_bf16, int64_t ldc, int streamk,
+                       int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_common(streamk, reduction, ctas, SK_BF16);
+    if (rc) return rc;
+    if (M < 0 || N < 0 || K < 0) return fail(SK_ERR_UNSUPPORTED, "negative size");
+    if (M == 0 || N == 0) return SK_OK;
+    if (!A8 || !B8 || !sa || !sb || !C_bf16) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    if (K < 16 || K % 16 != 0) return fail(SK_ERR_UNSUPPORTED, "K must be a positive multiple of 16, got %lld", (long long)K);
+    if (ldc < N || (ldc * 2) % 16) return fail(SK_ERR_UNSUPPORTED, "ldc must be >= N with 16-byte rows");
+    if (!aligned16(A8) || !aligned16(B8) || !aligned16(C_bf16))
+        return fail(SK_ERR_UNSUPPORTED, "A8, B8 and C must be 16-byte aligned");
+    rc = select_device_of(C_bf16);
+    if (rc) return rc;
+    rc = load_encoders();
+    if (rc) return rc;
+    sk_problem prob;
+    memset(&prob, 0, sizeof(prob));
+    prob.op = SK_OP_FP8_ROWCOL;
+    prob.ab_dtype = SK_E4M3;
+    prob.c_dtype = SK_BF16;
+    prob.M = M;
+    prob.N = N;
+    prob.K = K;
+    prob.groups = 1;
+    sk::KernelParams kp;
+    memset(&kp, 0, sizeof(kp));
+    rc = encode_2d(&kp.tmap_a, A8, 1, K, M, K, 128, 128);
+    if (rc) return rc;
+    rc = encode_2d(&kp.tmap_b, B8, 1, K, N, K, 128, 128);
+    if (rc) return rc;
+    kp.c = C_bf16;
+    kp.ldc = ldc;
+    kp.c_dtype = SK_BF16;
+    kp.sa = sa;
+    kp.sb = sb;
+    kp.idesc = sk::make_idesc(0, 0, false, false, 128, 128);
+    return run(prob, streamk, reduction, ctas, kp, C_bf16, ldc * 2, M, N * 2, ws, ws_bytes,
+               static_cast<cudaStream_t>(stream));
+}
+
+int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* x, const void* dy, void* dw,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream) {
+    if (in_dtype != SK_F16 && in_dtype != SK_BF16)
+        return fail(SK_ERR_UNSUPPORTED, "wgrad inputs must be f16 or bf16, got %s", dtype_name(in_dtype));
+    if (dw_dtype != SK_F32 && dw_dtype != in_dtype)
+        return fail(SK_ERR_UNSUPPORTED, "dW must be f32 or %s, got %s", dtype_name(in_dtype),
+                    dtype_name(dw_dtype));
+    int rc = check_common(streamk, reduction, ctas, dw_dtype);
+    if (rc) return rc;
+    if (N < 0 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1)
+        return fail(SK_ERR_UNSUPPORTED, "sizes must be positive");
+    if (groups < 1 || C % groups || K % groups)
+        return fail(SK_ERR_UNSUPPORTED, "groups must divide C and K");
+    if (stride_h < 1 || stride_w < 1 || stride_h > 8 || stride_w > 8)
+        return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
+    if (pad_h < 0 || pad_w < 0 || pad_h >= R || pad_w >= S)
+        return fail(SK_ERR_UNSUPPORTED, "padding must be in [0, filter size)");
+    if (R > 16 || S > 16) return fail(SK_ERR_UNSUPPORTED, "filter taps beyond 16 are not supported");
+    const int64_t Cg = C / groups, Kg = K / groups;
+    if (Cg % 64) return fail(SK_ERR_UNSUPPORTED, "channels per group must be a multiple of 64, got %lld", (long long)Cg);
+    if (Kg % 8) return fail(SK_ERR_UNSUPPORTED, "filters per group must be a multiple of 8, got %lld", (long long)Kg);
+    const int64_t Ho = (H + 2 * pad_h - R) / stride_h + 1;
+    const int64_t Wo = (W + 2 * pad_w - S) / stride_w + 1;
+    if (H + 2 * pad_h < R || W + 2 * pad_w < S || Ho < 1 || Wo < 1)
+        return fail(SK_ERR_UNSUPPORTED, "filter larger than the padded image");
+    const int64_t up_w = (Wo - 1) * stride_w - pad_w - (W - 1);
+    const int64_t up_h = (Ho - 1) * stride_h - pad_h - (H - 1);
+    if (up_w < -128 || up_h < -128 || up_w > 127 || up_h > 127 || -pad_w < -128 || -pad_h < -128)
+        return fail(SK_ERR_UNSUPPORTED, "im2col bounding box outside the 4-D TMA range");
+    if (N * Ho * Wo >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return fail(SK_ERR_UNSUPPORTED, "too many output pixels");
+    if (!x || !dy || !dw) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
+        return fail(SK_ERR_UNSUPPORTED, "x, dy and dw must be 16-byte aligned");
+    const int64_t RSC = R * S * Cg;
+    const int cs = dtype_size(dw_dtype);
+    if (N == 0) {   // empty reduction: dW = 0
+        rc = select_device_of(dw);
+        if (rc) return rc;
+        cudaError_t e = cudaMemsetAsync(dw, 0, static_cast<size_t>(K * RSC * cs), static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? SK_OK : cuda_fail(e, "cudaMemsetAsync(dw)");
+    }
+    rc = select_device_of(dw);
+    if (rc) return rc;
+    rc = load_encoders();
+    if (rc) return rc;
+    sk_problem prob;
+    memset(&prob, 0, sizeof(prob));
+    prob.op = SK_OP_WGRAD;
+    prob.ab_dtype = in_dtype;
+    prob.c_dtype = dw_dtype;
+    prob.n = N; prob.h = H; prob.w = W; prob.c = C; prob.k = K; prob.r = R; prob.s = S;
+    prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
+    prob.groups = groups;
+    sk::KernelParams kp;
+    memset(&kp, 0, sizeof(kp));
+    // dy as a [N*Ho*Wo][K] matrix: 64-filter x 64-pixel boxes (MN-major operand)
+    rc = encode_2d(&kp.tmap_a, dy, 2, K, N * Ho * Wo, K * 2, 64, 64);
+    if (rc) return rc;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+        const cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2),
+                                       (cuuint64_t)(H * W * C * 2)};
+        const int lower[2] = {-pad_w, -pad_h};
+        const int upper[2] = {static_cast<int>(up_w), static_cast<int>(up_h)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)stride_w, (cuuint32_t)stride_h, 1};
+        CUresult r = g_encode_im2col(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                     const_cast<void*>(x), dims, strides, lower, upper, 64, 64, estr,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
+    }
+    kp.c = dw;
+    kp.ldc = RSC;
+    kp.c_dtype = dw_dtype;
+    const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+    kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, 128);
+    kp.conv.HoWo = Ho * Wo;
+    kp.conv.Wo = static_cast<int32_t>(Wo);
+    kp.conv.sh = stride_h;
+    kp.conv.sw = stride_w;
+    kp.conv.ph = pad_h;
+    kp.conv.pw = pad_w;
+    kp.conv.R = static_cast<int32_t>(R);
+    kp.conv.S = static_cast<int32_t>(S);
+    kp.conv.Cg = static_cast<int32_t>(Cg);
+    kp.conv.Kg = static_cast<int32_t>(Kg);
+    return run(prob, streamk, reduction, ctas, kp, dw, RSC * cs, K, RSC * cs, ws, ws_bytes,
+               static_cast<cudaStream_t>(stream));
+}
+
+int sk_device_status(void* stream) {
+    long long info[3] = {0, 0, 0};
+    int code = sk::take_device_error(static_cast<cudaStream_t>(stream), info);
+    if (code < 0) return fail(SK_ERR_LAUNCH, "cannot read the device status");
+    if (code == 0) return SK_OK;
+    if (code == 1)
+        return fail(SK_ERR_LAUNCH, "linear/tree hand-off timed out: cta %lld tile %lld waiting on cta %lld",
+                    info[0], info[1], info[2]);
+    return fail(SK_ERR_LAUNCH, "pipeline wait timed out: cta %lld tile %lld (role %lld)", info[0],
+                info[1], info[2]);
+}
+
+}  // extern "C"

@@ -1,0 +1,674 @@
+// Stream-K mainloop, fixups and Stage-2 reduce for sm_103a.
+//
+// One kernel serves the three operations (rcr GEMM, implicit-GEMM wgrad, fp8 row/col GEMM). The
+// CTA walks the work the plan gives its logical id (sk_plan.h): data-parallel tiles and/or one
+// contiguous range of MAC iterations that may straddle tiles ("one bounded loop", rocm-libraries
+// PR #13151, commit "Port CK Tile's stream-K to the backward-weight convolution").
+//
+// Warp roles (192 threads):
+//   warp 0     TMA producer: stages A and B tiles into a ring of shared-memory stages.
+//   warp 1     MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM accumulator
+//              and commits it at every segment (tile) boundary; the warp owns the TMEM allocation.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, then per segment one of
+//                - complete tile: scale (fp8), convert, store;
+//                - linear / tree: receive the partials of later CTAs (acquire a per-CTA flag,
+//                  add in a fixed order), then either store the tile or publish this CTA's
+//                  partial and release its flag;
+//                - atomic: red.add.f32 into the fp32 output;
+//                - workspace: red.add.f32 into fp32 scratch (Stage-2 writes the output).
+//   (PR #13151, PR body "Wgrad kernel": linear and tree are deterministic hand-offs through
+//   per-CTA flags, atomic is fp32-only, workspace is fp32 scratch plus a Stage-2 reduce.)
+//
+// Logical CTA ids come from a ticket counter, so a CTA only ever waits on CTAs with larger ids,
+// which started after it; every wait is bounded and records an error instead of hanging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sk_kernels.h"
+#include "sk_plan.h"
+#include "sk_ptx.cuh"
+
+namespace sk {
+
+__device__ unsigned long long g_sk_error[4];   // code, cta, tile, detail (first error wins)
+
+enum : unsigned long long {
+    kErrFlagWait = 1,   // a linear/tree receive gave up waiting for a flag
+    kErrPipeline = 2,   // an mbarrier wait inside the CTA gave up
+};
+
+__device__ __noinline__ void record_error(unsigned long long code, long long cta, long long tile,
+                                          long long detail) {
+    if (atomicCAS(&g_sk_error[0], 0ull, code) == 0ull) {
+        g_sk_error[1] = static_cast<unsigned long long>(cta);
+        g_sk_error[2] = static_cast<unsigned long long>(tile);
+        g_sk_error[3] = static_cast<unsigned long long>(detail);
+    }
+}
+
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kEpiBarrier = 1;
+
+template <int OP, int TN>
+struct Cfg {
+    static constexpr int kElem = OP == kOpFp8 ? 1 : 2;
+    static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
+    static constexpr int kABytes = kTileM * 128;           // 16 KB
+    static constexpr int kBBytes = TN * 128;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = TN == 128 ? 6 : 4;
+    static constexpr int kTmemCols = 2 * TN;               // double-buffered fp32 accumulator
+    static constexpr int kMmaK = OP == kOpFp8 ? 32 : 16;
+    static constexpr int kMmasPerStage = TK / kMmaK;
+    static constexpr int kBarBytes = (2 * kStages + 4) * 8;
+    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes + 64;
+};
+
+struct SmemCtl {
+    uint32_t tmem_base;
+    uint32_t abort;
+    long long cta;
+    uint32_t epi_ok[2];   // epilogue: accumulator-ready verdict, one slot per alternate segment
+};
+
+// ---------------------------------------------------------------------------------------------
+// operand producer
+// ---------------------------------------------------------------------------------------------
+
+template <int OP, int TN>
+__device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
+                                            int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
+                                            uint32_t bar) {
+    using C = Cfg<OP, TN>;
+    if constexpr (OP != kOpWgrad16) {
+        const int32_t kx = static_cast<int32_t>(k * C::TK);
+        tma_load_2d(a_dst, &P.tmap_a, bar, kx, static_cast<int32_t>(mt * kTileM));
+        tma_load_2d(b_dst, &P.tmap_b, bar, kx, static_cast<int32_t>(nt * TN));
+    } else {
+        // A = dy viewed as [pixels][K]: two 64-filter slabs of TK pixel rows (MN-major).
+        const ConvGeom& cg = P.conv;
+        const int32_t p0 = static_cast<int32_t>(k * C::TK);
+        const int32_t k0 = static_cast<int32_t>(g * cg.Kg + mt * kTileM);
+#pragma unroll
+        for (int j = 0; j < kTileM / 64; ++j)
+            tma_load_2d(a_dst + j * (C::TK * 128), &P.tmap_a, bar, k0 + 64 * j, p0);
+        // B = im2col(x): per 64-column slab one filter tap (r, s) and 64 channels, TK pixels.
+        const int64_t n_img = p0 / cg.HoWo;
+        const int64_t rem = p0 - n_img * cg.HoWo;
+        const int32_t ho = static_cast<int32_t>(rem / cg.Wo);
+        const int32_t wo = static_cast<int32_t>(rem - int64_t(ho) * cg.Wo);
+        const int32_t RS = cg.R * cg.S;
+#pragma unroll
+        for (int j = 0; j < TN / 64; ++j) {
+            const int64_t n0 = nt * TN + 64 * j;
+            int32_t tap = static_cast<int32_t>(n0 / cg.Cg);
+            const int32_t c0 = static_cast<int32_t>(n0 - int64_t(tap) * cg.Cg);
+            if (tap >= RS) tap = RS - 1;   // slab past the last tap: any valid data, masked later
+            const int32_t r = tap / cg.S, s = tap - (tap / cg.S) * cg.S;
+            tma_load_im2col_4d(b_dst + j * (C::TK * 128), &P.tmap_b, bar,
+                               static_cast<int32_t>(g * cg.Cg + c0), wo * cg.sw - cg.pw,
+                               ho * cg.sh - cg.ph, static_cast<int32_t>(n_img),
+                               static_cast<uint16_t>(s), static_cast<uint16_t>(r));
+        }
+    }
+}
+
+template <int OP, int TN>
+__device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
+                             volatile SmemCtl* ctl) {
+    using C = Cfg<OP, TN>;
+    const sk_plan_t& plan = P.plan;
+    SegCursor cur;
+    seg_init(plan, cta, cur);
+    sk_segment_t seg;
+    uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    while (ok && seg_next(plan, cta, cur, seg)) {
+        int64_t g, mt, nt;
+        tile_coords(plan, seg.tile, g, mt, nt);
+        for (int64_t k = seg.k_begin; k < seg.k_end; ++k) {
+            const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
+            if (!mbar_wait(empty, phase ^ 1, P.mbar_timeout_ns) || ctl->abort) {
+                record_error(kErrPipeline, cta, seg.tile, 0);
+                ctl->abort = 1;
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(full, C::kStageBytes);
+            const uint32_t a_dst = ring + stage * C::kStageBytes;
+            issue_loads<OP, TN>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full);
+            ++issued;
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    }
+    if (!ok) {
+        // Let the copies already in flight land before the CTA can exit.
+        for (int i = 0; i < C::kStages && i < issued; ++i) {
+            if (stage == 0) {
+                stage = C::kStages;
+                phase ^= 1;
+            }
+            --stage;
+            mbar_wait(bars + stage * 8, phase, 10000000ull);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// MMA issuer
+// ---------------------------------------------------------------------------------------------
+
+template <int OP, int TN>
+__device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
+                        uint32_t tmem_base, volatile SmemCtl* ctl) {
+    using C = Cfg<OP, TN>;
+    const sk_plan_t& plan = P.plan;
+    SegCursor cur;
+    seg_init(plan, cta, cur);
+    sk_segment_t seg;
+    uint32_t stage = 0, phase = 0;
+    int64_t nseg = 0;
+    uint32_t last_empty = 0, last_parity = 0;
+    bool any = false, ok = true;
+    while (ok && seg_next(plan, cta, cur, seg)) {
+        const uint32_t acc = static_cast<uint32_t>(nseg & 1);
+        const uint32_t acc_phase = static_cast<uint32_t>((nseg >> 1) & 1);
+        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
+        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
+        if (!mbar_wait(tempty, acc_phase ^ 1, P.mbar_timeout_ns) || ctl->abort) {
+            record_error(kErrPipeline, cta, seg.tile, 1);
+            ctl->abort = 1;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * TN;
+        for (int64_t k = seg.k_begin; k < seg.k_end; ++k) {
+            const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
+            if (!mbar_wait(full, phase, P.mbar_timeout_ns) || ctl->abort) {
+                record_error(kErrPipeline, cta, seg.tile, 2);
+                ctl->abort = 1;
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = ring + stage * C::kStageBytes;
+            const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
+                uint64_t ad, bd;
+                if constexpr (OP == kOpWgrad16) {
+                    // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
+                    ad = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
+                    bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
+                } else {
+                    // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
+                    ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                    bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+                }
+                const uint32_t accumulate = (k > seg.k_begin || kk > 0) ? 1u : 0u;
+                if constexpr (OP == kOpFp8)
+                    mma_f8(d_tmem, ad, bd, P.idesc, accumulate);
+                else
+                    mma_f16(d_tmem, ad, bd, P.idesc, accumulate);
+            }
+            tc_commit(empty);
+            any = true;
+            last_empty = empty;
+            last_parity = phase;
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        if (!ok) break;
+        tc_commit(tfull);
+        ++nseg;
+    }
+    // The accumulator may only be freed once the last MMA has completed.
+    if (any) mbar_wait(last_empty, last_parity, 10000000ull);
+}
+
+// ---------------------------------------------------------------------------------------------
+// epilogue
+// ---------------------------------------------------------------------------------------------
+
+struct EpiCtx {
+    int64_t out_row;       // output row of this thread (g*gemm_m + m)
+    bool row_ok;           // m < gemm_m
+    int64_t n_base;        // first GEMM-view column of the tile
+    int row;               // accumulator row 0..127
+    float row_scale;       // fp8: sa[out_row]; else 1
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+// Store 32 consecutive columns (n_base + col0 ...) of this thread's row.
+template <int OP>
+__device__ __forceinline__ void store_out(const KernelParams& P, const EpiCtx& e, int col0,
+                                          float (&v)[32]) {
+    if (!e.row_ok) return;
+    const int64_t n0 = e.n_base + col0;
+    const int64_t ncols = P.plan.gemm_n;
+    if (n0 >= ncols) return;
+    if constexpr (OP == kOpFp8) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int64_t n = n0 + i;
+            v[i] *= e.row_scale * (n < ncols ? __ldg(P.sb + n) : 0.0f);
+        }
+    }
+    const bool full = n0 + 32 <= ncols;
+    if (P.c_dtype == SK_F32) {
+        float* dst = static_cast<float*>(P.c) + e.out_row * P.ldc + n0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < 32 && n0 + i < ncols; ++i) dst[i] = v[i];
+        }
+    } else if (P.c_dtype == SK_BF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(P.c) + e.out_row * P.ldc + n0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 w;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[i], v[i + 1]);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
+                __nv_bfloat162 h3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
+                w.x = *reinterpret_cast<uint32_t*>(&h0);
+                w.y = *reinterpret_cast<uint32_t*>(&h1);
+                w.z = *reinterpret_cast<uint32_t*>(&h2);
+                w.w = *reinterpret_cast<uint32_t*>(&h3);
+                *reinterpret_cast<uint4*>(dst + i) = w;
+            }
+        } else {
+            for (int i = 0; i < 32 && n0 + i < ncols; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+        }
+    } else {
+        __half* dst = static_cast<__half*>(P.c) + e.out_row * P.ldc + n0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 w;
+                __half2 h0 = __floats2half2_rn(v[i], v[i + 1]);
+                __half2 h1 = __floats2half2_rn(v[i + 2], v[i + 3]);
+                __half2 h2 = __floats2half2_rn(v[i + 4], v[i + 5]);
+                __half2 h3 = __floats2half2_rn(v[i + 6], v[i + 7]);
+                w.x = *reinterpret_cast<uint32_t*>(&h0);
+                w.y = *reinterpret_cast<uint32_t*>(&h1);
+                w.z = *reinterpret_cast<uint32_t*>(&h2);
+                w.w = *reinterpret_cast<uint32_t*>(&h3);
+                *reinterpret_cast<uint4*>(dst + i) = w;
+            }
+        } else {
+            for (int i = 0; i < 32 && n0 + i < ncols; ++i) dst[i] = __float2half_rn(v[i]);
+        }
+    }
+}
+
+// Partial tiles are fragment-major: float4 index (col/4) * 128 + row, so that a warp's 32 rows
+// touch 512 contiguous bytes.
+template <int TN>
+__device__ __forceinline__ float* frag_ptr(float* tile_base, int col0, int i, int row) {
+    return tile_base + ((static_cast<int64_t>((col0 + i) >> 2) * kTileM) + row) * 4;
+}
+
+__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = as_f(r[i]);
+}
+
+template <int OP, int TN>
+__device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
+                                 const EpiCtx& e, uint32_t t_acc, int ethread) {
+    const sk_plan_t& plan = P.plan;
+    constexpr int kChunks = TN / 32;
+    const int red = static_cast<int>(plan.reduction);
+
+    if (seg.kind == SK_SEG_FULL) {
+        for (int ch = 0; ch < kChunks; ++ch) {
+            float v[32];
+            load_acc(t_acc + ch * 32, v);
+            store_out<OP>(P, e, ch * 32, v);
+        }
+        return;
+    }
+    if (red == SK_ATOMIC) {
+        // tcgen05.ld is warp-collective (.sync.aligned): every lane loads, and only the lanes of
+        // rows inside the output add.
+        for (int ch = 0; ch < kChunks; ++ch) {
+            float v[32];
+            load_acc(t_acc + ch * 32, v);
+            if (!e.row_ok) continue;
+            const int64_t n0 = e.n_base + ch * 32;
+            float* dst = static_cast<float*>(P.c) + e.out_row * P.ldc + n0;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                if (n0 + i + 4 <= plan.gemm_n) {
+                    red_add_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+                } else {
+                    for (int j = 0; j < 4; ++j)
+                        if (n0 + i + j < plan.gemm_n) red_add_f32(dst + i + j, v[i + j]);
+                }
+            }
+        }
+        return;
+    }
+    if (red == SK_WORKSPACE) {
+        float* base = P.scratch + seg.tile * static_cast<int64_t>(kTileM * TN);
+        for (int ch = 0; ch < kChunks; ++ch) {
+            float v[32];
+            load_acc(t_acc + ch * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                red_add_v4(frag_ptr<TN>(base, ch * 32, i, e.row), v[i], v[i + 1], v[i + 2],
+                           v[i + 3]);
+        }
+        return;
+    }
+
+    // linear / tree: the contributor indices this one receives from, in fold order. Linear:
+    // the owner takes 1, 2, ..., n-1. Tree: at most one sender per round.
+    int32_t tree[32];
+    int64_t ns = 0;
+    const bool lin = red == SK_LINEAR;
+    if (lin) {
+        ns = seg.index == 0 ? seg.n_contrib - 1 : 0;
+    } else {
+        for_each_tree_sender(seg.index, seg.n_contrib, plan.tree_rounds, [&](int64_t j) {
+            if (ns < 32) tree[ns++] = static_cast<int32_t>(j);
+        });
+    }
+    auto sender = [&](int64_t i) -> int64_t { return lin ? i + 1 : tree[i]; };
+    if (ethread == 0) {
+        // One deadline for all of this segment's receives: a lost hand-off costs at most
+        // flag_timeout_ns, however many senders the segment has.
+        uint64_t t0 = 0;
+        bool late = false;
+        for (int64_t i = 0; i < ns && !late; ++i) {
+            const uint32_t* f = P.flags + seg.first_cta + sender(i);
+            while (ld_acquire_gpu(f) != 1u) {
+                if (t0 == 0) t0 = globaltimer_ns();
+                if (globaltimer_ns() - t0 > P.flag_timeout_ns) {
+                    record_error(kErrFlagWait, cta, seg.tile, seg.first_cta + sender(i));
+                    late = true;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+    }
+    named_bar_sync(kEpiBarrier, kEpiThreads);
+    if (ns > 0) (void)ld_acquire_gpu(P.flags + seg.first_cta + sender(ns - 1));
+
+    const bool publish = seg.kind == SK_SEG_PEER;
+    float* own = P.partials + cta * static_cast<int64_t>(kTileM * TN);
+    for (int ch = 0; ch < kChunks; ++ch) {
+        float v[32];
+        load_acc(t_acc + ch * 32, v);
+        for (int64_t s = 0; s < ns; ++s) {
+            const float* src =
+                P.partials + (seg.first_cta + sender(s)) * static_cast<int64_t>(kTileM * TN);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(
+                    frag_ptr<TN>(const_cast<float*>(src), ch * 32, i, e.row)));
+                v[i] += q.x;
+                v[i + 1] += q.y;
+                v[i + 2] += q.z;
+                v[i + 3] += q.w;
+            }
+        }
+        if (publish) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                __stcg(reinterpret_cast<float4*>(frag_ptr<TN>(own, ch * 32, i, e.row)),
+                       make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        } else {
+            store_out<OP>(P, e, ch * 32, v);
+        }
+    }
+    if (publish) {
+        __threadfence();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (ethread == 0) st_release_gpu(P.flags + cta, 1u);
+    }
+}
+
+template <int OP, int TN>
+__device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t bars,
+                             uint32_t tmem_base, int warp, volatile SmemCtl* ctl) {
+    using C = Cfg<OP, TN>;
+    const sk_plan_t& plan = P.plan;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int quarter = warp & 3;                 // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    const int ethread = static_cast<int>(threadIdx.x) - 64;
+    SegCursor cur;
+    seg_init(plan, cta, cur);
+    sk_segment_t seg;
+    int64_t nseg = 0;
+    while (seg_next(plan, cta, cur, seg)) {
+        const uint32_t acc = static_cast<uint32_t>(nseg & 1);
+        const uint32_t acc_phase = static_cast<uint32_t>((nseg >> 1) & 1);
+        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
+        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
+        // One thread waits (bounded) and the verdict goes to all 128 epilogue threads through a
+        // named barrier, so that every epilogue warp takes the same path and no barrier below
+        // can be left short of arrivals.
+        if (ethread == 0) {
+            const bool ready = mbar_wait(tfull, acc_phase, P.mbar_timeout_ns) && !ctl->abort;
+            if (!ready) {
+                record_error(kErrPipeline, cta, seg.tile, 3);
+                ctl->abort = 1;
+            }
+            ctl->epi_ok[nseg & 1] = ready ? 1u : 0u;
+        }
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (!ctl->epi_ok[nseg & 1]) break;
+        tc_fence_after();
+        int64_t g, mt, nt;
+        tile_coords(plan, seg.tile, g, mt, nt);
+        EpiCtx e;
+        e.row = row;
+        const int64_t m = mt * kTileM + row;
+        e.row_ok = m < plan.gemm_m;
+        e.out_row = g * plan.gemm_m + m;
+        e.n_base = nt * TN;
+        e.row_scale = 1.0f;
+        if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
+        const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
+        epilogue_segment<OP, TN>(P, cta, seg, e, t_acc, ethread);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+        ++nseg;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------------------------
+
+template <int OP, int TN>
+__global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_constant__ KernelParams P) {
+    using C = Cfg<OP, TN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t bars = ring + C::kStages * C::kStageBytes;
+    volatile SmemCtl* ctl =
+        reinterpret_cast<volatile SmemCtl*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bars + s * 8, 1);                    // full: producer arrive + tx bytes
+            mbar_init(bars + (C::kStages + s) * 8, 1);     // empty: MMA commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bars + (2 * C::kStages + a) * 8, 1);              // accumulator full
+            mbar_init(bars + (2 * C::kStages + 2 + a) * 8, kEpiThreads / 32);  // accumulator empty
+        }
+        fence_mbarrier_init();
+        ctl->abort = 0;
+        ctl->cta = static_cast<long long>(atomicAdd(P.control, 1u));
+        tma_prefetch_desc(&P.tmap_a);
+        tma_prefetch_desc(&P.tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(&ctl->tmem_base)), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int64_t cta = ctl->cta;
+
+    if (warp == 0) {
+        if (elect_one()) run_producer<OP, TN>(P, cta, ring, bars, ctl);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (elect_one()) run_mma<OP, TN>(P, cta, ring, bars, tmem_base, ctl);
+        __syncwarp();
+    } else {
+        run_epilogue<OP, TN>(P, cta, bars, tmem_base, warp, ctl);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Stage-2: fp32 scratch of the shared tiles -> output (scaled for fp8)
+// ---------------------------------------------------------------------------------------------
+
+template <int TN>
+__global__ void __launch_bounds__(256) sk_stage2_kernel(const __grid_constant__ Stage2Params P) {
+    const sk_plan_t& plan = P.plan;
+    const int64_t t = blockIdx.x;
+    int64_t first, n;
+    tile_contributors(plan, t, first, n);
+    if (n <= 1) return;   // written directly by its only contributor
+    int64_t g, mt, nt;
+    tile_coords(plan, t, g, mt, nt);
+    const float* base = P.scratch + t * static_cast<int64_t>(kTileM * TN);
+    for (int idx = threadIdx.x; idx < kTileM * TN / 4; idx += blockDim.x) {
+        const int q4 = idx / kTileM, row = idx - q4 * kTileM;
+        const int64_t m = mt * kTileM + row;
+        if (m >= plan.gemm_m) continue;
+        const int64_t n0 = nt * TN + q4 * 4;
+        if (n0 >= plan.gemm_n) continue;
+        const float4 q = *reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4);
+        float v[4] = {q.x, q.y, q.z, q.w};
+        const int64_t out_row = g * plan.gemm_m + m;
+        if (P.sa != nullptr) {
+            const float rs = P.sa[out_row];
+            for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
+        }
+        for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) {
+            const int64_t off = out_row * P.ldc + n0 + j;
+            if (P.c_dtype == SK_F32)
+                static_cast<float*>(P.c)[off] = v[j];
+            else if (P.c_dtype == SK_BF16)
+                static_cast<__nv_bfloat16*>(P.c)[off] = __float2bfloat16_rn(v[j]);
+            else
+                static_cast<__half*>(P.c)[off] = __float2half_rn(v[j]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host-side launch helpers
+// ---------------------------------------------------------------------------------------------
+
+template <int OP, int TN>
+static int launch_main_t(const KernelParams& p, cudaStream_t stream) {
+    using C = Cfg<OP, TN>;
+    auto kern = sk_main_kernel<OP, TN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmem));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (p.plan.grid <= 0) return 0;
+    kern<<<dim3(static_cast<unsigned>(p.plan.grid)), dim3(kThreads), C::kSmem, stream>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int OP, int TN>
+static int ctas_per_sm_t() {
+    using C = Cfg<OP, TN>;
+    auto kern = sk_main_kernel<OP, TN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmem)) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, C::kSmem) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+size_t main_smem_bytes(int op, int tn) {
+    (void)tn;
+    switch (op) {
+        case kOpGemm16: return Cfg<kOpGemm16, 128>::kSmem;
+        case kOpFp8: return Cfg<kOpFp8, 128>::kSmem;
+        default: return Cfg<kOpWgrad16, 128>::kSmem;
+    }
+}
+
+int main_ctas_per_sm(int op, int tn) {
+    (void)tn;
+    switch (op) {
+        case kOpGemm16: return ctas_per_sm_t<kOpGemm16, 128>();
+        case kOpFp8: return ctas_per_sm_t<kOpFp8, 128>();
+        default: return ctas_per_sm_t<kOpWgrad16, 128>();
+    }
+}
+
+int launch_main(const KernelParams& p, int op, int tn, cudaStream_t stream) {
+    (void)tn;
+    switch (op) {
+        case kOpGemm16: return launch_main_t<kOpGemm16, 128>(p, stream);
+        case kOpFp8: return launch_main_t<kOpFp8, 128>(p, stream);
+        default: return launch_main_t<kOpWgrad16, 128>(p, stream);
+    }
+}
+
+int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
+    const int64_t tiles = n_shared_candidates(p.plan);
+    if (tiles <= 0) return 0;
+    sk_stage2_kernel<128><<<dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int take_device_error(cudaStream_t stream, long long info[3]) {
+    unsigned long long h[4] = {0, 0, 0, 0};
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(h, g_sk_error, sizeof(h)) != cudaSuccess) return -1;
+    if (h[0] != 0) {
+        const unsigned long long z[4] = {0, 0, 0, 0};
+        if (cudaMemcpyToSymbol(g_sk_error, z, sizeof(z)) != cudaSuccess) return -1;
+    }
+    info[0] = static_cast<long long>(h[1]);
+    info[1] = static_cast<long long>(h[2]);
+    info[2] = static_cast<long long>(h[3]);
+    return static_cast<int>(h[0]);
+}
+
+}  // namespace sk

@@ -1,0 +1,76 @@
+// Kernel parameter blocks and launch entry points of the CUDA path (internal to libskgemm).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "skgemm.h"
+
+namespace sk {
+
+enum OpKind : int { kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2 };
+
+constexpr int kTileM = 128;
+
+// Instruction descriptor: fp32 accumulator, dense, M x N, A/B formats and majorness.
+//  kind::f16    : fmt 0 = f16, 1 = bf16.   kind::f8f6f4 : fmt 0 = e4m3, 1 = e5m2.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, bool a_mn_major,
+                                                  bool b_mn_major, uint32_t M, uint32_t N) {
+    return (1u << 4)                     // D format: f32
+           | (a_fmt << 7) | (b_fmt << 10)  //
+           | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Geometry the wgrad operand producer needs to turn an iteration into im2col coordinates.
+struct ConvGeom {
+    int64_t HoWo;          // output pixels per image
+    int32_t Wo;
+    int32_t sh, sw, ph, pw;
+    int32_t R, S;
+    int32_t Cg, Kg;        // channels and filters per group
+};
+
+struct KernelParams {
+    CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K]
+    CUtensorMap tmap_b;    // GEMM: B [N][K]; fp8: B8 [N][K]; wgrad: im2col view of x
+    sk_plan_t plan;
+    void* c;               // output
+    int64_t ldc;           // output row stride (elements)
+    const float* sa;       // fp8 row scales (else null)
+    const float* sb;       // fp8 column scales (else null)
+    uint32_t* flags;       // per-publisher flags (linear/tree)
+    uint32_t* control;     // [0] ticket counter
+    float* partials;       // linear/tree partial tiles, one slot per publisher
+    float* scratch;        // workspace reduction scratch, one tile per shared-tile candidate
+    ConvGeom conv;
+    uint64_t flag_timeout_ns;
+    uint64_t mbar_timeout_ns;
+    uint32_t idesc;
+    int32_t c_dtype;
+};
+
+struct Stage2Params {
+    sk_plan_t plan;
+    void* c;
+    int64_t ldc;
+    const float* sa;
+    const float* sb;
+    const float* scratch;
+    int32_t c_dtype;
+};
+
+// Dynamic shared memory of the main kernel for (op, tile N).
+size_t main_smem_bytes(int op, int tn);
+// How many CTAs of the main kernel fit on one SM (0 if the device query fails).
+int main_ctas_per_sm(int op, int tn);
+// Launch the main kernel with grid = p.plan.grid. Returns a cudaError_t value.
+int launch_main(const KernelParams& p, int op, int tn, cudaStream_t stream);
+// Launch the Stage-2 reduce over the shared tiles of a workspace plan.
+int launch_stage2(const Stage2Params& p, cudaStream_t stream);
+// Read and clear the device error record: returns the code (0 = none) and fills info[3].
+int take_device_error(cudaStream_t stream, long long info[3]);
+
+}  // namespace sk

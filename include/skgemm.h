@@ -1,0 +1,189 @@
+/*
+ * skgemm -- stream-K GEMM, implicit-GEMM convolution backward-weight and fp8 row/col-scaled
+ * GEMM on one NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *  [P1] "feat(ck-tile): stream-K GEMM TE to dispatcher bridge" (ROCm composable_kernel commit
+ *       58c1bcbe2e), Design note and Changes: a single-problem GEMM call with the same C ABI as the
+ *       regular GEMM, returning 0 on success, -1 on a launch error, -2 for unsupported arguments;
+ *       the launch owns the reduction workspace.
+ *  [P2] rocm-libraries PR #13151 "feat(rocke): stream-K for implicit-GEMM conv wgrad", PR body
+ *       (Technical Details: Partitioner, Wgrad kernel, Constraints) and commits: the stream-K
+ *       partition (data-parallel tiles + a pool of stream-K CTAs with contiguous balanced
+ *       iteration ranges), launch modes dp_sk / persistent, reductions linear / tree / atomic /
+ *       workspace, CTA pool -1 = arch default, conv groups folded into GEMM-M.
+ *  [P3] rocm-libraries PR #9979 (RowColQuant GEMM bridge), Scope: fp8 rcr GEMM with a per-row
+ *       scale of A and a per-column scale of B applied in the epilogue to an fp32 accumulator.
+ *
+ * Conventions for every compute call:
+ *  - Pointers A, B, x, dy, C, dw, sa, sb, ws are DEVICE pointers owned by the caller. The library
+ *    neither frees nor retains them. `stream` is a cudaStream_t passed as void* (NULL = the
+ *    legacy default stream). Calls are asynchronous: 0 means "enqueued".
+ *  - Return value: 0 ok; -1 a CUDA call or kernel launch failed (message in sk_last_error());
+ *    -2 the arguments are unsupported (nothing was enqueued, no memory was touched).
+ *  - `streamk`: SK_OFF (one CTA per output tile over the whole reduction), SK_DP_SK (grid = DP
+ *    tiles + stream-K CTAs), SK_PERSISTENT (grid = pool; each CTA runs its DP tiles, then its
+ *    stream-K range), or SK_SPLITK (comparator: every tile cut into s = max(1, pool/tiles) equal
+ *    K slices, combined by the same reductions).
+ *  - `reduction`: SK_LINEAR and SK_TREE are deterministic (bit-identical across launches with the
+ *    same plan); SK_ATOMIC needs an fp32 output; SK_WORKSPACE adds into fp32 scratch and runs a
+ *    second (Stage-2) kernel that writes the output.
+ *  - `ctas`: the CTA pool; -1 = default (one CTA per SM for linear/tree; SMs x min(4, CTAs that
+ *    fit on one SM) for atomic/workspace). 0 and values below -1 are rejected with -2.
+ *  - `ws`, `ws_bytes`: workspace of at least sk_workspace_bytes() bytes, 256-byte aligned. With
+ *    ws == NULL the library allocates it on `stream` (cudaMallocAsync) and frees it after the
+ *    launch (cudaFreeAsync). The workspace holds the per-CTA flag table, a control block, and
+ *    the partial tiles (linear/tree) or the fp32 scratch (workspace). The library zeroes the flags,
+ *    the control block and the scratch (and, for SK_ATOMIC, the output) on `stream` before every
+ *    launch; partial tiles are never zeroed.
+ *  - Concurrent calls that share one workspace must be ordered on one stream.
+ *  - Tiles are 128 x 128 (M x N); the reduction step is 64 elements for 16-bit inputs and 128 for
+ *    fp8.
+ */
+#ifndef SKGEMM_H
+#define SKGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { SK_F16 = 0, SK_BF16 = 1, SK_F32 = 2, SK_E4M3 = 3 };                  /* element types */
+enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3 };        /* streamk      */
+enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3 };       /* reduction    */
+enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2 };             /* operation    */
+enum { SK_SEG_FULL = 0, SK_SEG_OWNER = 1, SK_SEG_PEER = 2 };                /* segment kind */
+
+#define SK_OK 0
+#define SK_ERR_LAUNCH (-1)
+#define SK_ERR_UNSUPPORTED (-2)
+
+/* Problem description for the host-only planning calls. Fields not used by `op` are ignored. */
+typedef struct sk_problem {
+    int32_t op;        /* SK_OP_*                                                     */
+    int32_t ab_dtype;  /* input type: SK_F16 / SK_BF16 (GEMM, wgrad), SK_E4M3 (fp8)   */
+    int32_t c_dtype;   /* output type                                                 */
+    int32_t groups;    /* wgrad conv groups (>= 1)                                    */
+    int64_t M, N, K;   /* GEMM / fp8 GEMM: C[M][N] = A[M][K] * B[N][K]^T              */
+    int64_t n, h, w, c, k, r, s;          /* wgrad: x[n][h][w][c], dy[n][ho][wo][k], dw[k][r][s][c/groups] */
+    int32_t stride_h, stride_w, pad_h, pad_w;
+} sk_problem;
+
+/* The resolved partition ("plan"), computed once on the host and passed to the kernel by value.
+ * [P2] commit "Add StreamKIterPartition": the plan is returned by value so that no derived
+ * quantity can be recomputed with different rounding. All fields are int64 for a fixed layout. */
+typedef struct sk_plan_t {
+    int64_t op, mode, reduction;
+    int64_t tm, tn, tk;              /* tile M, tile N, reduction step                        */
+    int64_t gemm_m, gemm_n, kred;    /* GEMM view per group: rows, columns, reduction length  */
+    int64_t groups;
+    int64_t tiles_m, tiles_n;        /* per group                                              */
+    int64_t tiles;                   /* T = groups * tiles_m * tiles_n                         */
+    int64_t iters_per_tile;          /* I = ceil(kred / tk)                                    */
+    int64_t pool;                    /* P (resolved)                                           */
+    int64_t sk_tiles, dp_tiles;      /* SK tiles are ids [0, sk_tiles), DP tiles the rest      */
+    int64_t sk_ctas;                 /* CTAs with a stream-K range (0 = all data-parallel)     */
+    int64_t sk_iters;                /* sk_tiles * I                                            */
+    int64_t iters_per_sk_cta;        /* >= 1, also when sk_ctas == 0                           */
+    int64_t extra_iters;             /* the first extra_iters SK CTAs take one more iteration  */
+    int64_t splits;                  /* SK_SPLITK only: K slices per tile                      */
+    int64_t grid;                    /* CTAs launched                                           */
+    int64_t publishers;              /* CTAs owning a flag (and, linear/tree, a partial slot)  */
+    int64_t max_contributors;        /* most CTAs sharing one tile                              */
+    int64_t tree_rounds;             /* ceil(log2(max_contributors))                            */
+    int64_t shared_tiles;            /* tiles with more than one contributor                   */
+    int64_t flag_bytes;              /* round_up(4 * publishers, 256)                           */
+    int64_t control_offset;          /* = flag_bytes; 256-byte control block (ticket counter)  */
+    int64_t partial_offset, partial_bytes;   /* linear/tree: publishers * tm * tn * 4          */
+    int64_t scratch_offset, scratch_bytes;   /* workspace: (SK tiles) * tm * tn * 4            */
+    int64_t ws_bytes;                /* total workspace bytes                                   */
+} sk_plan_t;
+
+/* One piece of a CTA's work: iterations [k_begin, k_end) of tile `tile`. */
+typedef struct sk_segment_t {
+    int64_t tile;
+    int64_t k_begin, k_end;
+    int64_t kind;          /* SK_SEG_FULL: sole writer; SK_SEG_OWNER: first of several; SK_SEG_PEER */
+    int64_t index;         /* position among the tile's contributors (0 = owner)                    */
+    int64_t n_contrib;     /* contributors of the tile (1 for SK_SEG_FULL)                          */
+    int64_t first_cta;     /* logical id of the tile's owner (-1 for SK_SEG_FULL)                   */
+} sk_segment_t;
+
+/*
+ * C[M][N] = A[M][K] * B[N][K]^T ("rcr": A row-major, B column-major K x N, C row-major) with
+ * fp32 accumulation. [P1] Summary (fp16/rcr stream-K GEMM) and [P2] Technical Details.
+ *   ab_dtype: SK_F16 or SK_BF16. c_dtype: the same 16-bit type, or SK_F32.
+ *   lda, ldb: row strides in elements of A and B (>= K; lda*2 and ldb*2 multiples of 16 bytes;
+ *   K a multiple of 8). ldc: row stride of C in elements (>= N, 16-byte aligned rows).
+ *   SK_ATOMIC requires c_dtype == SK_F32.
+ */
+int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K,
+                const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                int streamk, int reduction, int ctas, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * C[m][n] = bf16( (sum_k e4m3(A8[m][k]) * e4m3(B8[n][k])) * sa[m] * sb[n] ). [P3] Scope: fp8
+ * rcr, per-row A scale and per-column B scale (one scale each, no quant groups), fp32
+ * accumulator narrowed only in the epilogue. A8: [M][K] row-major OCP E4M3 bytes (K a multiple
+ * of 16); B8: [N][K]; sa: M floats; sb: N floats; C_bf16: [M][ldc]. SK_ATOMIC is rejected (the
+ * output is 16-bit).
+ */
+int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                       const float* sa, const float* sb, void* C_bf16, int64_t ldc,
+                       int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Backward-weight 2-D convolution as an implicit GEMM. [P2] PR body "Wgrad kernel" and commit
+ * "Port CK Tile's stream-K to the backward-weight convolution": the output is filter-sized, the
+ * reduction runs over N*Ho*Wo, and conv groups fold into GEMM-M per group.
+ *   dw[g*Kg+k][r][s][c] = sum_{n,ho,wo} dy[n][ho][wo][g*Kg+k] * x[n][ho*sh-ph+r][wo*sw-pw+s][g*Cg+c]
+ *   x: [N][H][W][C] (NHWC), dy: [N][Ho][Wo][K], dw: [K][R][S][C/groups] dense,
+ *   Ho = (H + 2*pad_h - R)/stride_h + 1, Wo likewise; x outside the image reads as zero.
+ *   in_dtype: SK_F16 or SK_BF16; dw_dtype: SK_F32 or in_dtype.
+ *   Supported: (C/groups) a multiple of 64, K a multiple of 8, dilation 1, R, S <= 16, padding
+ *   < filter size.
+ */
+int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* x, const void* dy, void* dw,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Workspace bytes the call described by `p` needs (device query for ctas == -1). 0 / -2. */
+int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out);
+
+/*
+ * Host-only: resolve the partition for problem `p`. `num_sms` > 0 gives the SM count used for
+ * ctas == -1 (num_sms <= 0 queries the current device). Does not touch the GPU otherwise.
+ * Returns 0, or -2 (message in sk_last_error()).
+ */
+int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_sms,
+            sk_plan_t* out);
+
+/* Host-only: the work of logical CTA `cta` under `plan`, in execution order (the same walk the
+ * kernel makes). Writes up to max_out segments, the total count to *n_out. 0 / -2. */
+int sk_plan_cta_work(const sk_plan_t* plan, int64_t cta, sk_segment_t* out, int max_out,
+                     int* n_out);
+
+/* Host-only: default CTA pool for `reduction` given the SM count and the CTAs of the kernel that
+ * fit on one SM. [P2] commit "Resolve streamk_ctas=-1 from the reduction". 0 / -2. */
+int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out);
+
+/* Synchronise `stream`, then report whether a bounded wait in a kernel gave up since the last
+ * call: 0 = no, -1 = yes (details in sk_last_error()); clears the record. */
+int sk_device_status(void* stream);
+
+/* Reason for the last -1 / -2 returned on this thread (never NULL). */
+const char* sk_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int sk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKGEMM_H */

@@ -227,7 +227,10 @@ def _sk_segments(p: Plan, c: int) -> List[Segment]:
             kind = SEG_OWNER
         else:
             kind = SEG_PEER
-        out.append(Segment(t, it - t * p.I, stop - t * p.I, kind, c - cs[0], len(cs), cs[0]))
+        if kind == SEG_FULL:   # sole contributor: no hand-off partners
+            out.append(Segment(t, it - t * p.I, stop - t * p.I, kind, 0, 1, -1))
+        else:
+            out.append(Segment(t, it - t * p.I, stop - t * p.I, kind, c - cs[0], len(cs), cs[0]))
         it = stop
     return out
 

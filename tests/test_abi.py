@@ -1,0 +1,127 @@
+"""The C ABI library: it loads without a GPU, exports every call include/skgemm.h declares, and its
+argument gates return -2 (with a reason) before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import implicit_gemm_conv_gb300 as sk
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "skgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(sk_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = sk.library()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(sk.EXPORTS)
+
+
+def test_version_and_error_string():
+    assert sk.sk_version() >= 100
+    assert isinstance(sk.last_error(), str)
+
+
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: every call below stops at a gate
+
+
+def _gemm(**kw):
+    a = dict(ab=sk.F16, c=sk.F16, M=256, N=256, K=4096, A=FAKE, lda=4096, B=FAKE, ldb=4096,
+             C=FAKE, ldc=256, mode=sk.PERSISTENT, red=sk.LINEAR, ctas=3)
+    a.update(kw)
+    lib = sk.library()
+    rc = lib.sk_gemm_rcr(a["ab"], a["c"], a["M"], a["N"], a["K"], a["A"], a["lda"], a["B"],
+                         a["ldb"], a["C"], a["ldc"], a["mode"], a["red"], a["ctas"], None, 0, None)
+    return rc, sk.last_error()
+
+
+@pytest.mark.parametrize("kw,reason", [
+    (dict(red=sk.ATOMIC), "atomic"),                         # atomic needs an fp32 output
+    (dict(ctas=0), "streamk_ctas"),
+    (dict(ctas=-2), "streamk_ctas"),
+    (dict(mode=7), "mode"),
+    (dict(red=9), "reduction"),
+    (dict(ab=sk.F32), "f16 or bf16"),
+    (dict(c=sk.BF16), "output"),
+    (dict(K=4100, lda=4100, ldb=4100), "multiple of 8"),
+    (dict(lda=4099), "16 bytes"),
+    (dict(ldc=100), "leading dimension"),
+    (dict(A=FAKE + 2), "aligned"),
+    (dict(C=0), "NULL"),
+    (dict(M=-1), "negative"),
+])
+def test_gemm_rejections(kw, reason):
+    rc, msg = _gemm(**kw)
+    assert rc == -2
+    assert reason in msg, msg
+
+
+def test_empty_problem_is_a_noop():
+    rc, _ = _gemm(M=0)
+    assert rc == 0
+    rc, _ = _gemm(N=0, C=0)
+    assert rc == 0
+
+
+def test_valid_call_without_a_gpu_is_refused_not_computed():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, msg = _gemm()
+    assert rc == -2 and msg   # no device: nothing computed on the CPU
+
+
+def _wgrad(**kw):
+    a = dict(i=sk.F16, o=sk.F32, N=32, H=56, W=56, C=64, K=64, R=3, S=3, sh=1, sw=1, ph=1, pw=1,
+             g=1, mode=sk.DP_SK, red=sk.LINEAR, ctas=-1)
+    a.update(kw)
+    lib = sk.library()
+    rc = lib.sk_conv2d_wgrad_nhwc(a["i"], a["o"], a["N"], a["H"], a["W"], a["C"], a["K"], a["R"],
+                                  a["S"], a["sh"], a["sw"], a["ph"], a["pw"], a["g"], FAKE, FAKE,
+                                  FAKE, a["mode"], a["red"], a["ctas"], None, 0, None)
+    return rc, sk.last_error()
+
+
+@pytest.mark.parametrize("kw,reason", [
+    (dict(g=3), "groups"),
+    (dict(C=96, K=96), "multiple of 64"),
+    (dict(K=60), "multiple of 8"),
+    (dict(ph=3), "padding"),
+    (dict(sh=0), "stride"),
+    (dict(R=17, S=3), "16"),
+    (dict(o=sk.F16, red=sk.ATOMIC), "atomic"),
+    (dict(o=sk.BF16), "dW"),
+    (dict(H=1, W=1, ph=0, pw=0), "larger than"),
+])
+def test_wgrad_rejections(kw, reason):
+    rc, msg = _wgrad(**kw)
+    assert rc == -2
+    assert reason in msg, msg
+
+
+def test_fp8_rejections():
+    lib = sk.library()
+    rc = lib.sk_gemm_rowcol_fp8(64, 64, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 64, sk.DP_SK, sk.ATOMIC,
+                                -1, None, 0, None)
+    assert rc == -2 and "atomic" in sk.last_error()
+    rc = lib.sk_gemm_rowcol_fp8(64, 64, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 64, sk.DP_SK, sk.LINEAR,
+                                -1, None, 0, None)
+    assert rc == -2 and "multiple of 16" in sk.last_error()
+
+
+def test_default_pool():
+    assert sk.sk_default_pool("linear", 148, 1) == 148
+    assert sk.sk_default_pool("tree", 148, 2) == 148
+    assert sk.sk_default_pool("workspace", 148, 1) == 148
+    assert sk.sk_default_pool("atomic", 148, 2) == 296
+    assert sk.sk_default_pool("atomic", 304, 8) == 1216
+    with pytest.raises(sk.SkError):
+        sk.sk_default_pool("linear", 0, 1)

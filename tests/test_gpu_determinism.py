@@ -1,0 +1,53 @@
+"""linear and tree are bit-identical across 20 launches with the workspace (flags, control block,
+partial tiles) and the output poisoned with 0xFF bytes before every launch: a missing release or
+acquire on the partial hand-off would let an owner read poison (NaN) or a stale partial."""
+import pytest
+import torch
+
+from workloads import gemm_operands, wgrad_operands
+
+pytestmark = pytest.mark.gpu
+
+import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library must fail)
+from gpu_helpers import DEV, poisoned  # noqa: E402
+
+
+def _repeat(launch, out, ws, n=20):
+    first = None
+    for _ in range(n):
+        ws.fill_(0xFF)
+        out.view(torch.uint8).fill_(0xFF)
+        launch()
+        sk.sk_device_status()
+        b = out.view(torch.uint8).clone()
+        assert torch.isfinite(out.float()).all()
+        if first is None:
+            first = b
+        else:
+            assert torch.equal(first, b), "result changed between launches"
+
+
+@pytest.mark.parametrize("red", ["linear", "tree"])
+@pytest.mark.parametrize("mode,shape,ctas", [("persistent", (256, 256, 4096), 3),
+                                             ("dp_sk", (3840, 4096, 4096), 148),
+                                             ("dp_sk", (512, 512, 65536), 148)])
+def test_gemm_bit_identical(mode, shape, ctas, red):
+    M, N, K = shape
+    A, B = gemm_operands(M, N, K, "bf16", "n01")
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = poisoned((M, N), torch.bfloat16)
+    prob = sk.make_problem("gemm", ab_dtype="bf16", c_dtype="bf16", M=M, N=N, K=K)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, mode, red, ctas), dtype=torch.uint8, device=DEV)
+    _repeat(lambda: sk.sk_gemm_rcr(Ad, Bd, C, streamk=mode, reduction=red, ctas=ctas, ws=ws), C, ws)
+
+
+@pytest.mark.parametrize("red", ["linear", "tree"])
+def test_wgrad_bit_identical(red):
+    x, dy = wgrad_operands(32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), "f16", "u11")
+    xd, dyd = x.to(DEV), dy.to(DEV)
+    dw = poisoned((64, 3, 3, 64), torch.float32)
+    prob = sk.make_problem("wgrad", ab_dtype="f16", c_dtype="f32", n=32, h=56, w=56, c=64, k=64,
+                           r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", red, -1), dtype=torch.uint8, device=DEV)
+    _repeat(lambda: sk.sk_conv2d_wgrad_nhwc(xd, dyd, dw, 3, 3, (1, 1), (1, 1), 1, streamk="dp_sk",
+                                            reduction=red, ctas=-1, ws=ws), dw, ws)

@@ -1,0 +1,51 @@
+"""GPU parity of the fp8 e4m3 row/col-scaled GEMM (sk_gemm_rowcol_fp8 through the C ABI) against
+the oracle, which decodes the same e4m3 bytes (quantise -> dequantise) and applies the scales."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import numerics
+from workloads import fp8_operands
+
+pytestmark = pytest.mark.gpu
+
+import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library must fail)
+from gpu_helpers import DEV, bits, check_parity, poisoned, sample_points  # noqa: E402
+
+
+def run(A, B, sa, sb, mode, red, ctas):
+    M, N = A.shape[0], B.shape[0]
+    C = poisoned((M, N), torch.bfloat16)
+    sk.sk_gemm_rowcol_fp8(A.to(DEV), B.to(DEV), sa.to(DEV), sb.to(DEV), C, streamk=mode,
+                          reduction=red, ctas=ctas)
+    sk.sk_device_status()
+    return C
+
+
+@pytest.mark.parametrize("red", ["linear", "tree", "workspace"])
+@pytest.mark.parametrize("mode", ["off", "dp_sk", "persistent", "splitk"])
+def test_fp8_small(mode, red):
+    M, N, K = 200, 136, 1040
+    A, B, sa, sb = fp8_operands(M, N, K, seed_offset=2)
+    ref = numerics.fp8_rowcol_rows(bits(A), bits(B), sa.numpy(), sb.numpy())
+    C = run(A, B, sa, sb, mode, red, 5)
+    check_parity(C, ref, "bf16", K, kind="fp8", what=f"{mode}/{red}")
+
+
+def test_fp8_atomic_rejected():
+    A, B, sa, sb = fp8_operands(128, 128, 128)
+    with pytest.raises(sk.SkError) as e:
+        run(A, B, sa, sb, "dp_sk", "atomic", -1)
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("red", ["linear", "workspace"])
+def test_fp8_8192_sampled(red):
+    M = N = K = 8192
+    A, B, sa, sb = fp8_operands(M, N, K)
+    C = run(A, B, sa, sb, "dp_sk", red, -1)
+    ms, ns = sample_points(M, N, n_random=4096)
+    ref = numerics.fp8_rowcol_points(bits(A), bits(B), sa.numpy(), sb.numpy(), ms, ns)
+    out = C[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)]
+    check_parity(out, ref, "bf16", K, kind="fp8", what=f"8192^3 {red}")
+    assert torch.isfinite(C.float()).all()

@@ -1,0 +1,122 @@
+"""The CUDA path's host planner (sk_plan / sk_plan_cta_work in libskgemm) against the oracle's
+partition replica: every scalar field and every CTA's segment list must match bit for bit."""
+import itertools
+import random
+
+import pytest
+
+import implicit_gemm_conv_gb300 as sk
+from oracle import partition as P
+
+MODES = [("off", P.OFF), ("dp_sk", P.DP_SK), ("persistent", P.PERSISTENT), ("splitk", P.SPLITK)]
+REDS = [("linear", P.LINEAR), ("tree", P.TREE), ("atomic", P.ATOMIC), ("workspace", P.WORKSPACE)]
+
+FIELD_MAP = {  # C name -> oracle name
+    "tiles": "T", "iters_per_tile": "I", "pool": "P", "sk_tiles": "sk_tiles",
+    "dp_tiles": "dp_tiles", "sk_ctas": "sk_ctas", "sk_iters": "sk_iters",
+    "iters_per_sk_cta": "iters_per_sk_cta", "extra_iters": "extra", "grid": "grid",
+    "publishers": "publishers", "max_contributors": "max_contrib", "tree_rounds": "rounds",
+    "shared_tiles": "shared_tiles", "flag_bytes": "flag_bytes", "partial_bytes": "partial_bytes",
+    "scratch_bytes": "scratch_bytes", "ws_bytes": "ws_bytes", "tiles_m": "tiles_m",
+    "tiles_n": "tiles_n", "groups": "groups",
+}
+
+
+def compare(prob, oracle_kw, mode, red, ctas, num_sms=148, check_ctas=None):
+    cp = sk.sk_plan(prob, mode[0], red[0], ctas, num_sms)
+    pool = ctas if ctas > 0 else P.default_pool(red[1], num_sms, 1)
+    op = P.make_plan(pool=pool, mode=mode[1], reduction=red[1], **oracle_kw)
+    for c, o in FIELD_MAP.items():
+        assert getattr(cp, c) == getattr(op, o), (c, getattr(cp, c), getattr(op, o))
+    if mode[1] == P.SPLITK:
+        assert cp.splits == op.splits
+    ctas_to_check = range(cp.grid) if check_ctas is None else check_ctas(cp.grid)
+    for c in ctas_to_check:
+        got = [(s.tile, s.k_begin, s.k_end, s.kind, s.index, s.n_contrib, s.first_cta)
+               for s in sk.sk_plan_cta_work(cp, c)]
+        exp = [(s.tile, s.k_begin, s.k_end, s.kind, s.index, s.n_contrib, s.first_cta)
+               for s in P.cta_segments(op, c)]
+        assert got == exp, (c, got, exp)
+    return cp
+
+
+def gemm(M, N, K, ab="f16"):
+    tk = 128 if ab == "e4m3" else 64
+    prob = sk.make_problem("fp8" if ab == "e4m3" else "gemm", ab_dtype=ab,
+                           c_dtype="bf16" if ab == "e4m3" else ab, M=M, N=N, K=K)
+    kw = dict(tiles_m=-(-M // 128), tiles_n=-(-N // 128), groups=1, kred=K, tm=128, tn=128, tk=tk)
+    return prob, kw
+
+
+def wgrad(N, H, W, C, K, R, S, stride, pad, groups):
+    prob = sk.make_problem("wgrad", ab_dtype="bf16", c_dtype="f32", n=N, h=H, w=W, c=C, k=K, r=R,
+                           s=S, stride_h=stride, stride_w=stride, pad_h=pad, pad_w=pad,
+                           groups=groups)
+    Ho = (H + 2 * pad - R) // stride + 1
+    Wo = (W + 2 * pad - S) // stride + 1
+    Kg, Cg = K // groups, C // groups
+    kw = dict(tiles_m=-(-Kg // 128), tiles_n=-(-(R * S * Cg) // 128), groups=groups,
+              kred=N * Ho * Wo, tm=128, tn=128, tk=64)
+    return prob, kw
+
+
+NAMED = [
+    ("gemm 256x256x4096", gemm(256, 256, 4096), 3),
+    ("gemm 3840x4096x4096", gemm(3840, 4096, 4096, "bf16"), 148),
+    ("wgrad 32x56x56x64", wgrad(32, 56, 56, 64, 64, 3, 3, 1, 1, 1), -1),
+    ("wgrad 64x28x28x256 g4 s2", wgrad(64, 28, 28, 256, 256, 3, 3, 2, 1, 4), -1),
+    ("fp8 8192^3", gemm(8192, 8192, 8192, "e4m3"), -1),
+    ("gemm 512x512x65536", gemm(512, 512, 65536, "bf16"), 148),
+]
+
+
+@pytest.mark.parametrize("name,pk,ctas", NAMED, ids=[n[0] for n in NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_named_workloads(name, pk, ctas, mode, red):
+    prob, kw = pk
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    compare(prob, kw, mode, red, ctas, check_ctas=big)
+
+
+def test_worked_vector_values_through_c():
+    cp = sk.sk_plan(*gemm(3840, 4096, 4096, "bf16")[:1], "dp_sk", "linear", 148, 148)
+    assert (cp.tiles, cp.dp_tiles, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
+            cp.extra_iters, cp.grid) == (960, 888, 72, 4608, 31, 20, 1036)
+    cp = sk.sk_plan(wgrad(64, 28, 28, 256, 256, 3, 3, 2, 1, 4)[0], "dp_sk", "workspace", -1, 148)
+    assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.iters_per_sk_cta, cp.extra_iters) == \
+        (20, 196, 148, 26, 72)
+
+
+def test_random_sweep():
+    rng = random.Random(11)
+    for _ in range(300):
+        M, N = rng.randint(1, 1200), rng.randint(1, 1200)
+        K = 8 * rng.randint(1, 400)
+        mode = rng.choice(MODES)
+        red = rng.choice(REDS)
+        ctas = rng.choice([-1, 1, 2, 3, 5, 7, 31, 148, 300])
+        prob, kw = gemm(M, N, K)
+        compare(prob, kw, mode, red, ctas, num_sms=rng.choice([148, 152, 8]))
+
+
+def test_grouped_wgrad_sweep():
+    for N, H, C, K, R, s, p, g in itertools.product([1, 3], [5, 9], [64, 256], [64, 128],
+                                                    [1, 3], [1, 2], [0, 1], [1, 2]):
+        if C % g or K % g or (C // g) % 64 or p >= R:
+            continue
+        prob, kw = wgrad(N, H, H + 2, C, K, R, R, s, p, g)
+        for mode in MODES:
+            compare(prob, kw, mode, REDS[1], 7)
+
+
+def test_plan_rejections():
+    prob, _ = gemm(256, 256, 4096)
+    for ctas in (0, -5):
+        with pytest.raises(sk.SkError, match="streamk_ctas"):
+            sk.sk_plan(prob, "dp_sk", "linear", ctas, 148)
+    with pytest.raises(sk.SkError, match="mode"):
+        sk.sk_plan(prob, 9, "linear", 3, 148)
+    empty, _ = gemm(0, 256, 4096)
+    with pytest.raises(sk.SkError, match="empty"):
+        sk.sk_plan(empty, "dp_sk", "linear", 3, 148)
