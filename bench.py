@@ -1,0 +1,421 @@
+"""Benchmark of the stream-K GEMM / implicit-GEMM wgrad path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extra]
+
+Prints ONE JSON line (rank 0). The headline workload is the bf16 rcr GEMM 3840x4096x4096 on a
+148-CTA pool (960 tiles of 128x128), dp_sk mode, linear fixup. A step is one sk_gemm_rcr call: the
+flag/control memset and the stream-K kernel (the linear fixup runs inside it). Inputs are resident
+in HBM; L2 is flushed (256 MB write) before every timed step and the flush is outside the timed
+events. `value` = algorithmic FLOP (2*M*N*K per step, all ranks) / summed step time.
+
+Also reported: `roofline` (main kernel alone, timed with events the library records around it),
+`e2e` (same metric with pinned-host inputs copied in and the result copied out inside the timed
+region), `cpu_baseline` (the CPU oracle on a bounded row sample of the same GEMM), `clocks`
+(nvidia-smi sampled during the timed region), and under `extra` the variants the comparison needs
+(DP-only, split-K, tree, persistent) and the other named workloads.
+
+--impl reference times the CPU oracle (fp64, all host cores) as the reference arm on a bounded row
+sample per step of the same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "gemm_bf16_3840x4096x4096_pool148"
+METRIC = "TFLOP/s and % of dense tensor peak, Stream-K GEMM / conv wgrad, 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["implicit_gemm_conv_gb300/csrc/sk_kernels.cu",
+                  "implicit_gemm_conv_gb300/csrc/sk_ptx.cuh",
+                  "implicit_gemm_conv_gb300/csrc/sk_plan.h",
+                  "implicit_gemm_conv_gb300/csrc/sk_kernels.h"]
+PROFILE = os.path.join(ROOT, "profiles", "sk_main_kernel_gemm_bf16_3840x4096x4096.md")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
+    source; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("<!-- ") and ":" in line:
+            k, v = line[5:].rstrip(" ->").split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+
+def gemm_setup(torch, w, dev):
+    from workloads import gemm_operands
+    A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
+    return A, B
+
+
+def time_calls(torch, sk, call, steps, warmup, flush, stream):
+    """Per step: flush L2 (untimed), then time one call with events on `stream`. Returns
+    (summed step ms, summed main-kernel ms, main launches, all launches)."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    sk.sk_timing_enable(True)
+    with torch.cuda.stream(stream):
+        for s, e in evs:
+            flush.zero_()
+            s.record(stream)
+            call()
+            e.record(stream)
+    torch.cuda.synchronize()
+    step_ms = sum(s.elapsed_time(e) for s, e in evs)
+    main_ms, n_main, n_all = sk.sk_timing_read()
+    sk.sk_timing_enable(False)
+    return step_ms, main_ms, n_main, n_all
+
+
+def cpu_baseline_gemm(w, A, B, target_s=15.0):
+    """The fp64 oracle as it stands, all host cores, on a row sample of the GEMM."""
+    import numpy as np
+    from oracle import numerics
+    a = A.view(__import__("torch").int16).numpy().view(np.uint16)
+    b = B.view(__import__("torch").int16).numpy().view(np.uint16)
+    cores = numerics.threads()
+    t0 = time.perf_counter()
+    numerics.gemm_rcr_rows(w.ab, a, b, 0, 2)
+    t1 = time.perf_counter() - t0
+    rows = int(max(2, min(w.M, round(2 * target_s / max(t1, 1e-3)))))
+    t0 = time.perf_counter()
+    numerics.gemm_rcr_rows(w.ab, a, b, 0, rows)
+    dt = time.perf_counter() - t0
+    tflops = 2.0 * rows * w.N * w.K / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} {w.ab} GEMM "
+                      f"({rows}/{w.M} of the work), fp64, {dt:.1f} s"}
+
+
+def extra_measurements(torch, sk, dev, flush, stream, steps):
+    """Variants of the headline and the other named workloads (fewer steps each)."""
+    from workloads import WORKLOADS, fp8_operands, gemm_operands, wgrad_operands
+    out = {}
+    ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def rate(call, flops):
+        step_ms, main_ms, n_main, _ = time_calls(torch, sk, call, steps, 3, flush, stream)
+        return {"tflops": round(flops * steps / step_ms / 1e9, 1),
+                "us": round(step_ms / steps * 1e3, 1),
+                "main_us": round(main_ms / max(n_main, 1) * 1e3, 1)}
+
+    for name, w in WORKLOADS.items():
+        res = {}
+        if w.op == "gemm":
+            A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
+            A, B = A.to(dev), B.to(dev)
+            variants = [(m, r) for m in w.modes for r in w.reductions]
+            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear")]
+            for mode, red in variants:
+                out_dt = torch.float32 if red == "atomic" else A.dtype
+                C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
+                res[f"{mode}/{red}"] = rate(
+                    lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws), w.flops())
+        elif w.op == "wgrad":
+            c = w.conv
+            x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
+                                   c["stride"], c["pad"], w.ab, w.dist)
+            x, dy = x.to(dev), dy.to(dev)
+            dw = torch.empty(c["K"], c["R"], c["S"], c["C"] // c["groups"], dtype=torch.float32,
+                             device=dev)
+            variants = [(m, r) for m in w.modes for r in w.reductions]
+            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "atomic")]
+            for mode, red in variants:
+                res[f"{mode}/{red}"] = rate(
+                    lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
+                                                    c["pad"], c["groups"], mode, red, w.pool,
+                                                    ws=ws), w.flops())
+        else:
+            A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
+            A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
+            C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+            for mode, red in [(m, r) for m in w.modes for r in w.reductions] + \
+                    [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]:
+                res[f"{mode}/{red}"] = rate(
+                    lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool, ws=ws),
+                    w.flops())
+        out[name] = res
+    return out
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import implicit_gemm_conv_gb300 as sk
+    from workloads import WORKLOADS
+
+    w = WORKLOADS[HEADLINE]
+    mode, red = "dp_sk", "linear"
+    peaks, peak_src = measured_peaks()
+    A, B = gemm_setup(torch, w, dev)
+    Ad, Bd = A.to(dev), B.to(dev)
+    C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    prob = sk.make_problem("gemm", ab_dtype=w.ab, c_dtype=w.out, M=w.M, N=w.N, K=w.K)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, mode, red, w.pool), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    call = lambda: sk.sk_gemm_rcr(Ad, Bd, C, mode, red, w.pool, ws=ws)
+
+    # ---- the timed region ----
+    for _ in range(args.warmup):
+        call()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        step_ms, main_ms, n_main, n_all = time_calls(torch, sk, call, args.steps, 0, flush, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    sk.sk_device_status()
+    step_ms = max_over_ranks(torch, world, step_ms, dev)
+    main_ms = max_over_ranks(torch, world, main_ms, dev)
+    flops_step = w.flops()
+    value = flops_step * args.steps * world / (step_ms / 1e3) / 1e12
+    main_avg_s = main_ms / max(n_main, 1) / 1e3
+    achieved = flops_step / main_avg_s / 1e12
+    peak = peaks["bf16_tflops"]
+
+    # ---- end to end: pinned host in, result out, through the public call ----
+    Ah = A.pin_memory()
+    Bh = B.pin_memory()
+    Ch = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(20, args.steps))
+
+    def e2e_call():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        call()
+        Ch.copy_(C, non_blocking=True)
+
+    e2e_ms, _, _, _ = time_calls(torch, sk, e2e_call, e2e_steps, 2, flush, stream)
+    e2e_ms = max_over_ranks(torch, world, e2e_ms, dev)
+    e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(A.numel() * 2 + B.numel() * 2),
+           "d2h_bytes_per_step": int(C.numel() * 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE, "op": "gemm rcr", "M": w.M, "N": w.N, "K": w.K,
+                   "tiles": "960 x (128x128)", "pool": w.pool, "mode": mode, "reduction": red,
+                   "inputs": "bf16 N(0,1), seeds A=1 B=2", "out": "bf16",
+                   "l2": "flushed (256 MB write) before every timed step, outside the events",
+                   "parallelism": f"replicas x{world} (independent problems)"},
+        "pct_of_peak": round(100.0 * value / world / peak, 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(),
+                     "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
+                     "kernel": "sk_main_kernel<gemm16,128>"},
+        "e2e": e2e,
+        "gpu_launches": int(n_all),
+    }
+    if clk.summary() is not None:
+        line["clocks"] = clk.summary()
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_gemm(w, A, B)
+    if rank == 0 and not args.no_extra:
+        line["extra"] = extra_measurements(torch, sk, dev, flush, stream, args.extra_steps)
+    return line
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    import numpy as np
+    import torch
+    from oracle import numerics
+    from workloads import WORKLOADS, gemm_operands
+
+    w = WORKLOADS[HEADLINE]
+    A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
+    a = A.view(torch.int16).numpy().view(np.uint16)
+    b = B.view(torch.int16).numpy().view(np.uint16)
+    cores = numerics.threads()
+    rows = max(1, args.reference_rows)
+    for i in range(args.warmup):
+        numerics.gemm_rcr_rows(w.ab, a, b, 0, 1)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        m0 = (i * rows) % (w.M - rows + 1)
+        numerics.gemm_rcr_rows(w.ab, a, b, m0, m0 + rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    v = flops / dt / 1e12
+    sample = f"{rows} rows of the {w.M}x{w.N}x{w.K} GEMM per step ({rows}/{w.M} of a step's work)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "op": "gemm rcr", "M": w.M, "N": w.N, "K": w.K,
+                   "implementation": "CPU oracle (fp64, OpenMP), bounded row sample per step"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------------------------
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(torch, world, v, dev):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-steps", type=int, default=50)
+    ap.add_argument("--reference-rows", type=int, default=4)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

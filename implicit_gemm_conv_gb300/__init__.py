@@ -79,10 +79,13 @@ _lib.sk_default_pool.argtypes = [_i32, _i32, _i32, ctypes.POINTER(_i32)]
 _lib.sk_device_status.argtypes = [_p]
 _lib.sk_last_error.restype = ctypes.c_char_p
 _lib.sk_version.restype = _i32
+_lib.sk_timing_enable.argtypes = [_i32]
+_lib.sk_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
+                                ctypes.POINTER(_i64)]
 
 EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_workspace_bytes",
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
-           "sk_version"]
+           "sk_version", "sk_timing_enable", "sk_timing_read"]
 
 
 class SkError(RuntimeError):
@@ -231,3 +234,15 @@ def sk_version() -> int:
 
 def sk_last_error() -> str:
     return last_error()
+
+
+def sk_timing_enable(on: bool = True) -> int:
+    return _check(_lib.sk_timing_enable(1 if on else 0))
+
+
+def sk_timing_read():
+    """(summed main-kernel ms, main-kernel launches, all library kernel launches) since the last
+    enable/read; clears the records."""
+    ms, n_main, n_all = ctypes.c_double(0), _i64(0), _i64(0)
+    _check(_lib.sk_timing_read(ctypes.byref(ms), ctypes.byref(n_main), ctypes.byref(n_all)))
+    return ms.value, n_main.value, n_all.value

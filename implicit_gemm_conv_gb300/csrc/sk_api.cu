@@ -15,6 +15,8 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "sk_kernels.h"
 #include "sk_plan.h"
@@ -321,6 +323,39 @@ uint64_t flag_timeout_ns() {
     return static_cast<uint64_t>(ms) * 1000000ull;
 }
 
+// ---- instrumentation ------------------------------------------------------------------------
+
+struct Timing {
+    bool on = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> used, pool;
+    int64_t main_launches = 0, all_launches = 0;
+    ~Timing() {
+        for (auto& p : used) { cudaEventDestroy(p.first); cudaEventDestroy(p.second); }
+        for (auto& p : pool) { cudaEventDestroy(p.first); cudaEventDestroy(p.second); }
+    }
+    void recycle() {
+        pool.insert(pool.end(), used.begin(), used.end());
+        used.clear();
+        main_launches = all_launches = 0;
+    }
+};
+thread_local Timing g_timing;
+
+// Record the start event of one main-kernel launch; returns the pair index or -1.
+int timing_start(cudaStream_t s) {
+    if (!g_timing.on) return -1;
+    std::pair<cudaEvent_t, cudaEvent_t> ev;
+    if (!g_timing.pool.empty()) {
+        ev = g_timing.pool.back();
+        g_timing.pool.pop_back();
+    } else if (cudaEventCreate(&ev.first) != cudaSuccess || cudaEventCreate(&ev.second) != cudaSuccess) {
+        return -1;
+    }
+    cudaEventRecord(ev.first, s);
+    g_timing.used.push_back(ev);
+    return static_cast<int>(g_timing.used.size()) - 1;
+}
+
 // ---- launch sequence ------------------------------------------------------------------------
 
 int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelParams& kp,
@@ -370,8 +405,11 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
+        const int tslot = timing_start(stream);
         int le = sk::launch_main(kp, v.op_kind, 128, stream);
+        if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
+        if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
         if (reduction == SK_WORKSPACE && plan.shared_tiles > 0) {
             sk::Stage2Params s2;
             s2.plan = plan;
@@ -383,6 +421,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.c_dtype = kp.c_dtype;
             le = sk::launch_stage2(s2, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
+            if (g_timing.on) ++g_timing.all_launches;
         }
     } while (false);
     if (own_ws) {
@@ -480,10 +519,11 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
     if (!C || (K > 0 && (!A || !B))) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
     const int cs = dtype_size(c_dtype);
     if (K % 8 != 0) return fail(SK_ERR_UNSUPPORTED, "K must be a multiple of 8 (16-byte rows), got %lld", (long long)K);
-    if (lda < K || ldb < K || ldc < N) return fail(SK_ERR_UNSUPPORTED, "leading dimension smaller than the row");
-    if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldc * cs) % 16)
+    if (ldc < N || (K > 0 && (lda < K || ldb < K)))
+        return fail(SK_ERR_UNSUPPORTED, "leading dimension smaller than the row");
+    if ((ldc * cs) % 16 || (K > 0 && ((lda * 2) % 16 || (ldb * 2) % 16)))
         return fail(SK_ERR_UNSUPPORTED, "lda, ldb and ldc rows must be multiples of 16 bytes");
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))))
         return fail(SK_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned");
     rc = select_device_of(C);
     if (rc) return rc;
@@ -652,6 +692,29 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     kp.conv.Kg = static_cast<int32_t>(Kg);
     return run(prob, streamk, reduction, ctas, kp, dw, RSC * cs, K, RSC * cs, ws, ws_bytes,
                static_cast<cudaStream_t>(stream));
+}
+
+int sk_timing_enable(int on) {
+    g_timing.recycle();
+    g_timing.on = on != 0;
+    return SK_OK;
+}
+
+int sk_timing_read(double* main_ms, int64_t* main_launches, int64_t* all_launches) {
+    double total = 0.0;
+    for (auto& p : g_timing.used) {
+        cudaError_t e = cudaEventSynchronize(p.second);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, p.first, p.second);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        total += ms;
+    }
+    if (main_ms) *main_ms = total;
+    if (main_launches) *main_launches = g_timing.main_launches;
+    if (all_launches) *all_launches = g_timing.all_launches;
+    g_timing.recycle();
+    return SK_OK;
 }
 
 int sk_device_status(void* stream) {

@@ -182,6 +182,17 @@ const char* sk_last_error(void);
 /* Library version: major*10000 + minor*100 + patch. */
 int sk_version(void);
 
+/*
+ * Instrumentation (no counterpart on the pages; used by the benchmark to time the main kernel
+ * alone). sk_timing_enable(1) makes the calling thread's later compute calls record a pair of CUDA
+ * events on their stream around the main stream-K kernel, and count every kernel the library
+ * launches; sk_timing_enable(0) stops recording. Both clear earlier records.
+ * sk_timing_read waits for the recorded events, returns the summed main-kernel time in ms, the
+ * number of main-kernel launches and of all library kernel launches, and clears the records.
+ */
+int sk_timing_enable(int on);
+int sk_timing_read(double* main_ms, int64_t* main_launches, int64_t* all_launches);
+
 #ifdef __cplusplus
 }
 #endif
