@@ -79,13 +79,15 @@ _lib.sk_default_pool.argtypes = [_i32, _i32, _i32, ctypes.POINTER(_i32)]
 _lib.sk_device_status.argtypes = [_p]
 _lib.sk_last_error.restype = ctypes.c_char_p
 _lib.sk_version.restype = _i32
+_lib.sk_gemm_rcr_static_ws.argtypes = [_i32, _i32, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
+                                       _i32, _i32, _i32, _p]
 _lib.sk_timing_enable.argtypes = [_i32]
 _lib.sk_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
                                 ctypes.POINTER(_i64)]
 
 EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_workspace_bytes",
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
-           "sk_version", "sk_timing_enable", "sk_timing_read"]
+           "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws"]
 
 
 class SkError(RuntimeError):
@@ -145,6 +147,21 @@ def sk_gemm_rcr(A, B, C, streamk="dp_sk", reduction="linear", ctas=-1, ws=None, 
                                    A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
                                    C.data_ptr(), C.stride(0), _code(MODES, streamk),
                                    _code(REDUCTIONS, reduction), ctas, wp, wb, _stream_ptr(stream)))
+
+
+def sk_gemm_rcr_static_ws(A, B, C, streamk="dp_sk", reduction="linear", ctas=-1, stream=None):
+    """sk_gemm_rcr using the library's fixed 16 MiB device scratch instead of a workspace: for
+    callers that must not allocate device memory during the call. Calls sharing the scratch must
+    be ordered on one stream."""
+    M, K = A.shape
+    N = B.shape[0]
+    assert B.shape[1] == K and C.shape == (M, N)
+    assert A.stride(1) == 1 and B.stride(1) == 1 and C.stride(1) == 1
+    return _check(_lib.sk_gemm_rcr_static_ws(_torch_dtype_code(A), _torch_dtype_code(C), M, N, K,
+                                             A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                                             C.data_ptr(), C.stride(0), _code(MODES, streamk),
+                                             _code(REDUCTIONS, reduction), ctas,
+                                             _stream_ptr(stream)))
 
 
 def sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, streamk="dp_sk", reduction="linear", ctas=-1, ws=None,

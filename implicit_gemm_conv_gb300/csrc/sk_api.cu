@@ -729,4 +729,59 @@ int sk_device_status(void* stream) {
                 info[1], info[2]);
 }
 
+// ---- fixed-scratch variant (no device allocation) --------------------------------------------
+//
+// Workspace for callers that cannot allocate device memory at call time. The array lives in the
+// library's device image; host code only ever passes its per-device address, looked up below.
+static __device__ __align__(256) unsigned char g_sk_static_ws[SK_STATIC_WS_BYTES];
+
+static std::mutex g_static_ws_mu;
+static void* g_static_ws_ptr[64];
+
+int sk_gemm_rcr_static_ws(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                          int64_t ldc, int streamk, int reduction, int ctas, void* stream) {
+    if (M == 0 || N == 0 || K == 0)   // nothing that needs a workspace
+        return sk_gemm_rcr(ab_dtype, c_dtype, M, N, K, A, lda, B, ldb, C, ldc, streamk, reduction,
+                           ctas, nullptr, 0, stream);
+    if (!C) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    int rc = select_device_of(C);
+    if (rc) return rc;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(SK_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_ws_mu);
+        if (g_static_ws_ptr[dev] == nullptr) {   // once per device, with that device current
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_sk_static_ws);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+            g_static_ws_ptr[dev] = p;
+        }
+        ws = g_static_ws_ptr[dev];
+    }
+    // Size the plan the call will use and refuse it up front if it does not fit.
+    sk_problem prob;
+    memset(&prob, 0, sizeof(prob));
+    prob.op = SK_OP_GEMM;
+    prob.ab_dtype = ab_dtype;
+    prob.c_dtype = c_dtype;
+    prob.M = M;
+    prob.N = N;
+    prob.K = K;
+    prob.groups = 1;
+    sk_plan_t plan;
+    rc = sk_plan(&prob, streamk, reduction, ctas, 0, &plan);
+    if (rc) return rc;
+    if (plan.ws_bytes > static_cast<int64_t>(SK_STATIC_WS_BYTES))
+        return fail(SK_ERR_UNSUPPORTED,
+                    "this problem needs %lld bytes of workspace; the fixed scratch holds %u bytes "
+                    "(use sk_gemm_rcr with a caller workspace, a smaller pool, or atomic)",
+                    (long long)plan.ws_bytes, (unsigned)SK_STATIC_WS_BYTES);
+    return sk_gemm_rcr(ab_dtype, c_dtype, M, N, K, A, lda, B, ldb, C, ldc, streamk, reduction, ctas,
+                       ws, SK_STATIC_WS_BYTES, stream);
+}
+
 }  // extern "C"

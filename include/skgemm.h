@@ -152,6 +152,33 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
                          int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
                          void* stream);
 
+/*
+ * sk_gemm_rcr without any device allocation. (The pages have no counterpart; this call exists
+ * for users of this library.)
+ *
+ * Some callers cannot allocate device memory at call time: code whose GPU memory is owned by
+ * another allocator (a framework's caching allocator or an inference server that reserved the
+ * device and hands out only pre-sized buffers), and latency-bound callers that cannot absorb
+ * the device-wide synchronisation cudaMalloc/cudaFree can cause. This variant takes the same
+ * arguments as sk_gemm_rcr except the workspace: it uses a fixed scratch area compiled into the
+ * library as a static device array of SK_STATIC_WS_BYTES bytes (16 MiB), which every GPU that
+ * loads the library keeps until the process exits. It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *  - The first call on a device looks up that device's copy of the array (cudaGetSymbolAddress,
+ *    which can load the library's GPU module); make that first call before any stream capture.
+ *  - A problem whose plan needs more than SK_STATIC_WS_BYTES of workspace is rejected with -2
+ *    and a message giving both sizes (linear/tree need 64 KiB per stream-K CTA, workspace 64 KiB
+ *    per shared tile; atomic and off need only the 512-byte flag/control header).
+ *  - All calls share the one array and it keeps the previous call's contents: each call clears
+ *    the flags, the control block and the scratch it reads before use, on `stream`. Calls that
+ *    can overlap on the GPU (different streams, or several host threads) race on the array and
+ *    give wrong results; order them on one stream.
+ */
+#define SK_STATIC_WS_BYTES (16u << 20)
+int sk_gemm_rcr_static_ws(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                          int64_t ldc, int streamk, int reduction, int ctas, void* stream);
+
 /* Workspace bytes the call described by `p` needs (device query for ctas == -1). 0 / -2. */
 int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out);
 
