@@ -202,18 +202,22 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
                 "us": round(step_ms / steps * 1e3, 1),
                 "main_us": round(main_ms / max(n_main, 1) * 1e3, 1)}
 
+    def record(res, key, call, flops):
+        res[key] = rate(call, flops)
+
     for name, w in WORKLOADS.items():
         res = {}
         if w.op == "gemm":
             A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
             A, B = A.to(dev), B.to(dev)
             variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear")]
-            for mode, red in variants:
+            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear"),
+                         ("persistent", "linear")]
+            for mode, red in dict.fromkeys(variants):
                 out_dt = torch.float32 if red == "atomic" else A.dtype
                 C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
-                res[f"{mode}/{red}"] = rate(
-                    lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws), w.flops())
+                record(res, f"{mode}/{red}",
+                           lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws), w.flops())
         elif w.op == "wgrad":
             c = w.conv
             x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
@@ -224,21 +228,59 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
             variants = [(m, r) for m in w.modes for r in w.reductions]
             variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "atomic")]
             for mode, red in variants:
-                res[f"{mode}/{red}"] = rate(
-                    lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
-                                                    c["pad"], c["groups"], mode, red, w.pool,
-                                                    ws=ws), w.flops())
+                record(res, f"{mode}/{red}",
+                           lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
+                                                           c["pad"], c["groups"], mode, red,
+                                                           w.pool, ws=ws), w.flops())
         else:
             A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
             A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
             C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
             for mode, red in [(m, r) for m in w.modes for r in w.reductions] + \
                     [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]:
-                res[f"{mode}/{red}"] = rate(
-                    lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool, ws=ws),
-                    w.flops())
+                record(res, f"{mode}/{red}",
+                           lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool,
+                                                         ws=ws), w.flops())
         out[name] = res
     return out
+
+
+def run_variant(args, dev):
+    """--variant WORKLOAD:MODE/REDUCTION: launch only that variant (warm-up + steps), e.g. under
+    ncu; prints its step time."""
+    import torch
+    import implicit_gemm_conv_gb300 as sk
+    from workloads import WORKLOADS, fp8_operands, gemm_operands, wgrad_operands
+    name, mr = args.variant.split(":")
+    mode, red = mr.split("/")
+    w = WORKLOADS[name]
+    ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if w.op == "gemm":
+        A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
+        A, B = A.to(dev), B.to(dev)
+        C = torch.empty(w.M, w.N, dtype=torch.float32 if red == "atomic" else A.dtype, device=dev)
+        call = lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws)
+    elif w.op == "wgrad":
+        c = w.conv
+        x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],
+                               c["pad"], w.ab, w.dist)
+        x, dy = x.to(dev), dy.to(dev)
+        dw = torch.empty(c["K"], c["R"], c["S"], c["C"] // c["groups"], dtype=torch.float32,
+                         device=dev)
+        call = lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"], c["pad"],
+                                               c["groups"], mode, red, w.pool, ws=ws)
+    else:
+        A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
+        A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
+        C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+        call = lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool, ws=ws)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step_ms, main_ms, n_main, n_all = time_calls(torch, sk, call, args.steps, args.warmup, flush,
+                                                 torch.cuda.current_stream())
+    sk.sk_device_status()
+    return {"variant": args.variant, "steps": args.steps, "step_us": step_ms / args.steps * 1e3,
+            "main_us": main_ms / max(n_main, 1) * 1e3, "tflops": w.flops() * args.steps / step_ms / 1e9,
+            "launches": n_all}
 
 
 def run_ours(args, rank, world, dev):
@@ -390,6 +432,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-steps", type=int, default=50)
     ap.add_argument("--reference-rows", type=int, default=4)
+    ap.add_argument("--variant", default=None,
+                    help="WORKLOAD:MODE/REDUCTION - time only this variant (for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -405,6 +449,9 @@ def main():
     import torch
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.variant:
+        print(json.dumps(run_variant(args, dev)), flush=True)
+        return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)

@@ -263,3 +263,4 @@ def sk_timing_read():
     ms, n_main, n_all = ctypes.c_double(0), _i64(0), _i64(0)
     _check(_lib.sk_timing_read(ctypes.byref(ms), ctypes.byref(n_main), ctypes.byref(n_all)))
     return ms.value, n_main.value, n_all.value
+

@@ -201,7 +201,7 @@ int build_plan(const sk_problem& prob, int mode, int reduction, int ctas, int nu
     p.mode = mode;
     p.reduction = reduction;
     p.tm = sk::kTileM;
-    p.tn = 128;
+    p.tn = sk::kTileN;
     p.tk = prob.op == SK_OP_FP8_ROWCOL ? 128 : 64;
     p.gemm_m = v.gemm_m;
     p.gemm_n = v.gemm_n;
@@ -366,7 +366,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
     if (rc) return rc;
     View v;
     problem_view(prob, v);
-    const int per_sm = sk::main_ctas_per_sm(v.op_kind, 128);
+    const int per_sm = sk::main_ctas_per_sm(v.op_kind);
     sk_plan_t plan;
     rc = build_plan(prob, mode, reduction, ctas, dev.sms, per_sm, plan);
     if (rc) return rc;
@@ -395,18 +395,26 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
 
     rc = SK_OK;
     do {
-        e = cudaMemsetAsync(w, 0, static_cast<size_t>(plan.flag_bytes + sk::kControlBytes), stream);
-        if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags)"); break; }
-        if (plan.scratch_bytes > 0) {
-            e = cudaMemsetAsync(w + plan.scratch_offset, 0, static_cast<size_t>(plan.scratch_bytes), stream);
-            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
+        // Flags, control block and (workspace reduction) scratch: one memset when they are
+        // contiguous, i.e. whenever there are no partial slots between them.
+        const int64_t head = plan.flag_bytes + sk::kControlBytes;
+        if (plan.partial_bytes == 0) {
+            e = cudaMemsetAsync(w, 0, static_cast<size_t>(head + plan.scratch_bytes), stream);
+            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags, scratch)"); break; }
+        } else {
+            e = cudaMemsetAsync(w, 0, static_cast<size_t>(head), stream);
+            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags)"); break; }
+            if (plan.scratch_bytes > 0) {
+                e = cudaMemsetAsync(w + plan.scratch_offset, 0, static_cast<size_t>(plan.scratch_bytes), stream);
+                if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
+            }
         }
         if (reduction == SK_ATOMIC && plan.shared_tiles > 0) {
             e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
         const int tslot = timing_start(stream);
-        int le = sk::launch_main(kp, v.op_kind, 128, stream);
+        int le = sk::launch_main(kp, v.op_kind, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -475,7 +483,7 @@ int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_s
         if (rc) return rc;
         num_sms = d.sms;
         View v;
-        if (problem_view(*p, v) == SK_OK) per_sm = sk::main_ctas_per_sm(v.op_kind, 128);
+        if (problem_view(*p, v) == SK_OK) per_sm = sk::main_ctas_per_sm(v.op_kind);
     }
     return build_plan(*p, streamk, reduction, ctas, num_sms, per_sm, *out);
 }
@@ -548,13 +556,13 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
     memset(&kp, 0, sizeof(kp));
     rc = encode_2d(&kp.tmap_a, A, 2, K, M, lda * 2, 64, 128);
     if (rc) return rc;
-    rc = encode_2d(&kp.tmap_b, B, 2, K, N, ldb * 2, 64, 128);
+    rc = encode_2d(&kp.tmap_b, B, 2, K, N, ldb * 2, 64, static_cast<uint32_t>(sk::kTileN));
     if (rc) return rc;
     kp.c = C;
     kp.ldc = ldc;
     kp.c_dtype = c_dtype;
     const uint32_t fmt = ab_dtype == SK_BF16 ? 1u : 0u;
-    kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, 128);
+    kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, static_cast<uint32_t>(sk::kTileN));
     return run(prob, streamk, reduction, ctas, kp, C, ldc * cs, M, N * cs, ws, ws_bytes, st);
 }
 
@@ -587,14 +595,14 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
     memset(&kp, 0, sizeof(kp));
     rc = encode_2d(&kp.tmap_a, A8, 1, K, M, K, 128, 128);
     if (rc) return rc;
-    rc = encode_2d(&kp.tmap_b, B8, 1, K, N, K, 128, 128);
+    rc = encode_2d(&kp.tmap_b, B8, 1, K, N, K, 128, static_cast<uint32_t>(sk::kTileN));
     if (rc) return rc;
     kp.c = C_bf16;
     kp.ldc = ldc;
     kp.c_dtype = SK_BF16;
     kp.sa = sa;
     kp.sb = sb;
-    kp.idesc = sk::make_idesc(0, 0, false, false, 128, 128);
+    kp.idesc = sk::make_idesc(0, 0, false, false, 128, static_cast<uint32_t>(sk::kTileN));
     return run(prob, streamk, reduction, ctas, kp, C_bf16, ldc * 2, M, N * 2, ws, ws_bytes,
                static_cast<cudaStream_t>(stream));
 }
@@ -679,7 +687,7 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     kp.ldc = RSC;
     kp.c_dtype = dw_dtype;
     const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
-    kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, 128);
+    kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, static_cast<uint32_t>(sk::kTileN));
     kp.conv.HoWo = Ho * Wo;
     kp.conv.Wo = static_cast<int32_t>(Wo);
     kp.conv.sh = stride_h;

@@ -35,6 +35,7 @@ __device__ unsigned long long g_sk_error[4];   // code, cta, tile, detail (first
 enum : unsigned long long {
     kErrFlagWait = 1,   // a linear/tree receive gave up waiting for a flag
     kErrPipeline = 2,   // an mbarrier wait inside the CTA gave up
+    kErrBounds = 3,     // a self-check found an index outside its buffer (access skipped)
 };
 
 __device__ __noinline__ void record_error(unsigned long long code, long long cta, long long tile,
@@ -57,11 +58,18 @@ struct Cfg {
     static constexpr int kABytes = kTileM * 128;           // 16 KB
     static constexpr int kBBytes = TN * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = TN == 128 ? 6 : 4;
+    static constexpr int kStages = 6;
     static constexpr int kTmemCols = 2 * TN;               // double-buffered fp32 accumulator
     static constexpr int kMmaK = OP == kOpFp8 ? 32 : 16;
     static constexpr int kMmasPerStage = TK / kMmaK;
-    static constexpr int kBarBytes = (2 * kStages + 4) * 8;
+    // The owner's fold stages partial tiles through the (then idle) operand ring in 64 KB units
+    // (128 rows x 128 fp32 columns, contiguous in the fragment-major layout).
+    static constexpr int kFoldUnitChunks = 4;                       // 32-column chunks per unit
+    static constexpr int kFoldUnitBytes = kTileM * 32 * 4 * kFoldUnitChunks;
+    static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
+    static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
+    static_assert((TN / 32) % kFoldUnitChunks == 0, "tile N must be a multiple of 128");
+    static constexpr int kBarBytes = (2 * kStages + 4 + kFoldBufs) * 8;
     static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes + 64;
 };
 
@@ -114,6 +122,18 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
     }
 }
 
+// Start offset of a segment's iteration order: rotated for stream-K segments (see
+// sk_segment_rotation), natural order for data-parallel tiles and the off / split-K modes. Advances
+// `tau`, the stream-K iterations this CTA has run.
+__device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool dp,
+                                                    const sk_segment_t& seg, int64_t& tau) {
+    if (dp || (plan.mode != SK_DP_SK && plan.mode != SK_PERSISTENT)) return 0;
+    const int64_t len = seg.k_end - seg.k_begin;
+    const int64_t rot = sk_segment_rotation(plan.iters_per_sk_cta, seg.k_begin, len, tau);
+    tau += len;
+    return rot;
+}
+
 template <int OP, int TN>
 __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              volatile SmemCtl* ctl) {
@@ -123,12 +143,18 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
     seg_init(plan, cta, cur);
     sk_segment_t seg;
     uint32_t stage = 0, phase = 0;
-    int64_t issued = 0;
+    int64_t issued = 0, tau = 0;
     bool ok = true;
-    while (ok && seg_next(plan, cta, cur, seg)) {
+    while (true) {
+        const bool dp = cur.dp_next >= 0;
+        if (!ok || !seg_next(plan, cta, cur, seg)) break;
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
-        for (int64_t k = seg.k_begin; k < seg.k_end; ++k) {
+        const int64_t len = seg.k_end - seg.k_begin;
+        const int64_t rot = segment_rotation(plan, dp, seg, tau);
+        for (int64_t j = 0; j < len; ++j) {
+            int64_t k = seg.k_begin + rot + j;
+            if (k >= seg.k_end) k -= len;
             const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
             if (!mbar_wait(empty, phase ^ 1, P.mbar_timeout_ns) || ctl->abort) {
                 record_error(kErrPipeline, cta, seg.tile, 0);
@@ -175,7 +201,11 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
     int64_t nseg = 0;
     uint32_t last_empty = 0, last_parity = 0;
     bool any = false, ok = true;
-    while (ok && seg_next(plan, cta, cur, seg)) {
+    while (true) {
+        const bool dp = cur.dp_next >= 0;
+        if (!ok || !seg_next(plan, cta, cur, seg)) break;
+        (void)dp;
+        const int64_t len = seg.k_end - seg.k_begin;
         const uint32_t acc = static_cast<uint32_t>(nseg & 1);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg >> 1) & 1);
         const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
@@ -187,7 +217,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TN;
-        for (int64_t k = seg.k_begin; k < seg.k_end; ++k) {
+        for (int64_t j = 0; j < len; ++j) {
             const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
             if (!mbar_wait(full, phase, P.mbar_timeout_ns) || ctl->abort) {
                 record_error(kErrPipeline, cta, seg.tile, 2);
@@ -210,7 +240,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
                     ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
                     bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
                 }
-                const uint32_t accumulate = (k > seg.k_begin || kk > 0) ? 1u : 0u;
+                const uint32_t accumulate = (j > 0 || kk > 0) ? 1u : 0u;
                 if constexpr (OP == kOpFp8)
                     mma_f8(d_tmem, ad, bd, P.idesc, accumulate);
                 else
@@ -328,9 +358,80 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = as_f(r[i]);
 }
 
+// Owner's fold of its senders' partial tiles (linear, or the last tree round), staged through the
+// operand ring with bulk copies of 64 KB units, kFoldBufs of them in flight; the running sum stays
+// in the owner's TMEM accumulator. Per element the additions run in sender order, so the result
+// does not depend on timing. Only the owner segment, always a CTA's last, takes this path: by then
+// every stage of the ring has been consumed.
+template <int OP, int TN, typename SenderFn>
+__device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
+                            const EpiCtx& e, uint32_t t_acc, int ethread, int64_t ns,
+                            SenderFn sender, uint32_t ring, uint32_t fold_bars) {
+    using C = Cfg<OP, TN>;
+    constexpr int kChunks = TN / 32;
+    constexpr int kUnitsPerSender = kChunks / C::kFoldUnitChunks;
+    const int64_t units = ns * kUnitsPerSender;   // sender-major
+    auto issue = [&](int64_t u) {
+        const int64_t i = u / kUnitsPerSender, h = u - i * kUnitsPerSender;
+        const int64_t slot = seg.first_cta + sender(i);
+        const uint32_t buf = static_cast<uint32_t>(u % C::kFoldBufs);
+        const uint32_t bar = fold_bars + buf * 8;
+        if (slot < 0 || slot >= P.plan.publishers) {   // never expected: record and skip
+            record_error(kErrBounds, cta, seg.tile, slot);
+            return;
+        }
+        const float* src = P.partials + slot * static_cast<int64_t>(kTileM * TN) +
+                           h * (kTileM * 32 * C::kFoldUnitChunks);
+        mbar_arrive_expect_tx(bar, C::kFoldUnitBytes);
+        bulk_copy_g2s(ring + buf * C::kFoldUnitBytes, src, C::kFoldUnitBytes, bar);
+    };
+    if (ethread == 0) {
+        fence_proxy_async_global();   // the acquired partials are read by the async proxy
+        for (int64_t u = 0; u < units && u < C::kFoldBufs; ++u) issue(u);
+    }
+    const uint8_t* ring_ptr = nullptr;
+    asm volatile("cvta.shared.u64 %0, %1;" : "=l"(ring_ptr) : "l"(static_cast<uint64_t>(ring)));
+    bool ok = true;
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t h = u % kUnitsPerSender;
+        const uint32_t buf = static_cast<uint32_t>(u % C::kFoldBufs);
+        const uint32_t parity = static_cast<uint32_t>((u / C::kFoldBufs) & 1);
+        if (ok && !mbar_wait(fold_bars + buf * 8, parity, P.mbar_timeout_ns)) {
+            record_error(kErrPipeline, cta, seg.tile, 4);
+            ok = false;
+        }
+        const float4* src = reinterpret_cast<const float4*>(ring_ptr + buf * C::kFoldUnitBytes);
+#pragma unroll 1
+        for (int c = 0; c < C::kFoldUnitChunks; ++c) {
+            const int ch = static_cast<int>(h) * C::kFoldUnitChunks + c;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_acc + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = src[(c * 8 + q) * kTileM + e.row];
+                r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + x.x);
+                r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + x.y);
+                r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + x.z);
+                r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + x.w);
+            }
+            tmem_st_32x32b_x32(t_acc + ch * 32, r);
+        }
+        tmem_st_wait();
+        named_bar_sync(kEpiBarrier, kEpiThreads);   // buffer `buf` may be refilled
+        if (ethread == 0 && ok && u + C::kFoldBufs < units) issue(u + C::kFoldBufs);
+    }
+    for (int ch = 0; ch < kChunks; ++ch) {
+        float v[32];
+        load_acc(t_acc + ch * 32, v);
+        store_out<OP>(P, e, ch * 32, v);
+    }
+}
+
 template <int OP, int TN>
 __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
-                                 const EpiCtx& e, uint32_t t_acc, int ethread) {
+                                 const EpiCtx& e, uint32_t t_acc, int ethread, uint32_t ring,
+                                 uint32_t fold_bars) {
     const sk_plan_t& plan = P.plan;
     constexpr int kChunks = TN / 32;
     const int red = static_cast<int>(plan.reduction);
@@ -411,7 +512,16 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     named_bar_sync(kEpiBarrier, kEpiThreads);
     if (ns > 0) (void)ld_acquire_gpu(P.flags + seg.first_cta + sender(ns - 1));
 
-    const bool publish = seg.kind == SK_SEG_PEER;
+    if (seg.kind == SK_SEG_OWNER && ns > 0) {
+        staged_fold<OP, TN>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
+        return;
+    }
+
+    bool publish = seg.kind == SK_SEG_PEER;
+    if (publish && cta >= plan.publishers) {   // never expected: record and skip the stores
+        if (ethread == 0) record_error(kErrBounds, cta, seg.tile, -2);
+        publish = false;
+    }
     float* own = P.partials + cta * static_cast<int64_t>(kTileM * TN);
     for (int ch = 0; ch < kChunks; ++ch) {
         float v[32];
@@ -439,6 +549,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         }
     }
     if (publish) {
+        fence_proxy_async_global();   // a receiver may read this partial with bulk copies
         __threadfence();
         named_bar_sync(kEpiBarrier, kEpiThreads);
         if (ethread == 0) st_release_gpu(P.flags + cta, 1u);
@@ -446,7 +557,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
 }
 
 template <int OP, int TN>
-__device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t bars,
+__device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              uint32_t tmem_base, int warp, volatile SmemCtl* ctl) {
     using C = Cfg<OP, TN>;
     const sk_plan_t& plan = P.plan;
@@ -488,7 +599,8 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t bars,
         e.row_scale = 1.0f;
         if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
-        epilogue_segment<OP, TN>(P, cta, seg, e, t_acc, ethread);
+        epilogue_segment<OP, TN>(P, cta, seg, e, t_acc, ethread, ring,
+                                 bars + (2 * C::kStages + 4) * 8);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty);
@@ -521,6 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
             mbar_init(bars + (2 * C::kStages + a) * 8, 1);              // accumulator full
             mbar_init(bars + (2 * C::kStages + 2 + a) * 8, kEpiThreads / 32);  // accumulator empty
         }
+        for (int f = 0; f < C::kFoldBufs; ++f)
+            mbar_init(bars + (2 * C::kStages + 4 + f) * 8, 1);   // owner's fold buffers
         fence_mbarrier_init();
         ctl->abort = 0;
         ctl->cta = static_cast<long long>(atomicAdd(P.control, 1u));
@@ -536,6 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int64_t cta = ctl->cta;
+    if (threadIdx.x == 0 && ((tmem_base & 0xFFFFu) + C::kTmemCols > 512u || (tmem_base >> 16) != 0))
+        record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
 
     if (warp == 0) {
         if (elect_one()) run_producer<OP, TN>(P, cta, ring, bars, ctl);
@@ -544,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
         if (elect_one()) run_mma<OP, TN>(P, cta, ring, bars, tmem_base, ctl);
         __syncwarp();
     } else {
-        run_epilogue<OP, TN>(P, cta, bars, tmem_base, warp, ctl);
+        run_epilogue<OP, TN>(P, cta, ring, bars, tmem_base, warp, ctl);
     }
 
     tc_fence_before();
@@ -559,8 +675,12 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
 // Stage-2: fp32 scratch of the shared tiles -> output (scaled for fp8)
 // ---------------------------------------------------------------------------------------------
 
+constexpr int kStage2Threads = 256;
+
+// Grid (shared-tile candidates, tile float4s / 256): one float4 of fp32 scratch per thread, read in
+// the fragment-major order the fixup wrote it.
 template <int TN>
-__global__ void __launch_bounds__(256) sk_stage2_kernel(const __grid_constant__ Stage2Params P) {
+__global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_constant__ Stage2Params P) {
     const sk_plan_t& plan = P.plan;
     const int64_t t = blockIdx.x;
     int64_t first, n;
@@ -568,28 +688,46 @@ __global__ void __launch_bounds__(256) sk_stage2_kernel(const __grid_constant__ 
     if (n <= 1) return;   // written directly by its only contributor
     int64_t g, mt, nt;
     tile_coords(plan, t, g, mt, nt);
+    const int idx = static_cast<int>(blockIdx.y) * kStage2Threads + static_cast<int>(threadIdx.x);
+    const int q4 = idx / kTileM, row = idx - q4 * kTileM;
+    const int64_t m = mt * kTileM + row;
+    const int64_t n0 = nt * TN + q4 * 4;
+    if (m >= plan.gemm_m || n0 >= plan.gemm_n) return;
     const float* base = P.scratch + t * static_cast<int64_t>(kTileM * TN);
-    for (int idx = threadIdx.x; idx < kTileM * TN / 4; idx += blockDim.x) {
-        const int q4 = idx / kTileM, row = idx - q4 * kTileM;
-        const int64_t m = mt * kTileM + row;
-        if (m >= plan.gemm_m) continue;
-        const int64_t n0 = nt * TN + q4 * 4;
-        if (n0 >= plan.gemm_n) continue;
-        const float4 q = *reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4);
-        float v[4] = {q.x, q.y, q.z, q.w};
-        const int64_t out_row = g * plan.gemm_m + m;
-        if (P.sa != nullptr) {
-            const float rs = P.sa[out_row];
-            for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
+    const float4 q = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4));
+    float v[4] = {q.x, q.y, q.z, q.w};
+    const int64_t out_row = g * plan.gemm_m + m;
+    if (P.sa != nullptr) {
+        const float rs = P.sa[out_row];
+        for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
+    }
+    const int64_t off = out_row * P.ldc + n0;
+    const bool full = n0 + 4 <= plan.gemm_n;
+    if (P.c_dtype == SK_F32) {
+        float* dst = static_cast<float*>(P.c) + off;
+        if (full) *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        else for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = v[j];
+    } else if (P.c_dtype == SK_BF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(P.c) + off;
+        if (full) {
+            __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&a);
+            w.y = *reinterpret_cast<uint32_t*>(&b);
+            *reinterpret_cast<uint2*>(dst) = w;
+        } else {
+            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2bfloat16_rn(v[j]);
         }
-        for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) {
-            const int64_t off = out_row * P.ldc + n0 + j;
-            if (P.c_dtype == SK_F32)
-                static_cast<float*>(P.c)[off] = v[j];
-            else if (P.c_dtype == SK_BF16)
-                static_cast<__nv_bfloat16*>(P.c)[off] = __float2bfloat16_rn(v[j]);
-            else
-                static_cast<__half*>(P.c)[off] = __float2half_rn(v[j]);
+    } else {
+        __half* dst = static_cast<__half*>(P.c) + off;
+        if (full) {
+            __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&a);
+            w.y = *reinterpret_cast<uint32_t*>(&b);
+            *reinterpret_cast<uint2*>(dst) = w;
+        } else {
+            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2half_rn(v[j]);
         }
     }
 }
@@ -623,37 +761,30 @@ static int ctas_per_sm_t() {
     return n;
 }
 
-size_t main_smem_bytes(int op, int tn) {
-    (void)tn;
-    switch (op) {
-        case kOpGemm16: return Cfg<kOpGemm16, 128>::kSmem;
-        case kOpFp8: return Cfg<kOpFp8, 128>::kSmem;
-        default: return Cfg<kOpWgrad16, 128>::kSmem;
-    }
+#define SK_DISPATCH(op, fn, ...)                                                            \
+    ((op) == kOpGemm16 ? fn<kOpGemm16, 128>(__VA_ARGS__)                                    \
+     : (op) == kOpFp8  ? fn<kOpFp8, 128>(__VA_ARGS__)                                       \
+                       : fn<kOpWgrad16, 128>(__VA_ARGS__))
+
+template <int OP, int TN>
+static size_t smem_bytes_t() {
+    return Cfg<OP, TN>::kSmem;
 }
 
-int main_ctas_per_sm(int op, int tn) {
-    (void)tn;
-    switch (op) {
-        case kOpGemm16: return ctas_per_sm_t<kOpGemm16, 128>();
-        case kOpFp8: return ctas_per_sm_t<kOpFp8, 128>();
-        default: return ctas_per_sm_t<kOpWgrad16, 128>();
-    }
-}
+size_t main_smem_bytes(int op) { return SK_DISPATCH(op, smem_bytes_t); }
 
-int launch_main(const KernelParams& p, int op, int tn, cudaStream_t stream) {
-    (void)tn;
-    switch (op) {
-        case kOpGemm16: return launch_main_t<kOpGemm16, 128>(p, stream);
-        case kOpFp8: return launch_main_t<kOpFp8, 128>(p, stream);
-        default: return launch_main_t<kOpWgrad16, 128>(p, stream);
-    }
+int main_ctas_per_sm(int op) { return SK_DISPATCH(op, ctas_per_sm_t); }
+
+int launch_main(const KernelParams& p, int op, cudaStream_t stream) {
+    return SK_DISPATCH(op, launch_main_t, p, stream);
 }
 
 int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
-    sk_stage2_kernel<128><<<dim3(static_cast<unsigned>(tiles)), dim3(256), 0, stream>>>(p);
+    const unsigned slices = static_cast<unsigned>(kTileM * kTileN / 4 / kStage2Threads);
+    sk_stage2_kernel<kTileN><<<dim3(static_cast<unsigned>(tiles), slices), dim3(kStage2Threads), 0,
+                               stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -13,6 +13,7 @@ namespace sk {
 enum OpKind : int { kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2 };
 
 constexpr int kTileM = 128;
+constexpr int kTileN = 128;
 
 // Instruction descriptor: fp32 accumulator, dense, M x N, A/B formats and majorness.
 //  kind::f16    : fmt 0 = f16, 1 = bf16.   kind::f8f6f4 : fmt 0 = e4m3, 1 = e5m2.
@@ -62,12 +63,12 @@ struct Stage2Params {
     int32_t c_dtype;
 };
 
-// Dynamic shared memory of the main kernel for (op, tile N).
-size_t main_smem_bytes(int op, int tn);
+// Dynamic shared memory of the main kernel for an op.
+size_t main_smem_bytes(int op);
 // How many CTAs of the main kernel fit on one SM (0 if the device query fails).
-int main_ctas_per_sm(int op, int tn);
+int main_ctas_per_sm(int op);
 // Launch the main kernel with grid = p.plan.grid. Returns a cudaError_t value.
-int launch_main(const KernelParams& p, int op, int tn, cudaStream_t stream);
+int launch_main(const KernelParams& p, int op, cudaStream_t stream);
 // Launch the Stage-2 reduce over the shared tiles of a workspace plan.
 int launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Read and clear the device error record: returns the code (0 = none) and fills info[3].

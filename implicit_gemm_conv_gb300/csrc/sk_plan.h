@@ -156,6 +156,22 @@ SK_HD bool seg_next(const sk_plan_t& p, int64_t cta, SegCursor& c, sk_segment_t&
     return true;
 }
 
+// Order of the iterations inside one stream-K segment (an execution detail, not part of the
+// plan). A CTA that has already run `tau` stream-K iterations starts its next segment at the
+// iteration k whose k mod iters_per_sk_cta is closest above tau, and wraps around. Then every SK
+// CTA reads reduction block k at a time close to k mod iters_per_sk_cta, whatever tile it works on,
+// so tiles that share an A or B panel read each block of it at nearly the same moment and L2
+// serves the repeats. Returns the offset of the first iteration processed, in [0, len).
+SK_HD int64_t sk_segment_rotation(int64_t iters_per_sk_cta, int64_t k_begin, int64_t len,
+                                  int64_t tau) {
+    const int64_t q = iters_per_sk_cta;
+    int64_t r = (k_begin - tau) % q;
+    if (r < 0) r += q;
+    if (r == 0) return 0;
+    const int64_t i = q - r;
+    return i < len ? i : 0;
+}
+
 // Tile id -> (group, m-tile, n-tile), n-tile fastest.
 SK_HD void tile_coords(const sk_plan_t& p, int64_t t, int64_t& g, int64_t& mt, int64_t& nt) {
     nt = t % p.tiles_n;

@@ -120,6 +120,7 @@ def test_gemm_3840x4096x4096_pool148_sampled(red):
     _sampled("bf16", 3840, 4096, 4096, "n01", "dp_sk", red, 148)
 
 
+
 @pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("dp_sk", "tree"),
                                       ("persistent", "workspace"), ("splitk", "workspace"),
                                       ("off", "linear")])
