@@ -639,8 +639,8 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     const int64_t up_h = (Ho - 1) * stride_h - pad_h - (H - 1);
     if (up_w < -128 || up_h < -128 || up_w > 127 || up_h > 127 || -pad_w < -128 || -pad_h < -128)
         return fail(SK_ERR_UNSUPPORTED, "im2col bounding box outside the 4-D TMA range");
-    if (N * Ho * Wo >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
-        return fail(SK_ERR_UNSUPPORTED, "too many output pixels");
+    if (N * Ho * Wo + 64 >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return fail(SK_ERR_UNSUPPORTED, "too many output pixels (N*Ho*Wo must stay below 2^31 - 64)");
     if (!x || !dy || !dw) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
     if (!aligned16(x) || !aligned16(dy) || !aligned16(dw))
         return fail(SK_ERR_UNSUPPORTED, "x, dy and dw must be 16-byte aligned");

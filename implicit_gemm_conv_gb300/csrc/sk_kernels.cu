@@ -84,10 +84,36 @@ struct SmemCtl {
 // operand producer
 // ---------------------------------------------------------------------------------------------
 
+// Per-tile constants of the wgrad B operand: for each 64-column slab of the tile, its channel
+// coordinate and filter-tap offsets. Computed once per segment, so the per-iteration work of the
+// single producer thread is one pixel decomposition (32-bit divisions) and the TMA issues.
+template <int TN>
+struct WgradSlabs {
+    int32_t c[TN / 64];
+    uint16_t off_w[TN / 64], off_h[TN / 64];
+};
+
+template <int TN>
+__device__ __forceinline__ void wgrad_slabs(const ConvGeom& cg, int64_t g, int64_t nt,
+                                            WgradSlabs<TN>& sl) {
+    const int32_t RS = cg.R * cg.S;
+#pragma unroll
+    for (int j = 0; j < TN / 64; ++j) {
+        const int32_t n0 = static_cast<int32_t>(nt * TN + 64 * j);
+        int32_t tap = n0 / cg.Cg;
+        const int32_t c0 = n0 - tap * cg.Cg;
+        if (tap >= RS) tap = RS - 1;   // slab past the last tap: any valid data, masked later
+        const int32_t r = tap / cg.S;
+        sl.c[j] = static_cast<int32_t>(g) * cg.Cg + c0;
+        sl.off_w[j] = static_cast<uint16_t>(tap - r * cg.S);
+        sl.off_h[j] = static_cast<uint16_t>(r);
+    }
+}
+
 template <int OP, int TN>
 __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
                                             int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
-                                            uint32_t bar) {
+                                            uint32_t bar, const WgradSlabs<TN>& sl) {
     using C = Cfg<OP, TN>;
     if constexpr (OP != kOpWgrad16) {
         const int32_t kx = static_cast<int32_t>(k * C::TK);
@@ -96,29 +122,25 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
     } else {
         // A = dy viewed as [pixels][K]: two 64-filter slabs of TK pixel rows (MN-major).
         const ConvGeom& cg = P.conv;
-        const int32_t p0 = static_cast<int32_t>(k * C::TK);
+        const uint32_t p0 = static_cast<uint32_t>(k) * C::TK;   // < 2^31 (checked on the host)
         const int32_t k0 = static_cast<int32_t>(g * cg.Kg + mt * kTileM);
 #pragma unroll
         for (int j = 0; j < kTileM / 64; ++j)
-            tma_load_2d(a_dst + j * (C::TK * 128), &P.tmap_a, bar, k0 + 64 * j, p0);
-        // B = im2col(x): per 64-column slab one filter tap (r, s) and 64 channels, TK pixels.
-        const int64_t n_img = p0 / cg.HoWo;
-        const int64_t rem = p0 - n_img * cg.HoWo;
-        const int32_t ho = static_cast<int32_t>(rem / cg.Wo);
-        const int32_t wo = static_cast<int32_t>(rem - int64_t(ho) * cg.Wo);
-        const int32_t RS = cg.R * cg.S;
+            tma_load_2d(a_dst + j * (C::TK * 128), &P.tmap_a, bar, k0 + 64 * j,
+                        static_cast<int32_t>(p0));
+        // B = im2col(x): per 64-column slab one filter tap (r, s) and 64 channels, TK pixels
+        // starting at output pixel p0 = (n, ho, wo).
+        const uint32_t howo = static_cast<uint32_t>(cg.HoWo), wo_n = static_cast<uint32_t>(cg.Wo);
+        const uint32_t n_img = p0 / howo;
+        const uint32_t rem = p0 - n_img * howo;
+        const uint32_t ho = rem / wo_n;
+        const uint32_t wo = rem - ho * wo_n;
+        const int32_t w = static_cast<int32_t>(wo) * cg.sw - cg.pw;
+        const int32_t h = static_cast<int32_t>(ho) * cg.sh - cg.ph;
 #pragma unroll
-        for (int j = 0; j < TN / 64; ++j) {
-            const int64_t n0 = nt * TN + 64 * j;
-            int32_t tap = static_cast<int32_t>(n0 / cg.Cg);
-            const int32_t c0 = static_cast<int32_t>(n0 - int64_t(tap) * cg.Cg);
-            if (tap >= RS) tap = RS - 1;   // slab past the last tap: any valid data, masked later
-            const int32_t r = tap / cg.S, s = tap - (tap / cg.S) * cg.S;
-            tma_load_im2col_4d(b_dst + j * (C::TK * 128), &P.tmap_b, bar,
-                               static_cast<int32_t>(g * cg.Cg + c0), wo * cg.sw - cg.pw,
-                               ho * cg.sh - cg.ph, static_cast<int32_t>(n_img),
-                               static_cast<uint16_t>(s), static_cast<uint16_t>(r));
-        }
+        for (int j = 0; j < TN / 64; ++j)
+            tma_load_im2col_4d(b_dst + j * (C::TK * 128), &P.tmap_b, bar, sl.c[j], w, h,
+                               static_cast<int32_t>(n_img), sl.off_w[j], sl.off_h[j]);
     }
 }
 
@@ -150,6 +172,8 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
+        WgradSlabs<TN> slabs;
+        if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
         const int64_t len = seg.k_end - seg.k_begin;
         const int64_t rot = segment_rotation(plan, dp, seg, tau);
         for (int64_t j = 0; j < len; ++j) {
@@ -164,7 +188,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
             }
             mbar_arrive_expect_tx(full, C::kStageBytes);
             const uint32_t a_dst = ring + stage * C::kStageBytes;
-            issue_loads<OP, TN>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full);
+            issue_loads<OP, TN>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs);
             ++issued;
             if (++stage == C::kStages) {
                 stage = 0;
