@@ -315,7 +315,7 @@ def run_ours(args, rank, world, dev):
     step_ms = max_over_ranks(torch, world, step_ms, dev)
     main_ms = max_over_ranks(torch, world, main_ms, dev)
     flops_step = w.flops()
-    value = flops_step * args.steps * world / (step_ms / 1e3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, step_ms)
     main_avg_s = main_ms / max(n_main, 1) / 1e3
     achieved = flops_step / main_avg_s / 1e12
     peak = peaks["bf16_tflops"]
@@ -334,7 +334,7 @@ def run_ours(args, rank, world, dev):
 
     e2e_ms, _, _, _ = time_calls(torch, sk, e2e_call, e2e_steps, 2, flush, stream)
     e2e_ms = max_over_ranks(torch, world, e2e_ms, dev)
-    e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": whole_job_tflops(flops_step, e2e_steps, world, e2e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(A.numel() * 2 + B.numel() * 2),
            "d2h_bytes_per_step": int(C.numel() * 2)}
 
@@ -411,6 +411,12 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_step_ms: float) -> float:
+    """Weak scaling: every rank runs its own problem; the job's rate is all ranks' FLOP over the
+    slowest rank's time."""
+    return flops_per_step * steps * world / (max_step_ms / 1e3) / 1e12
 
 
 def max_over_ranks(torch, world, v, dev):

@@ -58,7 +58,7 @@ struct Cfg {
     static constexpr int kABytes = kTileM * 128;           // 16 KB
     static constexpr int kBBytes = TN * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 7;   // 7 x 32 KB: the most that fits in 227 KB with the control words
     static constexpr int kTmemCols = 2 * TN;               // double-buffered fp32 accumulator
     static constexpr int kMmaK = OP == kOpFp8 ? 32 : 16;
     static constexpr int kMmasPerStage = TK / kMmaK;
@@ -69,16 +69,21 @@ struct Cfg {
     static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
     static_assert((TN / 32) % kFoldUnitChunks == 0, "tile N must be a multiple of 128");
+    static constexpr int kRingBytes = kStages * kStageBytes;   // a multiple of 1024
+    static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (2 * kStages + 4 + kFoldBufs) * 8;
-    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes + 64;
+    static constexpr size_t kSmem = 1024 + size_t(kRingBytes) + kCtlBytes + kBarBytes;
 };
 
+// Per-CTA control words. The block starts right after the operand ring, so tmem_base (written by
+// tcgen05.alloc) sits at a 1024-byte aligned address.
 struct SmemCtl {
     uint32_t tmem_base;
     uint32_t abort;
     long long cta;
     uint32_t epi_ok[2];   // epilogue: accumulator-ready verdict, one slot per alternate segment
 };
+constexpr uint32_t kTmemSentinel = 0xFFFFFFFFu;   // not a TMEM address: lane and column out of range
 
 // ---------------------------------------------------------------------------------------------
 // operand producer
@@ -642,13 +647,18 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
+    static_assert(sizeof(SmemCtl) <= C::kCtlBytes, "control block");
     const uint32_t ring = smem_u32(smem);
-    const uint32_t bars = ring + C::kStages * C::kStageBytes;
-    volatile SmemCtl* ctl =
-        reinterpret_cast<volatile SmemCtl*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
+    volatile SmemCtl* ctl = reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes);
+    const uint32_t bars = ring + C::kRingBytes + C::kCtlBytes;
     const int warp = static_cast<int>(threadIdx.x >> 5);
 
     if (threadIdx.x == 0) {
+        // Take the ticket first: its round trip to L2 overlaps the barrier set-up below.
+        const uint32_t ticket = atomicAdd(P.control, 1u);
+        // The allocation below overwrites this; whatever a previous kernel left in shared memory
+        // can never be taken for a TMEM address.
+        ctl->tmem_base = kTmemSentinel;
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bars + s * 8, 1);                    // full: producer arrive + tx bytes
             mbar_init(bars + (C::kStages + s) * 8, 1);     // empty: MMA commit
@@ -661,10 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
             mbar_init(bars + (2 * C::kStages + 4 + f) * 8, 1);   // owner's fold buffers
         fence_mbarrier_init();
         ctl->abort = 0;
-        ctl->cta = static_cast<long long>(atomicAdd(P.control, 1u));
+        ctl->cta = static_cast<long long>(ticket);
         tma_prefetch_desc(&P.tmap_a);
         tma_prefetch_desc(&P.tmap_b);
     }
+    __syncthreads();   // the sentinel is in place before the allocation writes the slot
     if (warp == 1) {
         tmem_alloc(smem_u32(const_cast<uint32_t*>(&ctl->tmem_base)), C::kTmemCols);
         tmem_relinquish();
@@ -674,8 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int64_t cta = ctl->cta;
-    if (threadIdx.x == 0 && ((tmem_base & 0xFFFFu) + C::kTmemCols > 512u || (tmem_base >> 16) != 0))
-        record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
+    // Every thread reads the same slot, so the whole CTA takes this exit together. It is never
+    // expected; it keeps a bad slot from ever reaching a TMEM access.
+    if (tmem_base == kTmemSentinel || (tmem_base >> 16) != 0 ||
+        (tmem_base & 0xFFFFu) + C::kTmemCols > 512u) {
+        if (threadIdx.x == 0) record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
+        return;
+    }
 
     if (warp == 0) {
         if (elect_one()) run_producer<OP, TN>(P, cta, ring, bars, ctl);
@@ -786,9 +802,9 @@ static int ctas_per_sm_t() {
 }
 
 #define SK_DISPATCH(op, fn, ...)                                                            \
-    ((op) == kOpGemm16 ? fn<kOpGemm16, 128>(__VA_ARGS__)                                    \
-     : (op) == kOpFp8  ? fn<kOpFp8, 128>(__VA_ARGS__)                                       \
-                       : fn<kOpWgrad16, 128>(__VA_ARGS__))
+    ((op) == kOpGemm16 ? fn<kOpGemm16, kTileN>(__VA_ARGS__)                                 \
+     : (op) == kOpFp8  ? fn<kOpFp8, kTileN>(__VA_ARGS__)                                    \
+                       : fn<kOpWgrad16, kTileN>(__VA_ARGS__))
 
 template <int OP, int TN>
 static size_t smem_bytes_t() {
