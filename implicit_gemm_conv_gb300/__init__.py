@@ -22,13 +22,14 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 F16, BF16, F32, E4M3 = 0, 1, 2, 3
-OFF, DP_SK, PERSISTENT, SPLITK = 0, 1, 2, 3
-LINEAR, TREE, ATOMIC, WORKSPACE = 0, 1, 2, 3
+OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
+LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
 OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD = 0, 1, 2
 SEG_FULL, SEG_OWNER, SEG_PEER = 0, 1, 2
 
-MODES = {"off": OFF, "dp_sk": DP_SK, "persistent": PERSISTENT, "splitk": SPLITK}
-REDUCTIONS = {"linear": LINEAR, "tree": TREE, "atomic": ATOMIC, "workspace": WORKSPACE}
+MODES = {"off": OFF, "dp_sk": DP_SK, "persistent": PERSISTENT, "splitk": SPLITK, "auto": AUTO}
+REDUCTIONS = {"linear": LINEAR, "tree": TREE, "atomic": ATOMIC, "workspace": WORKSPACE,
+              "auto": REDUCTION_AUTO}
 DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}
 
 _i64, _i32, _p, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t

@@ -182,8 +182,26 @@ int problem_view(const sk_problem& p, View& v) {
     }
 }
 
+int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
+                        int ctas_per_sm, sk_plan_t& p);
+
+// SK_AUTO: stream-K for few tiles over a long reduction, and only when the partition the launch
+// would use has stream-K CTAs; split-K everywhere else.
+constexpr int64_t kAutoMinIterations = 1024;   // T * I at which the reduction counts as long
+
 int build_plan(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
                int ctas_per_sm, sk_plan_t& p) {
+    if (reduction == SK_REDUCTION_AUTO) reduction = SK_WORKSPACE;
+    if (mode != SK_AUTO) return build_plan_resolved(prob, mode, reduction, ctas, num_sms, ctas_per_sm, p);
+    int rc = build_plan_resolved(prob, SK_DP_SK, reduction, ctas, num_sms, ctas_per_sm, p);
+    if (rc) return rc;
+    if (p.tiles < p.pool && p.tiles * p.iters_per_tile >= kAutoMinIterations && p.sk_ctas > 0)
+        return SK_OK;
+    return build_plan_resolved(prob, SK_SPLITK, reduction, ctas, num_sms, ctas_per_sm, p);
+}
+
+int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
+                        int ctas_per_sm, sk_plan_t& p) {
     if (mode < SK_OFF || mode > SK_SPLITK) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
     if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
@@ -409,7 +427,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
                 if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
             }
         }
-        if (reduction == SK_ATOMIC && plan.shared_tiles > 0) {
+        if (plan.reduction == SK_ATOMIC && plan.shared_tiles > 0) {
             e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
@@ -418,7 +436,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
-        if (reduction == SK_WORKSPACE && plan.shared_tiles > 0) {
+        if (plan.reduction == SK_WORKSPACE && plan.shared_tiles > 0) {
             sk::Stage2Params s2;
             s2.plan = plan;
             s2.c = kp.c;
@@ -440,8 +458,8 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
 }
 
 int check_common(int mode, int reduction, int ctas, int c_dtype) {
-    if (mode < SK_OFF || mode > SK_SPLITK) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
-    if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
+    if (mode < SK_OFF || mode > SK_AUTO) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
+    if (reduction < SK_LINEAR || reduction > SK_REDUCTION_AUTO)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
     if (ctas == 0 || ctas < -1)
         return fail(SK_ERR_UNSUPPORTED, "streamk_ctas must be -1 (default) or >= 1, got %d", ctas);
@@ -465,6 +483,7 @@ int sk_version(void) { return 100; }
 
 int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out) {
     if (!out) return fail(SK_ERR_UNSUPPORTED, "out is NULL");
+    if (reduction == SK_REDUCTION_AUTO) reduction = SK_WORKSPACE;
     if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
     int64_t pool = 0;

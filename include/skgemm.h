@@ -25,9 +25,16 @@
  *    tiles + stream-K CTAs), SK_PERSISTENT (grid = pool; each CTA runs its DP tiles, then its
  *    stream-K range), or SK_SPLITK (comparator: every tile cut into s = max(1, pool/tiles) equal
  *    K slices, combined by the same reductions).
+ *    SK_AUTO picks between SK_DP_SK and SK_SPLITK ([P2] commits "ConvGroupedRequest.streamk now
+ *    defaults to auto" and the review fix "auto builds the launch partition, requires sk_ctas > 0";
+ *    this selection was later reverted from the pages' dispatcher): stream-K when the tiles do not
+ *    fill the pool (T < P) and the reduction is long (T * I >= 1024), and only if the plan the
+ *    launch would use has stream-K CTAs; split-K otherwise (plain data-parallel when T >= P). The
+ *    resolved mode is what sk_plan reports.
  *  - `reduction`: SK_LINEAR and SK_TREE are deterministic (bit-identical across launches with the
  *    same plan); SK_ATOMIC needs an fp32 output; SK_WORKSPACE adds into fp32 scratch and runs a
- *    second (Stage-2) kernel that writes the output.
+ *    second (Stage-2) kernel that writes the output. SK_REDUCTION_AUTO resolves to SK_WORKSPACE
+ *    ([P2] "streamk_reduction defaults to auto, which resolves to the workspace reduction").
  *  - `ctas`: the CTA pool; -1 = default (one CTA per SM for linear/tree; SMs x min(4, CTAs that
  *    fit on one SM) for atomic/workspace). 0 and values below -1 are rejected with -2.
  *  - `ws`, `ws_bytes`: workspace of at least sk_workspace_bytes() bytes, 256-byte aligned. With
@@ -51,8 +58,9 @@ extern "C" {
 #endif
 
 enum { SK_F16 = 0, SK_BF16 = 1, SK_F32 = 2, SK_E4M3 = 3 };                  /* element types */
-enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3 };        /* streamk      */
-enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3 };       /* reduction    */
+enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3, SK_AUTO = 4 };  /* streamk */
+enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3, SK_REDUCTION_AUTO = 4 };
+                                                                             /* reduction    */
 enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2 };             /* operation    */
 enum { SK_SEG_FULL = 0, SK_SEG_OWNER = 1, SK_SEG_PEER = 2 };                /* segment kind */
 

@@ -36,8 +36,12 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 from typing import List
 
-OFF, DP_SK, PERSISTENT, SPLITK = 0, 1, 2, 3
-LINEAR, TREE, ATOMIC, WORKSPACE = 0, 1, 2, 3
+OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
+LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
+
+# Auto selection: "long reduction" once the tiles hold this many MAC iterations in total (the
+# PR #13151 review thread shows the predicate passing for a one-tile shape from 1024 iterations).
+AUTO_MIN_ITERATIONS = 1024
 
 # segment kinds: a CTA's work on one tile
 SEG_FULL = 0    # the CTA computes the whole reduction of the tile and writes it
@@ -151,6 +155,20 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
         p.scratch_bytes = _n_sk_tiles(p) * tile_bytes
     p.ws_bytes = p.flag_bytes + CONTROL_BYTES + p.partial_bytes + p.scratch_bytes
     return p
+
+
+def make_auto_plan(**kw) -> Plan:
+    """streamk = auto (PR #13151, commit making "auto" the default, and the review fix that has it
+    build the launch's partition): stream-K when the tiles are few (T < P) over a long reduction
+    (T*I >= AUTO_MIN_ITERATIONS) and the partition really has stream-K CTAs; otherwise split-K.
+    reduction = auto resolves to workspace (same commit)."""
+    if kw.get("reduction") == REDUCTION_AUTO:
+        kw["reduction"] = WORKSPACE
+    kw.pop("mode", None)
+    p = make_plan(mode=DP_SK, **kw)
+    if p.T < p.P and p.T * p.I >= AUTO_MIN_ITERATIONS and p.sk_ctas > 0:
+        return p
+    return make_plan(mode=SPLITK, **kw)
 
 
 def _n_sk_tiles(p: Plan) -> int:

@@ -126,3 +126,17 @@ def test_gemm_3840x4096x4096_pool148_sampled(red):
                                       ("off", "linear")])
 def test_gemm_512x512x65536_pool148_sampled(mode, red):
     _sampled("bf16", 512, 512, 65536, "n01", mode, red, 148)
+
+
+def test_gemm_auto_selection():
+    # few tiles over a long reduction -> stream-K; reduction auto -> workspace
+    prob = sk.make_problem("gemm", ab_dtype="bf16", c_dtype="bf16", M=512, N=512, K=65536)
+    plan = sk.sk_plan(prob, "auto", "auto", 148)
+    assert plan.mode == sk.DP_SK and plan.reduction == sk.WORKSPACE
+    _sampled("bf16", 512, 512, 65536, "n01", "auto", "auto", 148)
+    # the tiles fill the pool -> split-K with one slice, i.e. data-parallel
+    A, B, ref = ref_full("f16", 256, 256, 4096, "u11", 0)
+    assert sk.sk_plan(sk.make_problem("gemm", ab_dtype="f16", c_dtype="f16", M=256, N=256,
+                                      K=4096), "auto", "linear", 3).mode == sk.SPLITK
+    C = run_gemm(A, B, "f16", "auto", "linear", 3)
+    check_parity(C, ref, "f16", 4096, what="auto pool 3")

@@ -87,3 +87,9 @@ def test_wgrad_n64_28x28_g4_s2(mode, red):
     x, dy, ref = case("bf16", 64, 28, 28, 256, 256, 3, 3, (2, 2), (1, 1), 4, "n0.5")
     dw = run(x, dy, 256, 3, 3, (2, 2), (1, 1), 4, "f32", mode, red, -1)
     check_parity(dw, ref, "f32", 64 * 14 * 14, what=f"cfg g4 {mode}/{red}")
+
+
+def test_wgrad_auto_selection():
+    x, dy, ref = case("f16", 32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), 1, "u11")
+    dw = run(x, dy, 64, 3, 3, (1, 1), (1, 1), 1, "f32", "auto", "auto", -1)
+    check_parity(dw, ref, "f32", 32 * 56 * 56, what="wgrad auto")

@@ -157,6 +157,27 @@ def test_forward_progress_simulation():
 
 # --- planted mistakes: each must be caught by the checks above -------------------------------
 
+def test_auto_selection_page_example():
+    # review thread: pool 1216, one tile with 1024..1215 iterations passes the long-reduction
+    # predicate but has no stream-K CTAs, so auto must keep split-K; from 1216 it is stream-K.
+    kw = dict(tiles_m=1, tiles_n=1, groups=1, tm=128, tn=128, tk=64, pool=1216,
+              reduction=P.WORKSPACE)
+    for I in (1024, 1100, 1215):
+        assert P.make_auto_plan(kred=I * 64, **kw).mode == P.SPLITK
+    assert P.make_auto_plan(kred=1216 * 64, **kw).mode == P.DP_SK
+    # many tiles: split-K, which degenerates to one slice per tile
+    many = P.make_auto_plan(tiles_m=30, tiles_n=32, groups=1, kred=4096, tm=128, tn=128, tk=64,
+                            pool=148, reduction=P.LINEAR)
+    assert many.mode == P.SPLITK and many.splits == 1
+    # few tiles, short reduction (T*I < 1024): split-K
+    short = P.make_auto_plan(tiles_m=2, tiles_n=2, groups=1, kred=64 * 100, tm=128, tn=128, tk=64,
+                             pool=148, reduction=P.LINEAR)
+    assert short.mode == P.SPLITK
+    # reduction auto -> workspace
+    assert P.make_auto_plan(tiles_m=4, tiles_n=4, groups=1, kred=65536, tm=128, tn=128, tk=64,
+                            pool=148, reduction=P.REDUCTION_AUTO).reduction == P.WORKSPACE
+
+
 def test_single_slot_linear_owner_blocks():
     # with one resident CTA the owner of a shared tile waits for a CTA that never starts
     assert not P.simulate_progress(plan(4, 64, 3, P.DP_SK, P.LINEAR), 1, P.LINEAR)

@@ -110,6 +110,24 @@ def test_grouped_wgrad_sweep():
             compare(prob, kw, mode, REDS[1], 7)
 
 
+def test_auto_mode_matches_oracle():
+    rng = random.Random(17)
+    cases = [gemm(512, 512, 65536, "bf16"), gemm(3840, 4096, 4096, "bf16"), gemm(256, 256, 4096),
+             gemm(128, 128, 64 * 1216), gemm(128, 128, 64 * 1215)]
+    cases += [gemm(rng.randint(1, 900), rng.randint(1, 900), 8 * rng.randint(1, 4000))
+              for _ in range(200)]
+    for prob, kw in cases:
+        for red, ored in [("linear", P.LINEAR), ("auto", P.REDUCTION_AUTO)]:
+            for ctas in (-1, 148, 1216):
+                cp = sk.sk_plan(prob, "auto", red, ctas, 152)
+                pool = ctas if ctas > 0 else P.default_pool(
+                    P.WORKSPACE if ored == P.REDUCTION_AUTO else ored, 152, 1)
+                op = P.make_auto_plan(pool=pool, reduction=ored, **kw)
+                assert cp.mode == op.mode and cp.reduction == op.reduction
+                for c, o in FIELD_MAP.items():
+                    assert getattr(cp, c) == getattr(op, o), (c, kw, ctas)
+
+
 def test_plan_rejections():
     prob, _ = gemm(256, 256, 4096)
     for ctas in (0, -5):
