@@ -229,6 +229,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
     uint32_t stage = 0, phase = 0;
     int64_t nseg = 0;
     uint32_t last_empty = 0, last_parity = 0;
+    int64_t total_commits = 0;
     bool any = false, ok = true;
     while (true) {
         const bool dp = cur.dp_next >= 0;
@@ -276,6 +277,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
                     mma_f16(d_tmem, ad, bd, P.idesc, accumulate);
             }
             tc_commit(empty);
+            ++total_commits;
             any = true;
             last_empty = empty;
             last_parity = phase;
@@ -288,8 +290,23 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         tc_commit(tfull);
         ++nseg;
     }
-    // The accumulator may only be freed once the last MMA has completed.
-    if (any) mbar_wait(last_empty, last_parity, 10000000ull);
+    // Before the CTA may exit, every commit it issued must have landed: the last commit of each
+    // stage of the ring is awaited, so that no arrival can reach this SM's shared memory after the
+    // CTA is gone (the next CTA there may lay it out differently).
+    (void)last_empty;
+    (void)last_parity;
+    if (any) {
+        int64_t n = total_commits < C::kStages ? total_commits : C::kStages;
+        uint32_t st = stage, ph = phase;
+        for (int64_t i = 0; i < n; ++i) {
+            if (st == 0) {
+                st = C::kStages;
+                ph ^= 1;
+            }
+            --st;
+            mbar_wait(bars + (C::kStages + st) * 8, ph, 10000000ull);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
