@@ -254,12 +254,13 @@ def run_variant(args, dev):
     name, mr = args.variant.split(":")
     mode, red = mr.split("/")
     w = WORKLOADS[name]
+    pool = args.pool if args.pool is not None else w.pool
     ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     if w.op == "gemm":
         A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
         A, B = A.to(dev), B.to(dev)
         C = torch.empty(w.M, w.N, dtype=torch.float32 if red == "atomic" else A.dtype, device=dev)
-        call = lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws)
+        call = lambda: sk.sk_gemm_rcr(A, B, C, mode, red, pool, ws=ws)
     elif w.op == "wgrad":
         c = w.conv
         x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],
@@ -268,17 +269,17 @@ def run_variant(args, dev):
         dw = torch.empty(c["K"], c["R"], c["S"], c["C"] // c["groups"], dtype=torch.float32,
                          device=dev)
         call = lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"], c["pad"],
-                                               c["groups"], mode, red, w.pool, ws=ws)
+                                               c["groups"], mode, red, pool, ws=ws)
     else:
         A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
         A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
         C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
-        call = lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool, ws=ws)
+        call = lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, pool, ws=ws)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     step_ms, main_ms, n_main, n_all = time_calls(torch, sk, call, args.steps, args.warmup, flush,
                                                  torch.cuda.current_stream())
     sk.sk_device_status()
-    return {"variant": args.variant, "steps": args.steps, "step_us": step_ms / args.steps * 1e3,
+    return {"variant": args.variant, "pool": pool, "steps": args.steps, "step_us": step_ms / args.steps * 1e3,
             "main_us": main_ms / max(n_main, 1) * 1e3, "tflops": w.flops() * args.steps / step_ms / 1e9,
             "launches": n_all}
 
@@ -440,6 +441,9 @@ def main():
     ap.add_argument("--reference-rows", type=int, default=4)
     ap.add_argument("--variant", default=None,
                     help="WORKLOAD:MODE/REDUCTION - time only this variant (for profiling)")
+    ap.add_argument("--tile", default=None, choices=["auto", "128", "256_pair", "256x256_pair"],
+                    help="tile shape of the --variant run (sk_set_tile)")
+    ap.add_argument("--pool", type=int, default=None, help="CTA pool of the --variant run")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -456,7 +460,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.variant:
-        print(json.dumps(run_variant(args, dev)), flush=True)
+        import implicit_gemm_conv_gb300 as sk
+        with sk.tile(args.tile or "auto"):
+            res = run_variant(args, dev)
+        res["tile"] = args.tile or "auto"
+        print(json.dumps(res), flush=True)
         return 0
     if world > 1:
         import torch.distributed as dist

@@ -8,6 +8,7 @@ library is missing, and every call raises ``SkError`` on a non-zero return code.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -26,11 +27,14 @@ OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
 LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
 OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD = 0, 1, 2
 SEG_FULL, SEG_OWNER, SEG_PEER = 0, 1, 2
+TILE_AUTO, TILE_128, TILE_256_PAIR, TILE_256x256_PAIR = 0, 1, 2, 3
 
 MODES = {"off": OFF, "dp_sk": DP_SK, "persistent": PERSISTENT, "splitk": SPLITK, "auto": AUTO}
 REDUCTIONS = {"linear": LINEAR, "tree": TREE, "atomic": ATOMIC, "workspace": WORKSPACE,
               "auto": REDUCTION_AUTO}
 DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}
+TILES = {"auto": TILE_AUTO, "128": TILE_128, "256_pair": TILE_256_PAIR,
+         "256x256_pair": TILE_256x256_PAIR}
 
 _i64, _i32, _p, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
 
@@ -83,12 +87,14 @@ _lib.sk_version.restype = _i32
 _lib.sk_gemm_rcr_static_ws.argtypes = [_i32, _i32, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
                                        _i32, _i32, _i32, _p]
 _lib.sk_timing_enable.argtypes = [_i32]
+_lib.sk_set_tile.argtypes = [_i32]
 _lib.sk_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
                                 ctypes.POINTER(_i64)]
 
 EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_workspace_bytes",
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
-           "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws"]
+           "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws",
+           "sk_set_tile"]
 
 
 class SkError(RuntimeError):
@@ -132,6 +138,25 @@ def _ws(ws):
     if ws is None:
         return None, 0
     return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def sk_set_tile(tile) -> int:
+    """Tile shape for later calls of this thread ("auto", "128", "256_pair", "256x256_pair" or the
+    TILE_* code); returns the previous code."""
+    rc = _lib.sk_set_tile(_code(TILES, tile))
+    if rc < 0:
+        raise SkError(rc, last_error())
+    return rc
+
+
+@contextlib.contextmanager
+def tile(t):
+    """``with tile("256x256_pair"): ...`` -- sk_set_tile for the block, restored afterwards."""
+    prev = sk_set_tile(t)
+    try:
+        yield
+    finally:
+        sk_set_tile(prev)
 
 
 # ---- compute calls -----------------------------------------------------------------------------

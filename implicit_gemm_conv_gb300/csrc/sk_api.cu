@@ -25,6 +25,7 @@
 namespace {
 
 thread_local char g_err[512] = "";
+thread_local int g_tile = SK_TILE_AUTO;   // sk_set_tile
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -185,6 +186,32 @@ int problem_view(const sk_problem& p, View& v) {
 int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
                         int ctas_per_sm, sk_plan_t& p);
 
+// The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
+// (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
+struct TileCfg {
+    int cg, tn;
+};
+int tile_cfg(const View& v, TileCfg& t) {
+    t = {1, sk::kTileN};
+    switch (g_tile) {
+        case SK_TILE_128: return SK_OK;
+        case SK_TILE_256_PAIR:
+        case SK_TILE_256x256_PAIR:
+            if (v.op_kind == sk::kOpWgrad16)
+                return fail(SK_ERR_UNSUPPORTED, "the CTA-pair tiles serve the GEMMs only");
+            t = {2, g_tile == SK_TILE_256_PAIR ? 128 : 256};
+            return SK_OK;
+        default:   // SK_TILE_AUTO
+            return SK_OK;
+    }
+}
+int problem_tile(const sk_problem& prob, TileCfg& t) {
+    View v;
+    int rc = problem_view(prob, v);
+    if (rc) return rc;
+    return tile_cfg(v, t);
+}
+
 // SK_AUTO: stream-K for few tiles over a long reduction, and only when the partition the launch
 // would use has stream-K CTAs; split-K everywhere else.
 constexpr int64_t kAutoMinIterations = 1024;   // T * I at which the reduction counts as long
@@ -211,15 +238,20 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
     if (v.gemm_m < 1 || v.gemm_n < 1 || v.kred < 1 || v.groups < 1)
         return fail(SK_ERR_UNSUPPORTED, "empty problem (M=%lld N=%lld K=%lld)", (long long)v.gemm_m,
                     (long long)v.gemm_n, (long long)v.kred);
+    TileCfg tc;
+    rc = tile_cfg(v, tc);
+    if (rc) return rc;
+    const int cg = tc.cg;
+    // A pair kernel's pool counts pairs: its default is resolved over SM pairs.
     int64_t P = 0;
-    rc = resolve_pool(reduction, ctas, num_sms, ctas_per_sm, P);
+    rc = resolve_pool(reduction, ctas, num_sms / cg, ctas_per_sm, P);
     if (rc) return rc;
     memset(&p, 0, sizeof(p));
     p.op = prob.op;
     p.mode = mode;
     p.reduction = reduction;
-    p.tm = sk::kTileM;
-    p.tn = sk::kTileN;
+    p.tm = sk::kTileM * cg;
+    p.tn = tc.tn;
     p.tk = prob.op == SK_OP_FP8_ROWCOL ? 128 : 64;
     p.gemm_m = v.gemm_m;
     p.gemm_n = v.gemm_n;
@@ -274,7 +306,8 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
     if (reduction == SK_TREE && p.tree_rounds > 32)
         return fail(SK_ERR_UNSUPPORTED, "tree reduction supports at most 2^32 contributors");
     const int64_t tile_bytes = p.tm * p.tn * 4;
-    p.flag_bytes = sk::round_up(4 * p.publishers, 256);
+    // One flag per 128-row half: each CTA of a pair publishes and receives its half on its own.
+    p.flag_bytes = sk::round_up(4 * p.publishers * cg, 256);
     p.control_offset = p.flag_bytes;
     p.partial_offset = p.control_offset + sk::kControlBytes;
     p.partial_bytes = (reduction == SK_LINEAR || reduction == SK_TREE) ? p.publishers * tile_bytes : 0;
@@ -384,7 +417,10 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
     if (rc) return rc;
     View v;
     problem_view(prob, v);
-    const int per_sm = sk::main_ctas_per_sm(v.op_kind);
+    TileCfg tc;
+    rc = tile_cfg(v, tc);
+    if (rc) return rc;
+    const int per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn);
     sk_plan_t plan;
     rc = build_plan(prob, mode, reduction, ctas, dev.sms, per_sm, plan);
     if (rc) return rc;
@@ -432,7 +468,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
         const int tslot = timing_start(stream);
-        int le = sk::launch_main(kp, v.op_kind, stream);
+        int le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -481,6 +517,15 @@ const char* sk_last_error(void) { return g_err; }
 
 int sk_version(void) { return 100; }
 
+int sk_set_tile(int tile) {
+    if (tile != SK_TILE_AUTO && tile != SK_TILE_128 && tile != SK_TILE_256_PAIR &&
+        tile != SK_TILE_256x256_PAIR)
+        return fail(SK_ERR_UNSUPPORTED, "unknown tile setting %d", tile);
+    const int prev = g_tile;
+    g_tile = tile;
+    return prev;
+}
+
 int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out) {
     if (!out) return fail(SK_ERR_UNSUPPORTED, "out is NULL");
     if (reduction == SK_REDUCTION_AUTO) reduction = SK_WORKSPACE;
@@ -502,7 +547,12 @@ int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_s
         if (rc) return rc;
         num_sms = d.sms;
         View v;
-        if (problem_view(*p, v) == SK_OK) per_sm = sk::main_ctas_per_sm(v.op_kind);
+        if (problem_view(*p, v) == SK_OK) {
+            TileCfg tc;
+            rc = tile_cfg(v, tc);
+            if (rc) return rc;
+            per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn);
+        }
     }
     return build_plan(*p, streamk, reduction, ctas, num_sms, per_sm, *out);
 }
@@ -571,17 +621,22 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
     prob.N = N;
     prob.K = K;
     prob.groups = 1;
+    TileCfg tc;
+    rc = problem_tile(prob, tc);
+    if (rc) return rc;
     sk::KernelParams kp;
     memset(&kp, 0, sizeof(kp));
+    // Each CTA stages 128 rows of A and tile_n / cg rows of B per step.
     rc = encode_2d(&kp.tmap_a, A, 2, K, M, lda * 2, 64, 128);
     if (rc) return rc;
-    rc = encode_2d(&kp.tmap_b, B, 2, K, N, ldb * 2, 64, static_cast<uint32_t>(sk::kTileN));
+    rc = encode_2d(&kp.tmap_b, B, 2, K, N, ldb * 2, 64, static_cast<uint32_t>(tc.tn / tc.cg));
     if (rc) return rc;
     kp.c = C;
     kp.ldc = ldc;
     kp.c_dtype = c_dtype;
     const uint32_t fmt = ab_dtype == SK_BF16 ? 1u : 0u;
-    kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, static_cast<uint32_t>(sk::kTileN));
+    kp.idesc = sk::make_idesc(fmt, fmt, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
+                              static_cast<uint32_t>(tc.tn));
     return run(prob, streamk, reduction, ctas, kp, C, ldc * cs, M, N * cs, ws, ws_bytes, st);
 }
 
@@ -610,18 +665,22 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
     prob.N = N;
     prob.K = K;
     prob.groups = 1;
+    TileCfg tc;
+    rc = problem_tile(prob, tc);
+    if (rc) return rc;
     sk::KernelParams kp;
     memset(&kp, 0, sizeof(kp));
     rc = encode_2d(&kp.tmap_a, A8, 1, K, M, K, 128, 128);
     if (rc) return rc;
-    rc = encode_2d(&kp.tmap_b, B8, 1, K, N, K, 128, static_cast<uint32_t>(sk::kTileN));
+    rc = encode_2d(&kp.tmap_b, B8, 1, K, N, K, 128, static_cast<uint32_t>(tc.tn / tc.cg));
     if (rc) return rc;
     kp.c = C_bf16;
     kp.ldc = ldc;
     kp.c_dtype = SK_BF16;
     kp.sa = sa;
     kp.sb = sb;
-    kp.idesc = sk::make_idesc(0, 0, false, false, 128, static_cast<uint32_t>(sk::kTileN));
+    kp.idesc = sk::make_idesc(0, 0, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
+                              static_cast<uint32_t>(tc.tn));
     return run(prob, streamk, reduction, ctas, kp, C_bf16, ldc * 2, M, N * 2, ws, ws_bytes,
                static_cast<cudaStream_t>(stream));
 }

@@ -21,6 +21,18 @@
 //
 // Logical CTA ids come from a ticket counter, so a CTA only ever waits on CTAs with larger ids,
 // which started after it; every wait is bounded and records an error instead of hanging.
+//
+// CG = 2 runs each logical CTA as a cluster of two CTAs on neighbouring SMs (a "pair") that
+// computes a 256 x TN tile with the two-SM tensor-core instruction (tcgen05 cta_group::2): each CTA
+// stages its 128 rows of A and TN/2 of the TN rows of B, so one SM takes in fewer operand bytes
+// per MMA cycle than with a 128 x 128 tile (24 KB per 256 cycles for TN = 128, 32 KB per 512
+// cycles for TN = 256, against 32 KB per 256). The even CTA issues the MMAs and its commits arrive
+// on the barriers of both CTAs; both CTAs' producers count their bytes on the even CTA's stage
+// barrier. Each CTA's epilogue owns its 128 accumulator rows, and for the fixups each half of a
+// pair acts as a CTA of its own: partial slot and flag (pair * 2 + rank), scratch half
+// (tile * 2 + rank).
+#include <stddef.h>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -51,24 +63,36 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 struct Cfg {
+    static_assert(CG == 1 || (CG == 2 && OP != kOpWgrad16), "CTA pairs serve the GEMMs only");
+    static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
     static constexpr int kElem = OP == kOpFp8 ? 1 : 2;
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
+    static constexpr int kTileMAll = kTileM * CG;          // tile rows of the CTA (pair)
+    static constexpr int kBRows = TN / CG;                 // B rows this CTA stages
     static constexpr int kABytes = kTileM * 128;           // 16 KB
-    static constexpr int kBBytes = TN * 128;
+    static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = 7;   // 7 x 32 KB: the most that fits in 227 KB with the control words
-    static constexpr int kTmemCols = 2 * TN;               // double-buffered fp32 accumulator
+    // One CTA per SM: 7 x 32 KB, the most that fits in 227 KB with the control words. Pairs:
+    // about 96 KB of stages (4 x 24 KB for a 256 x 128 tile, 3 x 32 KB for 256 x 256), so that
+    // two CTAs could share an SM.
+    static constexpr int kStages = CG == 1 ? 7 : (TN == 128 ? 4 : 3);
+    static constexpr int kMinBlocks = CG == 1 ? 1 : 2;
+    // fp32 accumulator buffers in TMEM: two (the epilogue of one segment overlaps the MMAs of the
+    // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
+    static constexpr int kAccBufs = TN == 256 ? 1 : 2;
+    static constexpr int kTmemCols = kAccBufs * TN;
     static constexpr int kMmaK = OP == kOpFp8 ? 32 : 16;
     static constexpr int kMmasPerStage = TK / kMmaK;
-    // The owner's fold stages partial tiles through the (then idle) operand ring in 64 KB units
-    // (128 rows x 128 fp32 columns, contiguous in the fragment-major layout).
-    static constexpr int kFoldUnitChunks = 4;                       // 32-column chunks per unit
+    // The owner's fold stages partial tiles through the (then idle) operand ring in units of
+    // 128 rows x (32 x kFoldUnitChunks) fp32 columns, contiguous in the fragment-major layout:
+    // 64 KB with one CTA per SM, 32 KB in the smaller ring of a pair.
+    static constexpr int kFoldUnitChunks = CG == 1 ? 4 : 2;          // 32-column chunks per unit
     static constexpr int kFoldUnitBytes = kTileM * 32 * 4 * kFoldUnitChunks;
     static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
-    static_assert((TN / 32) % kFoldUnitChunks == 0, "tile N must be a multiple of 128");
+    static_assert((TN / 32) % kFoldUnitChunks == 0, "tile N must be a multiple of the fold unit");
     static constexpr int kRingBytes = kStages * kStageBytes;   // a multiple of 1024
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (2 * kStages + 4 + kFoldBufs) * 8;
@@ -115,12 +139,19 @@ __device__ __forceinline__ void wgrad_slabs(const ConvGeom& cg, int64_t g, int64
     }
 }
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
                                             int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
-                                            uint32_t bar, const WgradSlabs<TN>& sl) {
-    using C = Cfg<OP, TN>;
-    if constexpr (OP != kOpWgrad16) {
+                                            uint32_t bar, const WgradSlabs<TN>& sl, uint32_t rank) {
+    using C = Cfg<OP, TN, CG>;
+    if constexpr (CG == 2) {
+        // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
+        const int32_t kx = static_cast<int32_t>(k * C::TK);
+        tma_load_2d_pair(a_dst, &P.tmap_a, bar, kx,
+                         static_cast<int32_t>(mt * C::kTileMAll + rank * kTileM));
+        tma_load_2d_pair(b_dst, &P.tmap_b, bar, kx,
+                         static_cast<int32_t>(nt * TN + rank * C::kBRows));
+    } else if constexpr (OP != kOpWgrad16) {
         const int32_t kx = static_cast<int32_t>(k * C::TK);
         tma_load_2d(a_dst, &P.tmap_a, bar, kx, static_cast<int32_t>(mt * kTileM));
         tma_load_2d(b_dst, &P.tmap_b, bar, kx, static_cast<int32_t>(nt * TN));
@@ -161,10 +192,10 @@ __device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool 
     return rot;
 }
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
-                             volatile SmemCtl* ctl) {
-    using C = Cfg<OP, TN>;
+                             volatile SmemCtl* ctl, uint32_t rank) {
+    using C = Cfg<OP, TN, CG>;
     const sk_plan_t& plan = P.plan;
     SegCursor cur;
     seg_init(plan, cta, cur);
@@ -191,9 +222,17 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(full, C::kStageBytes);
             const uint32_t a_dst = ring + stage * C::kStageBytes;
-            issue_loads<OP, TN>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs);
+            if constexpr (CG == 2) {
+                // Both CTAs' bytes are counted on the even CTA's barrier, which expects them all.
+                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::kStageBytes);
+                issue_loads<OP, TN, CG>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
+                                        mapa_shared(full, 0), slabs, rank);
+            } else {
+                mbar_arrive_expect_tx(full, C::kStageBytes);
+                issue_loads<OP, TN, CG>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs,
+                                        rank);
+            }
             ++issued;
             if (++stage == C::kStages) {
                 stage = 0;
@@ -201,7 +240,19 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
             }
         }
     }
-    if (!ok) {
+    if constexpr (CG == 2) {
+        // The copies of a pair complete on the even CTA's barriers, so this CTA waits until the
+        // MMAs have consumed its last stages (their commits arrive here too): then nothing is
+        // still in flight into this CTA's shared memory, nor any commit on its way to it.
+        for (int i = 0; i < C::kStages && i < issued; ++i) {
+            if (stage == 0) {
+                stage = C::kStages;
+                phase ^= 1;
+            }
+            --stage;
+            mbar_wait(bars + (C::kStages + stage) * 8, phase, 10000000ull);
+        }
+    } else if (!ok) {
         // Let the copies already in flight land before the CTA can exit.
         for (int i = 0; i < C::kStages && i < issued; ++i) {
             if (stage == 0) {
@@ -218,17 +269,16 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
 // MMA issuer
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                         uint32_t tmem_base, volatile SmemCtl* ctl) {
-    using C = Cfg<OP, TN>;
+    using C = Cfg<OP, TN, CG>;
     const sk_plan_t& plan = P.plan;
     SegCursor cur;
     seg_init(plan, cta, cur);
     sk_segment_t seg;
     uint32_t stage = 0, phase = 0;
     int64_t nseg = 0;
-    uint32_t last_empty = 0, last_parity = 0;
     int64_t total_commits = 0;
     bool any = false, ok = true;
     while (true) {
@@ -236,11 +286,14 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
         (void)dp;
         const int64_t len = seg.k_end - seg.k_begin;
-        const uint32_t acc = static_cast<uint32_t>(nseg & 1);
-        const uint32_t acc_phase = static_cast<uint32_t>((nseg >> 1) & 1);
+        const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
+        const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
         const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
         const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
-        if (!mbar_wait(tempty, acc_phase ^ 1, P.mbar_timeout_ns) || ctl->abort) {
+        // A pair's accumulator is free once the epilogues of both CTAs have released it.
+        const bool free_acc = CG == 2 ? mbar_wait_cluster(tempty, acc_phase ^ 1, P.mbar_timeout_ns)
+                                      : mbar_wait(tempty, acc_phase ^ 1, P.mbar_timeout_ns);
+        if (!free_acc || ctl->abort) {
             record_error(kErrPipeline, cta, seg.tile, 1);
             ctl->abort = 1;
             break;
@@ -272,29 +325,25 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
                 }
                 const uint32_t accumulate = (j > 0 || kk > 0) ? 1u : 0u;
                 if constexpr (OP == kOpFp8)
-                    mma_f8(d_tmem, ad, bd, P.idesc, accumulate);
+                    mma_f8<CG>(d_tmem, ad, bd, P.idesc, accumulate);
                 else
-                    mma_f16(d_tmem, ad, bd, P.idesc, accumulate);
+                    mma_f16<CG>(d_tmem, ad, bd, P.idesc, accumulate);
             }
-            tc_commit(empty);
+            tc_commit<CG>(empty);
             ++total_commits;
             any = true;
-            last_empty = empty;
-            last_parity = phase;
             if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1;
             }
         }
         if (!ok) break;
-        tc_commit(tfull);
+        tc_commit<CG>(tfull);
         ++nseg;
     }
     // Before the CTA may exit, every commit it issued must have landed: the last commit of each
     // stage of the ring is awaited, so that no arrival can reach this SM's shared memory after the
     // CTA is gone (the next CTA there may lay it out differently).
-    (void)last_empty;
-    (void)last_parity;
     if (any) {
         int64_t n = total_commits < C::kStages ? total_commits : C::kStages;
         uint32_t st = stage, ph = phase;
@@ -307,6 +356,11 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
             mbar_wait(bars + (C::kStages + st) * 8, ph, 10000000ull);
         }
     }
+    if (nseg > 0) {   // and the last accumulator commit
+        const int64_t last = nseg - 1;
+        mbar_wait(bars + (2 * C::kStages + last % C::kAccBufs) * 8,
+                  static_cast<uint32_t>((last / C::kAccBufs) & 1), 10000000ull);
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -318,6 +372,7 @@ struct EpiCtx {
     bool row_ok;           // m < gemm_m
     int64_t n_base;        // first GEMM-view column of the tile
     int row;               // accumulator row 0..127
+    int64_t half;          // CG = 2: rank of this CTA in its pair (which 128 rows of the tile); else 0
     float row_scale;       // fp8: sa[out_row]; else 1
 };
 
@@ -409,11 +464,11 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32]) {
 // in the owner's TMEM accumulator. Per element the additions run in sender order, so the result
 // does not depend on timing. Only the owner segment, always a CTA's last, takes this path: by then
 // every stage of the ring has been consumed.
-template <int OP, int TN, typename SenderFn>
+template <int OP, int TN, int CG, typename SenderFn>
 __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
                             const EpiCtx& e, uint32_t t_acc, int ethread, int64_t ns,
                             SenderFn sender, uint32_t ring, uint32_t fold_bars) {
-    using C = Cfg<OP, TN>;
+    using C = Cfg<OP, TN, CG>;
     constexpr int kChunks = TN / 32;
     constexpr int kUnitsPerSender = kChunks / C::kFoldUnitChunks;
     const int64_t units = ns * kUnitsPerSender;   // sender-major
@@ -426,7 +481,7 @@ __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment
             record_error(kErrBounds, cta, seg.tile, slot);
             return;
         }
-        const float* src = P.partials + slot * static_cast<int64_t>(kTileM * TN) +
+        const float* src = P.partials + (slot * CG + e.half) * static_cast<int64_t>(kTileM * TN) +
                            h * (kTileM * 32 * C::kFoldUnitChunks);
         mbar_arrive_expect_tx(bar, C::kFoldUnitBytes);
         bulk_copy_g2s(ring + buf * C::kFoldUnitBytes, src, C::kFoldUnitBytes, bar);
@@ -474,7 +529,7 @@ __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment
     }
 }
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
                                  const EpiCtx& e, uint32_t t_acc, int ethread, uint32_t ring,
                                  uint32_t fold_bars) {
@@ -512,7 +567,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         return;
     }
     if (red == SK_WORKSPACE) {
-        float* base = P.scratch + seg.tile * static_cast<int64_t>(kTileM * TN);
+        float* base = P.scratch + (seg.tile * CG + e.half) * static_cast<int64_t>(kTileM * TN);
         for (int ch = 0; ch < kChunks; ++ch) {
             float v[32];
             load_acc(t_acc + ch * 32, v);
@@ -543,7 +598,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         uint64_t t0 = 0;
         bool late = false;
         for (int64_t i = 0; i < ns && !late; ++i) {
-            const uint32_t* f = P.flags + seg.first_cta + sender(i);
+            const uint32_t* f = P.flags + (seg.first_cta + sender(i)) * CG + e.half;
             while (ld_acquire_gpu(f) != 1u) {
                 if (t0 == 0) t0 = globaltimer_ns();
                 if (globaltimer_ns() - t0 > P.flag_timeout_ns) {
@@ -556,10 +611,10 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         }
     }
     named_bar_sync(kEpiBarrier, kEpiThreads);
-    if (ns > 0) (void)ld_acquire_gpu(P.flags + seg.first_cta + sender(ns - 1));
+    if (ns > 0) (void)ld_acquire_gpu(P.flags + (seg.first_cta + sender(ns - 1)) * CG + e.half);
 
     if (seg.kind == SK_SEG_OWNER && ns > 0) {
-        staged_fold<OP, TN>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
+        staged_fold<OP, TN, CG>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
         return;
     }
 
@@ -568,13 +623,13 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         if (ethread == 0) record_error(kErrBounds, cta, seg.tile, -2);
         publish = false;
     }
-    float* own = P.partials + cta * static_cast<int64_t>(kTileM * TN);
+    float* own = P.partials + (cta * CG + e.half) * static_cast<int64_t>(kTileM * TN);
     for (int ch = 0; ch < kChunks; ++ch) {
         float v[32];
         load_acc(t_acc + ch * 32, v);
         for (int64_t s = 0; s < ns; ++s) {
-            const float* src =
-                P.partials + (seg.first_cta + sender(s)) * static_cast<int64_t>(kTileM * TN);
+            const float* src = P.partials + ((seg.first_cta + sender(s)) * CG + e.half) *
+                                                static_cast<int64_t>(kTileM * TN);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 const float4 q = __ldcg(reinterpret_cast<const float4*>(
@@ -598,14 +653,14 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         fence_proxy_async_global();   // a receiver may read this partial with bulk copies
         __threadfence();
         named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (ethread == 0) st_release_gpu(P.flags + cta, 1u);
+        if (ethread == 0) st_release_gpu(P.flags + cta * CG + e.half, 1u);
     }
 }
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
-                             uint32_t tmem_base, int warp, volatile SmemCtl* ctl) {
-    using C = Cfg<OP, TN>;
+                             uint32_t tmem_base, int warp, volatile SmemCtl* ctl, uint32_t rank) {
+    using C = Cfg<OP, TN, CG>;
     const sk_plan_t& plan = P.plan;
     const int lane = static_cast<int>(threadIdx.x & 31);
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
@@ -616,8 +671,8 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     sk_segment_t seg;
     int64_t nseg = 0;
     while (seg_next(plan, cta, cur, seg)) {
-        const uint32_t acc = static_cast<uint32_t>(nseg & 1);
-        const uint32_t acc_phase = static_cast<uint32_t>((nseg >> 1) & 1);
+        const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
+        const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
         const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
         const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
         // One thread waits (bounded) and the verdict goes to all 128 epilogue threads through a
@@ -638,18 +693,25 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         tile_coords(plan, seg.tile, g, mt, nt);
         EpiCtx e;
         e.row = row;
-        const int64_t m = mt * kTileM + row;
+        e.half = static_cast<int64_t>(rank);
+        const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
         e.row_ok = m < plan.gemm_m;
         e.out_row = g * plan.gemm_m + m;
         e.n_base = nt * TN;
         e.row_scale = 1.0f;
         if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
-        epilogue_segment<OP, TN>(P, cta, seg, e, t_acc, ethread, ring,
-                                 bars + (2 * C::kStages + 4) * 8);
+        epilogue_segment<OP, TN, CG>(P, cta, seg, e, t_acc, ethread, ring,
+                                     bars + (2 * C::kStages + 4) * 8);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty);
+        if (lane == 0) {
+            // A pair's accumulator-empty barrier lives in the even CTA, whose thread issues the MMAs.
+            if (CG == 2 && rank != 0)
+                mbar_arrive_cluster(mapa_shared(tempty, 0));
+            else
+                mbar_arrive(tempty);
+        }
         ++nseg;
     }
 }
@@ -658,9 +720,10 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
 // kernel
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN>
-__global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_constant__ KernelParams P) {
-    using C = Cfg<OP, TN>;
+template <int OP, int TN, int CG>
+__global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG>::kMinBlocks)
+    sk_main_kernel(const __grid_constant__ KernelParams P) {
+    using C = Cfg<OP, TN, CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -669,10 +732,14 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
     volatile SmemCtl* ctl = reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes);
     const uint32_t bars = ring + C::kRingBytes + C::kCtlBytes;
     const int warp = static_cast<int>(threadIdx.x >> 5);
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const uint32_t ctl_addr = smem_u32(const_cast<SmemCtl*>(ctl));
 
+    uint32_t ticket = 0;
     if (threadIdx.x == 0) {
-        // Take the ticket first: its round trip to L2 overlaps the barrier set-up below.
-        const uint32_t ticket = atomicAdd(P.control, 1u);
+        // Take the ticket first: its round trip to L2 overlaps the barrier set-up below. A pair
+        // takes one ticket, in its even CTA.
+        if (rank == 0) ticket = atomicAdd(P.control, 1u);
         // The allocation below overwrites this; whatever a previous kernel left in shared memory
         // can never be taken for a TMEM address.
         ctl->tmem_base = kTmemSentinel;
@@ -681,50 +748,74 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
             mbar_init(bars + (C::kStages + s) * 8, 1);     // empty: MMA commit
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(bars + (2 * C::kStages + a) * 8, 1);              // accumulator full
-            mbar_init(bars + (2 * C::kStages + 2 + a) * 8, kEpiThreads / 32);  // accumulator empty
+            mbar_init(bars + (2 * C::kStages + a) * 8, 1);                   // accumulator full
+            mbar_init(bars + (2 * C::kStages + 2 + a) * 8, CG * kEpiThreads / 32);  // ... empty
         }
         for (int f = 0; f < C::kFoldBufs; ++f)
             mbar_init(bars + (2 * C::kStages + 4 + f) * 8, 1);   // owner's fold buffers
         fence_mbarrier_init();
         ctl->abort = 0;
-        ctl->cta = static_cast<long long>(ticket);
+        if (CG == 1) ctl->cta = static_cast<long long>(ticket);
         tma_prefetch_desc(&P.tmap_a);
         tma_prefetch_desc(&P.tmap_b);
     }
-    __syncthreads();   // the sentinel is in place before the allocation writes the slot
+    if constexpr (CG == 2) {
+        // Both CTAs of the pair have started and initialised their barriers; then the even CTA
+        // hands its ticket to both.
+        cluster_sync();
+        if (threadIdx.x == 0 && rank == 0) {
+            const uint32_t cta_off = ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, cta));
+            st_shared_cluster_u64(mapa_shared(cta_off, 0), ticket);
+            st_shared_cluster_u64(mapa_shared(cta_off, 1), ticket);
+        }
+    } else {
+        __syncthreads();   // the sentinel is in place before the allocation writes the slot
+    }
     if (warp == 1) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(&ctl->tmem_base)), C::kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)),
+                       C::kTmemCols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int64_t cta = ctl->cta;
     // Every thread reads the same slot, so the whole CTA takes this exit together. It is never
-    // expected; it keeps a bad slot from ever reaching a TMEM access.
-    if (tmem_base == kTmemSentinel || (tmem_base >> 16) != 0 ||
-        (tmem_base & 0xFFFFu) + C::kTmemCols > 512u) {
+    // expected; it keeps a bad slot from ever reaching a TMEM access. A pair takes the verdict
+    // of both its slots, so that both CTAs leave together.
+    auto bad_slot = [](uint32_t t) {
+        return t == kTmemSentinel || (t >> 16) != 0 || (t & 0xFFFFu) + C::kTmemCols > 512u;
+    };
+    bool bad = bad_slot(tmem_base);
+    if constexpr (CG == 2) {
+        const uint32_t peer = ld_shared_cluster_u32(
+            mapa_shared(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)), rank ^ 1u));
+        bad = bad || bad_slot(peer) || peer != tmem_base;
+        cluster_sync();   // the peer's slot has been read before either CTA can leave
+    }
+    if (bad) {
         if (threadIdx.x == 0) record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
         return;
     }
 
     if (warp == 0) {
-        if (elect_one()) run_producer<OP, TN>(P, cta, ring, bars, ctl);
+        if (elect_one()) run_producer<OP, TN, CG>(P, cta, ring, bars, ctl, rank);
         __syncwarp();
     } else if (warp == 1) {
-        if (elect_one()) run_mma<OP, TN>(P, cta, ring, bars, tmem_base, ctl);
+        if (rank == 0 && elect_one()) run_mma<OP, TN, CG>(P, cta, ring, bars, tmem_base, ctl);
         __syncwarp();
     } else {
-        run_epilogue<OP, TN>(P, cta, ring, bars, tmem_base, warp, ctl);
+        run_epilogue<OP, TN, CG>(P, cta, ring, bars, tmem_base, warp, ctl, rank);
     }
 
     tc_fence_before();
-    __syncthreads();
+    // A pair leaves together: no arrival or shared-memory access of one CTA can reach the other
+    // after it has gone.
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc<CG>(tmem_base, C::kTmemCols);
     }
 }
 
@@ -735,8 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1) sk_main_kernel(const __grid_const
 constexpr int kStage2Threads = 256;
 
 // Grid (shared-tile candidates, tile float4s / 256): one float4 of fp32 scratch per thread, read in
-// the fragment-major order the fixup wrote it.
-template <int TN>
+// the fragment-major order the fixup wrote it. A pair tile (CG = 2) is two such 128-row halves.
+template <int TN, int CG>
 __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_constant__ Stage2Params P) {
     const sk_plan_t& plan = P.plan;
     const int64_t t = blockIdx.x;
@@ -746,11 +837,13 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     int64_t g, mt, nt;
     tile_coords(plan, t, g, mt, nt);
     const int idx = static_cast<int>(blockIdx.y) * kStage2Threads + static_cast<int>(threadIdx.x);
-    const int q4 = idx / kTileM, row = idx - q4 * kTileM;
-    const int64_t m = mt * kTileM + row;
+    constexpr int kHalf = kTileM * TN / 4;   // float4s of one 128-row half
+    const int half = idx / kHalf, r = idx - half * kHalf;
+    const int q4 = r / kTileM, row = r - q4 * kTileM;
+    const int64_t m = mt * (kTileM * CG) + half * kTileM + row;
     const int64_t n0 = nt * TN + q4 * 4;
     if (m >= plan.gemm_m || n0 >= plan.gemm_n) return;
-    const float* base = P.scratch + t * static_cast<int64_t>(kTileM * TN);
+    const float* base = P.scratch + t * static_cast<int64_t>(kTileM * CG * TN);
     const float4 q = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4));
     float v[4] = {q.x, q.y, q.z, q.w};
     const int64_t out_row = g * plan.gemm_m + m;
@@ -793,22 +886,39 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
 // host-side launch helpers
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 static int launch_main_t(const KernelParams& p, cudaStream_t stream) {
-    using C = Cfg<OP, TN>;
-    auto kern = sk_main_kernel<OP, TN>;
+    using C = Cfg<OP, TN, CG>;
+    auto kern = sk_main_kernel<OP, TN, CG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmem));
     if (e != cudaSuccess) return static_cast<int>(e);
     if (p.plan.grid <= 0) return 0;
-    kern<<<dim3(static_cast<unsigned>(p.plan.grid)), dim3(kThreads), C::kSmem, stream>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    if constexpr (CG == 1) {
+        kern<<<dim3(static_cast<unsigned>(p.plan.grid)), dim3(kThreads), C::kSmem, stream>>>(p);
+        return static_cast<int>(cudaGetLastError());
+    } else {
+        // One cluster of two CTAs per logical CTA.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.plan.grid * CG));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CG;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return static_cast<int>(cudaLaunchKernelEx(&cfg, kern, p));
+    }
 }
 
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 static int ctas_per_sm_t() {
-    using C = Cfg<OP, TN>;
-    auto kern = sk_main_kernel<OP, TN>;
+    using C = Cfg<OP, TN, CG>;
+    auto kern = sk_main_kernel<OP, TN, CG>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
         return 0;
@@ -818,30 +928,43 @@ static int ctas_per_sm_t() {
     return n;
 }
 
-#define SK_DISPATCH(op, fn, ...)                                                            \
-    ((op) == kOpGemm16 ? fn<kOpGemm16, kTileN>(__VA_ARGS__)                                 \
-     : (op) == kOpFp8  ? fn<kOpFp8, kTileN>(__VA_ARGS__)                                    \
-                       : fn<kOpWgrad16, kTileN>(__VA_ARGS__))
-
-template <int OP, int TN>
+template <int OP, int TN, int CG>
 static size_t smem_bytes_t() {
-    return Cfg<OP, TN>::kSmem;
+    return Cfg<OP, TN, CG>::kSmem;
 }
 
-size_t main_smem_bytes(int op) { return SK_DISPATCH(op, smem_bytes_t); }
+// (op, cg, tn) -> the kernel instantiation; wgrad has no pair form (the host rejects it first).
+#define SK_DISPATCH(op, cg, tn, fn, ...)                                                    \
+    ((cg) == 2 ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2>(__VA_ARGS__)             \
+                                                : fn<kOpGemm16, 256, 2>(__VA_ARGS__))         \
+                              : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2>(__VA_ARGS__)             \
+                                                : fn<kOpGemm16, 128, 2>(__VA_ARGS__)))        \
+     : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1>(__VA_ARGS__)                                 \
+     : (op) == kOpFp8    ? fn<kOpFp8, 128, 1>(__VA_ARGS__)                                    \
+                         : fn<kOpWgrad16, 128, 1>(__VA_ARGS__))
 
-int main_ctas_per_sm(int op) { return SK_DISPATCH(op, ctas_per_sm_t); }
+size_t main_smem_bytes(int op, int cg, int tn) { return SK_DISPATCH(op, cg, tn, smem_bytes_t); }
 
-int launch_main(const KernelParams& p, int op, cudaStream_t stream) {
-    return SK_DISPATCH(op, launch_main_t, p, stream);
+int main_ctas_per_sm(int op, int cg, int tn) { return SK_DISPATCH(op, cg, tn, ctas_per_sm_t); }
+
+int launch_main(const KernelParams& p, int op, int cg, int tn, cudaStream_t stream) {
+    if (cg == 2 && op == kOpWgrad16) return static_cast<int>(cudaErrorInvalidValue);
+    return SK_DISPATCH(op, cg, tn, launch_main_t, p, stream);
 }
 
 int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
-    const unsigned slices = static_cast<unsigned>(kTileM * kTileN / 4 / kStage2Threads);
-    sk_stage2_kernel<kTileN><<<dim3(static_cast<unsigned>(tiles), slices), dim3(kStage2Threads), 0,
-                               stream>>>(p);
+    const int cg = p.plan.tm == 2 * kTileM ? 2 : 1;
+    const int tn = p.plan.tn == 256 ? 256 : 128;
+    const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
+    const dim3 grid(static_cast<unsigned>(tiles), slices);
+    if (cg == 2 && tn == 256)
+        sk_stage2_kernel<256, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    else if (cg == 2)
+        sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    else
+        sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

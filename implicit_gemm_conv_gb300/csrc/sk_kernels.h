@@ -63,12 +63,14 @@ struct Stage2Params {
     int32_t c_dtype;
 };
 
-// Dynamic shared memory of the main kernel for an op.
-size_t main_smem_bytes(int op);
+// cg: 1 = one CTA per 128 x 128 tile; 2 = a cluster of two CTAs per 256 x tn tile, tn 128 or 256
+// (GEMMs only). Dynamic shared memory of one CTA of the main kernel.
+size_t main_smem_bytes(int op, int cg, int tn);
 // How many CTAs of the main kernel fit on one SM (0 if the device query fails).
-int main_ctas_per_sm(int op);
-// Launch the main kernel with grid = p.plan.grid. Returns a cudaError_t value.
-int launch_main(const KernelParams& p, int op, cudaStream_t stream);
+int main_ctas_per_sm(int op, int cg, int tn);
+// Launch the main kernel: p.plan.grid logical CTAs, each one CTA (cg 1) or one cluster of two
+// (cg 2). Returns a cudaError_t value.
+int launch_main(const KernelParams& p, int op, int cg, int tn, cudaStream_t stream);
 // Launch the Stage-2 reduce over the shared tiles of a workspace plan.
 int launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Read and clear the device error record: returns the code (0 = none) and fills info[3].

@@ -44,8 +44,8 @@
  *    the control block and the scratch (and, for SK_ATOMIC, the output) on `stream` before every
  *    launch; partial tiles are never zeroed.
  *  - Concurrent calls that share one workspace must be ordered on one stream.
- *  - Tiles are 128 x 128 (M x N); the reduction step is 64 elements for 16-bit inputs and 128 for
- *    fp8.
+ *  - Tiles are 128 x 128 (M x N), or 256 x 128 / 256 x 256 for a CTA pair (sk_set_tile); the
+ *    reduction step is 64 elements for 16-bit inputs and 128 for fp8.
  */
 #ifndef SKGEMM_H
 #define SKGEMM_H
@@ -102,7 +102,7 @@ typedef struct sk_plan_t {
     int64_t max_contributors;        /* most CTAs sharing one tile                              */
     int64_t tree_rounds;             /* ceil(log2(max_contributors))                            */
     int64_t shared_tiles;            /* tiles with more than one contributor                   */
-    int64_t flag_bytes;              /* round_up(4 * publishers, 256)                           */
+    int64_t flag_bytes;              /* round_up(4 * publishers * tm / 128, 256)                */
     int64_t control_offset;          /* = flag_bytes; 256-byte control block (ticket counter)  */
     int64_t partial_offset, partial_bytes;   /* linear/tree: publishers * tm * tn * 4          */
     int64_t scratch_offset, scratch_bytes;   /* workspace: (SK tiles) * tm * tn * 4            */
@@ -216,6 +216,24 @@ const char* sk_last_error(void);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int sk_version(void);
+
+/*
+ * Tile shape for the later calls of the calling thread, planning calls included. (No counterpart on
+ * the pages, whose tiles are one workgroup's; this is a GB300 kernel choice.)
+ *  SK_TILE_AUTO (the default): currently the 128 x 128 tile.
+ *  SK_TILE_128: one CTA computes each 128 x 128 output tile.
+ *  SK_TILE_256_PAIR: a cluster of two CTAs on neighbouring SMs computes each 256 x 128 tile with the
+ *    two-SM tensor-core instruction; each CTA stages its 128 rows of A and 64 of the 128 rows of B,
+ *    which cuts the operand bytes each SM takes in per MMA by a quarter.
+ *  SK_TILE_256x256_PAIR: the same with 256 x 256 tiles; each CTA stages 128 rows of A and 128 of B,
+ *    half the bytes per MMA of the 128 x 128 tile.
+ *  For the pair tiles the stream-K partition is the same algorithm over the pair tiles, and its CTA
+ *  pool `ctas` counts pairs (the default pool is resolved over SMs / 2). GEMM and fp8 GEMM only:
+ *  the wgrad call returns -2.
+ * Returns the previous setting, or -2 for an unknown value.
+ */
+enum { SK_TILE_AUTO = 0, SK_TILE_128 = 1, SK_TILE_256_PAIR = 2, SK_TILE_256x256_PAIR = 3 };
+int sk_set_tile(int tile);
 
 /*
  * Instrumentation (no counterpart on the pages; used by the benchmark to time the main kernel

@@ -29,7 +29,9 @@ Readings where the pages are silent (each is listed in the design notes):
   ``off``: one CTA per tile over the whole reduction.
 * Split-K comparator: ``s = clamp(P // T, 1, I)`` slices per tile, slice ``j`` covering
   iterations ``[j*I//s, (j+1)*I//s)``.
-* Flag table: one 32-bit flag per CTA that can publish, rounded up to 256 bytes.
+* Flag table: one 32-bit flag per CTA that can publish, rounded up to 256 bytes. When a logical CTA
+  is a cluster of ``cluster`` CTAs that each hand on their own rows of the tile, each of those CTAs
+  has its flag: ``4 * publishers * cluster`` bytes.
 """
 from __future__ import annotations
 
@@ -99,7 +101,7 @@ def default_pool(reduction: int, num_sms: int, ctas_per_sm: int) -> int:
 
 
 def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn: int, tk: int,
-              pool: int, mode: int, reduction: int) -> Plan:
+              pool: int, mode: int, reduction: int, cluster: int = 1) -> Plan:
     """Steps 1-8 of the partition, in order."""
     # 1. tile and iteration counts
     T = groups * tiles_m * tiles_n
@@ -147,7 +149,7 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
     while (1 << p.rounds) < mc:
         p.rounds += 1
     # 8. workspace: [flags][control][partials | scratch]
-    p.flag_bytes = round_up(4 * p.publishers, 256)
+    p.flag_bytes = round_up(4 * p.publishers * cluster, 256)
     tile_bytes = tm * tn * 4
     if reduction in (LINEAR, TREE):
         p.partial_bytes = p.publishers * tile_bytes

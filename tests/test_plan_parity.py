@@ -22,10 +22,11 @@ FIELD_MAP = {  # C name -> oracle name
 }
 
 
-def compare(prob, oracle_kw, mode, red, ctas, num_sms=148, check_ctas=None):
+def compare(prob, oracle_kw, mode, red, ctas, num_sms=148, check_ctas=None, cluster=1):
     cp = sk.sk_plan(prob, mode[0], red[0], ctas, num_sms)
-    pool = ctas if ctas > 0 else P.default_pool(red[1], num_sms, 1)
-    op = P.make_plan(pool=pool, mode=mode[1], reduction=red[1], **oracle_kw)
+    # a pair kernel's default pool is resolved over SM pairs
+    pool = ctas if ctas > 0 else P.default_pool(red[1], num_sms // cluster, 1)
+    op = P.make_plan(pool=pool, mode=mode[1], reduction=red[1], cluster=cluster, **oracle_kw)
     for c, o in FIELD_MAP.items():
         assert getattr(cp, c) == getattr(op, o), (c, getattr(cp, c), getattr(op, o))
     if mode[1] == P.SPLITK:
@@ -40,11 +41,11 @@ def compare(prob, oracle_kw, mode, red, ctas, num_sms=148, check_ctas=None):
     return cp
 
 
-def gemm(M, N, K, ab="f16"):
+def gemm(M, N, K, ab="f16", tm=128, tn=128):
     tk = 128 if ab == "e4m3" else 64
     prob = sk.make_problem("fp8" if ab == "e4m3" else "gemm", ab_dtype=ab,
                            c_dtype="bf16" if ab == "e4m3" else ab, M=M, N=N, K=K)
-    kw = dict(tiles_m=-(-M // 128), tiles_n=-(-N // 128), groups=1, kred=K, tm=128, tn=128, tk=tk)
+    kw = dict(tiles_m=-(-M // tm), tiles_n=-(-N // tn), groups=1, kred=K, tm=tm, tn=tn, tk=tk)
     return prob, kw
 
 
@@ -138,3 +139,57 @@ def test_plan_rejections():
     empty, _ = gemm(0, 256, 4096)
     with pytest.raises(sk.SkError, match="empty"):
         sk.sk_plan(empty, "dp_sk", "linear", 3, 148)
+
+
+# ---- CTA-pair tiles: the same partition over pair tiles, pool in pairs, a flag per CTA
+
+PAIR_TILES = [("256_pair", 128), ("256x256_pair", 256)]
+PAIR_NAMED = [
+    ("gemm 3840x4096x4096", (3840, 4096, 4096, "bf16"), 148),
+    ("gemm 3840x4096x4096 pool 74", (3840, 4096, 4096, "bf16"), 74),
+    ("gemm 512x512x65536", (512, 512, 65536, "bf16"), 148),
+    ("fp8 8192^3", (8192, 8192, 8192, "e4m3"), -1),
+    ("gemm 300x392x520", (300, 392, 520, "bf16"), 5),
+]
+
+
+@pytest.mark.parametrize("tile,tn", PAIR_TILES, ids=[t[0] for t in PAIR_TILES])
+@pytest.mark.parametrize("name,shape,ctas", PAIR_NAMED, ids=[n[0] for n in PAIR_NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_pair_tile_plans(tile, tn, name, shape, ctas, mode, red):
+    prob, kw = gemm(*shape, tm=256, tn=tn)
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    with sk.tile(tile):
+        cp = compare(prob, kw, mode, red, ctas, num_sms=152, check_ctas=big, cluster=2)
+    assert (cp.tm, cp.tn) == (256, tn)
+    assert cp.flag_bytes >= 8 * cp.publishers
+
+
+@pytest.mark.parametrize("tile,tn", PAIR_TILES, ids=[t[0] for t in PAIR_TILES])
+def test_pair_tile_random_sweep(tile, tn):
+    rng = random.Random(23)
+    with sk.tile(tile):
+        for _ in range(200):
+            M, N = rng.randint(1, 1500), rng.randint(1, 1200)
+            K = 8 * rng.randint(1, 400)
+            prob, kw = gemm(M, N, K, tm=256, tn=tn)
+            compare(prob, kw, rng.choice(MODES), rng.choice(REDS),
+                    rng.choice([-1, 1, 2, 3, 5, 74, 148]), num_sms=rng.choice([148, 152, 8]),
+                    cluster=2)
+
+
+def test_pair_tile_setting():
+    prob, _ = gemm(3840, 4096, 4096, "bf16")
+    with sk.tile("128"):
+        assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm == 128
+    with sk.tile("256_pair"):
+        assert (sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm,
+                sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn) == (256, 128)
+        w, _ = wgrad(32, 56, 56, 64, 64, 3, 3, 1, 1, 1)
+        with pytest.raises(sk.SkError, match="GEMMs only"):
+            sk.sk_plan(w, "dp_sk", "linear", -1, 148)
+    with sk.tile("256x256_pair"):
+        assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn == 256
+    with pytest.raises(sk.SkError, match="tile setting"):
+        sk.sk_set_tile(7)
