@@ -189,17 +189,19 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
 // The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
 // (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
 struct TileCfg {
-    int cg, tn;
+    int cg, tn, st;   // CTAs per logical CTA, tile N, operand-ring stages
 };
 int tile_cfg(const View& v, TileCfg& t) {
-    t = {1, sk::kTileN};
+    t = {1, sk::kTileN, 7};
     switch (g_tile) {
         case SK_TILE_128: return SK_OK;
         case SK_TILE_256_PAIR:
         case SK_TILE_256x256_PAIR:
             if (v.op_kind == sk::kOpWgrad16)
                 return fail(SK_ERR_UNSUPPORTED, "the CTA-pair tiles serve the GEMMs only");
-            t = {2, g_tile == SK_TILE_256_PAIR ? 128 : 256};
+            // Rings of about 96 KB, so that two CTAs share an SM and one's epilogue overlaps the
+            // other's mainloop (measured faster than one CTA per SM with twice the stages).
+            t = g_tile == SK_TILE_256_PAIR ? TileCfg{2, 128, 4} : TileCfg{2, 256, 3};
             return SK_OK;
         default:   // SK_TILE_AUTO
             return SK_OK;
@@ -420,7 +422,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
     TileCfg tc;
     rc = tile_cfg(v, tc);
     if (rc) return rc;
-    const int per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn);
+    const int per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn, tc.st);
     sk_plan_t plan;
     rc = build_plan(prob, mode, reduction, ctas, dev.sms, per_sm, plan);
     if (rc) return rc;
@@ -468,7 +470,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
         const int tslot = timing_start(stream);
-        int le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, stream);
+        int le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -551,7 +553,7 @@ int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_s
             TileCfg tc;
             rc = tile_cfg(v, tc);
             if (rc) return rc;
-            per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn);
+            per_sm = sk::main_ctas_per_sm(v.op_kind, tc.cg, tc.tn, tc.st);
         }
     }
     return build_plan(*p, streamk, reduction, ctas, num_sms, per_sm, *out);
@@ -634,6 +636,11 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
     kp.c = C;
     kp.ldc = ldc;
     kp.c_dtype = c_dtype;
+    if (c_dtype != SK_F32) {   // 16-bit C: complete tiles leave through TMA tile stores
+        rc = encode_2d(&kp.tmap_c, C, 2, N, M, ldc * 2, 64, 32);
+        if (rc) return rc;
+        kp.c_tma = 1;
+    }
     const uint32_t fmt = ab_dtype == SK_BF16 ? 1u : 0u;
     kp.idesc = sk::make_idesc(fmt, fmt, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
                               static_cast<uint32_t>(tc.tn));
@@ -677,6 +684,9 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
     kp.c = C_bf16;
     kp.ldc = ldc;
     kp.c_dtype = SK_BF16;
+    rc = encode_2d(&kp.tmap_c, C_bf16, 2, N, M, ldc * 2, 64, 32);
+    if (rc) return rc;
+    kp.c_tma = 1;
     kp.sa = sa;
     kp.sb = sb;
     kp.idesc = sk::make_idesc(0, 0, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),

@@ -63,7 +63,7 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 struct Cfg {
     static_assert(CG == 1 || (CG == 2 && OP != kOpWgrad16), "CTA pairs serve the GEMMs only");
     static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
@@ -74,11 +74,9 @@ struct Cfg {
     static constexpr int kABytes = kTileM * 128;           // 16 KB
     static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    // One CTA per SM: 7 x 32 KB, the most that fits in 227 KB with the control words. Pairs:
-    // about 96 KB of stages (4 x 24 KB for a 256 x 128 tile, 3 x 32 KB for 256 x 256), so that
-    // two CTAs could share an SM.
-    static constexpr int kStages = CG == 1 ? 7 : (TN == 128 ? 4 : 3);
-    static constexpr int kMinBlocks = CG == 1 ? 1 : 2;
+    // ST stages in the ring; two CTAs share an SM when the ring is at most 96 KB.
+    static constexpr int kStages = ST;
+    static constexpr int kMinBlocks = ST * kStageBytes <= 96 * 1024 ? 2 : 1;
     // fp32 accumulator buffers in TMEM: two (the epilogue of one segment overlaps the MMAs of the
     // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
     static constexpr int kAccBufs = TN == 256 ? 1 : 2;
@@ -139,11 +137,11 @@ __device__ __forceinline__ void wgrad_slabs(const ConvGeom& cg, int64_t g, int64
     }
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
                                             int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
                                             uint32_t bar, const WgradSlabs<TN>& sl, uint32_t rank) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     if constexpr (CG == 2) {
         // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
         const int32_t kx = static_cast<int32_t>(k * C::TK);
@@ -192,10 +190,10 @@ __device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool 
     return rot;
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              volatile SmemCtl* ctl, uint32_t rank) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     const sk_plan_t& plan = P.plan;
     SegCursor cur;
     seg_init(plan, cta, cur);
@@ -226,11 +224,11 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
             if constexpr (CG == 2) {
                 // Both CTAs' bytes are counted on the even CTA's barrier, which expects them all.
                 if (rank == 0) mbar_arrive_expect_tx(full, CG * C::kStageBytes);
-                issue_loads<OP, TN, CG>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
+                issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
                                         mapa_shared(full, 0), slabs, rank);
             } else {
                 mbar_arrive_expect_tx(full, C::kStageBytes);
-                issue_loads<OP, TN, CG>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs,
+                issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs,
                                         rank);
             }
             ++issued;
@@ -269,10 +267,10 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
 // MMA issuer
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                         uint32_t tmem_base, volatile SmemCtl* ctl) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     const sk_plan_t& plan = P.plan;
     SegCursor cur;
     seg_init(plan, cta, cur);
@@ -451,12 +449,86 @@ __device__ __forceinline__ float* frag_ptr(float* tile_base, int col0, int i, in
     return tile_base + ((static_cast<int64_t>((col0 + i) >> 2) * kTileM) + row) * 4;
 }
 
-__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr, r);
-    tmem_ld_wait();
+// Calls f(chunk, v) for every 32-column chunk of this thread's accumulator row, in order. Two
+// chunks are read per TMEM round trip (two loads, one wait): the epilogue is bound by these round
+// trips, not by the arithmetic between them.
+template <int kChunks, typename F>
+__device__ __forceinline__ void for_each_chunk(uint32_t t_acc, F&& f) {
+    static_assert(kChunks % 2 == 0, "chunks are read in pairs");
+#pragma unroll 1
+    for (int ch = 0; ch < kChunks; ch += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(t_acc + ch * 32, r0);
+        tmem_ld_32x32b_x32(t_acc + (ch + 1) * 32, r1);
+        tmem_ld_wait();
+        float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = as_f(r[i]);
+        for (int i = 0; i < 32; ++i) v[i] = as_f(r0[i]);
+        f(ch, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = as_f(r1[i]);
+        f(ch + 1, v);
+    }
+}
+
+// Writes this thread's accumulator row of a complete tile (16-bit output, GEMM or fp8, one group)
+// with TMA tile stores: each epilogue warp stages its 32 rows x 64 columns in the then idle operand
+// ring (128-byte rows, 128-byte swizzled, so that the 16-byte writes of a warp hit distinct banks)
+// and one lane stores the box. Full-line writes replace the per-row 16-byte writes of store_out,
+// whose 32 rows per warp instruction cost one L2 request each. The tensor map clips rows and
+// columns outside C. Only for a CTA's last segment, when no operand load can still land in the
+// ring; the warp waits until its boxes have been read out of shared memory.
+template <int OP, int TN>
+__device__ void store_tile_tma(const KernelParams& P, const EpiCtx& e, uint32_t t_acc,
+                               uint32_t ring, int quarter, int lane) {
+    constexpr int kSlabs = TN / 64;
+    const int64_t ncols = P.plan.gemm_n;
+    const bool bf16 = P.c_dtype == SK_BF16;
+    const int32_t y0 = static_cast<int32_t>(e.out_row - lane);   // the warp's first row
+#pragma unroll 1
+    for (int sl = 0; sl < kSlabs; ++sl) {
+        uint32_t r[2][32];
+        tmem_ld_32x32b_x32(t_acc + sl * 64, r[0]);
+        tmem_ld_32x32b_x32(t_acc + sl * 64 + 32, r[1]);
+        tmem_ld_wait();
+        uint32_t packed[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float a = as_f(r[h][i]), b = as_f(r[h][i + 1]);
+                if constexpr (OP == kOpFp8) {
+                    const int64_t n = e.n_base + sl * 64 + h * 32 + i;
+                    a *= e.row_scale * (n < ncols ? __ldg(P.sb + n) : 0.0f);
+                    b *= e.row_scale * (n + 1 < ncols ? __ldg(P.sb + n + 1) : 0.0f);
+                }
+                uint32_t w;
+                if (bf16) {
+                    __nv_bfloat162 x = __floats2bfloat162_rn(a, b);
+                    w = *reinterpret_cast<uint32_t*>(&x);
+                } else {
+                    __half2 x = __floats2half2_rn(a, b);
+                    w = *reinterpret_cast<uint32_t*>(&x);
+                }
+                packed[h * 16 + i / 2] = w;
+            }
+        }
+        const uint32_t buf = ring + static_cast<uint32_t>((quarter * kSlabs + sl) * 4096);
+        const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                         packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            tma_store_2d(&P.tmap_c, buf, static_cast<int32_t>(e.n_base + sl * 64), y0);
+    }
+    if (lane == 0) {
+        bulk_commit_group();
+        bulk_wait_group_read0();
+    }
+    __syncwarp();
 }
 
 // Owner's fold of its senders' partial tiles (linear, or the last tree round), staged through the
@@ -464,11 +536,11 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32]) {
 // in the owner's TMEM accumulator. Per element the additions run in sender order, so the result
 // does not depend on timing. Only the owner segment, always a CTA's last, takes this path: by then
 // every stage of the ring has been consumed.
-template <int OP, int TN, int CG, typename SenderFn>
+template <int OP, int TN, int CG, int ST, typename SenderFn>
 __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
                             const EpiCtx& e, uint32_t t_acc, int ethread, int64_t ns,
                             SenderFn sender, uint32_t ring, uint32_t fold_bars) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     constexpr int kChunks = TN / 32;
     constexpr int kUnitsPerSender = kChunks / C::kFoldUnitChunks;
     const int64_t units = ns * kUnitsPerSender;   // sender-major
@@ -522,36 +594,35 @@ __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment
         named_bar_sync(kEpiBarrier, kEpiThreads);   // buffer `buf` may be refilled
         if (ethread == 0 && ok && u + C::kFoldBufs < units) issue(u + C::kFoldBufs);
     }
-    for (int ch = 0; ch < kChunks; ++ch) {
-        float v[32];
-        load_acc(t_acc + ch * 32, v);
-        store_out<OP>(P, e, ch * 32, v);
+    if (P.c_tma) {   // the owner segment is its CTA's last, and the fold has left the ring
+        store_tile_tma<OP, TN>(P, e, t_acc, ring, e.row >> 5, e.row & 31);
+        return;
     }
+    for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) { store_out<OP>(P, e, ch * 32, v); });
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg,
                                  const EpiCtx& e, uint32_t t_acc, int ethread, uint32_t ring,
-                                 uint32_t fold_bars) {
+                                 uint32_t fold_bars, bool last) {
     const sk_plan_t& plan = P.plan;
     constexpr int kChunks = TN / 32;
     const int red = static_cast<int>(plan.reduction);
 
     if (seg.kind == SK_SEG_FULL) {
-        for (int ch = 0; ch < kChunks; ++ch) {
-            float v[32];
-            load_acc(t_acc + ch * 32, v);
-            store_out<OP>(P, e, ch * 32, v);
+        if (P.c_tma && last) {
+            store_tile_tma<OP, TN>(P, e, t_acc, ring, e.row >> 5, e.row & 31);
+            return;
         }
+        for_each_chunk<kChunks>(t_acc,
+                                [&](int ch, float (&v)[32]) { store_out<OP>(P, e, ch * 32, v); });
         return;
     }
     if (red == SK_ATOMIC) {
         // tcgen05.ld is warp-collective (.sync.aligned): every lane loads, and only the lanes of
         // rows inside the output add.
-        for (int ch = 0; ch < kChunks; ++ch) {
-            float v[32];
-            load_acc(t_acc + ch * 32, v);
-            if (!e.row_ok) continue;
+        for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
+            if (!e.row_ok) return;
             const int64_t n0 = e.n_base + ch * 32;
             float* dst = static_cast<float*>(P.c) + e.out_row * P.ldc + n0;
 #pragma unroll
@@ -563,19 +634,17 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
                         if (n0 + i + j < plan.gemm_n) red_add_f32(dst + i + j, v[i + j]);
                 }
             }
-        }
+        });
         return;
     }
     if (red == SK_WORKSPACE) {
         float* base = P.scratch + (seg.tile * CG + e.half) * static_cast<int64_t>(kTileM * TN);
-        for (int ch = 0; ch < kChunks; ++ch) {
-            float v[32];
-            load_acc(t_acc + ch * 32, v);
+        for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 red_add_v4(frag_ptr<TN>(base, ch * 32, i, e.row), v[i], v[i + 1], v[i + 2],
                            v[i + 3]);
-        }
+        });
         return;
     }
 
@@ -614,7 +683,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     if (ns > 0) (void)ld_acquire_gpu(P.flags + (seg.first_cta + sender(ns - 1)) * CG + e.half);
 
     if (seg.kind == SK_SEG_OWNER && ns > 0) {
-        staged_fold<OP, TN, CG>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
+        staged_fold<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
         return;
     }
 
@@ -624,9 +693,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         publish = false;
     }
     float* own = P.partials + (cta * CG + e.half) * static_cast<int64_t>(kTileM * TN);
-    for (int ch = 0; ch < kChunks; ++ch) {
-        float v[32];
-        load_acc(t_acc + ch * 32, v);
+    for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
         for (int64_t s = 0; s < ns; ++s) {
             const float* src = P.partials + ((seg.first_cta + sender(s)) * CG + e.half) *
                                                 static_cast<int64_t>(kTileM * TN);
@@ -648,7 +715,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         } else {
             store_out<OP>(P, e, ch * 32, v);
         }
-    }
+    });
     if (publish) {
         fence_proxy_async_global();   // a receiver may read this partial with bulk copies
         __threadfence();
@@ -657,10 +724,10 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     }
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              uint32_t tmem_base, int warp, volatile SmemCtl* ctl, uint32_t rank) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     const sk_plan_t& plan = P.plan;
     const int lane = static_cast<int>(threadIdx.x & 31);
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
@@ -701,8 +768,11 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         e.row_scale = 1.0f;
         if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
-        epilogue_segment<OP, TN, CG>(P, cta, seg, e, t_acc, ethread, ring,
-                                     bars + (2 * C::kStages + 4) * 8);
+        SegCursor ahead = cur;
+        sk_segment_t next;
+        const bool last = !seg_next(plan, cta, ahead, next);
+        epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ring,
+                                         bars + (2 * C::kStages + 4) * 8, last);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -720,10 +790,10 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
 // kernel
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN, int CG>
-__global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG>::kMinBlocks)
+template <int OP, int TN, int CG, int ST>
+__global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     sk_main_kernel(const __grid_constant__ KernelParams P) {
-    using C = Cfg<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -800,13 +870,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG>::kMinBlocks)
     }
 
     if (warp == 0) {
-        if (elect_one()) run_producer<OP, TN, CG>(P, cta, ring, bars, ctl, rank);
+        if (elect_one()) run_producer<OP, TN, CG, ST>(P, cta, ring, bars, ctl, rank);
         __syncwarp();
     } else if (warp == 1) {
-        if (rank == 0 && elect_one()) run_mma<OP, TN, CG>(P, cta, ring, bars, tmem_base, ctl);
+        if (rank == 0 && elect_one()) run_mma<OP, TN, CG, ST>(P, cta, ring, bars, tmem_base, ctl);
         __syncwarp();
     } else {
-        run_epilogue<OP, TN, CG>(P, cta, ring, bars, tmem_base, warp, ctl, rank);
+        run_epilogue<OP, TN, CG, ST>(P, cta, ring, bars, tmem_base, warp, ctl, rank);
     }
 
     tc_fence_before();
@@ -886,10 +956,10 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
 // host-side launch helpers
 // ---------------------------------------------------------------------------------------------
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 static int launch_main_t(const KernelParams& p, cudaStream_t stream) {
-    using C = Cfg<OP, TN, CG>;
-    auto kern = sk_main_kernel<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
+    auto kern = sk_main_kernel<OP, TN, CG, ST>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmem));
     if (e != cudaSuccess) return static_cast<int>(e);
@@ -915,10 +985,10 @@ static int launch_main_t(const KernelParams& p, cudaStream_t stream) {
     }
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 static int ctas_per_sm_t() {
-    using C = Cfg<OP, TN, CG>;
-    auto kern = sk_main_kernel<OP, TN, CG>;
+    using C = Cfg<OP, TN, CG, ST>;
+    auto kern = sk_main_kernel<OP, TN, CG, ST>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
         return 0;
@@ -928,28 +998,34 @@ static int ctas_per_sm_t() {
     return n;
 }
 
-template <int OP, int TN, int CG>
+template <int OP, int TN, int CG, int ST>
 static size_t smem_bytes_t() {
-    return Cfg<OP, TN, CG>::kSmem;
+    return Cfg<OP, TN, CG, ST>::kSmem;
 }
 
-// (op, cg, tn) -> the kernel instantiation; wgrad has no pair form (the host rejects it first).
-#define SK_DISPATCH(op, cg, tn, fn, ...)                                                    \
-    ((cg) == 2 ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2>(__VA_ARGS__)             \
-                                                : fn<kOpGemm16, 256, 2>(__VA_ARGS__))         \
-                              : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2>(__VA_ARGS__)             \
-                                                : fn<kOpGemm16, 128, 2>(__VA_ARGS__)))        \
-     : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1>(__VA_ARGS__)                                 \
-     : (op) == kOpFp8    ? fn<kOpFp8, 128, 1>(__VA_ARGS__)                                    \
-                         : fn<kOpWgrad16, 128, 1>(__VA_ARGS__))
+// (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); wgrad has no
+// pair form (the host rejects it first).
+#define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
+    ((cg) == 2                                                                              \
+         ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)                \
+                                          : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
+                        : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \
+                                          : fn<kOpGemm16, 128, 2, 4>(__VA_ARGS__)))           \
+     : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 7>(__VA_ARGS__)                              \
+     : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 7>(__VA_ARGS__)                                 \
+                         : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
-size_t main_smem_bytes(int op, int cg, int tn) { return SK_DISPATCH(op, cg, tn, smem_bytes_t); }
+size_t main_smem_bytes(int op, int cg, int tn, int st) {
+    return SK_DISPATCH(op, cg, tn, st, smem_bytes_t);
+}
 
-int main_ctas_per_sm(int op, int cg, int tn) { return SK_DISPATCH(op, cg, tn, ctas_per_sm_t); }
+int main_ctas_per_sm(int op, int cg, int tn, int st) {
+    return SK_DISPATCH(op, cg, tn, st, ctas_per_sm_t);
+}
 
-int launch_main(const KernelParams& p, int op, int cg, int tn, cudaStream_t stream) {
+int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream) {
     if (cg == 2 && op == kOpWgrad16) return static_cast<int>(cudaErrorInvalidValue);
-    return SK_DISPATCH(op, cg, tn, launch_main_t, p, stream);
+    return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, stream);
 }
 
 int launch_stage2(const Stage2Params& p, cudaStream_t stream) {

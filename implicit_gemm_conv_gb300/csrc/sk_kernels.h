@@ -37,6 +37,7 @@ struct ConvGeom {
 struct KernelParams {
     CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K]
     CUtensorMap tmap_b;    // GEMM: B [N][K]; fp8: B8 [N][K]; wgrad: im2col view of x
+    CUtensorMap tmap_c;    // when c_tma: C [M][N] 16-bit, 64 x 32 boxes, 128-byte swizzle
     sk_plan_t plan;
     void* c;               // output
     int64_t ldc;           // output row stride (elements)
@@ -51,6 +52,7 @@ struct KernelParams {
     uint64_t mbar_timeout_ns;
     uint32_t idesc;
     int32_t c_dtype;
+    int32_t c_tma;         // 1: a CTA's last complete tile is written with TMA stores (tmap_c)
 };
 
 struct Stage2Params {
@@ -63,14 +65,15 @@ struct Stage2Params {
     int32_t c_dtype;
 };
 
-// cg: 1 = one CTA per 128 x 128 tile; 2 = a cluster of two CTAs per 256 x tn tile, tn 128 or 256
-// (GEMMs only). Dynamic shared memory of one CTA of the main kernel.
-size_t main_smem_bytes(int op, int cg, int tn);
+// cg: 1 = one CTA per 128 x 128 tile (7 stages); 2 = a cluster of two CTAs per 256 x tn tile
+// (GEMMs only): tn 128 with 4 stages, tn 256 with 3. st: stages of the operand ring.
+// Dynamic shared memory of one CTA of the main kernel.
+size_t main_smem_bytes(int op, int cg, int tn, int st);
 // How many CTAs of the main kernel fit on one SM (0 if the device query fails).
-int main_ctas_per_sm(int op, int cg, int tn);
+int main_ctas_per_sm(int op, int cg, int tn, int st);
 // Launch the main kernel: p.plan.grid logical CTAs, each one CTA (cg 1) or one cluster of two
 // (cg 2). Returns a cudaError_t value.
-int launch_main(const KernelParams& p, int op, int cg, int tn, cudaStream_t stream);
+int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream);
 // Launch the Stage-2 reduce over the shared tiles of a workspace plan.
 int launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Read and clear the device error record: returns the code (0 = none) and fills info[3].
