@@ -3,7 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extra]
 
 Prints ONE JSON line (rank 0). The headline workload is the bf16 rcr GEMM 3840x4096x4096 on a
-148-CTA pool (960 tiles of 128x128), dp_sk mode, linear fixup. A step is one sk_gemm_rcr call: the
+148-SM pool, dp_sk mode, linear fixup, computed with the library's default tile for it: 240 tiles of
+256x256, each by a pair of CTAs on neighbouring SMs (the pool is 74 pairs). The same workload with
+the 128x128 tile (960 tiles, 148 CTAs) is reported under `extra`. A step is one sk_gemm_rcr call: the
 flag/control memset and the stream-K kernel (the linear fixup runs inside it). Inputs are resident
 in HBM; L2 is flushed (256 MB write) before every timed step and the flush is outside the timed
 events. `value` = algorithmic FLOP (2*M*N*K per step, all ranks) / summed step time.
@@ -38,7 +40,8 @@ KERNEL_SOURCES = ["implicit_gemm_conv_gb300/csrc/sk_kernels.cu",
                   "implicit_gemm_conv_gb300/csrc/sk_ptx.cuh",
                   "implicit_gemm_conv_gb300/csrc/sk_plan.h",
                   "implicit_gemm_conv_gb300/csrc/sk_kernels.h"]
-PROFILE = os.path.join(ROOT, "profiles", "sk_main_kernel_gemm_bf16_3840x4096x4096.md")
+PROFILE = os.path.join(ROOT, "profiles", "sk_main_kernel_pair256_gemm_bf16_3840x4096x4096.md")
+HEADLINE_TILE = "256x256_pair"
 
 
 def kernel_source_hash() -> str:
@@ -191,7 +194,9 @@ def cpu_baseline_gemm(w, A, B, target_s=15.0):
 
 
 def extra_measurements(torch, sk, dev, flush, stream, steps):
-    """Variants of the headline and the other named workloads (fewer steps each)."""
+    """Variants of the headline and the other named workloads (fewer steps each). GEMM and fp8
+    workloads run with the 128x128 tile (their stated pool of CTAs) and with the 256x256 CTA-pair
+    tile (half as many pairs); keys are "tile:mode/reduction"."""
     from workloads import WORKLOADS, fp8_operands, gemm_operands, wgrad_operands
     out = {}
     ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -202,8 +207,8 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
                 "us": round(step_ms / steps * 1e3, 1),
                 "main_us": round(main_ms / max(n_main, 1) * 1e3, 1)}
 
-    def record(res, key, call, flops):
-        res[key] = rate(call, flops)
+    def tiles(w):
+        return [("128", w.pool), ("256x256_pair", w.pool // 2 if w.pool > 0 else -1)]
 
     for name, w in WORKLOADS.items():
         res = {}
@@ -213,11 +218,13 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
             variants = [(m, r) for m in w.modes for r in w.reductions]
             variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear"),
                          ("persistent", "linear")]
-            for mode, red in dict.fromkeys(variants):
-                out_dt = torch.float32 if red == "atomic" else A.dtype
-                C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
-                record(res, f"{mode}/{red}",
-                           lambda: sk.sk_gemm_rcr(A, B, C, mode, red, w.pool, ws=ws), w.flops())
+            for tile, pool in tiles(w):
+                with sk.tile(tile):
+                    for mode, red in dict.fromkeys(variants):
+                        out_dt = torch.float32 if red == "atomic" else A.dtype
+                        C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
+                        res[f"{tile}:{mode}/{red}"] = rate(
+                            lambda: sk.sk_gemm_rcr(A, B, C, mode, red, pool, ws=ws), w.flops())
         elif w.op == "wgrad":
             c = w.conv
             x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
@@ -228,19 +235,22 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
             variants = [(m, r) for m in w.modes for r in w.reductions]
             variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "atomic")]
             for mode, red in variants:
-                record(res, f"{mode}/{red}",
-                           lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
-                                                           c["pad"], c["groups"], mode, red,
-                                                           w.pool, ws=ws), w.flops())
+                res[f"128:{mode}/{red}"] = rate(
+                    lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
+                                                    c["pad"], c["groups"], mode, red, w.pool,
+                                                    ws=ws), w.flops())
         else:
             A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
             A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
             C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
-            for mode, red in [(m, r) for m in w.modes for r in w.reductions] + \
-                    [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]:
-                record(res, f"{mode}/{red}",
-                           lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, w.pool,
-                                                         ws=ws), w.flops())
+            variants = [(m, r) for m in w.modes for r in w.reductions]
+            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]
+            for tile, pool in tiles(w):
+                with sk.tile(tile):
+                    for mode, red in variants:
+                        res[f"{tile}:{mode}/{red}"] = rate(
+                            lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, pool,
+                                                          ws=ws), w.flops())
         out[name] = res
     return out
 
@@ -291,15 +301,17 @@ def run_ours(args, rank, world, dev):
 
     w = WORKLOADS[HEADLINE]
     mode, red = "dp_sk", "linear"
+    pool = w.pool // 2   # 148 SMs = 74 CTA pairs
+    sk.sk_set_tile(HEADLINE_TILE)
     peaks, peak_src = measured_peaks()
     A, B = gemm_setup(torch, w, dev)
     Ad, Bd = A.to(dev), B.to(dev)
     C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
     prob = sk.make_problem("gemm", ab_dtype=w.ab, c_dtype=w.out, M=w.M, N=w.N, K=w.K)
-    ws = torch.empty(sk.sk_workspace_bytes(prob, mode, red, w.pool), dtype=torch.uint8, device=dev)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, mode, red, pool), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    call = lambda: sk.sk_gemm_rcr(Ad, Bd, C, mode, red, w.pool, ws=ws)
+    call = lambda: sk.sk_gemm_rcr(Ad, Bd, C, mode, red, pool, ws=ws)
 
     # ---- the timed region ----
     for _ in range(args.warmup):
@@ -345,7 +357,8 @@ def run_ours(args, rank, world, dev):
         "ms_per_step": round(step_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": HEADLINE, "op": "gemm rcr", "M": w.M, "N": w.N, "K": w.K,
-                   "tiles": "960 x (128x128)", "pool": w.pool, "mode": mode, "reduction": red,
+                   "tiles": "240 x (256x256), each by a CTA pair (tcgen05 cta_group::2)",
+                   "pool": f"{pool} pairs ({2 * pool} SMs)", "mode": mode, "reduction": red,
                    "inputs": "bf16 N(0,1), seeds A=1 B=2", "out": "bf16",
                    "l2": "flushed (256 MB write) before every timed step, outside the events",
                    "parallelism": f"replicas x{world} (independent problems)"},
@@ -354,7 +367,7 @@ def run_ours(args, rank, world, dev):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(),
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
-                     "kernel": "sk_main_kernel<gemm16,128>"},
+                     "kernel": "sk_main_kernel<gemm16, 256x256 pair>"},
         "e2e": e2e,
         "gpu_launches": int(n_all),
     }
@@ -362,6 +375,7 @@ def run_ours(args, rank, world, dev):
         line["clocks"] = clk.summary()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_gemm(w, A, B)
+    sk.sk_set_tile("auto")
     if rank == 0 and not args.no_extra:
         line["extra"] = extra_measurements(torch, sk, dev, flush, stream, args.extra_steps)
     return line

@@ -186,6 +186,8 @@ int problem_view(const sk_problem& p, View& v) {
 int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
                         int ctas_per_sm, sk_plan_t& p);
 
+constexpr int64_t kAutoPairMinTiles = 64;   // SK_TILE_AUTO: pair tiles needed for the pair kernel
+
 // The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
 // (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
 struct TileCfg {
@@ -203,8 +205,15 @@ int tile_cfg(const View& v, TileCfg& t) {
             // other's mainloop (measured faster than one CTA per SM with twice the stages).
             t = g_tile == SK_TILE_256_PAIR ? TileCfg{2, 128, 4} : TileCfg{2, 256, 3};
             return SK_OK;
-        default:   // SK_TILE_AUTO
+        default: {   // SK_TILE_AUTO
+            // The 256 x 256 pair where the problem has rows for it and enough pair tiles that the
+            // data-parallel part carries the work. With few tiles over a long reduction, the
+            // smaller tile splits the reduction among fewer CTAs per tile (cheaper fixups).
+            const int64_t pair_tiles = sk::ceil_div(v.gemm_m, 2 * sk::kTileM) * sk::ceil_div(v.gemm_n, 256);
+            if (v.op_kind != sk::kOpWgrad16 && v.gemm_m > sk::kTileM && pair_tiles >= kAutoPairMinTiles)
+                t = TileCfg{2, 256, 3};
             return SK_OK;
+        }
     }
 }
 int problem_tile(const sk_problem& prob, TileCfg& t) {

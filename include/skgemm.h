@@ -175,8 +175,9 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
  *  - The first call on a device looks up that device's copy of the array (cudaGetSymbolAddress,
  *    which can load the library's GPU module); make that first call before any stream capture.
  *  - A problem whose plan needs more than SK_STATIC_WS_BYTES of workspace is rejected with -2
- *    and a message giving both sizes (linear/tree need 64 KiB per stream-K CTA, workspace 64 KiB
- *    per shared tile; atomic and off need only the 512-byte flag/control header).
+ *    and a message giving both sizes (linear/tree need one fp32 tile per stream-K CTA, workspace
+ *    one per shared tile: 64 KiB with the 128 x 128 tile, 256 KiB with the 256 x 256 pair tile,
+ *    the default for GEMMs with M > 128; atomic and off need only the flag/control header).
  *  - All calls share the one array and it keeps the previous call's contents: each call clears
  *    the flags, the control block and the scratch it reads before use, on `stream`. Calls that
  *    can overlap on the GPU (different streams, or several host threads) race on the array and
@@ -220,7 +221,10 @@ int sk_version(void);
 /*
  * Tile shape for the later calls of the calling thread, planning calls included. (No counterpart on
  * the pages, whose tiles are one workgroup's; this is a GB300 kernel choice.)
- *  SK_TILE_AUTO (the default): currently the 128 x 128 tile.
+ *  SK_TILE_AUTO (the default): SK_TILE_256x256_PAIR for the GEMM and fp8 GEMM when M > 128 and
+ *    the output has at least 64 tiles of 256 x 256; SK_TILE_128 otherwise (and always for wgrad,
+ *    whose GEMM M per group is K / groups). Few large tiles over a long reduction would be shared
+ *    by many CTAs each; the 128 x 128 tile keeps those fixups smaller.
  *  SK_TILE_128: one CTA computes each 128 x 128 output tile.
  *  SK_TILE_256_PAIR: a cluster of two CTAs on neighbouring SMs computes each 256 x 128 tile with the
  *    two-SM tensor-core instruction; each CTA stages its 128 rows of A and 64 of the 128 rows of B,

@@ -12,6 +12,14 @@ import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library
 from gpu_helpers import DEV, poisoned  # noqa: E402
 
 
+@pytest.fixture(autouse=True)
+def tile_128():
+    """The configurations these tests follow fix 128 x 128 tiles; the pair tiles have their own
+    tests."""
+    with sk.tile("128"):
+        yield
+
+
 def _repeat(launch, out, ws, n=20):
     first = None
     for _ in range(n):

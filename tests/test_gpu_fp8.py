@@ -13,6 +13,14 @@ import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library
 from gpu_helpers import DEV, bits, check_parity, poisoned, sample_points  # noqa: E402
 
 
+@pytest.fixture(autouse=True)
+def tile_128():
+    """The configurations these tests follow fix 128 x 128 tiles; the pair tiles have their own
+    tests."""
+    with sk.tile("128"):
+        yield
+
+
 def run(A, B, sa, sb, mode, red, ctas):
     M, N = A.shape[0], B.shape[0]
     C = poisoned((M, N), torch.bfloat16)

@@ -13,6 +13,14 @@ pytestmark = pytest.mark.gpu
 import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library must fail)
 from gpu_helpers import DEV, bits, check_parity, poisoned, sample_points  # noqa: E402
 
+
+@pytest.fixture(autouse=True)
+def tile_128():
+    """The configurations these tests follow fix 128 x 128 tiles; the pair tiles have their own
+    tests."""
+    with sk.tile("128"):
+        yield
+
 MODES = ["off", "dp_sk", "persistent", "splitk"]
 REDS = ["linear", "tree", "atomic", "workspace"]
 TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}

@@ -8,6 +8,14 @@ import pytest
 import implicit_gemm_conv_gb300 as sk
 from oracle import partition as P
 
+
+@pytest.fixture(autouse=True)
+def tile_128():
+    """The configurations these tests follow fix 128 x 128 tiles; the pair tiles have their own
+    tests."""
+    with sk.tile("128"):
+        yield
+
 MODES = [("off", P.OFF), ("dp_sk", P.DP_SK), ("persistent", P.PERSISTENT), ("splitk", P.SPLITK)]
 REDS = [("linear", P.LINEAR), ("tree", P.TREE), ("atomic", P.ATOMIC), ("workspace", P.WORKSPACE)]
 
@@ -181,6 +189,13 @@ def test_pair_tile_random_sweep(tile, tn):
 
 def test_pair_tile_setting():
     prob, _ = gemm(3840, 4096, 4096, "bf16")
+    with sk.tile("auto"):   # 240 pair tiles: the pair; 4 pair tiles or 128 rows: one CTA per tile
+        assert (sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tm,
+                sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tn) == (256, 256)
+        assert sk.sk_plan(gemm(512, 512, 65536, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
+        assert sk.sk_plan(gemm(128, 8192, 4096, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
+        assert sk.sk_plan(gemm(2048, 2048, 4096, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 256
+        assert sk.sk_plan(gemm(2048, 1792, 4096, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 128
     with sk.tile("128"):
         assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm == 128
     with sk.tile("256_pair"):

@@ -34,22 +34,25 @@ def _abi_static(A, B, C, mode, red, ctas):
                                      torch.cuda.current_stream().cuda_stream)
 
 
-CASES = [  # (dtype, out, M, N, K, mode, reduction, pool)
-    ("f16", "f16", 256, 256, 4096, "persistent", "linear", 3),
-    ("bf16", "f32", 200, 136, 520, "dp_sk", "workspace", 5),
-    ("bf16", "bf16", 512, 512, 8192, "dp_sk", "tree", 148),
+CASES = [  # (tile, dtype, out, M, N, K, mode, reduction, pool)
+    ("128", "f16", "f16", 256, 256, 4096, "persistent", "linear", 3),
+    ("128", "bf16", "f32", 200, 136, 520, "dp_sk", "workspace", 5),
+    ("128", "bf16", "bf16", 512, 512, 8192, "dp_sk", "tree", 148),
+    # 256x256 CTA-pair tiles: 40 pairs x 256 KiB partial slots fit the fixed scratch
+    ("256x256_pair", "bf16", "bf16", 768, 512, 8192, "dp_sk", "linear", 40),
 ]
 TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
 
 def test_static_scratch_matches_regular_entry_point_twice_in_a_row():
-    for i, (ab, out, M, N, K, mode, red, pool) in enumerate(CASES):
+    for i, (tile, ab, out, M, N, K, mode, red, pool) in enumerate(CASES):
         A, B = gemm_operands(M, N, K, ab, "u11", seed_offset=40 + i)
         Ad, Bd = A.to(DEV), B.to(DEV)
         ref = poisoned((M, N), TD[out])
-        sk.sk_gemm_rcr(Ad, Bd, ref, streamk=mode, reduction=red, ctas=pool)
         got = poisoned((M, N), TD[out])
-        rc = _abi_static(Ad, Bd, got, mode, red, pool)
+        with sk.tile(tile):   # both calls plan with the same tile
+            sk.sk_gemm_rcr(Ad, Bd, ref, streamk=mode, reduction=red, ctas=pool)
+            rc = _abi_static(Ad, Bd, got, mode, red, pool)
         assert rc == 0, sk.last_error()
         sk.sk_device_status()
         r = ref.double().cpu().numpy()
@@ -67,11 +70,12 @@ def test_static_scratch_refuses_oversized_plans():
     A = torch.zeros((M, K), dtype=torch.bfloat16, device=DEV)
     B = torch.zeros((N, K), dtype=torch.bfloat16, device=DEV)
     C = torch.zeros((M, N), dtype=torch.bfloat16, device=DEV)
-    # 300 stream-K CTAs x 64 KiB partial slots = 19.7 MB > 16 MiB
-    rc = _abi_static(A, B, C, "dp_sk", "linear", 300)
-    assert rc == -2
-    assert "fixed scratch holds" in sk.last_error()
-    # in off mode the plan needs only the 512-byte flag/control header, which fits
-    rc = _abi_static(A, B, C, "off", "linear", 300)
-    assert rc == 0, sk.last_error()
+    with sk.tile("128"):
+        # 300 stream-K CTAs x 64 KiB partial slots = 19.7 MB > 16 MiB
+        rc = _abi_static(A, B, C, "dp_sk", "linear", 300)
+        assert rc == -2
+        assert "fixed scratch holds" in sk.last_error()
+        # in off mode the plan needs only the 512-byte flag/control header, which fits
+        rc = _abi_static(A, B, C, "off", "linear", 300)
+        assert rc == 0, sk.last_error()
     torch.cuda.synchronize()
