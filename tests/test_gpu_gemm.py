@@ -148,3 +148,16 @@ def test_gemm_auto_selection():
                                       K=4096), "auto", "linear", 3).mode == sk.SPLITK
     C = run_gemm(A, B, "f16", "auto", "linear", 3)
     check_parity(C, ref, "f16", 4096, what="auto pool 3")
+
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("off", "linear"), ("persistent", "tree")])
+def test_gemm_strided_16bit_output(mode, red):
+    # 16-bit C with a row stride larger than N (TMA-store epilogue, 128x128 tile)
+    M, N, K = 200, 136, 520
+    A, B, ref = ref_full("bf16", M, N, K, "n01", 7)
+    Cbig = poisoned((M, 256), torch.bfloat16)
+    C = Cbig[:, :N]
+    sk.sk_gemm_rcr(A.to(DEV), B.to(DEV), C, streamk=mode, reduction=red, ctas=5)
+    sk.sk_device_status()
+    check_parity(C, ref, "bf16", 520, what=f"strided 16-bit C {mode}/{red}")
+    assert torch.isnan(Cbig[:, N:].float()).all(), "wrote outside the [M, N] window"

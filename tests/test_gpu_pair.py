@@ -177,3 +177,18 @@ def test_pair_rejects_wgrad():
         sk.sk_conv2d_wgrad_nhwc(x, dy, dw, 1, 1, (1, 1), (0, 0), 1, streamk="dp_sk",
                                 reduction="linear", ctas=-1)
     assert e.value.code == -2 and "GEMMs only" in str(e.value)
+
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("off", "linear"), ("dp_sk", "tree"),
+                                      ("persistent", "workspace")])
+def test_pair_strided_16bit_output(mode, red):
+    # A 16-bit C with a row stride larger than N: complete tiles leave through TMA tile stores
+    # whose tensor map carries ldc; nothing outside the [M, N] window may be written.
+    M, N, K = 520, 392, 1032
+    A, B, ref = ref_full("bf16", M, N, K, "n01", 31)
+    Cbig = poisoned((M, 512), torch.bfloat16)
+    C = Cbig[:, :N]
+    sk.sk_gemm_rcr(A.to(DEV), B.to(DEV), C, streamk=mode, reduction=red, ctas=5)
+    sk.sk_device_status()
+    check_parity(C, ref, "bf16", K, what=f"strided 16-bit C {mode}/{red}")
+    assert torch.isnan(Cbig[:, N:].float()).all(), "wrote outside the [M, N] window"
