@@ -192,3 +192,20 @@ def test_pair_strided_16bit_output(mode, red):
     sk.sk_device_status()
     check_parity(C, ref, "bf16", K, what=f"strided 16-bit C {mode}/{red}")
     assert torch.isnan(Cbig[:, N:].float()).all(), "wrote outside the [M, N] window"
+
+
+def test_pair_auto_mode_and_reduction(pair_tile):
+    # streamk = auto / reduction = auto over pair tiles: 2 tiles, a long reduction, 74 pairs ->
+    # stream-K with the workspace reduction; 24 tiles on a pool of 3 pairs -> split-K (one slice)
+    n = 256 if pair_tile == "256x256_pair" else 128
+    prob = sk.make_problem("gemm", ab_dtype="bf16", c_dtype="bf16", M=512, N=n, K=32768)
+    plan = sk.sk_plan(prob, "auto", "auto", 74)
+    assert plan.mode == sk.DP_SK and plan.reduction == sk.WORKSPACE and plan.sk_ctas == 74
+    A, B, ref = ref_full("bf16", 512, n, 32768, "n01", 13)
+    C = run_gemm(A, B, "bf16", "auto", "auto", 74)
+    check_parity(C, ref, "bf16", 32768, what="pair auto -> dp_sk/workspace")
+    prob = sk.make_problem("gemm", ab_dtype="f16", c_dtype="f16", M=1536, N=1024, K=1024)
+    assert sk.sk_plan(prob, "auto", "linear", 3).mode == sk.SPLITK
+    A, B, ref = ref_full("f16", 1536, 1024, 1024, "u11", 14)
+    C = run_gemm(A, B, "f16", "auto", "linear", 3)
+    check_parity(C, ref, "f16", 1024, what="pair auto -> split-K")

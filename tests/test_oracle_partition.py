@@ -140,6 +140,26 @@ def test_workspace_layout():
     assert a.ws_bytes == 256 + P.CONTROL_BYTES
 
 
+def test_flag_table_gives_every_cta_of_a_cluster_its_own_flag():
+    # A logical CTA made of `cluster` CTAs that each hand on their own rows publishes one flag per
+    # CTA: the flag of CTA r of publisher p sits at byte 4*(p*cluster + r), inside the table, and
+    # no two (p, r) share one; the table still starts the 256-byte aligned control block.
+    for T, I, Pool in [(240, 64, 74), (18, 64, 74), (5, 1568, 152), (1, 4096, 1216)]:
+        for cluster in (1, 2):
+            p = plan(T, I, Pool, tm=128 * cluster)
+            p2 = P.make_plan(tiles_m=1, tiles_n=T, groups=1, kred=I * 64, tm=128 * cluster, tn=128,
+                             tk=64, pool=Pool, mode=P.DP_SK, reduction=P.LINEAR, cluster=cluster)
+            offs = {4 * (pub * cluster + r) for pub in range(p2.publishers) for r in range(cluster)}
+            assert len(offs) == p2.publishers * cluster
+            assert all(o + 4 <= p2.flag_bytes for o in offs)
+            assert p2.flag_bytes % 256 == 0 and p2.flag_bytes - 256 < 4 * p2.publishers * cluster
+            # the partition itself does not depend on how many CTAs make a logical CTA
+            assert (p2.sk_tiles, p2.sk_ctas, p2.iters_per_sk_cta, p2.extra, p2.grid) == \
+                (p.sk_tiles, p.sk_ctas, p.iters_per_sk_cta, p.extra, p.grid)
+            # one fp32 partial slot per CTA of each publisher: tm x tn x 4 bytes per publisher
+            assert p2.partial_bytes == p2.publishers * (128 * cluster) * 128 * 4
+
+
 def test_forward_progress_simulation():
     rng = random.Random(5)
     cases = [(4, 64, 3), (5, 1568 // 16, 148 // 4), (7, 5, 6), (3, 40, 12)]
