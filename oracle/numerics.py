@@ -50,6 +50,10 @@ def _load():
         lib.oracle_fp8_rowcol_rows.argtypes = [i64, i64, i64, i64, p, i64, p, i64, p, p, p, i32]
         lib.oracle_wgrad_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
                                           i32, i32, p, p, i64, i64, p, i32]
+        lib.oracle_fprop_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
+                                          i32, i32, p, p, i64, i64, p, i32]
+        lib.oracle_dgrad_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
+                                          i32, i32, p, p, i64, i64, p, i32]
         _lib = lib
     return _lib
 
@@ -136,6 +140,38 @@ def wgrad_nhwc(fmt, x_bits, dy_bits, R, S, stride=(1, 1), pad=(0, 0), groups=1, 
     out = np.empty((k1 - k0, R, S, Cg), dtype=np.float64)
     _load().oracle_wgrad_nhwc(FMT[fmt], N, H, W, C, K, R, S, stride[0], stride[1], pad[0], pad[1],
                               groups, _ptr(x), _ptr(dy), k0, k1, _ptr(out), nthreads)
+    return out
+
+
+def fprop_nhwc(fmt, x_bits, w_bits, stride=(1, 1), pad=(0, 0), groups=1, p0=0, p1=None,
+               nthreads=0):
+    """fp64 y[p0:p1] ([output pixel][K]) of the NHWC forward convolution, filter w [K][R][S][C/G]."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, H, W, C = x.shape
+    K, R, S = w.shape[0], w.shape[1], w.shape[2]
+    Ho, Wo = conv_out_size(H, R, stride[0], pad[0]), conv_out_size(W, S, stride[1], pad[1])
+    p1 = N * Ho * Wo if p1 is None else p1
+    out = np.empty((p1 - p0, K), dtype=np.float64)
+    _load().oracle_fprop_nhwc(FMT[fmt], N, H, W, C, K, R, S, stride[0], stride[1], pad[0], pad[1],
+                              groups, _ptr(x), _ptr(w), p0, p1, _ptr(out), nthreads)
+    return out
+
+
+def dgrad_nhwc(fmt, dy_bits, w_bits, H, W, stride=(1, 1), pad=(0, 0), groups=1, p0=0, p1=None,
+               nthreads=0):
+    """fp64 dx[p0:p1] ([input pixel][C]) of the NHWC convolution's data gradient; (H, W) is the
+    input image size, dy [N][Ho][Wo][K], filter w [K][R][S][C/G]."""
+    dy = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, Ho, Wo, K = dy.shape
+    R, S, Cg = w.shape[1], w.shape[2], w.shape[3]
+    C = Cg * groups
+    assert (Ho, Wo) == (conv_out_size(H, R, stride[0], pad[0]), conv_out_size(W, S, stride[1], pad[1]))
+    p1 = N * H * W if p1 is None else p1
+    out = np.empty((p1 - p0, C), dtype=np.float64)
+    _load().oracle_dgrad_nhwc(FMT[fmt], N, H, W, C, K, R, S, stride[0], stride[1], pad[0], pad[1],
+                              groups, _ptr(dy), _ptr(w), p0, p1, _ptr(out), nthreads)
     return out
 
 

@@ -20,6 +20,11 @@
  *   RowColQuant fp8 GEMM (rocm-libraries PR #9979, Scope: per-row scale of A, per-column scale
  *   of B, fp32 accumulator narrowed only at the end):
  *       C[m][n] = (sum_k deq(A8[m][k]) * deq(B8[n][k])) * sa[m] * sb[n]
+ *   Forward convolution and data gradient (PR #13151 lists the forward convolution as future work
+ *   on the same machinery; both are the plain definitions, NHWC activations, KRSC filters):
+ *       y[n][ho][wo][g*Kg+k]  = sum_{r,s,c} x[n][ho*sh-ph+r][wo*sw-pw+s][g*Cg+c] * w[g*Kg+k][r][s][c]
+ *       dx[n][h][w][g*Cg+c]   = sum_{r,s,k} dy[n][ho][wo][g*Kg+k] * w[g*Kg+k][r][s][c]
+ *                               over the (ho, wo) with ho*sh-ph+r = h and wo*sw-pw+s = w
  *
  * Inputs are the raw 16-bit or 8-bit patterns; they are decoded here from the format
  * definitions (binary16, bfloat16, OCP E4M3). Outputs are fp64 and are rounded to the output
@@ -195,5 +200,79 @@ void oracle_wgrad_nhwc(int fmt, int64_t N, int64_t H, int64_t W, int64_t C, int6
                     dw[(((k - k0) * R + r) * S + s) * Cg + c] = acc;
                 }
             }
+    free(tab);
+}
+
+/*
+ * Forward convolution, direct loops. x: [N][H][W][C], w: [K][R][S][Cg] (Cg = C/groups),
+ * y: [N*Ho*Wo][K] for the output pixels p in [p0, p1), p = (n*Ho + ho)*Wo + wo.
+ */
+void oracle_fprop_nhwc(int fmt, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                       int64_t S, int sh, int sw, int ph, int pw, int groups, const uint16_t *x,
+                       const uint16_t *w, int64_t p0, int64_t p1, double *y, int nthreads) {
+    double *tab = make_table(fmt);
+    set_threads(nthreads);
+    const int64_t Ho = (H + 2 * ph - R) / sh + 1;
+    const int64_t Wo = (W + 2 * pw - S) / sw + 1;
+    const int64_t Kg = K / groups, Cg = C / groups;
+    (void)N;
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (int64_t p = p0; p < p1; ++p)
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t n = p / (Ho * Wo), ho = (p / Wo) % Ho, wo = p % Wo;
+            const int64_t g = k / Kg;
+            double acc = 0.0;
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t h = ho * sh - ph + r;
+                if (h < 0 || h >= H) continue;
+                for (int64_t s = 0; s < S; ++s) {
+                    const int64_t ww = wo * sw - pw + s;
+                    if (ww < 0 || ww >= W) continue;
+                    for (int64_t c = 0; c < Cg; ++c)
+                        acc += tab[x[((n * H + h) * W + ww) * C + g * Cg + c]] *
+                               tab[w[((k * R + r) * S + s) * Cg + c]];
+                }
+            }
+            y[(p - p0) * K + k] = acc;
+        }
+    free(tab);
+}
+
+/*
+ * Data gradient of the convolution, direct loops. dy: [N][Ho][Wo][K], w: [K][R][S][Cg],
+ * dx: [N*H*W][C] for the input pixels p in [p0, p1), p = (n*H + h)*W + w. Every stride.
+ */
+void oracle_dgrad_nhwc(int fmt, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R,
+                       int64_t S, int sh, int sw, int ph, int pw, int groups, const uint16_t *dy,
+                       const uint16_t *w, int64_t p0, int64_t p1, double *dx, int nthreads) {
+    double *tab = make_table(fmt);
+    set_threads(nthreads);
+    const int64_t Ho = (H + 2 * ph - R) / sh + 1;
+    const int64_t Wo = (W + 2 * pw - S) / sw + 1;
+    const int64_t Kg = K / groups, Cg = C / groups;
+    (void)N;
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (int64_t p = p0; p < p1; ++p)
+        for (int64_t ci = 0; ci < C; ++ci) {
+            const int64_t n = p / (H * W), h = (p / W) % H, ww = p % W;
+            const int64_t g = ci / Cg, c = ci % Cg;
+            double acc = 0.0;
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t th = h + ph - r;   /* = ho * sh */
+                if (th < 0 || th % sh) continue;
+                const int64_t ho = th / sh;
+                if (ho >= Ho) continue;
+                for (int64_t s = 0; s < S; ++s) {
+                    const int64_t tw = ww + pw - s;
+                    if (tw < 0 || tw % sw) continue;
+                    const int64_t wo = tw / sw;
+                    if (wo >= Wo) continue;
+                    for (int64_t k = 0; k < Kg; ++k)
+                        acc += tab[dy[((n * Ho + ho) * Wo + wo) * K + g * Kg + k]] *
+                               tab[w[(((g * Kg + k) * R + r) * S + s) * Cg + c]];
+                }
+            }
+            dx[(p - p0) * C + ci] = acc;
+        }
     free(tab);
 }

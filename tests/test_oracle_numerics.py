@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from oracle import codec, numerics
-from workloads import gemm_operands, wgrad_operands, fp8_operands
+from workloads import dgrad_operands, fp8_operands, fprop_operands, gemm_operands, wgrad_operands
 
 
 def _bits(t):
@@ -83,6 +83,79 @@ def test_wgrad_all_ones_closed_form(oracle_lib):
         for s_ in range(S):
             cols = sum(0 <= wo * sw - pw + s_ < W for wo in range(Wo))
             assert np.all(out[:, r, s_, :] == N * rows * cols)
+
+
+CONV_SHAPES = [
+    dict(N=2, H=7, W=9, C=8, K=6, R=3, S=3, stride=(1, 1), pad=(1, 1), groups=1, dt="f16"),
+    dict(N=3, H=10, W=8, C=16, K=8, R=3, S=2, stride=(2, 2), pad=(1, 0), groups=2, dt="bf16"),
+    dict(N=1, H=9, W=11, C=12, K=12, R=1, S=3, stride=(2, 1), pad=(0, 2), groups=4, dt="f16"),
+    dict(N=2, H=5, W=5, C=4, K=4, R=5, S=5, stride=(3, 3), pad=(2, 2), groups=1, dt="bf16"),
+    dict(N=2, H=6, W=5, C=6, K=9, R=2, S=3, stride=(1, 1), pad=(0, 1), groups=3, dt="f16"),
+]
+
+
+def _nhwc(t):          # NCHW fp64 -> NHWC numpy
+    return t.permute(0, 2, 3, 1).numpy()
+
+
+@pytest.mark.parametrize("shape", CONV_SHAPES)
+def test_fprop_vs_torch_conv2d(oracle_lib, shape):
+    s = shape
+    x, w = fprop_operands(s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"], s["groups"],
+                          s["dt"], "u11", seed_offset=6)
+    ref = torch.nn.functional.conv2d(x.double().permute(0, 3, 1, 2), w.double().permute(0, 3, 1, 2),
+                                     stride=s["stride"], padding=s["pad"], groups=s["groups"])
+    ref = _nhwc(ref).reshape(-1, s["K"])                  # [output pixel][K]
+    out = numerics.fprop_nhwc(s["dt"], _bits(x), _bits(w), s["stride"], s["pad"], s["groups"])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    p0 = ref.shape[0] // 3
+    part = numerics.fprop_nhwc(s["dt"], _bits(x), _bits(w), s["stride"], s["pad"], s["groups"],
+                               p0=p0, p1=p0 + 5)
+    np.testing.assert_array_equal(part, out[p0:p0 + 5])
+
+
+@pytest.mark.parametrize("shape", CONV_SHAPES)
+def test_dgrad_vs_torch_conv2d_input(oracle_lib, shape):
+    s = shape
+    dy, w = dgrad_operands(s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"], s["stride"],
+                           s["pad"], s["groups"], s["dt"], "u11", seed_offset=7)
+    ref = torch.nn.grad.conv2d_input((s["N"], s["C"], s["H"], s["W"]),
+                                     w.double().permute(0, 3, 1, 2),
+                                     dy.double().permute(0, 3, 1, 2), stride=s["stride"],
+                                     padding=s["pad"], groups=s["groups"])
+    ref = _nhwc(ref).reshape(-1, s["C"])                  # [input pixel][C]
+    out = numerics.dgrad_nhwc(s["dt"], _bits(dy), _bits(w), s["H"], s["W"], s["stride"], s["pad"],
+                              s["groups"])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    part = numerics.dgrad_nhwc(s["dt"], _bits(dy), _bits(w), s["H"], s["W"], s["stride"], s["pad"],
+                               s["groups"], p0=3, p1=11)
+    np.testing.assert_array_equal(part, out[3:11])
+
+
+def test_fprop_and_dgrad_all_ones_closed_form(oracle_lib):
+    # x = w = 1: y counts the in-image taps of each output pixel, times C/G. dy = w = 1: dx counts
+    # the (r, s) whose output position (h+ph-r)/sh, (w+pw-s)/sw is whole and inside, times K/G.
+    N, H, W, C, K, R, S, sh, sw, ph, pw, G = 2, 6, 7, 4, 6, 3, 2, 2, 1, 1, 1, 2
+    Ho, Wo = (H + 2 * ph - R) // sh + 1, (W + 2 * pw - S) // sw + 1
+    one = 0x3C00
+    y = numerics.fprop_nhwc("f16", np.full((N, H, W, C), one, np.uint16),
+                            np.full((K, R, S, C // G), one, np.uint16), (sh, sw), (ph, pw), G)
+    for n in range(N):
+        for ho in range(Ho):
+            rows = sum(0 <= ho * sh - ph + r < H for r in range(R))
+            for wo in range(Wo):
+                cols = sum(0 <= wo * sw - pw + s_ < W for s_ in range(S))
+                assert np.all(y[(n * Ho + ho) * Wo + wo] == rows * cols * (C // G))
+    dx = numerics.dgrad_nhwc("f16", np.full((N, Ho, Wo, K), one, np.uint16),
+                             np.full((K, R, S, C // G), one, np.uint16), H, W, (sh, sw), (ph, pw), G)
+    for h in range(H):
+        rows = sum((h + ph - r) % sh == 0 and 0 <= (h + ph - r) // sh < Ho and h + ph - r >= 0
+                   for r in range(R))
+        for w_ in range(W):
+            cols = sum((w_ + pw - s_) % sw == 0 and 0 <= (w_ + pw - s_) // sw < Wo and w_ + pw - s_ >= 0
+                       for s_ in range(S))
+            for n in range(N):
+                assert np.all(dx[(n * H + h) * W + w_] == rows * cols * (K // G))
 
 
 def test_round_output_and_tolerance():

@@ -5,7 +5,8 @@ shapes, seeds and random-number draws only -- none of the method's arithmetic. V
 the CPU with ``torch.Generator().manual_seed(seed)`` and cast to the storage type once; every
 consumer reads the same bytes.
 
-Seeds: A=1, B=2, x=3, dy=4, sa=5, sb=6 (a shape-specific offset is added for the small test cases).
+Seeds: A=1, B=2, x=3, dy=4, sa=5, sb=6, conv filter w=7 (a shape-specific offset is added for the small
+test cases).
 """
 from __future__ import annotations
 
@@ -15,7 +16,7 @@ from typing import Optional, Tuple
 
 import torch
 
-SEED_A, SEED_B, SEED_X, SEED_DY, SEED_SA, SEED_SB = 1, 2, 3, 4, 5, 6
+SEED_A, SEED_B, SEED_X, SEED_DY, SEED_SA, SEED_SB, SEED_W = 1, 2, 3, 4, 5, 6, 7
 
 TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
@@ -68,6 +69,21 @@ def wgrad_operands(N, H, W, C, K, R, S, stride, pad, dtype, dist, seed_offset: i
     x = draw((N, H, W, C), dist, SEED_X + seed_offset).to(TORCH_DTYPE[dtype])
     dy = draw((N, Ho, Wo, K), dist, SEED_DY + seed_offset).to(TORCH_DTYPE[dtype])
     return x, dy
+
+
+def fprop_operands(N, H, W, C, K, R, S, groups, dtype, dist, seed_offset: int = 0):
+    """NHWC x [N][H][W][C] and the filter w [K][R][S][C/groups]."""
+    x = draw((N, H, W, C), dist, SEED_X + seed_offset).to(TORCH_DTYPE[dtype])
+    w = draw((K, R, S, C // groups), dist, SEED_W + seed_offset).to(TORCH_DTYPE[dtype])
+    return x, w
+
+
+def dgrad_operands(N, H, W, C, K, R, S, stride, pad, groups, dtype, dist, seed_offset: int = 0):
+    """NHWC dy [N][Ho][Wo][K] and the filter w [K][R][S][C/groups]."""
+    Ho, Wo = conv_out(H, R, stride[0], pad[0]), conv_out(W, S, stride[1], pad[1])
+    dy = draw((N, Ho, Wo, K), dist, SEED_DY + seed_offset).to(TORCH_DTYPE[dtype])
+    w = draw((K, R, S, C // groups), dist, SEED_W + seed_offset).to(TORCH_DTYPE[dtype])
+    return dy, w
 
 
 @dataclass
