@@ -25,7 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 F16, BF16, F32, E4M3 = 0, 1, 2, 3
 OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
 LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
-OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD = 0, 1, 2
+OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD, OP_FPROP, OP_DGRAD = 0, 1, 2, 3, 4
 SEG_FULL, SEG_OWNER, SEG_PEER = 0, 1, 2
 TILE_AUTO, TILE_128, TILE_256_PAIR, TILE_256x256_PAIR = 0, 1, 2, 3
 
@@ -74,6 +74,8 @@ _lib.sk_gemm_rowcol_fp8.argtypes = [_i64, _i64, _i64, _p, _p, _p, _p, _p, _i64, 
 _lib.sk_conv2d_wgrad_nhwc.argtypes = [_i32, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
                                       _i32, _i32, _i32, _i32, _p, _p, _p, _i32, _i32, _i32, _p,
                                       _sz, _p]
+_lib.sk_conv2d_fprop_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
+_lib.sk_conv2d_dgrad_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
 _lib.sk_workspace_bytes.argtypes = [ctypes.POINTER(sk_problem), _i32, _i32, _i32,
                                     ctypes.POINTER(_sz)]
 _lib.sk_plan.argtypes = [ctypes.POINTER(sk_problem), _i32, _i32, _i32, _i32,
@@ -94,7 +96,7 @@ _lib.sk_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(
 EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_workspace_bytes",
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
            "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws",
-           "sk_set_tile"]
+           "sk_set_tile", "sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc"]
 
 
 class SkError(RuntimeError):
@@ -225,11 +227,42 @@ def sk_conv2d_wgrad_nhwc(x, dy, dw, R, S, stride=(1, 1), pad=(0, 0), groups=1, s
                                             ctas, wp, wb, _stream_ptr(stream)))
 
 
+def sk_conv2d_fprop_nhwc(x, w, y, stride=(1, 1), pad=(0, 0), groups=1, streamk="dp_sk",
+                         reduction="linear", ctas=-1, ws=None, stream=None):
+    """y [N, Ho, Wo, K] = forward 2-D convolution of NHWC x [N, H, W, C] with the KRSC filter
+    w [K, R, S, C/groups]."""
+    N, H, W, C = x.shape
+    K, R, S = w.shape[0], w.shape[1], w.shape[2]
+    assert x.is_contiguous() and w.is_contiguous() and y.is_contiguous()
+    wp, wb = _ws(ws)
+    return _check(_lib.sk_conv2d_fprop_nhwc(_torch_dtype_code(x), _torch_dtype_code(y), N, H, W, C,
+                                            K, R, S, stride[0], stride[1], pad[0], pad[1], groups,
+                                            x.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                            _code(MODES, streamk), _code(REDUCTIONS, reduction),
+                                            ctas, wp, wb, _stream_ptr(stream)))
+
+
+def sk_conv2d_dgrad_nhwc(dy, w, dx, stride=(1, 1), pad=(0, 0), groups=1, streamk="dp_sk",
+                         reduction="linear", ctas=-1, ws=None, stream=None):
+    """dx [N, H, W, C] = data gradient of a 2-D convolution, from NHWC dy [N, Ho, Wo, K] and the
+    KRSC filter w [K, R, S, C/groups]; dx's shape gives the input size."""
+    N, H, W, C = dx.shape
+    K, R, S = w.shape[0], w.shape[1], w.shape[2]
+    assert dy.is_contiguous() and w.is_contiguous() and dx.is_contiguous()
+    wp, wb = _ws(ws)
+    return _check(_lib.sk_conv2d_dgrad_nhwc(_torch_dtype_code(dy), _torch_dtype_code(dx), N, H, W,
+                                            C, K, R, S, stride[0], stride[1], pad[0], pad[1], groups,
+                                            dy.data_ptr(), w.data_ptr(), dx.data_ptr(),
+                                            _code(MODES, streamk), _code(REDUCTIONS, reduction),
+                                            ctas, wp, wb, _stream_ptr(stream)))
+
+
 # ---- planning (host only) --------------------------------------------------------------------
 
 def make_problem(op, **kw) -> sk_problem:
     p = sk_problem()
-    p.op = _code({"gemm": OP_GEMM, "fp8": OP_FP8_ROWCOL, "wgrad": OP_WGRAD}, op)
+    p.op = _code({"gemm": OP_GEMM, "fp8": OP_FP8_ROWCOL, "wgrad": OP_WGRAD, "fprop": OP_FPROP,
+                  "dgrad": OP_DGRAD}, op)
     p.groups = 1
     for k, v in kw.items():
         if k in ("ab_dtype", "c_dtype"):

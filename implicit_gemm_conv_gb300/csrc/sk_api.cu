@@ -164,6 +164,28 @@ int problem_view(const sk_problem& p, View& v) {
             v.groups = 1;
             v.op_kind = p.op == SK_OP_GEMM ? sk::kOpGemm16 : sk::kOpFp8;
             return SK_OK;
+        case SK_OP_FPROP:
+        case SK_OP_DGRAD: {
+            if (p.groups < 1) return fail(SK_ERR_UNSUPPORTED, "groups must be >= 1");
+            if (p.stride_h < 1 || p.stride_w < 1) return fail(SK_ERR_UNSUPPORTED, "stride must be >= 1");
+            const int64_t Ho = (p.h + 2 * p.pad_h - p.r) / p.stride_h + 1;
+            const int64_t Wo = (p.w + 2 * p.pad_w - p.s) / p.stride_w + 1;
+            if (p.h + 2 * p.pad_h < p.r || p.w + 2 * p.pad_w < p.s || Ho < 1 || Wo < 1)
+                return fail(SK_ERR_UNSUPPORTED, "filter larger than the padded image");
+            v.groups = p.groups;
+            if (p.op == SK_OP_FPROP) {   // output pixels x filters, reduction over (r, s, c)
+                v.gemm_m = p.n * Ho * Wo;
+                v.gemm_n = p.k / p.groups;
+                v.kred = p.r * p.s * (p.c / p.groups);
+                v.op_kind = sk::kOpFprop16;
+            } else {                     // input pixels x channels, reduction over (r, s, k)
+                v.gemm_m = p.n * p.h * p.w;
+                v.gemm_n = p.c / p.groups;
+                v.kred = p.r * p.s * (p.k / p.groups);
+                v.op_kind = sk::kOpDgrad16;
+            }
+            return SK_OK;
+        }
         case SK_OP_WGRAD: {
             if (p.groups < 1) return fail(SK_ERR_UNSUPPORTED, "groups must be >= 1");
             if (p.stride_h < 1 || p.stride_w < 1) return fail(SK_ERR_UNSUPPORTED, "stride must be >= 1");
@@ -199,7 +221,7 @@ int tile_cfg(const View& v, TileCfg& t) {
         case SK_TILE_128: return SK_OK;
         case SK_TILE_256_PAIR:
         case SK_TILE_256x256_PAIR:
-            if (v.op_kind == sk::kOpWgrad16)
+            if (v.op_kind != sk::kOpGemm16 && v.op_kind != sk::kOpFp8)
                 return fail(SK_ERR_UNSUPPORTED, "the CTA-pair tiles serve the GEMMs only");
             // Rings of about 96 KB, so that two CTAs share an SM and one's epilogue overlaps the
             // other's mainloop (measured faster than one CTA per SM with twice the stages).
@@ -210,7 +232,8 @@ int tile_cfg(const View& v, TileCfg& t) {
             // data-parallel part carries the work. With few tiles over a long reduction, the
             // smaller tile splits the reduction among fewer CTAs per tile (cheaper fixups).
             const int64_t pair_tiles = sk::ceil_div(v.gemm_m, 2 * sk::kTileM) * sk::ceil_div(v.gemm_n, 256);
-            if (v.op_kind != sk::kOpWgrad16 && v.gemm_m > sk::kTileM && pair_tiles >= kAutoPairMinTiles)
+            if ((v.op_kind == sk::kOpGemm16 || v.op_kind == sk::kOpFp8) && v.gemm_m > sk::kTileM &&
+                pair_tiles >= kAutoPairMinTiles)
                 t = TileCfg{2, 256, 3};
             return SK_OK;
         }
@@ -492,6 +515,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.sb = kp.sb;
             s2.scratch = kp.scratch;
             s2.c_dtype = kp.c_dtype;
+            s2.op_kind = v.op_kind;
             le = sk::launch_stage2(s2, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
             if (g_timing.on) ++g_timing.all_launches;
@@ -797,6 +821,148 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     kp.conv.Kg = static_cast<int32_t>(Kg);
     return run(prob, streamk, reduction, ctas, kp, dw, RSC * cs, K, RSC * cs, ws, ws_bytes,
                static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// Shared checks and set-up of the forward-convolution and data-gradient calls. `act` is the
+// im2col'd activation (x for fprop, dy for dgrad) of shape [N][AH][AW][AC]; the traversal runs
+// over a TH x TW grid with stride (tsh, tsw) and padding (tph, tpw).
+int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                  int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h, int pad_w,
+                  int groups, const void* act, const void* wt, void* out, int streamk,
+                  int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    const bool fprop = op == SK_OP_FPROP;
+    const char* name = fprop ? "fprop" : "dgrad";
+    if (in_dtype != SK_F16 && in_dtype != SK_BF16)
+        return fail(SK_ERR_UNSUPPORTED, "%s inputs must be f16 or bf16, got %s", name, dtype_name(in_dtype));
+    if (out_dtype != SK_F32 && out_dtype != in_dtype)
+        return fail(SK_ERR_UNSUPPORTED, "%s output must be f32 or %s, got %s", name,
+                    dtype_name(in_dtype), dtype_name(out_dtype));
+    int rc = check_common(streamk, reduction, ctas, out_dtype);
+    if (rc) return rc;
+    if (N < 0 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1)
+        return fail(SK_ERR_UNSUPPORTED, "sizes must be positive");
+    if (groups < 1 || C % groups || K % groups)
+        return fail(SK_ERR_UNSUPPORTED, "groups must divide C and K");
+    if (stride_h < 1 || stride_w < 1 || stride_h > 8 || stride_w > 8)
+        return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
+    if (!fprop && (stride_h != 1 || stride_w != 1))
+        return fail(SK_ERR_UNSUPPORTED, "dgrad supports stride 1 only, got (%d, %d)", stride_h, stride_w);
+    if (pad_h < 0 || pad_w < 0 || pad_h >= R || pad_w >= S)
+        return fail(SK_ERR_UNSUPPORTED, "padding must be in [0, filter size)");
+    if (R > 16 || S > 16) return fail(SK_ERR_UNSUPPORTED, "filter taps beyond 16 are not supported");
+    const int64_t Cg = C / groups, Kg = K / groups;
+    const int64_t red_ch = fprop ? Cg : Kg;   // channels per group the reduction walks
+    if (red_ch % 64)
+        return fail(SK_ERR_UNSUPPORTED, "%s per group must be a multiple of 64, got %lld",
+                    fprop ? "channels" : "filters", (long long)red_ch);
+    if (C % 8 || K % 8 || Cg % 8)
+        return fail(SK_ERR_UNSUPPORTED, "C, K and C/groups must be multiples of 8 (16-byte rows)");
+    const int64_t Ho = (H + 2 * pad_h - R) / stride_h + 1;
+    const int64_t Wo = (W + 2 * pad_w - S) / stride_w + 1;
+    if (H + 2 * pad_h < R || W + 2 * pad_w < S || Ho < 1 || Wo < 1)
+        return fail(SK_ERR_UNSUPPORTED, "filter larger than the padded image");
+    // The activation read by im2col and the grid the traversal walks.
+    const int64_t AH = fprop ? H : Ho, AW = fprop ? W : Wo, AC = fprop ? C : K;
+    const int64_t TH = fprop ? Ho : H, TW = fprop ? Wo : W;
+    const int tsh = fprop ? stride_h : 1, tsw = fprop ? stride_w : 1;
+    const int tph = fprop ? pad_h : static_cast<int>(R - 1 - pad_h);
+    const int tpw = fprop ? pad_w : static_cast<int>(S - 1 - pad_w);
+    const int64_t up_w = (TW - 1) * tsw - tpw - (AW - 1);
+    const int64_t up_h = (TH - 1) * tsh - tph - (AH - 1);
+    if (up_w < -128 || up_h < -128 || up_w > 127 || up_h > 127 || -tpw < -128 || -tph < -128)
+        return fail(SK_ERR_UNSUPPORTED, "im2col bounding box outside the 4-D TMA range");
+    const int64_t pixels = N * TH * TW;
+    if (pixels + 128 >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return fail(SK_ERR_UNSUPPORTED, "too many pixels (must stay below 2^31 - 128)");
+    if (!act || !wt || !out) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    if (!aligned16(act) || !aligned16(wt) || !aligned16(out))
+        return fail(SK_ERR_UNSUPPORTED, "activations, filter and output must be 16-byte aligned");
+    rc = select_device_of(out);
+    if (rc) return rc;
+    if (N == 0) return SK_OK;   // no pixels: nothing to write
+    rc = load_encoders();
+    if (rc) return rc;
+    sk_problem prob;
+    memset(&prob, 0, sizeof(prob));
+    prob.op = op;
+    prob.ab_dtype = in_dtype;
+    prob.c_dtype = out_dtype;
+    prob.n = N; prob.h = H; prob.w = W; prob.c = C; prob.k = K; prob.r = R; prob.s = S;
+    prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
+    prob.groups = groups;
+    TileCfg tc;
+    rc = problem_tile(prob, tc);
+    if (rc) return rc;
+    sk::KernelParams kp;
+    memset(&kp, 0, sizeof(kp));
+    {   // A: im2col of the activation, 128 pixels x 64 channels per load (K-major)
+        const cuuint64_t dims[4] = {(cuuint64_t)AC, (cuuint64_t)AW, (cuuint64_t)AH, (cuuint64_t)N};
+        const cuuint64_t strides[3] = {(cuuint64_t)(AC * 2), (cuuint64_t)(AW * AC * 2),
+                                       (cuuint64_t)(AH * AW * AC * 2)};
+        const int lower[2] = {-tpw, -tph};
+        const int upper[2] = {static_cast<int>(up_w), static_cast<int>(up_h)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)tsw, (cuuint32_t)tsh, 1};
+        CUresult r = g_encode_im2col(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                     const_cast<void*>(act), dims, strides, lower, upper, 64, 128,
+                                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
+    }
+    // B: the filter as [K][R*S*C/G]; fprop 64 x 128-row boxes (K-major), dgrad 64 x 64 boxes
+    // (two per step, MN-major).
+    const int64_t RSC = R * S * Cg;
+    rc = encode_2d(&kp.tmap_b, wt, 2, RSC, K, RSC * 2, 64, fprop ? 128 : 64);
+    if (rc) return rc;
+    const int cs = dtype_size(out_dtype);
+    const int64_t ldc = fprop ? K : C;
+    kp.c = out;
+    kp.ldc = ldc;
+    kp.c_dtype = out_dtype;
+    if (out_dtype != SK_F32 && groups == 1) {   // one group: complete tiles leave through TMA
+        rc = encode_2d(&kp.tmap_c, out, 2, ldc, pixels, ldc * 2, 64, 32);
+        if (rc) return rc;
+        kp.c_tma = 1;
+    }
+    const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+    kp.idesc = sk::make_idesc(fmt, fmt, false, !fprop, 128, static_cast<uint32_t>(sk::kTileN));
+    kp.conv.HoWo = TH * TW;
+    kp.conv.Wo = static_cast<int32_t>(TW);
+    kp.conv.sh = tsh;
+    kp.conv.sw = tsw;
+    kp.conv.ph = tph;
+    kp.conv.pw = tpw;
+    kp.conv.R = static_cast<int32_t>(R);
+    kp.conv.S = static_cast<int32_t>(S);
+    kp.conv.Cg = static_cast<int32_t>(red_ch);
+    kp.conv.Kg = static_cast<int32_t>(Kg);
+    kp.conv.Cw = static_cast<int32_t>(Cg);
+    return run(prob, streamk, reduction, ctas, kp, out, ldc * cs, pixels, ldc * cs, ws, ws_bytes,
+               static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* x, const void* w, void* y,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream) {
+    return conv_fwd_like(SK_OP_FPROP, in_dtype, y_dtype, N, H, W, C, K, R, S, stride_h, stride_w,
+                         pad_h, pad_w, groups, x, w, y, streamk, reduction, ctas, ws, ws_bytes,
+                         stream);
+}
+
+int sk_conv2d_dgrad_nhwc(int in_dtype, int dx_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* dy, const void* w, void* dx,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream) {
+    return conv_fwd_like(SK_OP_DGRAD, in_dtype, dx_dtype, N, H, W, C, K, R, S, stride_h, stride_w,
+                         pad_h, pad_w, groups, dy, w, dx, streamk, reduction, ctas, ws, ws_bytes,
+                         stream);
 }
 
 int sk_timing_enable(int on) {

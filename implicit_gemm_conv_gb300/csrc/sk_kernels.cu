@@ -65,7 +65,7 @@ constexpr uint32_t kEpiBarrier = 1;
 
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
-    static_assert(CG == 1 || (CG == 2 && OP != kOpWgrad16), "CTA pairs serve the GEMMs only");
+    static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8, "CTA pairs serve the GEMMs only");
     static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
     static constexpr int kElem = OP == kOpFp8 ? 1 : 2;
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
@@ -137,12 +137,55 @@ __device__ __forceinline__ void wgrad_slabs(const ConvGeom& cg, int64_t g, int64
     }
 }
 
+// fprop / dgrad: the first pixel of an M tile in the im2col traversal, decomposed once per segment.
+struct PixelStart {
+    int32_t w, h, n;   // traversal start (w, h) with the padding applied, image n
+};
+
+__device__ __forceinline__ void pixel_start(const ConvGeom& cg, int64_t mt, PixelStart& ps) {
+    const uint32_t p0 = static_cast<uint32_t>(mt * kTileM);   // < 2^31 (checked on the host)
+    const uint32_t howo = static_cast<uint32_t>(cg.HoWo), wo_n = static_cast<uint32_t>(cg.Wo);
+    const uint32_t n_img = p0 / howo;
+    const uint32_t rem = p0 - n_img * howo;
+    const uint32_t ho = rem / wo_n;
+    const uint32_t wo = rem - ho * wo_n;
+    ps.w = static_cast<int32_t>(wo) * cg.sw - cg.pw;
+    ps.h = static_cast<int32_t>(ho) * cg.sh - cg.ph;
+    ps.n = static_cast<int32_t>(n_img);
+}
+
 template <int OP, int TN, int CG, int ST>
 __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
                                             int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
-                                            uint32_t bar, const WgradSlabs<TN>& sl, uint32_t rank) {
+                                            uint32_t bar, const WgradSlabs<TN>& sl, uint32_t rank,
+                                            const PixelStart& ps) {
     using C = Cfg<OP, TN, CG, ST>;
-    if constexpr (CG == 2) {
+    if constexpr (folds_groups_into_columns(OP)) {
+        // Reduction index k*64 = (tap, channel block) with the channels fastest.
+        const ConvGeom& cg = P.conv;
+        const int32_t kk = static_cast<int32_t>(k) * C::TK;
+        const int32_t tap = kk / cg.Cg;
+        const int32_t c0 = kk - tap * cg.Cg;
+        const int32_t r = tap / cg.S;
+        const int32_t s = tap - r * cg.S;
+        // A: 128 pixels x 64 channels of the im2col'd tensor at tap (r, s) (K-major).
+        tma_load_im2col_4d(a_dst, &P.tmap_a, bar, static_cast<int32_t>(g) * cg.Cg + c0, ps.w, ps.h,
+                           ps.n, static_cast<uint16_t>(s), static_cast<uint16_t>(r));
+        if constexpr (OP == kOpFprop16) {
+            // B: 128 filters x 64 of their (r, s, c) entries, w viewed as [K][R*S*C/G] (K-major).
+            tma_load_2d(b_dst, &P.tmap_b, bar, kk,
+                        static_cast<int32_t>(g * cg.Kg + nt * TN));
+        } else {
+            // B: the filter at the flipped tap, 64 output-gradient channels (rows of w) x 128 input
+            // channels as two 64-channel slabs (MN-major).
+            const int32_t col = ((cg.R - 1 - r) * cg.S + (cg.S - 1 - s)) * cg.Cw +
+                                static_cast<int32_t>(nt * TN);
+#pragma unroll
+            for (int j = 0; j < TN / 64; ++j)
+                tma_load_2d(b_dst + j * (C::TK * 128), &P.tmap_b, bar, col + 64 * j,
+                            static_cast<int32_t>(g) * cg.Kg + c0);
+        }
+    } else if constexpr (CG == 2) {
         // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
         const int32_t kx = static_cast<int32_t>(k * C::TK);
         tma_load_2d_pair(a_dst, &P.tmap_a, bar, kx,
@@ -208,6 +251,8 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         tile_coords(plan, seg.tile, g, mt, nt);
         WgradSlabs<TN> slabs;
         if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
+        PixelStart ps{0, 0, 0};
+        if constexpr (folds_groups_into_columns(OP)) pixel_start(P.conv, mt, ps);
         const int64_t len = seg.k_end - seg.k_begin;
         const int64_t rot = segment_rotation(plan, dp, seg, tau);
         for (int64_t j = 0; j < len; ++j) {
@@ -225,11 +270,11 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
                 // Both CTAs' bytes are counted on the even CTA's barrier, which expects them all.
                 if (rank == 0) mbar_arrive_expect_tx(full, CG * C::kStageBytes);
                 issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
-                                        mapa_shared(full, 0), slabs, rank);
+                                            mapa_shared(full, 0), slabs, rank, ps);
             } else {
                 mbar_arrive_expect_tx(full, C::kStageBytes);
                 issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs,
-                                        rank);
+                                            rank, ps);
             }
             ++issued;
             if (++stage == C::kStages) {
@@ -312,15 +357,16 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
 #pragma unroll
             for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
                 uint64_t ad, bd;
-                if constexpr (OP == kOpWgrad16) {
-                    // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
+                // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
+                // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
+                if constexpr (OP == kOpWgrad16)
                     ad = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
-                    bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
-                } else {
-                    // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
+                else
                     ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                if constexpr (OP == kOpWgrad16 || OP == kOpDgrad16)
+                    bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
+                else
                     bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                }
                 const uint32_t accumulate = (j > 0 || kk > 0) ? 1u : 0u;
                 if constexpr (OP == kOpFp8)
                     mma_f8<CG>(d_tmem, ad, bd, P.idesc, accumulate);
@@ -368,7 +414,8 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
 struct EpiCtx {
     int64_t out_row;       // output row of this thread (g*gemm_m + m)
     bool row_ok;           // m < gemm_m
-    int64_t n_base;        // first GEMM-view column of the tile
+    int64_t n_base;        // first output column of the tile
+    int64_t n_end;         // output columns of this tile's group end here (exclusive)
     int row;               // accumulator row 0..127
     int64_t half;          // CG = 2: rank of this CTA in its pair (which 128 rows of the tile); else 0
     float row_scale;       // fp8: sa[out_row]; else 1
@@ -382,7 +429,7 @@ __device__ __forceinline__ void store_out(const KernelParams& P, const EpiCtx& e
                                           float (&v)[32]) {
     if (!e.row_ok) return;
     const int64_t n0 = e.n_base + col0;
-    const int64_t ncols = P.plan.gemm_n;
+    const int64_t ncols = e.n_end;
     if (n0 >= ncols) return;
     if constexpr (OP == kOpFp8) {
 #pragma unroll
@@ -627,11 +674,11 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
             float* dst = static_cast<float*>(P.c) + e.out_row * P.ldc + n0;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                if (n0 + i + 4 <= plan.gemm_n) {
+                if (n0 + i + 4 <= e.n_end) {
                     red_add_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
                 } else {
                     for (int j = 0; j < 4; ++j)
-                        if (n0 + i + j < plan.gemm_n) red_add_f32(dst + i + j, v[i + j]);
+                        if (n0 + i + j < e.n_end) red_add_f32(dst + i + j, v[i + j]);
                 }
             }
         });
@@ -763,8 +810,15 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         e.half = static_cast<int64_t>(rank);
         const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
         e.row_ok = m < plan.gemm_m;
-        e.out_row = g * plan.gemm_m + m;
-        e.n_base = nt * TN;
+        if constexpr (folds_groups_into_columns(OP)) {
+            e.out_row = m;
+            e.n_base = g * plan.gemm_n + nt * TN;
+            e.n_end = (g + 1) * plan.gemm_n;
+        } else {
+            e.out_row = g * plan.gemm_m + m;
+            e.n_base = nt * TN;
+            e.n_end = plan.gemm_n;
+        }
         e.row_scale = 1.0f;
         if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
@@ -913,15 +967,17 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     const int64_t m = mt * (kTileM * CG) + half * kTileM + row;
     const int64_t n0 = nt * TN + q4 * 4;
     if (m >= plan.gemm_m || n0 >= plan.gemm_n) return;
+    const bool fold_cols = folds_groups_into_columns(static_cast<int>(P.op_kind));
+    const int64_t col = fold_cols ? g * plan.gemm_n + n0 : n0;   // output column of n0
     const float* base = P.scratch + t * static_cast<int64_t>(kTileM * CG * TN);
     const float4 q = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4));
     float v[4] = {q.x, q.y, q.z, q.w};
-    const int64_t out_row = g * plan.gemm_m + m;
+    const int64_t out_row = fold_cols ? m : g * plan.gemm_m + m;
     if (P.sa != nullptr) {
         const float rs = P.sa[out_row];
         for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
     }
-    const int64_t off = out_row * P.ldc + n0;
+    const int64_t off = out_row * P.ldc + col;
     const bool full = n0 + 4 <= plan.gemm_n;
     if (P.c_dtype == SK_F32) {
         float* dst = static_cast<float*>(P.c) + off;
@@ -1013,6 +1069,8 @@ static size_t smem_bytes_t() {
                                           : fn<kOpGemm16, 128, 2, 4>(__VA_ARGS__)))           \
      : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 7>(__VA_ARGS__)                              \
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 7>(__VA_ARGS__)                                 \
+     : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 7>(__VA_ARGS__)                            \
+     : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 7>(__VA_ARGS__)                            \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
 size_t main_smem_bytes(int op, int cg, int tn, int st) {
@@ -1024,7 +1082,7 @@ int main_ctas_per_sm(int op, int cg, int tn, int st) {
 }
 
 int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream) {
-    if (cg == 2 && op == kOpWgrad16) return static_cast<int>(cudaErrorInvalidValue);
+    if (cg == 2 && op != kOpGemm16 && op != kOpFp8) return static_cast<int>(cudaErrorInvalidValue);
     return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, stream);
 }
 

@@ -10,7 +10,13 @@
 
 namespace sk {
 
-enum OpKind : int { kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2 };
+enum OpKind : int { kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2, kOpFprop16 = 3, kOpDgrad16 = 4 };
+
+// Forward convolution and data gradient fold conv groups into the output's columns (the output
+// is [pixels][channels]); wgrad folds them into its rows.
+__host__ __device__ constexpr bool folds_groups_into_columns(int op) {
+    return op == kOpFprop16 || op == kOpDgrad16;
+}
 
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
@@ -25,13 +31,17 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// Geometry the wgrad operand producer needs to turn an iteration into im2col coordinates.
+// Geometry the convolution producers need to turn an iteration into im2col coordinates. The im2col
+// traversal runs over the pixels of one image grid: wgrad and fprop the output grid (Ho x Wo), dgrad
+// the input grid (H x W, stride 1, padding R-1-ph / S-1-pw with the taps flipped).
 struct ConvGeom {
-    int64_t HoWo;          // output pixels per image
-    int32_t Wo;
-    int32_t sh, sw, ph, pw;
+    int64_t HoWo;          // pixels per image of the traversal grid
+    int32_t Wo;            // width of the traversal grid
+    int32_t sh, sw, ph, pw;   // traversal stride and padding
     int32_t R, S;
-    int32_t Cg, Kg;        // channels and filters per group
+    int32_t Cg, Kg;        // wgrad: channels and filters per group; fprop / dgrad: channels per
+                           // group of the im2col'd tensor (x: C/G, dy: K/G) and filter rows per group
+    int32_t Cw;            // fprop / dgrad: channels per group of the filter (C/G)
 };
 
 struct KernelParams {
@@ -57,6 +67,7 @@ struct KernelParams {
 
 struct Stage2Params {
     sk_plan_t plan;
+    int32_t op_kind;       // OpKind: where the group of a tile goes in the output
     void* c;
     int64_t ldc;
     const float* sa;

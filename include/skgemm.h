@@ -61,7 +61,8 @@ enum { SK_F16 = 0, SK_BF16 = 1, SK_F32 = 2, SK_E4M3 = 3 };                  /* e
 enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3, SK_AUTO = 4 };  /* streamk */
 enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3, SK_REDUCTION_AUTO = 4 };
                                                                              /* reduction    */
-enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2 };             /* operation    */
+enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2, SK_OP_FPROP = 3, SK_OP_DGRAD = 4 };
+                                                                             /* operation    */
 enum { SK_SEG_FULL = 0, SK_SEG_OWNER = 1, SK_SEG_PEER = 2 };                /* segment kind */
 
 #define SK_OK 0
@@ -75,7 +76,8 @@ typedef struct sk_problem {
     int32_t c_dtype;   /* output type                                                 */
     int32_t groups;    /* wgrad conv groups (>= 1)                                    */
     int64_t M, N, K;   /* GEMM / fp8 GEMM: C[M][N] = A[M][K] * B[N][K]^T              */
-    int64_t n, h, w, c, k, r, s;          /* wgrad: x[n][h][w][c], dy[n][ho][wo][k], dw[k][r][s][c/groups] */
+    int64_t n, h, w, c, k, r, s;          /* convolutions: x[n][h][w][c], dy / y [n][ho][wo][k],
+                                             filter [k][r][s][c/groups]                           */
     int32_t stride_h, stride_w, pad_h, pad_w;
 } sk_problem;
 
@@ -157,6 +159,41 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
 int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
                          int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
                          int pad_w, int groups, const void* x, const void* dy, void* dw,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/*
+ * Forward convolution as an implicit GEMM on the same stream-K machinery. [P2] lists the forward
+ * convolution as future work of the wgrad port; this call is that extension (no page gives its
+ * kernel).
+ *   y[n][ho][wo][g*Kg+k] = sum_{r,s,c} x[n][ho*sh-ph+r][wo*sw-pw+s][g*Cg+c] * w[g*Kg+k][r][s][c]
+ *   x: [N][H][W][C] (NHWC), w: [K][R][S][C/groups] (KRSC), y: [N][Ho][Wo][K] (NHWC),
+ *   Ho = (H + 2*pad_h - R)/stride_h + 1, Wo likewise; x outside the image reads as zero.
+ *   GEMM view per group: M = N*Ho*Wo output pixels, N = K/groups filters, reduction R*S*C/groups.
+ *   in_dtype: SK_F16 or SK_BF16; y_dtype: in_dtype or SK_F32 (SK_ATOMIC needs SK_F32).
+ *   Supported: (C/groups) a multiple of 64, K a multiple of 8, dilation 1, R, S <= 16, padding
+ *   < filter size. The 128 x 128 tile (sk_set_tile's pair tiles return -2).
+ */
+int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* x, const void* w, void* y,
+                         int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/*
+ * Data gradient of the convolution (the backward pass to the input) as an implicit GEMM, with the
+ * same conventions as sk_conv2d_fprop_nhwc. Same source as above: future work of the wgrad port.
+ *   dx[n][h][w][g*Cg+c] = sum_{r,s,k} dy[n][ho][wo][g*Kg+k] * w[g*Kg+k][r][s][c]
+ *                         over the (ho, wo) with ho*sh-ph+r = h, wo*sw-pw+s = w
+ *   dy: [N][Ho][Wo][K], w: [K][R][S][C/groups], dx: [N][H][W][C] (written whole).
+ *   GEMM view per group: M = N*H*W input pixels, N = C/groups channels, reduction R*S*K/groups,
+ *   computed as a stride-1 convolution of dy with the flipped filter.
+ *   Supported: stride 1 (other strides return -2), (K/groups) a multiple of 64, C/groups a
+ *   multiple of 8, dilation 1, R, S <= 16, padding < filter size. The 128 x 128 tile.
+ */
+int sk_conv2d_dgrad_nhwc(int in_dtype, int dx_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
+                         int pad_w, int groups, const void* dy, const void* w, void* dx,
                          int streamk, int reduction, int ctas, void* ws, size_t ws_bytes,
                          void* stream);
 

@@ -107,6 +107,48 @@ def test_wgrad_rejections(kw, reason):
     assert reason in msg, msg
 
 
+def _conv(fn, **kw):
+    a = dict(i=sk.BF16, o=sk.BF16, N=8, H=28, W=28, C=128, K=128, R=3, S=3, sh=1, sw=1, ph=1, pw=1,
+             g=1, mode=sk.DP_SK, red=sk.LINEAR, ctas=-1)
+    a.update(kw)
+    rc = getattr(sk.library(), fn)(a["i"], a["o"], a["N"], a["H"], a["W"], a["C"], a["K"], a["R"],
+                                   a["S"], a["sh"], a["sw"], a["ph"], a["pw"], a["g"], FAKE, FAKE,
+                                   FAKE, a["mode"], a["red"], a["ctas"], None, 0, None)
+    return rc, sk.last_error()
+
+
+@pytest.mark.parametrize("fn", ["sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc"])
+@pytest.mark.parametrize("kw,reason", [
+    (dict(g=3), "groups"),
+    (dict(C=96, K=96), "multiple of 64"),
+    (dict(ph=3), "padding"),
+    (dict(sh=0), "stride"),
+    (dict(R=17, S=3), "16"),
+    (dict(red=sk.ATOMIC), "atomic"),
+    (dict(i=sk.F16, o=sk.BF16), "output"),
+    (dict(H=1, W=1, ph=0, pw=0), "larger than"),
+])
+def test_conv_rejections(fn, kw, reason):
+    rc, msg = _conv(fn, **kw)
+    assert rc == -2
+    assert reason in msg, msg
+
+
+def test_dgrad_stride_and_fprop_tiles():
+    rc, msg = _conv("sk_conv2d_dgrad_nhwc", sh=2, sw=2)
+    assert rc == -2 and "stride 1" in msg
+    with sk.tile("256x256_pair"):
+        rc, msg = _conv("sk_conv2d_fprop_nhwc", N=0)   # checked before any device work
+    assert rc in (0, -2)
+    prob = sk.make_problem("fprop", ab_dtype="bf16", c_dtype="bf16", n=8, h=28, w=28, c=128,
+                           k=128, r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    with sk.tile("256x256_pair"):
+        with pytest.raises(sk.SkError, match="GEMMs only"):
+            sk.sk_plan(prob, "dp_sk", "linear", 148, 148)
+    plan = sk.sk_plan(prob, "dp_sk", "linear", 148, 148)   # auto: the 128x128 tile
+    assert (plan.tm, plan.gemm_m, plan.gemm_n, plan.kred) == (128, 8 * 28 * 28, 128, 9 * 128)
+
+
 def test_fp8_rejections():
     lib = sk.library()
     rc = lib.sk_gemm_rowcol_fp8(64, 64, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 64, sk.DP_SK, sk.ATOMIC,

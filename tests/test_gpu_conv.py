@@ -1,0 +1,179 @@
+"""GPU parity of the forward convolution and the data gradient (sk_conv2d_fprop_nhwc and
+sk_conv2d_dgrad_nhwc through the C ABI) against the fp64 oracle: every mode x reduction on ragged
+shapes (pixel counts that leave partial tiles, partial channel tiles), groups, strides and padding,
+a 1x1 convolution, sampled tile-edge pixels of a 32x56x56 workload, and bit-identical linear/tree
+hand-offs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import numerics
+from workloads import dgrad_operands, fprop_operands
+
+pytestmark = pytest.mark.gpu
+
+import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library must fail)
+from gpu_helpers import DEV, bits, check_parity, poisoned  # noqa: E402
+
+MODES = ["off", "dp_sk", "persistent", "splitk"]
+REDS = ["linear", "tree", "atomic", "workspace"]
+TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def out_size(H, R, s, p):
+    return (H + 2 * p - R) // s + 1
+
+
+def run_fprop(x, w, out, stride, pad, groups, mode, red, ctas, ws=None):
+    N, H, W, _ = x.shape
+    K, R, S = w.shape[0], w.shape[1], w.shape[2]
+    y = poisoned((N, out_size(H, R, stride[0], pad[0]), out_size(W, S, stride[1], pad[1]), K), TD[out])
+    sk.sk_conv2d_fprop_nhwc(x.to(DEV), w.to(DEV), y, stride, pad, groups, mode, red, ctas, ws=ws)
+    sk.sk_device_status()
+    return y
+
+
+def run_dgrad(dy, w, H, W, C, out, pad, groups, mode, red, ctas, ws=None):
+    N = dy.shape[0]
+    dx = poisoned((N, H, W, C), TD[out])
+    sk.sk_conv2d_dgrad_nhwc(dy.to(DEV), w.to(DEV), dx, (1, 1), pad, groups, mode, red, ctas, ws=ws)
+    sk.sk_device_status()
+    return dx
+
+
+_REF = {}
+
+
+def fprop_case(N, H, W, C, K, R, S, stride, pad, groups, dt, off):
+    key = ("f", N, H, W, C, K, R, S, stride, pad, groups, dt, off)
+    if key not in _REF:
+        x, w = fprop_operands(N, H, W, C, K, R, S, groups, dt, "u11", seed_offset=off)
+        _REF[key] = (x, w, numerics.fprop_nhwc(dt, bits(x), bits(w), stride, pad, groups))
+    return _REF[key]
+
+
+def dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, off):
+    key = ("d", N, H, W, C, K, R, S, pad, groups, dt, off)
+    if key not in _REF:
+        dy, w = dgrad_operands(N, H, W, C, K, R, S, (1, 1), pad, groups, dt, "u11", seed_offset=off)
+        _REF[key] = (dy, w, numerics.dgrad_nhwc(dt, bits(dy), bits(w), H, W, (1, 1), pad, groups))
+    return _REF[key]
+
+
+@pytest.mark.parametrize("red", REDS)
+@pytest.mark.parametrize("mode", MODES)
+def test_fprop_ragged(mode, red):
+    # 198 output pixels (a partial second tile), 72 filters (a partial tile), 9 reduction steps
+    x, w, ref = fprop_case(2, 9, 11, 64, 72, 3, 3, (1, 1), (1, 1), 1, "f16", 1)
+    out = "f32" if red == "atomic" else "f16"
+    y = run_fprop(x, w, out, (1, 1), (1, 1), 1, mode, red, 5)
+    check_parity(y.reshape(-1, 72), ref, out, 9 * 64, what=f"fprop {mode}/{red}")
+
+
+@pytest.mark.parametrize("red", REDS)
+@pytest.mark.parametrize("mode", MODES)
+def test_dgrad_ragged(mode, red):
+    # 198 input pixels, 72 channels, 9 reduction steps over (r, s, k)
+    dy, w, ref = dgrad_case(2, 9, 11, 72, 64, 3, 3, (1, 1), 1, "f16", 2)
+    out = "f32" if red == "atomic" else "f16"
+    dx = run_dgrad(dy, w, 9, 11, 72, out, (1, 1), 1, mode, red, 5)
+    check_parity(dx.reshape(-1, 72), ref, out, 9 * 64, what=f"dgrad {mode}/{red}")
+
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("persistent", "tree"), ("off", "linear"),
+                                      ("splitk", "workspace"), ("dp_sk", "atomic")])
+def test_fprop_grouped_strided(mode, red):
+    # 2 groups of 64 channels and 48 filters, stride (2, 1), padding (1, 0), R != S, bf16
+    x, w, ref = fprop_case(3, 10, 13, 128, 96, 3, 2, (2, 1), (1, 0), 2, "bf16", 3)
+    out = "f32" if red == "atomic" else "bf16"
+    y = run_fprop(x, w, out, (2, 1), (1, 0), 2, mode, red, 7)
+    check_parity(y.reshape(-1, 96), ref, out, 6 * 64, what=f"fprop grouped {mode}/{red}")
+
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("persistent", "tree"), ("off", "linear"),
+                                      ("splitk", "workspace"), ("dp_sk", "atomic")])
+def test_dgrad_grouped(mode, red):
+    # 2 groups of 48 channels and 64 filters, padding (1, 0), R != S, bf16
+    dy, w, ref = dgrad_case(3, 8, 10, 96, 128, 3, 2, (1, 0), 2, "bf16", 4)
+    out = "f32" if red == "atomic" else "bf16"
+    dx = run_dgrad(dy, w, 8, 10, 96, out, (1, 0), 2, mode, red, 7)
+    check_parity(dx.reshape(-1, 96), ref, out, 6 * 64, what=f"dgrad grouped {mode}/{red}")
+
+
+def test_fprop_1x1_and_padding_free():
+    x, w, ref = fprop_case(4, 7, 7, 192, 256, 1, 1, (1, 1), (0, 0), 1, "bf16", 5)
+    for mode, red in [("dp_sk", "linear"), ("off", "linear"), ("splitk", "tree")]:
+        y = run_fprop(x, w, "bf16", (1, 1), (0, 0), 1, mode, red, 11)
+        check_parity(y.reshape(-1, 256), ref, "bf16", 192, what=f"fprop 1x1 {mode}/{red}")
+
+
+def test_dgrad_5x5_no_padding():
+    dy, w, ref = dgrad_case(2, 12, 9, 64, 64, 5, 5, (0, 0), 1, "f16", 6)
+    for mode, red in [("dp_sk", "linear"), ("persistent", "workspace")]:
+        dx = run_dgrad(dy, w, 12, 9, 64, "f16", (0, 0), 1, mode, red, 9)
+        check_parity(dx.reshape(-1, 64), ref, "f16", 25 * 64, what=f"dgrad 5x5 {mode}/{red}")
+
+
+def _pixel_ranges(P):
+    """Tile-edge pixel ranges of a P-pixel output: the first tiles, a middle stretch and the end."""
+    return [(0, 300), (P // 2 - 130, P // 2 + 130), (P - 300, P)]
+
+
+@pytest.mark.parametrize("red", ["linear", "atomic"])
+def test_fprop_32x56x56_sampled(red):
+    N, H, W, C, K = 32, 56, 56, 64, 64
+    x, w = fprop_operands(N, H, W, C, K, 3, 3, 1, "f16", "u11")
+    out = "f32" if red == "atomic" else "f16"
+    y = run_fprop(x, w, out, (1, 1), (1, 1), 1, "dp_sk", red, -1).reshape(-1, K)
+    assert torch.isfinite(y.float()).all(), "unwritten outputs"
+    for p0, p1 in _pixel_ranges(N * H * W):
+        ref = numerics.fprop_nhwc("f16", bits(x), bits(w), (1, 1), (1, 1), 1, p0=p0, p1=p1)
+        check_parity(y[p0:p1], ref, out, 9 * C, what=f"fprop 32x56x56 {red} pixels {p0}..{p1}")
+
+
+@pytest.mark.parametrize("red", ["linear", "workspace"])
+def test_dgrad_32x56x56_sampled(red):
+    N, H, W, C, K = 32, 56, 56, 64, 64
+    dy, w = dgrad_operands(N, H, W, C, K, 3, 3, (1, 1), (1, 1), 1, "f16", "u11")
+    dx = run_dgrad(dy, w, H, W, C, "f16", (1, 1), 1, "dp_sk", red, -1).reshape(-1, C)
+    assert torch.isfinite(dx.float()).all(), "unwritten outputs"
+    for p0, p1 in _pixel_ranges(N * H * W):
+        ref = numerics.dgrad_nhwc("f16", bits(dy), bits(w), H, W, (1, 1), (1, 1), 1, p0=p0, p1=p1)
+        check_parity(dx[p0:p1], ref, "f16", 9 * K, what=f"dgrad 32x56x56 {red} pixels {p0}..{p1}")
+
+
+@pytest.mark.parametrize("op", ["fprop", "dgrad"])
+@pytest.mark.parametrize("red", ["linear", "tree"])
+def test_conv_bit_identical(op, red):
+    # 20 launches with the workspace and the output poisoned before each one; a small pool so
+    # that tiles are shared by several CTAs
+    if op == "fprop":
+        x, w, _ = fprop_case(2, 9, 11, 64, 72, 3, 3, (1, 1), (1, 1), 1, "f16", 1)
+        launch = lambda o, ws: sk.sk_conv2d_fprop_nhwc(xd, wd, o, (1, 1), (1, 1), 1, "dp_sk", red,
+                                                       5, ws=ws)
+        shape = (2, 9, 11, 72)
+        xd, wd = x.to(DEV), w.to(DEV)
+        prob = sk.make_problem("fprop", ab_dtype="f16", c_dtype="f16", n=2, h=9, w=11, c=64, k=72,
+                               r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    else:
+        dy, w, _ = dgrad_case(2, 9, 11, 72, 64, 3, 3, (1, 1), 1, "f16", 2)
+        launch = lambda o, ws: sk.sk_conv2d_dgrad_nhwc(xd, wd, o, (1, 1), (1, 1), 1, "dp_sk", red,
+                                                       5, ws=ws)
+        shape = (2, 9, 11, 72)
+        xd, wd = dy.to(DEV), w.to(DEV)
+        prob = sk.make_problem("dgrad", ab_dtype="f16", c_dtype="f16", n=2, h=9, w=11, c=72, k=64,
+                               r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", red, 5), dtype=torch.uint8, device=DEV)
+    o = poisoned(shape, torch.float16)
+    first = None
+    for _ in range(20):
+        ws.fill_(0xFF)
+        o.view(torch.uint8).fill_(0xFF)
+        launch(o, ws)
+        sk.sk_device_status()
+        b = o.view(torch.uint8).clone()
+        assert torch.isfinite(o.float()).all()
+        if first is None:
+            first = b
+        else:
+            assert torch.equal(first, b), "result changed between launches"

@@ -69,6 +69,21 @@ def wgrad(N, H, W, C, K, R, S, stride, pad, groups):
     return prob, kw
 
 
+def conv(op, N, H, W, C, K, R, S, stride, pad, groups):
+    prob = sk.make_problem(op, ab_dtype="bf16", c_dtype="bf16", n=N, h=H, w=W, c=C, k=K, r=R, s=S,
+                           stride_h=stride, stride_w=stride, pad_h=pad, pad_w=pad, groups=groups)
+    Ho = (H + 2 * pad - R) // stride + 1
+    Wo = (W + 2 * pad - S) // stride + 1
+    Kg, Cg = K // groups, C // groups
+    if op == "fprop":   # output pixels x filters per group, reduction (r, s, c)
+        m, n, kred = N * Ho * Wo, Kg, R * S * Cg
+    else:               # input pixels x channels per group, reduction (r, s, k)
+        m, n, kred = N * H * W, Cg, R * S * Kg
+    kw = dict(tiles_m=-(-m // 128), tiles_n=-(-n // 128), groups=groups, kred=kred, tm=128, tn=128,
+              tk=64)
+    return prob, kw
+
+
 NAMED = [
     ("gemm 256x256x4096", gemm(256, 256, 4096), 3),
     ("gemm 3840x4096x4096", gemm(3840, 4096, 4096, "bf16"), 148),
@@ -76,6 +91,10 @@ NAMED = [
     ("wgrad 64x28x28x256 g4 s2", wgrad(64, 28, 28, 256, 256, 3, 3, 2, 1, 4), -1),
     ("fp8 8192^3", gemm(8192, 8192, 8192, "e4m3"), -1),
     ("gemm 512x512x65536", gemm(512, 512, 65536, "bf16"), 148),
+    ("fprop 32x56x56x64 3x3", conv("fprop", 32, 56, 56, 64, 64, 3, 3, 1, 1, 1), -1),
+    ("fprop 8x28x28x256 g2 s2", conv("fprop", 8, 28, 28, 256, 256, 3, 3, 2, 1, 2), 148),
+    ("dgrad 32x56x56x64 3x3", conv("dgrad", 32, 56, 56, 64, 64, 3, 3, 1, 1, 1), -1),
+    ("dgrad 4x14x14x128 g2", conv("dgrad", 4, 14, 14, 128, 256, 3, 3, 1, 1, 2), 148),
 ]
 
 
