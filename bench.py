@@ -225,6 +225,12 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
                         C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
                         res[f"{tile}:{mode}/{red}"] = rate(
                             lambda: sk.sk_gemm_rcr(A, B, C, mode, red, pool, ws=ws), w.flops())
+        elif w.op in ("fprop", "dgrad"):
+            call, _ = conv_call(torch, sk, w, dev, ws)
+            variants = [(m, r) for m in w.modes for r in w.reductions]
+            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear")]
+            for mode, red in variants:
+                res[f"128:{mode}/{red}"] = rate(lambda: call(mode, red, w.pool), w.flops())
         elif w.op == "wgrad":
             c = w.conv
             x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
@@ -255,6 +261,27 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
     return out
 
 
+def conv_call(torch, sk, w, dev, ws):
+    """A launcher for a forward-convolution or data-gradient workload: call(mode, red, pool)."""
+    from workloads import TORCH_DTYPE, conv_out, dgrad_operands, fprop_operands
+    c = w.conv
+    Ho = conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0])
+    Wo = conv_out(c["W"], c["S"], c["stride"][1], c["pad"][1])
+    if w.op == "fprop":
+        x, f = fprop_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["groups"],
+                              w.ab, w.dist)
+        x, f = x.to(dev), f.to(dev)
+        y = torch.empty(c["N"], Ho, Wo, c["K"], dtype=TORCH_DTYPE[w.out], device=dev)
+        return (lambda mode, red, pool: sk.sk_conv2d_fprop_nhwc(
+            x, f, y, c["stride"], c["pad"], c["groups"], mode, red, pool, ws=ws)), y
+    dy, f = dgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],
+                           c["pad"], c["groups"], w.ab, w.dist)
+    dy, f = dy.to(dev), f.to(dev)
+    dx = torch.empty(c["N"], c["H"], c["W"], c["C"], dtype=TORCH_DTYPE[w.out], device=dev)
+    return (lambda mode, red, pool: sk.sk_conv2d_dgrad_nhwc(
+        dy, f, dx, c["stride"], c["pad"], c["groups"], mode, red, pool, ws=ws)), dx
+
+
 def run_variant(args, dev):
     """--variant WORKLOAD:MODE/REDUCTION: launch only that variant (warm-up + steps), e.g. under
     ncu; prints its step time."""
@@ -271,6 +298,9 @@ def run_variant(args, dev):
         A, B = A.to(dev), B.to(dev)
         C = torch.empty(w.M, w.N, dtype=torch.float32 if red == "atomic" else A.dtype, device=dev)
         call = lambda: sk.sk_gemm_rcr(A, B, C, mode, red, pool, ws=ws)
+    elif w.op in ("fprop", "dgrad"):
+        conv, _ = conv_call(torch, sk, w, dev, ws)
+        call = lambda: conv(mode, red, pool)
     elif w.op == "wgrad":
         c = w.conv
         x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],

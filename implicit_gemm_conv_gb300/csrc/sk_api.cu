@@ -216,7 +216,7 @@ struct TileCfg {
     int cg, tn, st;   // CTAs per logical CTA, tile N, operand-ring stages
 };
 int tile_cfg(const View& v, TileCfg& t) {
-    t = {1, sk::kTileN, 7};
+    t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : 6};
     switch (g_tile) {
         case SK_TILE_128: return SK_OK;
         case SK_TILE_256_PAIR:

@@ -92,9 +92,14 @@ struct Cfg {
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
     static_assert((TN / 32) % kFoldUnitChunks == 0, "tile N must be a multiple of the fold unit");
     static constexpr int kRingBytes = kStages * kStageBytes;   // a multiple of 1024
+    // One CTA per SM with a 16-bit output (every op but wgrad): a dedicated 32 KB buffer where the
+    // epilogue stages each complete 128 x 128 tile for its TMA stores, so that every tile, not only
+    // a CTA's last, leaves that way while the producer already fills the ring for the next one.
+    static constexpr int kEpiStageBytes = (CG == 1 && OP != kOpWgrad16) ? kTileM * TN * 2 : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (2 * kStages + 4 + kFoldBufs) * 8;
-    static constexpr size_t kSmem = 1024 + size_t(kRingBytes) + kCtlBytes + kBarBytes;
+    static constexpr size_t kSmem =
+        1024 + size_t(kRingBytes) + kEpiStageBytes + kCtlBytes + kBarBytes;
 };
 
 // Per-CTA control words. The block starts right after the operand ring, so tmem_base (written by
@@ -518,13 +523,14 @@ __device__ __forceinline__ void for_each_chunk(uint32_t t_acc, F&& f) {
     }
 }
 
-// Writes this thread's accumulator row of a complete tile (16-bit output, GEMM or fp8, one group)
-// with TMA tile stores: each epilogue warp stages its 32 rows x 64 columns in the then idle operand
-// ring (128-byte rows, 128-byte swizzled, so that the 16-byte writes of a warp hit distinct banks)
-// and one lane stores the box. Full-line writes replace the per-row 16-byte writes of store_out,
-// whose 32 rows per warp instruction cost one L2 request each. The tensor map clips rows and
-// columns outside C. Only for a CTA's last segment, when no operand load can still land in the
-// ring; the warp waits until its boxes have been read out of shared memory.
+// Writes this thread's accumulator row of a complete tile (16-bit output, one group in the output)
+// with TMA tile stores: each epilogue warp stages its 32 rows x 64 columns in `ring` (128-byte rows,
+// 128-byte swizzled, so that the 16-byte writes of a warp hit distinct banks) and one lane stores
+// the box. Full-line writes replace the per-row 16-byte writes of store_out, whose 32 rows per warp
+// instruction cost one L2 request each. The tensor map clips rows and columns outside C. `ring`
+// is the dedicated epilogue buffer of a one-CTA kernel, or for a CTA pair the operand ring, which
+// is idle only during a CTA's last segment. The warp waits until its boxes have been read out of
+// shared memory, so the buffer is free again on return.
 template <int OP, int TN>
 __device__ void store_tile_tma(const KernelParams& P, const EpiCtx& e, uint32_t t_acc,
                                uint32_t ring, int quarter, int lane) {
@@ -642,7 +648,8 @@ __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment
         if (ethread == 0 && ok && u + C::kFoldBufs < units) issue(u + C::kFoldBufs);
     }
     if (P.c_tma) {   // the owner segment is its CTA's last, and the fold has left the ring
-        store_tile_tma<OP, TN>(P, e, t_acc, ring, e.row >> 5, e.row & 31);
+        store_tile_tma<OP, TN>(P, e, t_acc, C::kEpiStageBytes ? ring + C::kRingBytes : ring,
+                               e.row >> 5, e.row & 31);
         return;
     }
     for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) { store_out<OP>(P, e, ch * 32, v); });
@@ -657,8 +664,10 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     const int red = static_cast<int>(plan.reduction);
 
     if (seg.kind == SK_SEG_FULL) {
-        if (P.c_tma && last) {
-            store_tile_tma<OP, TN>(P, e, t_acc, ring, e.row >> 5, e.row & 31);
+        using C = Cfg<OP, TN, CG, ST>;
+        if (P.c_tma && (C::kEpiStageBytes > 0 || last)) {
+            store_tile_tma<OP, TN>(P, e, t_acc, C::kEpiStageBytes ? ring + C::kRingBytes : ring,
+                                   e.row >> 5, e.row & 31);
             return;
         }
         for_each_chunk<kChunks>(t_acc,
@@ -853,8 +862,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
                                                ~uintptr_t(1023));
     static_assert(sizeof(SmemCtl) <= C::kCtlBytes, "control block");
     const uint32_t ring = smem_u32(smem);
-    volatile SmemCtl* ctl = reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes);
-    const uint32_t bars = ring + C::kRingBytes + C::kCtlBytes;
+    volatile SmemCtl* ctl =
+        reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes + C::kEpiStageBytes);
+    const uint32_t bars = ring + C::kRingBytes + C::kEpiStageBytes + C::kCtlBytes;
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const uint32_t ctl_addr = smem_u32(const_cast<SmemCtl*>(ctl));
@@ -1067,10 +1077,10 @@ static size_t smem_bytes_t() {
                                           : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
                         : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \
                                           : fn<kOpGemm16, 128, 2, 4>(__VA_ARGS__)))           \
-     : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 7>(__VA_ARGS__)                              \
-     : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 7>(__VA_ARGS__)                                 \
-     : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 7>(__VA_ARGS__)                            \
-     : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 7>(__VA_ARGS__)                            \
+     : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 6>(__VA_ARGS__)                              \
+     : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
+     : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 6>(__VA_ARGS__)                            \
+     : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 6>(__VA_ARGS__)                            \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
 size_t main_smem_bytes(int op, int cg, int tn, int st) {

@@ -89,7 +89,7 @@ def dgrad_operands(N, H, W, C, K, R, S, stride, pad, groups, dtype, dist, seed_o
 @dataclass
 class Workload:
     name: str
-    op: str                      # "gemm" | "wgrad" | "fp8"
+    op: str                      # "gemm" | "wgrad" | "fp8" | "fprop" | "dgrad"
     ab: str                      # input storage type
     out: str                     # output type
     dist: str
@@ -101,7 +101,18 @@ class Workload:
     modes: Tuple[str, ...] = ("dp_sk",)
     reductions: Tuple[str, ...] = ("linear",)
 
+    def _conv_dims(self):
+        c = self.conv
+        Ho = conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0])
+        Wo = conv_out(c["W"], c["S"], c["stride"][1], c["pad"][1])
+        return c, Ho, Wo
+
     def flops(self) -> float:
+        if self.op in ("fprop", "dgrad"):
+            c, Ho, Wo = self._conv_dims()
+            if self.op == "fprop":   # output pixels x filters x (r, s, c per group)
+                return 2.0 * c["N"] * Ho * Wo * c["K"] * c["R"] * c["S"] * (c["C"] // c["groups"])
+            return 2.0 * c["N"] * c["H"] * c["W"] * c["C"] * c["R"] * c["S"] * (c["K"] // c["groups"])
         if self.op == "wgrad":
             c = self.conv
             Ho = conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0])
@@ -111,6 +122,10 @@ class Workload:
         return 2.0 * self.M * self.N * self.K
 
     def kred(self) -> int:
+        if self.op in ("fprop", "dgrad"):
+            c = self.conv
+            per = (c["C"] if self.op == "fprop" else c["K"]) // c["groups"]
+            return c["R"] * c["S"] * per
         if self.op == "wgrad":
             c = self.conv
             return c["N"] * conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0]) * \
@@ -120,6 +135,13 @@ class Workload:
     def min_bytes(self) -> float:
         """Each operand read once, the output written once."""
         sz = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1}
+        if self.op in ("fprop", "dgrad"):
+            c, Ho, Wo = self._conv_dims()
+            x = c["N"] * c["H"] * c["W"] * c["C"]
+            dy = c["N"] * Ho * Wo * c["K"]
+            w = c["K"] * c["R"] * c["S"] * (c["C"] // c["groups"])
+            inp, out = (x, dy) if self.op == "fprop" else (dy, x)
+            return (inp + w) * sz[self.ab] + out * sz[self.out]
         if self.op == "wgrad":
             c = self.conv
             Ho = conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0])
@@ -152,5 +174,14 @@ WORKLOADS = {
         Workload("gemm_bf16_512x512x65536_pool148", "gemm", "bf16", "bf16", "n01", 512, 512, 65536,
                  pool=148, modes=("dp_sk", "persistent"),
                  reductions=("linear", "tree", "workspace")),
+        # The same 3x3 layer as the wgrad workload, forward and data gradient.
+        Workload("fprop_f16_n32_56x56_c64_k64_3x3", "fprop", "f16", "f16", "u11",
+                 conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
+                           groups=1),
+                 pool=-1, modes=("dp_sk",), reductions=("linear", "tree")),
+        Workload("dgrad_f16_n32_56x56_c64_k64_3x3", "dgrad", "f16", "f16", "u11",
+                 conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
+                           groups=1),
+                 pool=-1, modes=("dp_sk",), reductions=("linear", "tree")),
     ]
 }
