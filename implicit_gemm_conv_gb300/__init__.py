@@ -74,6 +74,8 @@ _lib.sk_gemm_rowcol_fp8.argtypes = [_i64, _i64, _i64, _p, _p, _p, _p, _p, _i64, 
 _lib.sk_conv2d_wgrad_nhwc.argtypes = [_i32, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
                                       _i32, _i32, _i32, _i32, _p, _p, _p, _i32, _i32, _i32, _p,
                                       _sz, _p]
+_lib.sk_gemm_tensorquant_fp8.argtypes = [_i64, _i64, _i64, _p, _p, ctypes.c_float, ctypes.c_float,
+                                         _p, _i64, _i32, _i32, _i32, _p, _sz, _p]
 _lib.sk_conv2d_fprop_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
 _lib.sk_conv2d_dgrad_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
 _lib.sk_workspace_bytes.argtypes = [ctypes.POINTER(sk_problem), _i32, _i32, _i32,
@@ -96,7 +98,8 @@ _lib.sk_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(
 EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_workspace_bytes",
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
            "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws",
-           "sk_set_tile", "sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc"]
+           "sk_set_tile", "sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc",
+           "sk_gemm_tensorquant_fp8"]
 
 
 class SkError(RuntimeError):
@@ -210,6 +213,21 @@ def sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, streamk="dp_sk", reduction="linear", c
                                           sb.data_ptr(), C.data_ptr(), C.stride(0),
                                           _code(MODES, streamk), _code(REDUCTIONS, reduction),
                                           ctas, wp, wb, _stream_ptr(stream)))
+
+
+def sk_gemm_tensorquant_fp8(A8, B8, scale_a, scale_b, C, streamk="dp_sk", reduction="linear",
+                            ctas=-1, ws=None, stream=None):
+    """C [M, N] bf16 = (A8 @ B8.T) * scale_a * scale_b for e4m3 A8 [M, K], B8 [N, K] and two
+    scalar (per-tensor) scales."""
+    M, K = A8.shape
+    N = B8.shape[0]
+    assert A8.is_contiguous() and B8.is_contiguous() and C.stride(1) == 1
+    wp, wb = _ws(ws)
+    return _check(_lib.sk_gemm_tensorquant_fp8(M, N, K, A8.data_ptr(), B8.data_ptr(),
+                                               float(scale_a), float(scale_b), C.data_ptr(),
+                                               C.stride(0), _code(MODES, streamk),
+                                               _code(REDUCTIONS, reduction), ctas, wp, wb,
+                                               _stream_ptr(stream)))
 
 
 def sk_conv2d_wgrad_nhwc(x, dy, dw, R, S, stride=(1, 1), pad=(0, 0), groups=1, streamk="dp_sk",

@@ -513,6 +513,8 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.ldc = kp.ldc;
             s2.sa = kp.sa;
             s2.sb = kp.sb;
+            s2.scale = kp.scale;
+            s2.tensor_scaled = (v.op_kind == sk::kOpFp8 && kp.sa == nullptr) ? 1 : 0;
             s2.scratch = kp.scratch;
             s2.c_dtype = kp.c_dtype;
             s2.op_kind = v.op_kind;
@@ -680,14 +682,19 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
     return run(prob, streamk, reduction, ctas, kp, C, ldc * cs, M, N * cs, ws, ws_bytes, st);
 }
 
-int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
-                       const float* sa, const float* sb, void* C_bf16, int64_t ldc, int streamk,
-                       int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+// The fp8 GEMM with either per-row / per-column scales (sa, sb) or per-tensor scales (sa == sb ==
+// null, `scale` = scale_a * scale_b).
+int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, const float* sa,
+             const float* sb, float scale, void* C_bf16, int64_t ldc, int streamk, int reduction,
+             int ctas, void* ws, size_t ws_bytes, void* stream) {
     int rc = check_common(streamk, reduction, ctas, SK_BF16);
     if (rc) return rc;
     if (M < 0 || N < 0 || K < 0) return fail(SK_ERR_UNSUPPORTED, "negative size");
     if (M == 0 || N == 0) return SK_OK;
-    if (!A8 || !B8 || !sa || !sb || !C_bf16) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    if (!A8 || !B8 || !C_bf16 || (sa == nullptr) != (sb == nullptr))
+        return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
     if (K < 16 || K % 16 != 0) return fail(SK_ERR_UNSUPPORTED, "K must be a positive multiple of 16, got %lld", (long long)K);
     if (ldc < N || (ldc * 2) % 16) return fail(SK_ERR_UNSUPPORTED, "ldc must be >= N with 16-byte rows");
     if (!aligned16(A8) || !aligned16(B8) || !aligned16(C_bf16))
@@ -722,10 +729,28 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
     kp.c_tma = 1;
     kp.sa = sa;
     kp.sb = sb;
+    kp.scale = scale;
     kp.idesc = sk::make_idesc(0, 0, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
                               static_cast<uint32_t>(tc.tn));
     return run(prob, streamk, reduction, ctas, kp, C_bf16, ldc * 2, M, N * 2, ws, ws_bytes,
                static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                       const float* sa, const float* sb, void* C_bf16, int64_t ldc, int streamk,
+                       int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    if (M > 0 && N > 0 && (!sa || !sb)) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
+    return fp8_gemm(M, N, K, A8, B8, sa, sb, 1.0f, C_bf16, ldc, streamk, reduction, ctas, ws,
+                    ws_bytes, stream);
+}
+
+int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                            float scale_a, float scale_b, void* C_bf16, int64_t ldc, int streamk,
+                            int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    return fp8_gemm(M, N, K, A8, B8, nullptr, nullptr, scale_a * scale_b, C_bf16, ldc, streamk,
+                    reduction, ctas, ws, ws_bytes, stream);
 }
 
 int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64_t W, int64_t C,

@@ -423,7 +423,7 @@ struct EpiCtx {
     int64_t n_end;         // output columns of this tile's group end here (exclusive)
     int row;               // accumulator row 0..127
     int64_t half;          // CG = 2: rank of this CTA in its pair (which 128 rows of the tile); else 0
-    float row_scale;       // fp8: sa[out_row]; else 1
+    float row_scale;       // fp8: sa[out_row] (per-tensor: the scale product); else 1
 };
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
@@ -440,7 +440,7 @@ __device__ __forceinline__ void store_out(const KernelParams& P, const EpiCtx& e
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int64_t n = n0 + i;
-            v[i] *= e.row_scale * (n < ncols ? __ldg(P.sb + n) : 0.0f);
+            v[i] *= e.row_scale * (n < ncols ? (P.sb ? __ldg(P.sb + n) : 1.0f) : 0.0f);
         }
     }
     const bool full = n0 + 32 <= ncols;
@@ -552,8 +552,8 @@ __device__ void store_tile_tma(const KernelParams& P, const EpiCtx& e, uint32_t 
                 float a = as_f(r[h][i]), b = as_f(r[h][i + 1]);
                 if constexpr (OP == kOpFp8) {
                     const int64_t n = e.n_base + sl * 64 + h * 32 + i;
-                    a *= e.row_scale * (n < ncols ? __ldg(P.sb + n) : 0.0f);
-                    b *= e.row_scale * (n + 1 < ncols ? __ldg(P.sb + n + 1) : 0.0f);
+                    a *= e.row_scale * (n < ncols ? (P.sb ? __ldg(P.sb + n) : 1.0f) : 0.0f);
+                    b *= e.row_scale * (n + 1 < ncols ? (P.sb ? __ldg(P.sb + n + 1) : 1.0f) : 0.0f);
                 }
                 uint32_t w;
                 if (bf16) {
@@ -829,7 +829,8 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             e.n_end = plan.gemm_n;
         }
         e.row_scale = 1.0f;
-        if constexpr (OP == kOpFp8) e.row_scale = e.row_ok ? __ldg(P.sa + e.out_row) : 0.0f;
+        if constexpr (OP == kOpFp8)
+            e.row_scale = e.row_ok ? (P.sa ? __ldg(P.sa + e.out_row) : P.scale) : 0.0f;
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
         SegCursor ahead = cur;
         sk_segment_t next;
@@ -986,6 +987,8 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     if (P.sa != nullptr) {
         const float rs = P.sa[out_row];
         for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
+    } else if (P.tensor_scaled) {
+        for (int j = 0; j < 4; ++j) v[j] *= P.scale;
     }
     const int64_t off = out_row * P.ldc + col;
     const bool full = n0 + 4 <= plan.gemm_n;

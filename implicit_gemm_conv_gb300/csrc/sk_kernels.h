@@ -51,8 +51,9 @@ struct KernelParams {
     sk_plan_t plan;
     void* c;               // output
     int64_t ldc;           // output row stride (elements)
-    const float* sa;       // fp8 row scales (else null)
-    const float* sb;       // fp8 column scales (else null)
+    const float* sa;       // fp8 row scales; null for the per-tensor scaling below
+    const float* sb;       // fp8 column scales; null for the per-tensor scaling below
+    float scale;           // fp8 with sa == sb == null: the product of the two tensor scales
     uint32_t* flags;       // per-publisher flags (linear/tree)
     uint32_t* control;     // [0] ticket counter
     float* partials;       // linear/tree partial tiles, one slot per publisher
@@ -72,6 +73,8 @@ struct Stage2Params {
     int64_t ldc;
     const float* sa;
     const float* sb;
+    float scale;           // fp8 per-tensor scaling (sa == sb == null)
+    int32_t tensor_scaled; // 1: multiply by `scale`
     const float* scratch;
     int32_t c_dtype;
 };

@@ -146,6 +146,16 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
                        void* stream);
 
 /*
+ * C[m][n] = bf16( (sum_k e4m3(A8[m][k]) * e4m3(B8[n][k])) * scale_a * scale_b ). PR #10439 (the
+ * five block-scale quant GEMM bridges), Summary, "tensor_quant": one scalar scale for the whole A
+ * matrix and one for the whole B matrix, applied in the epilogue. Same operands, layouts and
+ * limits as sk_gemm_rowcol_fp8; the scales are passed by value.
+ */
+int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                            float scale_a, float scale_b, void* C_bf16, int64_t ldc, int streamk,
+                            int reduction, int ctas, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Backward-weight 2-D convolution as an implicit GEMM. [P2] PR body "Wgrad kernel" and commit
  * "Port CK Tile's stream-K to the backward-weight convolution": the output is filter-sized, the
  * reduction runs over N*Ho*Wo, and conv groups fold into GEMM-M per group.

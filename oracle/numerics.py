@@ -128,6 +128,19 @@ def fp8_rowcol_points(A8, B8, sa, sb, ms, ns, nthreads=0):
     return out
 
 
+def fp8_tensorquant_rows(A8, B8, scale_a, scale_b, m0=0, m1=None):
+    """Per-tensor fp8 GEMM (PR #10439, Summary, "tensor_quant": one scalar scale for all of A,
+    one for all of B): C[m][n] = (sum_k deq(A8[m][k]) * deq(B8[n][k])) * scale_a * scale_b, rows
+    [m0, m1), in fp64 from the E4M3 definitions (the product of decoded operands is exact in
+    fp64; numpy's matmul sums it). The scales are the fp32 values the kernel receives."""
+    A = decode(np.ascontiguousarray(A8), "e4m3")
+    B = decode(np.ascontiguousarray(B8), "e4m3")
+    m1 = A.shape[0] if m1 is None else m1
+    sa = float(np.float32(scale_a))
+    sb = float(np.float32(scale_b))
+    return (A[m0:m1] @ B.T) * sa * sb
+
+
 def wgrad_nhwc(fmt, x_bits, dy_bits, R, S, stride=(1, 1), pad=(0, 0), groups=1, k0=0, k1=None,
                nthreads=0):
     """fp64 dW[k0:k1] ([k][r][s][c], c per group) of the NHWC backward-weight convolution."""

@@ -158,6 +158,21 @@ def test_fprop_and_dgrad_all_ones_closed_form(oracle_lib):
                 assert np.all(dx[(n * H + h) * W + w_] == rows * cols * (K // G))
 
 
+def test_fp8_tensorquant_vs_torch(oracle_lib):
+    # per-tensor scales: torch's own e4m3 decode and fp64 matmul, times the two scalars
+    A, B, _, _ = fp8_operands(37, 29, 96, seed_offset=9)
+    sa, sb = 0.75, 1.625
+    ref = (A.double() @ B.double().T) * sa * sb
+    out = numerics.fp8_tensorquant_rows(_bits(A), _bits(B), sa, sb)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    # the same as row/col scales with constant vectors
+    rc = numerics.fp8_rowcol_rows(_bits(A), _bits(B), np.full(37, sa, np.float32),
+                                  np.full(29, sb, np.float32))
+    np.testing.assert_allclose(out, rc, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(numerics.fp8_tensorquant_rows(_bits(A), _bits(B), sa, sb, 5, 9),
+                                  out[5:9])
+
+
 def test_round_output_and_tolerance():
     ref = np.array([1.0 + 2.0 ** -12, -3.0, 0.1])
     np.testing.assert_array_equal(numerics.round_output(ref, "f16"), codec.round_to(ref, "f16"))
