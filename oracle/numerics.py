@@ -50,6 +50,8 @@ def _load():
         lib.oracle_fp8_rowcol_rows.argtypes = [i64, i64, i64, i64, p, i64, p, i64, p, p, p, i32]
         lib.oracle_wgrad_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
                                           i32, i32, p, p, i64, i64, p, i32]
+        lib.oracle_fp8_blockscale_points.argtypes = [i64, i64, i64, p, p, p, i64, p, i64, i64, p,
+                                                     p, i64, p, i32]
         lib.oracle_fprop_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
                                           i32, i32, p, p, i64, i64, p, i32]
         lib.oracle_dgrad_nhwc.argtypes = [i32, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32,
@@ -139,6 +141,34 @@ def fp8_tensorquant_rows(A8, B8, scale_a, scale_b, m0=0, m1=None):
     sa = float(np.float32(scale_a))
     sb = float(np.float32(scale_b))
     return (A[m0:m1] @ B.T) * sa * sb
+
+
+def fp8_blockscale_points(A8, B8, sa, gka, sb, gnb, gkb, ms, ns, nthreads=0):
+    """Block-scaled fp8 GEMM at the points (ms[i], ns[i]), fp64: sa [M][ceil(K/gka)] or None,
+    sb [ceil(N/gnb)][ceil(K/gkb)] or None (a missing scale is 1)."""
+    A = np.ascontiguousarray(A8, dtype=np.uint8)
+    B = np.ascontiguousarray(B8, dtype=np.uint8)
+    M, K = A.shape
+    N = B.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    sa_ = None if sa is None else np.ascontiguousarray(sa, dtype=np.float32)
+    sb_ = None if sb is None else np.ascontiguousarray(sb, dtype=np.float32)
+    out = np.empty(ms.size, dtype=np.float64)
+    _load().oracle_fp8_blockscale_points(M, N, K, _ptr(A), _ptr(B),
+                                         None if sa_ is None else _ptr(sa_), gka,
+                                         None if sb_ is None else _ptr(sb_), gnb, gkb, _ptr(ms),
+                                         _ptr(ns), ms.size, _ptr(out), nthreads)
+    return out
+
+
+def fp8_blockscale_rows(A8, B8, sa, gka, sb, gnb, gkb, m0=0, m1=None, nthreads=0):
+    """Rows [m0, m1) of the block-scaled fp8 GEMM (see fp8_blockscale_points)."""
+    M, N = A8.shape[0], B8.shape[0]
+    m1 = M if m1 is None else m1
+    mm, nn = np.meshgrid(np.arange(m0, m1), np.arange(N), indexing="ij")
+    return fp8_blockscale_points(A8, B8, sa, gka, sb, gnb, gkb, mm.ravel(), nn.ravel(),
+                                 nthreads).reshape(m1 - m0, N)
 
 
 def wgrad_nhwc(fmt, x_bits, dy_bits, R, S, stride=(1, 1), pad=(0, 0), groups=1, k0=0, k1=None,

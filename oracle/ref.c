@@ -20,6 +20,9 @@
  *   RowColQuant fp8 GEMM (rocm-libraries PR #9979, Scope: per-row scale of A, per-column scale
  *   of B, fp32 accumulator narrowed only at the end):
  *       C[m][n] = (sum_k deq(A8[m][k]) * deq(B8[n][k])) * sa[m] * sb[n]
+ *   Block-scaled fp8 GEMM (PR #10439, Summary: "aquant" scales A in blocks along K, "bquant" scales
+ *   B in blocks along N and K, "abquant" both), with a missing scale read as 1:
+ *       C[m][n] = sum_k sa[m][k/gka] * sb[n/gnb][k/gkb] * deq(A8[m][k]) * deq(B8[n][k])
  *   Forward convolution and data gradient (PR #13151 lists the forward convolution as future work
  *   on the same machinery; both are the plain definitions, NHWC activations, KRSC filters):
  *       y[n][ho][wo][g*Kg+k]  = sum_{r,s,c} x[n][ho*sh-ph+r][wo*sw-pw+s][g*Cg+c] * w[g*Kg+k][r][s][c]
@@ -274,5 +277,33 @@ void oracle_dgrad_nhwc(int fmt, int64_t N, int64_t H, int64_t W, int64_t C, int6
             }
             dx[(p - p0) * C + ci] = acc;
         }
+    free(tab);
+}
+
+/*
+ * Block-scaled fp8 GEMM for the listed (m, n): sa [M][ceil(K/gka)] or NULL, sb [ceil(N/gnb)]
+ * [ceil(K/gkb)] or NULL; A8 [M][K], B8 [N][K] row-major E4M3.
+ */
+void oracle_fp8_blockscale_points(int64_t M, int64_t N, int64_t K, const uint8_t *A8,
+                                  const uint8_t *B8, const float *sa, int64_t gka, const float *sb,
+                                  int64_t gnb, int64_t gkb, const int64_t *ms, const int64_t *ns,
+                                  int64_t npts, double *out, int nthreads) {
+    double *tab = make_table(3);
+    set_threads(nthreads);
+    const int64_t nka = sa ? (K + gka - 1) / gka : 0;
+    const int64_t nkb = sb ? (K + gkb - 1) / gkb : 0;
+    (void)M;
+    (void)N;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < npts; ++i) {
+        const int64_t m = ms[i], n = ns[i];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double s = (sa ? (double)sa[m * nka + k / gka] : 1.0) *
+                             (sb ? (double)sb[(n / gnb) * nkb + k / gkb] : 1.0);
+            acc += s * tab[A8[m * K + k]] * tab[B8[n * K + k]];
+        }
+        out[i] = acc;
+    }
     free(tab);
 }

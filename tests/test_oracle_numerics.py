@@ -6,7 +6,8 @@ import pytest
 import torch
 
 from oracle import codec, numerics
-from workloads import dgrad_operands, fp8_operands, fprop_operands, gemm_operands, wgrad_operands
+from workloads import (blockscale_scales, dgrad_operands, fp8_operands, fprop_operands,
+                       gemm_operands, wgrad_operands)
 
 
 def _bits(t):
@@ -171,6 +172,33 @@ def test_fp8_tensorquant_vs_torch(oracle_lib):
     np.testing.assert_allclose(out, rc, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(numerics.fp8_tensorquant_rows(_bits(A), _bits(B), sa, sb, 5, 9),
                                   out[5:9])
+
+
+@pytest.mark.parametrize("case", [
+    dict(M=37, N=29, K=300, gka=128, gnb=8, gkb=64, a=True, b=False),    # aquant, ragged K block
+    dict(M=20, N=50, K=256, gka=64, gnb=16, gkb=128, a=False, b=True),   # bquant
+    dict(M=33, N=40, K=384, gka=128, gnb=32, gkb=128, a=True, b=True),   # abquant
+    dict(M=9, N=7, K=96, gka=32, gnb=3, gkb=48, a=True, b=True),
+])
+def test_fp8_blockscale_vs_torch_scaled_operands(oracle_lib, case):
+    # Independent formulation: scale every element of A and B by its block's scale in fp64, then
+    # one matmul in torch (fp64).
+    c = case
+    A, B, _, _ = fp8_operands(c["M"], c["N"], c["K"], seed_offset=14)
+    sa, sb = blockscale_scales(c["M"], c["N"], c["K"], c["gka"], c["gnb"], c["gkb"], seed_offset=14)
+    k = torch.arange(c["K"])
+    As = A.double() * (sa.double()[:, k // c["gka"]] if c["a"] else 1.0)
+    Bs = B.double() * (sb.double()[torch.arange(c["N"]) // c["gnb"]][:, k // c["gkb"]] if c["b"] else 1.0)
+    ref = (As @ Bs.T).numpy()
+    out = numerics.fp8_blockscale_rows(_bits(A), _bits(B), sa.numpy() if c["a"] else None, c["gka"],
+                                       sb.numpy() if c["b"] else None, c["gnb"], c["gkb"])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    if not c["a"] and not c["b"]:
+        return
+    # with every scale 1 it is the plain fp8 product
+    one = numerics.fp8_blockscale_rows(_bits(A), _bits(B), np.ones_like(sa.numpy()), c["gka"],
+                                       np.ones_like(sb.numpy()), c["gnb"], c["gkb"])
+    np.testing.assert_allclose(one, (A.double() @ B.double().T).numpy(), rtol=1e-12, atol=1e-12)
 
 
 def test_round_output_and_tolerance():

@@ -59,6 +59,14 @@ def fp8_operands(M: int, N: int, K: int, seed_offset: int = 0):
     return A, B, sa, sb
 
 
+def blockscale_scales(M: int, N: int, K: int, gka: int, gnb: int, gkb: int, seed_offset: int = 0):
+    """Block scales from uniform[0.5, 2]: sa [M][ceil(K/gka)] (A blocks along K) and
+    sb [ceil(N/gnb)][ceil(K/gkb)] (B blocks along N and K)."""
+    sa = draw((M, -(-K // gka)), "u0.5_2", SEED_SA + seed_offset)
+    sb = draw((-(-N // gnb), -(-K // gkb)), "u0.5_2", SEED_SB + seed_offset)
+    return sa, sb
+
+
 def conv_out(H: int, R: int, stride: int, pad: int) -> int:
     return (H + 2 * pad - R) // stride + 1
 
