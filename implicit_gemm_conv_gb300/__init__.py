@@ -25,7 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 F16, BF16, F32, E4M3 = 0, 1, 2, 3
 OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
 LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
-OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD, OP_FPROP, OP_DGRAD = 0, 1, 2, 3, 4
+OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD, OP_FPROP, OP_DGRAD, OP_FP8_BLOCK = 0, 1, 2, 3, 4, 5
 SEG_FULL, SEG_OWNER, SEG_PEER = 0, 1, 2
 TILE_AUTO, TILE_128, TILE_256_PAIR, TILE_256x256_PAIR = 0, 1, 2, 3
 
@@ -76,6 +76,8 @@ _lib.sk_conv2d_wgrad_nhwc.argtypes = [_i32, _i32, _i64, _i64, _i64, _i64, _i64, 
                                       _sz, _p]
 _lib.sk_gemm_tensorquant_fp8.argtypes = [_i64, _i64, _i64, _p, _p, ctypes.c_float, ctypes.c_float,
                                          _p, _i64, _i32, _i32, _i32, _p, _sz, _p]
+_lib.sk_gemm_blockscale_fp8.argtypes = [_i64, _i64, _i64, _p, _p, _p, _i64, _p, _i64, _i64, _p,
+                                        _i64, _i32, _i32, _i32, _p, _sz, _p]
 _lib.sk_conv2d_fprop_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
 _lib.sk_conv2d_dgrad_nhwc.argtypes = _lib.sk_conv2d_wgrad_nhwc.argtypes
 _lib.sk_workspace_bytes.argtypes = [ctypes.POINTER(sk_problem), _i32, _i32, _i32,
@@ -99,7 +101,7 @@ EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_work
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
            "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws",
            "sk_set_tile", "sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc",
-           "sk_gemm_tensorquant_fp8"]
+           "sk_gemm_tensorquant_fp8", "sk_gemm_blockscale_fp8"]
 
 
 class SkError(RuntimeError):
@@ -230,6 +232,29 @@ def sk_gemm_tensorquant_fp8(A8, B8, scale_a, scale_b, C, streamk="dp_sk", reduct
                                                _stream_ptr(stream)))
 
 
+def sk_gemm_blockscale_fp8(A8, B8, sa, a_group_k, sb, b_group_n, b_group_k, C, streamk="dp_sk",
+                           reduction="linear", ctas=-1, ws=None, stream=None):
+    """C [M, N] bf16 = sum_k A8[m, k] * B8[n, k] * sa[m, k // a_group_k] *
+    sb[n // b_group_n, k // b_group_k] for e4m3 A8 [M, K], B8 [N, K]; sa [M, ceil(K/a_group_k)]
+    and sb [ceil(N/b_group_n), ceil(K/b_group_k)] float32, either may be None (scale 1)."""
+    import torch
+    M, K = A8.shape
+    N = B8.shape[0]
+    if A8.element_size() != 1 or B8.element_size() != 1:
+        raise TypeError("A8 and B8 must hold one byte per element (float8_e4m3fn or uint8)")
+    for name, t in (("sa", sa), ("sb", sb)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous float32 tensor")
+    if C.dtype != torch.bfloat16:
+        raise TypeError("C must be bfloat16")
+    assert A8.is_contiguous() and B8.is_contiguous() and C.stride(1) == 1
+    wp, wb = _ws(ws)
+    return _check(_lib.sk_gemm_blockscale_fp8(
+        M, N, K, A8.data_ptr(), B8.data_ptr(), None if sa is None else sa.data_ptr(), a_group_k,
+        None if sb is None else sb.data_ptr(), b_group_n, b_group_k, C.data_ptr(), C.stride(0),
+        _code(MODES, streamk), _code(REDUCTIONS, reduction), ctas, wp, wb, _stream_ptr(stream)))
+
+
 def sk_conv2d_wgrad_nhwc(x, dy, dw, R, S, stride=(1, 1), pad=(0, 0), groups=1, streamk="dp_sk",
                          reduction="linear", ctas=-1, ws=None, stream=None):
     """dw [K, R, S, C/groups] = backward-weight of a 2-D convolution with NHWC x [N, H, W, C] and
@@ -280,7 +305,7 @@ def sk_conv2d_dgrad_nhwc(dy, w, dx, stride=(1, 1), pad=(0, 0), groups=1, streamk
 def make_problem(op, **kw) -> sk_problem:
     p = sk_problem()
     p.op = _code({"gemm": OP_GEMM, "fp8": OP_FP8_ROWCOL, "wgrad": OP_WGRAD, "fprop": OP_FPROP,
-                  "dgrad": OP_DGRAD}, op)
+                  "dgrad": OP_DGRAD, "fp8_block": OP_FP8_BLOCK}, op)
     p.groups = 1
     for k, v in kw.items():
         if k in ("ab_dtype", "c_dtype"):

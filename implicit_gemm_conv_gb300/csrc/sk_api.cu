@@ -158,11 +158,14 @@ int problem_view(const sk_problem& p, View& v) {
     switch (p.op) {
         case SK_OP_GEMM:
         case SK_OP_FP8_ROWCOL:
+        case SK_OP_FP8_BLOCK:
             v.gemm_m = p.M;
             v.gemm_n = p.N;
             v.kred = p.K;
             v.groups = 1;
-            v.op_kind = p.op == SK_OP_GEMM ? sk::kOpGemm16 : sk::kOpFp8;
+            v.op_kind = p.op == SK_OP_GEMM       ? sk::kOpGemm16
+                        : p.op == SK_OP_FP8_BLOCK ? sk::kOpFp8Block
+                                                  : sk::kOpFp8;
             return SK_OK;
         case SK_OP_FPROP:
         case SK_OP_DGRAD: {
@@ -216,6 +219,14 @@ struct TileCfg {
     int cg, tn, st;   // CTAs per logical CTA, tile N, operand-ring stages
 };
 int tile_cfg(const View& v, TileCfg& t) {
+    if (v.op_kind == sk::kOpFp8Block) {
+        // One 128 x 64 form: two 64-column partial buffers and the running sum fit 256 TMEM
+        // columns, and the epilogue's per-step promotion keeps pace with the MMAs.
+        if (g_tile == SK_TILE_256_PAIR || g_tile == SK_TILE_256x256_PAIR)
+            return fail(SK_ERR_UNSUPPORTED, "the block-scaled fp8 GEMM has no CTA-pair tile");
+        t = {1, 64, 8};
+        return SK_OK;
+    }
     t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : 6};
     switch (g_tile) {
         case SK_TILE_128: return SK_OK;
@@ -286,7 +297,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
     p.reduction = reduction;
     p.tm = sk::kTileM * cg;
     p.tn = tc.tn;
-    p.tk = prob.op == SK_OP_FP8_ROWCOL ? 128 : 64;
+    p.tk = (prob.op == SK_OP_FP8_ROWCOL || prob.op == SK_OP_FP8_BLOCK) ? 128 : 64;
     p.gemm_m = v.gemm_m;
     p.gemm_n = v.gemm_n;
     p.kred = v.kred;
@@ -686,9 +697,16 @@ namespace {
 
 // The fp8 GEMM with either per-row / per-column scales (sa, sb) or per-tensor scales (sa == sb ==
 // null, `scale` = scale_a * scale_b).
+struct BlockScales {   // the block-scaled form; blocked == false for the other two
+    bool blocked = false;
+    const float* sa = nullptr;
+    const float* sb = nullptr;
+    int64_t gka = 0, gnb = 0, gkb = 0;
+};
+
 int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, const float* sa,
              const float* sb, float scale, void* C_bf16, int64_t ldc, int streamk, int reduction,
-             int ctas, void* ws, size_t ws_bytes, void* stream) {
+             int ctas, void* ws, size_t ws_bytes, void* stream, const BlockScales& bs = BlockScales()) {
     int rc = check_common(streamk, reduction, ctas, SK_BF16);
     if (rc) return rc;
     if (M < 0 || N < 0 || K < 0) return fail(SK_ERR_UNSUPPORTED, "negative size");
@@ -705,7 +723,7 @@ int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, co
     if (rc) return rc;
     sk_problem prob;
     memset(&prob, 0, sizeof(prob));
-    prob.op = SK_OP_FP8_ROWCOL;
+    prob.op = bs.blocked ? SK_OP_FP8_BLOCK : SK_OP_FP8_ROWCOL;
     prob.ab_dtype = SK_E4M3;
     prob.c_dtype = SK_BF16;
     prob.M = M;
@@ -730,6 +748,15 @@ int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, co
     kp.sa = sa;
     kp.sb = sb;
     kp.scale = scale;
+    if (bs.blocked) {
+        kp.bsa = bs.sa;
+        kp.bsb = bs.sb;
+        kp.nka = bs.sa ? sk::ceil_div(K, bs.gka) : 0;
+        kp.nkb = bs.sb ? sk::ceil_div(K, bs.gkb) : 0;
+        kp.gka = static_cast<int32_t>(bs.sa ? bs.gka : 128);
+        kp.gnb = static_cast<int32_t>(bs.sb ? bs.gnb : 64);
+        kp.gkb = static_cast<int32_t>(bs.sb ? bs.gkb : 128);
+    }
     kp.idesc = sk::make_idesc(0, 0, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
                               static_cast<uint32_t>(tc.tn));
     return run(prob, streamk, reduction, ctas, kp, C_bf16, ldc * 2, M, N * 2, ws, ws_bytes,
@@ -751,6 +778,30 @@ int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, con
                             int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
     return fp8_gemm(M, N, K, A8, B8, nullptr, nullptr, scale_a * scale_b, C_bf16, ldc, streamk,
                     reduction, ctas, ws, ws_bytes, stream);
+}
+
+int sk_gemm_blockscale_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                           const float* sa, int64_t a_group_k, const float* sb, int64_t b_group_n,
+                           int64_t b_group_k, void* C_bf16, int64_t ldc, int streamk,
+                           int reduction, int ctas, void* ws, size_t ws_bytes, void* stream) {
+    if (sa && (a_group_k < 128 || a_group_k % 128 != 0 || a_group_k > 0x40000000LL))
+        return fail(SK_ERR_UNSUPPORTED, "a_group_k must be a positive multiple of 128, got %lld",
+                    (long long)a_group_k);
+    if (sb && (b_group_k < 128 || b_group_k % 128 != 0 || b_group_k > 0x40000000LL))
+        return fail(SK_ERR_UNSUPPORTED, "b_group_k must be a positive multiple of 128, got %lld",
+                    (long long)b_group_k);
+    if (sb && (b_group_n < 64 || b_group_n % 64 != 0 || b_group_n > 0x40000000LL))
+        return fail(SK_ERR_UNSUPPORTED, "b_group_n must be a positive multiple of 64, got %lld",
+                    (long long)b_group_n);
+    BlockScales bs;
+    bs.blocked = true;
+    bs.sa = sa;
+    bs.sb = sb;
+    bs.gka = a_group_k;
+    bs.gnb = b_group_n;
+    bs.gkb = b_group_k;
+    return fp8_gemm(M, N, K, A8, B8, nullptr, nullptr, 1.0f, C_bf16, ldc, streamk, reduction, ctas,
+                    ws, ws_bytes, stream, bs);
 }
 
 int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64_t W, int64_t C,

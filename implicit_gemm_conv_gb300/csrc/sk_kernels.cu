@@ -66,8 +66,10 @@ constexpr uint32_t kEpiBarrier = 1;
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
     static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8, "CTA pairs serve the GEMMs only");
-    static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
-    static constexpr int kElem = OP == kOpFp8 ? 1 : 2;
+    static_assert(CG == 2 || TN == 128 || (OP == kOpFp8Block && TN == 64),
+                  "one CTA computes 128 x 128 tiles (128 x 64 for the block-scaled fp8 GEMM)");
+    static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
+    static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
     static constexpr int kTileMAll = kTileM * CG;          // tile rows of the CTA (pair)
     static constexpr int kBRows = TN / CG;                 // B rows this CTA stages
@@ -80,13 +82,14 @@ struct Cfg {
     // fp32 accumulator buffers in TMEM: two (the epilogue of one segment overlaps the MMAs of the
     // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
     static constexpr int kAccBufs = TN == 256 ? 1 : 2;
-    static constexpr int kTmemCols = kAccBufs * TN;
-    static constexpr int kMmaK = OP == kOpFp8 ? 32 : 16;
+    // Block-scaled fp8: two partial buffers and a running sum (3 x 64 columns, allocated as 256).
+    static constexpr int kTmemCols = OP == kOpFp8Block ? 256 : kAccBufs * TN;
+    static constexpr int kMmaK = kFp8 ? 32 : 16;
     static constexpr int kMmasPerStage = TK / kMmaK;
     // The owner's fold stages partial tiles through the (then idle) operand ring in units of
     // 128 rows x (32 x kFoldUnitChunks) fp32 columns, contiguous in the fragment-major layout:
     // 64 KB with one CTA per SM, 32 KB in the smaller ring of a pair.
-    static constexpr int kFoldUnitChunks = CG == 1 ? 4 : 2;          // 32-column chunks per unit
+    static constexpr int kFoldUnitChunks = (CG == 1 && TN >= 128) ? 4 : 2;   // 32-column chunks per unit
     static constexpr int kFoldUnitBytes = kTileM * 32 * 4 * kFoldUnitChunks;
     static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
@@ -317,6 +320,50 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
 // MMA issuer
 // ---------------------------------------------------------------------------------------------
 
+// Waits for one ring stage and issues its MMAs into d_tmem (accumulating onto what is there when
+// `accumulate`), then commits the stage back to the producer. False if the wait gave up.
+template <int OP, int TN, int CG, int ST>
+__device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
+                                          const sk_segment_t& seg, uint32_t ring, uint32_t bars,
+                                          volatile SmemCtl* ctl, uint32_t d_tmem, bool accumulate,
+                                          uint32_t& stage, uint32_t& phase) {
+    using C = Cfg<OP, TN, CG, ST>;
+    const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
+    if (!mbar_wait(full, phase, P.mbar_timeout_ns) || ctl->abort) {
+        record_error(kErrPipeline, cta, seg.tile, 2);
+        ctl->abort = 1;
+        return false;
+    }
+    tc_fence_after();
+    const uint32_t a_addr = ring + stage * C::kStageBytes;
+    const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+    for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
+        uint64_t ad, bd;
+        // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
+        // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
+        if constexpr (OP == kOpWgrad16)
+            ad = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
+        else
+            ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+        if constexpr (OP == kOpWgrad16 || OP == kOpDgrad16)
+            bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
+        else
+            bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+        const uint32_t acc_in = (accumulate || kk > 0) ? 1u : 0u;
+        if constexpr (C::kFp8)
+            mma_f8<CG>(d_tmem, ad, bd, P.idesc, acc_in);
+        else
+            mma_f16<CG>(d_tmem, ad, bd, P.idesc, acc_in);
+    }
+    tc_commit<CG>(empty);
+    if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1;
+    }
+    return true;
+}
+
 template <int OP, int TN, int CG, int ST>
 __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                         uint32_t tmem_base, volatile SmemCtl* ctl) {
@@ -336,7 +383,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         const int64_t len = seg.k_end - seg.k_begin;
         const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
-        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
+        uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
         const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
         // A pair's accumulator is free once the epilogues of both CTAs have released it.
         const bool free_acc = CG == 2 ? mbar_wait_cluster(tempty, acc_phase ^ 1, P.mbar_timeout_ns)
@@ -347,48 +394,42 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
             break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * TN;
+        uint32_t d_tmem = tmem_base + acc * TN;
         for (int64_t j = 0; j < len; ++j) {
-            const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
-            if (!mbar_wait(full, phase, P.mbar_timeout_ns) || ctl->abort) {
-                record_error(kErrPipeline, cta, seg.tile, 2);
-                ctl->abort = 1;
+            // Block scales: every K step starts a fresh partial.
+            const bool accumulate = OP == kOpFp8Block ? false : j > 0;
+            if (!mma_stage<OP, TN, CG, ST>(P, cta, seg, ring, bars, ctl, d_tmem, accumulate, stage,
+                                           phase)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            const uint32_t a_addr = ring + stage * C::kStageBytes;
-            const uint32_t b_addr = a_addr + C::kABytes;
-#pragma unroll
-            for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
-                uint64_t ad, bd;
-                // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
-                // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
-                if constexpr (OP == kOpWgrad16)
-                    ad = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
-                else
-                    ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                if constexpr (OP == kOpWgrad16 || OP == kOpDgrad16)
-                    bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
-                else
-                    bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                const uint32_t accumulate = (j > 0 || kk > 0) ? 1u : 0u;
-                if constexpr (OP == kOpFp8)
-                    mma_f8<CG>(d_tmem, ad, bd, P.idesc, accumulate);
-                else
-                    mma_f16<CG>(d_tmem, ad, bd, P.idesc, accumulate);
-            }
-            tc_commit<CG>(empty);
             ++total_commits;
             any = true;
-            if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1;
+            if constexpr (OP == kOpFp8Block) {
+                // One partial per K step: the epilogue scales it with that step's block scales.
+                tc_commit<CG>(tfull);
+                ++nseg;
+                if (j + 1 < len) {
+                    const uint32_t a2 = static_cast<uint32_t>(nseg % C::kAccBufs);
+                    const uint32_t ph2 = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
+                    tfull = bars + (2 * C::kStages + a2) * 8;
+                    if (!mbar_wait(bars + (2 * C::kStages + 2 + a2) * 8, ph2 ^ 1, P.mbar_timeout_ns) ||
+                        ctl->abort) {
+                        record_error(kErrPipeline, cta, seg.tile, 1);
+                        ctl->abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    d_tmem = tmem_base + a2 * TN;
+                }
             }
         }
         if (!ok) break;
-        tc_commit<CG>(tfull);
-        ++nseg;
+        if constexpr (OP != kOpFp8Block) {
+            tc_commit<CG>(tfull);
+            ++nseg;
+        }
     }
     // Before the CTA may exit, every commit it issued must have landed: the last commit of each
     // stage of the ring is awaited, so that no arrival can reach this SM's shared memory after the
@@ -780,6 +821,94 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     }
 }
 
+// Block-scaled fp8, one segment: for each K step (in the order the MMAs ran it) wait for its fresh
+// partial in TMEM, load it and free its buffer, scale every row by sa[m][kb] * sb[n-block][kb] and
+// add it to the running sum, which each thread keeps for its row in registers; at the segment's
+// end the sum is written to TMEM columns 2*TN .. and goes through the usual fixups. False if a
+// wait gave up.
+template <int TN, int CG, int ST>
+__device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg, bool dp,
+                                int64_t& tau, int64_t& nstep, uint32_t tmem_base, uint32_t bars,
+                                volatile SmemCtl* ctl, uint32_t ring, int warp, int ethread,
+                                bool last) {
+    constexpr int OP = kOpFp8Block;
+    using C = Cfg<OP, TN, CG, ST>;
+    const sk_plan_t& plan = P.plan;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int64_t g, mt, nt;
+    tile_coords(plan, seg.tile, g, mt, nt);
+    EpiCtx e;
+    e.row = row;
+    e.half = 0;
+    const int64_t m = mt * kTileM + row;
+    e.row_ok = m < plan.gemm_m;
+    e.out_row = m;
+    e.n_base = nt * TN;
+    e.n_end = plan.gemm_n;
+    e.row_scale = 1.0f;
+    const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_run = tmem_base + lanes + 2 * TN;
+    const int64_t len = seg.k_end - seg.k_begin;
+    const int64_t rot = segment_rotation(plan, dp, seg, tau);
+    const float* sa_row = (P.bsa != nullptr && e.row_ok) ? P.bsa + m * P.nka : nullptr;
+    const float* sb_blk = P.bsb != nullptr ? P.bsb + (e.n_base / P.gnb) * P.nkb : nullptr;
+    float run[TN];   // this thread's row of the running sum
+#pragma unroll
+    for (int i = 0; i < TN; ++i) run[i] = 0.0f;
+    for (int64_t j = 0; j < len; ++j) {
+        int64_t k = seg.k_begin + rot + j;
+        if (k >= seg.k_end) k -= len;
+        const uint32_t acc = static_cast<uint32_t>(nstep % C::kAccBufs);
+        const uint32_t acc_phase = static_cast<uint32_t>((nstep / C::kAccBufs) & 1);
+        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
+        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
+        if (ethread == 0) {
+            const bool ready = mbar_wait(tfull, acc_phase, P.mbar_timeout_ns) && !ctl->abort;
+            if (!ready) {
+                record_error(kErrPipeline, cta, seg.tile, 3);
+                ctl->abort = 1;
+            }
+            ctl->epi_ok[nstep & 1] = ready ? 1u : 0u;
+        }
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (!ctl->epi_ok[nstep & 1]) return false;
+        tc_fence_after();
+        const int64_t kpos = k * C::TK;   // first reduction index of this step
+        float s = e.row_ok ? 1.0f : 0.0f;
+        if (sa_row) s *= __ldg(sa_row + kpos / P.gka);
+        if (sb_blk) s *= __ldg(sb_blk + kpos / P.gkb);
+        const uint32_t t_part = tmem_base + lanes + acc * TN;
+        uint32_t p[TN / 32][32];
+#pragma unroll
+        for (int c = 0; c < TN / 32; ++c) tmem_ld_32x32b_x32(t_part + c * 32, p[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);   // the partial is in registers: its buffer is free
+#pragma unroll
+        for (int c = 0; c < TN / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                run[c * 32 + i] = fmaf(s, as_f(p[c][i]), run[c * 32 + i]);
+        ++nstep;
+    }
+    // The segment's sum goes to TMEM, where the fixups and the stores read accumulators.
+#pragma unroll
+    for (int c = 0; c < TN / 32; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(run[c * 32 + i]);
+        tmem_st_32x32b_x32(t_run + c * 32, r);
+    }
+    tmem_st_wait();
+    tc_fence_after();
+    epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_run, ethread, ring,
+                                     bars + (2 * C::kStages + 4) * 8, last);
+    return true;
+}
+
 template <int OP, int TN, int CG, int ST>
 __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              uint32_t tmem_base, int warp, volatile SmemCtl* ctl, uint32_t rank) {
@@ -792,8 +921,19 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     SegCursor cur;
     seg_init(plan, cta, cur);
     sk_segment_t seg;
-    int64_t nseg = 0;
-    while (seg_next(plan, cta, cur, seg)) {
+    int64_t nseg = 0, tau = 0;
+    while (true) {
+        const bool dp = cur.dp_next >= 0;
+        if (!seg_next(plan, cta, cur, seg)) break;
+        if constexpr (OP == kOpFp8Block) {
+            SegCursor ahead = cur;
+            sk_segment_t next;
+            const bool last = !seg_next(plan, cta, ahead, next);
+            if (!promote_segment<TN, CG, ST>(P, cta, seg, dp, tau, nseg, tmem_base, bars, ctl,
+                                             ring, warp, ethread, last))
+                break;
+            continue;
+        }
         const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
         const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
@@ -1073,7 +1213,7 @@ static size_t smem_bytes_t() {
 }
 
 // (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); wgrad has no
-// pair form (the host rejects it first).
+// pair form (the host rejects it first); the block-scaled fp8 GEMM has one 128 x 64 form.
 #define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
     ((cg) == 2                                                                              \
          ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)                \
@@ -1084,6 +1224,7 @@ static size_t smem_bytes_t() {
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
      : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 6>(__VA_ARGS__)                            \
      : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 6>(__VA_ARGS__)                            \
+     : (op) == kOpFp8Block ? fn<kOpFp8Block, 64, 1, 8>(__VA_ARGS__)                           \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
 size_t main_smem_bytes(int op, int cg, int tn, int st) {
@@ -1103,13 +1244,15 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
     const int cg = p.plan.tm == 2 * kTileM ? 2 : 1;
-    const int tn = p.plan.tn == 256 ? 256 : 128;
+    const int tn = p.plan.tn == 256 ? 256 : p.plan.tn == 64 ? 64 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
     if (cg == 2 && tn == 256)
         sk_stage2_kernel<256, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else if (cg == 2)
         sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    else if (tn == 64)
+        sk_stage2_kernel<64, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else
         sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     return static_cast<int>(cudaGetLastError());

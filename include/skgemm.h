@@ -44,8 +44,9 @@
  *    the control block and the scratch (and, for SK_ATOMIC, the output) on `stream` before every
  *    launch; partial tiles are never zeroed.
  *  - Concurrent calls that share one workspace must be ordered on one stream.
- *  - Tiles are 128 x 128 (M x N), or 256 x 128 / 256 x 256 for a CTA pair (sk_set_tile); the
- *    reduction step is 64 elements for 16-bit inputs and 128 for fp8.
+ *  - Tiles are 128 x 128 (M x N), or 256 x 128 / 256 x 256 for a CTA pair (sk_set_tile), and
+ *    128 x 64 for the block-scaled fp8 GEMM; the reduction step is 64 elements for 16-bit inputs
+ *    and 128 for fp8.
  */
 #ifndef SKGEMM_H
 #define SKGEMM_H
@@ -61,7 +62,8 @@ enum { SK_F16 = 0, SK_BF16 = 1, SK_F32 = 2, SK_E4M3 = 3 };                  /* e
 enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3, SK_AUTO = 4 };  /* streamk */
 enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3, SK_REDUCTION_AUTO = 4 };
                                                                              /* reduction    */
-enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2, SK_OP_FPROP = 3, SK_OP_DGRAD = 4 };
+enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2, SK_OP_FPROP = 3, SK_OP_DGRAD = 4,
+       SK_OP_FP8_BLOCK = 5 };
                                                                              /* operation    */
 enum { SK_SEG_FULL = 0, SK_SEG_OWNER = 1, SK_SEG_PEER = 2 };                /* segment kind */
 
@@ -154,6 +156,25 @@ int sk_gemm_rowcol_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const vo
 int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
                             float scale_a, float scale_b, void* C_bf16, int64_t ldc, int streamk,
                             int reduction, int ctas, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Block-scaled fp8 GEMM. PR #10439 (the five block-scale quant GEMM bridges), Summary: "aquant"
+ * (A scaled in blocks along K), "bquant" (B scaled in 2-D blocks along N and K) and "abquant"
+ * (both). With ka = k / a_group_k and kb = k / b_group_k (integer division),
+ *   C[m][n] = bf16( sum_k e4m3(A8[m][k]) * e4m3(B8[n][k]) * sa[m][ka] * sb[n / b_group_n][kb] ),
+ * summed in fp32: the tensor cores form the exact-product partial of each 128-wide K step, and
+ * the epilogue scales it by that step's block scales and adds it to the running fp32 sum.
+ *   sa: [M][ceil(K / a_group_k)] fp32, row-major, or NULL (aquant off: scale 1);
+ *   sb: [ceil(N / b_group_n)][ceil(K / b_group_k)] fp32, row-major, or NULL (bquant off).
+ *   a_group_k, b_group_k: multiples of 128 (one K step never straddles two blocks);
+ *   b_group_n: a multiple of 64 (one 64-column tile never straddles two blocks). Group sizes of
+ *   a NULL scale are ignored. Operands, layouts and limits otherwise as sk_gemm_rowcol_fp8
+ *   (SK_ATOMIC rejected); the tile is 128 x 64 (sk_set_tile's pair settings are rejected).
+ */
+int sk_gemm_blockscale_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
+                           const float* sa, int64_t a_group_k, const float* sb, int64_t b_group_n,
+                           int64_t b_group_k, void* C_bf16, int64_t ldc, int streamk,
+                           int reduction, int ctas, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Backward-weight 2-D convolution as an implicit GEMM. [P2] PR body "Wgrad kernel" and commit

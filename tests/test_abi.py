@@ -159,6 +159,35 @@ def test_fp8_rejections():
     assert rc == -2 and "multiple of 16" in sk.last_error()
 
 
+@pytest.mark.parametrize("kw,reason", [
+    (dict(gka=64), "a_group_k"),
+    (dict(gka=200), "a_group_k"),
+    (dict(gkb=0), "b_group_k"),
+    (dict(gnb=32), "b_group_n"),
+    (dict(gnb=96), "b_group_n"),
+    (dict(red=sk.ATOMIC), "atomic"),
+    (dict(K=100), "multiple of 16"),
+    (dict(ldc=32), "ldc"),
+])
+def test_blockscale_rejections(kw, reason):
+    a = dict(M=256, N=256, K=1024, sa=FAKE, gka=128, sb=FAKE, gnb=128, gkb=256, ldc=256,
+             red=sk.LINEAR)
+    a.update(kw)
+    lib = sk.library()
+    rc = lib.sk_gemm_blockscale_fp8(a["M"], a["N"], a["K"], FAKE, FAKE, a["sa"], a["gka"], a["sb"],
+                                    a["gnb"], a["gkb"], FAKE, a["ldc"], sk.DP_SK, a["red"], -1, None,
+                                    0, None)
+    assert rc == -2 and reason in sk.last_error(), (rc, sk.last_error())
+
+
+def test_blockscale_group_sizes_of_a_missing_scale_are_ignored():
+    # sb == NULL: b_group_n / b_group_k are not checked; the call then stops at the device gate
+    lib = sk.library()
+    rc = lib.sk_gemm_blockscale_fp8(256, 256, 1024, FAKE, FAKE, FAKE, 128, None, 0, 0, FAKE, 256,
+                                    sk.DP_SK, sk.LINEAR, -1, None, 0, None)
+    assert rc == -2 and "group" not in sk.last_error()
+
+
 def test_default_pool():
     assert sk.sk_default_pool("linear", 148, 1) == 148
     assert sk.sk_default_pool("tree", 148, 2) == 148
