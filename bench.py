@@ -245,6 +245,12 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
                     lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
                                                     c["pad"], c["groups"], mode, red, w.pool,
                                                     ws=ws), w.flops())
+        elif w.op == "fp8_block":   # one tile shape (128 x 128)
+            call = blockscale_call(torch, sk, w, dev, ws)
+            variants = [(m, r) for m in w.modes for r in w.reductions]
+            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]
+            for mode, red in dict.fromkeys(variants):
+                res[f"128:{mode}/{red}"] = rate(lambda: call(mode, red, w.pool), w.flops())
         else:
             A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
             A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
@@ -259,6 +265,18 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
                                                           ws=ws), w.flops())
         out[name] = res
     return out
+
+
+def blockscale_call(torch, sk, w, dev, ws):
+    """A launcher for a block-scaled fp8 workload: call(mode, red, pool)."""
+    from workloads import blockscale_scales, fp8_operands
+    gka, gnb, gkb = w.blocks
+    A8, B8, _, _ = fp8_operands(w.M, w.N, w.K)
+    sa, sb = blockscale_scales(w.M, w.N, w.K, gka, gnb, gkb)
+    A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
+    C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    return lambda mode, red, pool: sk.sk_gemm_blockscale_fp8(A8, B8, sa, gka, sb, gnb, gkb, C, mode,
+                                                             red, pool, ws=ws)
 
 
 def conv_call(torch, sk, w, dev, ws):
@@ -301,6 +319,9 @@ def run_variant(args, dev):
     elif w.op in ("fprop", "dgrad"):
         conv, _ = conv_call(torch, sk, w, dev, ws)
         call = lambda: conv(mode, red, pool)
+    elif w.op == "fp8_block":
+        blk = blockscale_call(torch, sk, w, dev, ws)
+        call = lambda: blk(mode, red, pool)
     elif w.op == "wgrad":
         c = w.conv
         x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],

@@ -220,11 +220,12 @@ struct TileCfg {
 };
 int tile_cfg(const View& v, TileCfg& t) {
     if (v.op_kind == sk::kOpFp8Block) {
-        // One 128 x 64 form: two 64-column partial buffers and the running sum fit 256 TMEM
-        // columns, and the epilogue's per-step promotion keeps pace with the MMAs.
+        // One 128 x 128 form: two 128-column partial buffers fill 256 TMEM columns (the running
+        // sum stays in the epilogue's registers); 5 ring stages beside the store staging and the
+        // scale ring.
         if (g_tile == SK_TILE_256_PAIR || g_tile == SK_TILE_256x256_PAIR)
             return fail(SK_ERR_UNSUPPORTED, "the block-scaled fp8 GEMM has no CTA-pair tile");
-        t = {1, 64, 8};
+        t = {1, 128, 5};
         return SK_OK;
     }
     t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : 6};
@@ -754,7 +755,7 @@ int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, co
         kp.nka = bs.sa ? sk::ceil_div(K, bs.gka) : 0;
         kp.nkb = bs.sb ? sk::ceil_div(K, bs.gkb) : 0;
         kp.gka = static_cast<int32_t>(bs.sa ? bs.gka : 128);
-        kp.gnb = static_cast<int32_t>(bs.sb ? bs.gnb : 64);
+        kp.gnb = static_cast<int32_t>(bs.sb ? bs.gnb : 128);
         kp.gkb = static_cast<int32_t>(bs.sb ? bs.gkb : 128);
     }
     kp.idesc = sk::make_idesc(0, 0, false, false, static_cast<uint32_t>(sk::kTileM * tc.cg),
@@ -790,8 +791,8 @@ int sk_gemm_blockscale_fp8(int64_t M, int64_t N, int64_t K, const void* A8, cons
     if (sb && (b_group_k < 128 || b_group_k % 128 != 0 || b_group_k > 0x40000000LL))
         return fail(SK_ERR_UNSUPPORTED, "b_group_k must be a positive multiple of 128, got %lld",
                     (long long)b_group_k);
-    if (sb && (b_group_n < 64 || b_group_n % 64 != 0 || b_group_n > 0x40000000LL))
-        return fail(SK_ERR_UNSUPPORTED, "b_group_n must be a positive multiple of 64, got %lld",
+    if (sb && (b_group_n < 128 || b_group_n % 128 != 0 || b_group_n > 0x40000000LL))
+        return fail(SK_ERR_UNSUPPORTED, "b_group_n must be a positive multiple of 128, got %lld",
                     (long long)b_group_n);
     BlockScales bs;
     bs.blocked = true;

@@ -66,8 +66,7 @@ constexpr uint32_t kEpiBarrier = 1;
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
     static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8, "CTA pairs serve the GEMMs only");
-    static_assert(CG == 2 || TN == 128 || (OP == kOpFp8Block && TN == 64),
-                  "one CTA computes 128 x 128 tiles (128 x 64 for the block-scaled fp8 GEMM)");
+    static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
     static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
     static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
@@ -81,9 +80,15 @@ struct Cfg {
     static constexpr int kMinBlocks = ST * kStageBytes <= 96 * 1024 ? 2 : 1;
     // fp32 accumulator buffers in TMEM: two (the epilogue of one segment overlaps the MMAs of the
     // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
+    // Block-scaled fp8: the two buffers take one K step's partial each (the MMAs run up to two steps
+    // ahead of the epilogue's promotion); the last step's buffer then holds the segment's sum.
     static constexpr int kAccBufs = TN == 256 ? 1 : 2;
-    // Block-scaled fp8: two partial buffers and a running sum (3 x 64 columns, allocated as 256).
-    static constexpr int kTmemCols = OP == kOpFp8Block ? 256 : kAccBufs * TN;
+    static constexpr int kTmemCols = kAccBufs * TN;
+    // Barrier slots: [full x ST][empty x ST][acc full x kAccBars][acc empty x kAccBars][fold].
+    static constexpr int kAccBars = kAccBufs < 2 ? 2 : kAccBufs;
+    static constexpr int kBarTfull = 2 * kStages;
+    static constexpr int kBarTempty = 2 * kStages + kAccBars;
+    static constexpr int kBarFold = 2 * kStages + 2 * kAccBars;
     static constexpr int kMmaK = kFp8 ? 32 : 16;
     static constexpr int kMmasPerStage = TK / kMmaK;
     // The owner's fold stages partial tiles through the (then idle) operand ring in units of
@@ -100,9 +105,13 @@ struct Cfg {
     // a CTA's last, leaves that way while the producer already fills the ring for the next one.
     static constexpr int kEpiStageBytes = (CG == 1 && OP != kOpWgrad16) ? kTileM * TN * 2 : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
-    static constexpr int kBarBytes = (2 * kStages + 4 + kFoldBufs) * 8;
+    static constexpr int kBarBytes = (kBarFold + kFoldBufs) * 8;
+    // Block-scaled fp8: each epilogue thread's ring of block scales (A and B) copied kScaleAhead
+    // K steps ahead of their use, so that their global-memory latency stays off the per-step path.
+    static constexpr int kScaleAhead = OP == kOpFp8Block ? 8 : 0;
+    static constexpr int kScaleBytes = kScaleAhead * kEpiThreads * 2 * 4;
     static constexpr size_t kSmem =
-        1024 + size_t(kRingBytes) + kEpiStageBytes + kCtlBytes + kBarBytes;
+        1024 + size_t(kRingBytes) + kEpiStageBytes + kScaleBytes + kCtlBytes + kBarBytes;
 };
 
 // Per-CTA control words. The block starts right after the operand ring, so tmem_base (written by
@@ -112,7 +121,9 @@ struct SmemCtl {
     uint32_t abort;
     long long cta;
     uint32_t epi_ok[2];   // epilogue: accumulator-ready verdict, one slot per alternate segment
+    uint32_t warp_ok[2][4];   // block-scaled fp8: each epilogue warp's verdict on a segment's steps
 };
+static_assert(sizeof(SmemCtl) <= 64, "SmemCtl must fit its 64-byte slot");
 constexpr uint32_t kTmemSentinel = 0xFFFFFFFFu;   // not a TMEM address: lane and column out of range
 
 // ---------------------------------------------------------------------------------------------
@@ -383,8 +394,8 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         const int64_t len = seg.k_end - seg.k_begin;
         const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
-        uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
-        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
+        uint32_t tfull = bars + (C::kBarTfull + acc) * 8;
+        const uint32_t tempty = bars + (C::kBarTempty + acc) * 8;
         // A pair's accumulator is free once the epilogues of both CTAs have released it.
         const bool free_acc = CG == 2 ? mbar_wait_cluster(tempty, acc_phase ^ 1, P.mbar_timeout_ns)
                                       : mbar_wait(tempty, acc_phase ^ 1, P.mbar_timeout_ns);
@@ -412,8 +423,8 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
                 if (j + 1 < len) {
                     const uint32_t a2 = static_cast<uint32_t>(nseg % C::kAccBufs);
                     const uint32_t ph2 = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
-                    tfull = bars + (2 * C::kStages + a2) * 8;
-                    if (!mbar_wait(bars + (2 * C::kStages + 2 + a2) * 8, ph2 ^ 1, P.mbar_timeout_ns) ||
+                    tfull = bars + (C::kBarTfull + a2) * 8;
+                    if (!mbar_wait(bars + (C::kBarTempty + a2) * 8, ph2 ^ 1, P.mbar_timeout_ns) ||
                         ctl->abort) {
                         record_error(kErrPipeline, cta, seg.tile, 1);
                         ctl->abort = 1;
@@ -448,7 +459,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
     }
     if (nseg > 0) {   // and the last accumulator commit
         const int64_t last = nseg - 1;
-        mbar_wait(bars + (2 * C::kStages + last % C::kAccBufs) * 8,
+        mbar_wait(bars + (C::kBarTfull + last % C::kAccBufs) * 8,
                   static_cast<uint32_t>((last / C::kAccBufs) & 1), 10000000ull);
     }
 }
@@ -824,11 +835,12 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
 // Block-scaled fp8, one segment: for each K step (in the order the MMAs ran it) wait for its fresh
 // partial in TMEM, load it and free its buffer, scale every row by sa[m][kb] * sb[n-block][kb] and
 // add it to the running sum, which each thread keeps for its row in registers; at the segment's
-// end the sum is written to TMEM columns 2*TN .. and goes through the usual fixups. False if a
-// wait gave up.
+// end the sum is written to the TMEM columns after the partial buffers and goes through the usual
+// fixups. False if a wait gave up.
 template <int TN, int CG, int ST>
 __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_segment_t& seg, bool dp,
-                                int64_t& tau, int64_t& nstep, uint32_t tmem_base, uint32_t bars,
+                                int64_t& tau, int64_t& nstep, int64_t seg_count, uint32_t tmem_base,
+                                uint32_t bars,
                                 volatile SmemCtl* ctl, uint32_t ring, int warp, int ethread,
                                 bool last) {
     constexpr int OP = kOpFp8Block;
@@ -849,63 +861,128 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
     e.n_end = plan.gemm_n;
     e.row_scale = 1.0f;
     const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_run = tmem_base + lanes + 2 * TN;
     const int64_t len = seg.k_end - seg.k_begin;
     const int64_t rot = segment_rotation(plan, dp, seg, tau);
     const float* sa_row = (P.bsa != nullptr && e.row_ok) ? P.bsa + m * P.nka : nullptr;
     const float* sb_blk = P.bsb != nullptr ? P.bsb + (e.n_base / P.gnb) * P.nkb : nullptr;
+    // Scale ring: slot d of this thread holds the (A, B) block scales of step j = d (mod D).
+    constexpr int D = C::kScaleAhead;
+    static_assert((D & (D - 1)) == 0, "the scale ring's depth is a power of two");
+    const uint32_t scl = ring + C::kRingBytes + C::kEpiStageBytes + static_cast<uint32_t>(ethread) * 8u;
+    // Fetch cursor: the K step kf of the next step to fetch (the MMAs' rotated order) and its A / B
+    // block index and offset inside the block, advanced by one step at a time (the block sizes are
+    // whole K steps), so that no division is on the per-step path.
+    const int32_t ga = P.gka / C::TK, gb = P.gkb / C::TK;
+    int64_t kf = seg.k_begin + rot, qa = kf / ga, qb = kf / gb;
+    int32_t ra = static_cast<int32_t>(kf - qa * ga), rb = static_cast<int32_t>(kf - qb * gb);
+    int64_t jf = 0;
+    auto fetch = [&]() {   // one commit group per step, empty past the segment's end
+        if (jf < len) {
+            const uint32_t slot = scl + static_cast<uint32_t>(jf & (D - 1)) * (kEpiThreads * 8u);
+            if (sa_row) cp_async_4(slot, sa_row + qa);
+            if (sb_blk) cp_async_4(slot + 4, sb_blk + qb);
+            if (++kf == seg.k_end) {   // the rotation wraps to the segment's start
+                kf = seg.k_begin;
+                qa = kf / ga;
+                qb = kf / gb;
+                ra = static_cast<int32_t>(kf - qa * ga);
+                rb = static_cast<int32_t>(kf - qb * gb);
+            } else {
+                if (++ra == ga) { ra = 0; ++qa; }
+                if (++rb == gb) { rb = 0; ++qb; }
+            }
+        }
+        ++jf;
+        cp_async_commit();
+    };
+    for (int d = 0; d < D; ++d) fetch();
+    // Partial buffer and its phase for this CTA's nstep-th K step, advanced by counting.
+    uint32_t acc = static_cast<uint32_t>(nstep % C::kAccBufs);
+    uint32_t acc_phase = static_cast<uint32_t>((nstep / C::kAccBufs) & 1);
     float run[TN];   // this thread's row of the running sum
 #pragma unroll
     for (int i = 0; i < TN; ++i) run[i] = 0.0f;
+    // Each warp waits for the partials on its own (lane 0, bounded; the verdict is shuffled to the
+    // warp), so that no barrier of all four warps is on the per-step path; after a failed wait a
+    // warp only runs the loop out. The four verdicts meet at one barrier after the loop, so every
+    // warp takes the same path into the fixups.
+    uint32_t ok = 1;
     for (int64_t j = 0; j < len; ++j) {
-        int64_t k = seg.k_begin + rot + j;
-        if (k >= seg.k_end) k -= len;
-        const uint32_t acc = static_cast<uint32_t>(nstep % C::kAccBufs);
-        const uint32_t acc_phase = static_cast<uint32_t>((nstep / C::kAccBufs) & 1);
-        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
-        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
-        if (ethread == 0) {
-            const bool ready = mbar_wait(tfull, acc_phase, P.mbar_timeout_ns) && !ctl->abort;
-            if (!ready) {
-                record_error(kErrPipeline, cta, seg.tile, 3);
-                ctl->abort = 1;
+        const uint32_t tfull = bars + (C::kBarTfull + acc) * 8;
+        const uint32_t tempty = bars + (C::kBarTempty + acc) * 8;
+        if (ok) {
+            uint32_t v = 0;
+            if (lane == 0) {
+                v = (mbar_wait(tfull, acc_phase, P.mbar_timeout_ns) && !ctl->abort) ? 1u : 0u;
+                if (!v) {
+                    record_error(kErrPipeline, cta, seg.tile, 3);
+                    ctl->abort = 1;
+                }
             }
-            ctl->epi_ok[nstep & 1] = ready ? 1u : 0u;
+            ok = __shfl_sync(0xffffffffu, v, 0);
         }
-        named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (!ctl->epi_ok[nstep & 1]) return false;
+        if (!ok) {
+            fetch();
+            continue;
+        }
         tc_fence_after();
-        const int64_t kpos = k * C::TK;   // first reduction index of this step
+        cp_async_wait<D - 1>();   // this step's group (the oldest in flight) has landed
+        const uint32_t slot = scl + static_cast<uint32_t>(j & (D - 1)) * (kEpiThreads * 8u);
         float s = e.row_ok ? 1.0f : 0.0f;
-        if (sa_row) s *= __ldg(sa_row + kpos / P.gka);
-        if (sb_blk) s *= __ldg(sb_blk + kpos / P.gkb);
+        if (sa_row) s *= ld_shared_f32(slot);
+        if (sb_blk) s *= ld_shared_f32(slot + 4);
         const uint32_t t_part = tmem_base + lanes + acc * TN;
-        uint32_t p[TN / 32][32];
+        // Two 32-column chunks per TMEM round trip, each scaled into the running sum.
 #pragma unroll
-        for (int c = 0; c < TN / 32; ++c) tmem_ld_32x32b_x32(t_part + c * 32, p[c]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty);   // the partial is in registers: its buffer is free
+        for (int c = 0; c < TN / 32; c += 2) {
+            uint32_t p0[32], p1[32];
+            tmem_ld_32x32b_x32(t_part + c * 32, p0);
+            tmem_ld_32x32b_x32(t_part + (c + 1) * 32, p1);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < TN / 32; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                run[c * 32 + i] = fmaf(s, as_f(p[c][i]), run[c * 32 + i]);
-        ++nstep;
+            for (int i = 0; i < 32; ++i) {
+                run[c * 32 + i] = fmaf(s, as_f(p0[i]), run[c * 32 + i]);
+                run[(c + 1) * 32 + i] = fmaf(s, as_f(p1[i]), run[(c + 1) * 32 + i]);
+            }
+        }
+        fetch();   // step j + D, into the slot just read (its value is consumed above)
+        if (j + 1 < len) {   // the last step's buffer is kept: it takes the segment's sum below
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+            ++nstep;
+            if (++acc == C::kAccBufs) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
     }
-    // The segment's sum goes to TMEM, where the fixups and the stores read accumulators.
+    cp_async_wait_all();
+    const int par = static_cast<int>(seg_count & 1);
+    if (lane == 0) ctl->warp_ok[par][quarter] = ok;
+    named_bar_sync(kEpiBarrier, kEpiThreads);
+    // A slot of this parity is written again only after every warp has passed the next segment's
+    // barrier, i.e. after all four have read it here.
+    if (!(ctl->warp_ok[par][0] & ctl->warp_ok[par][1] & ctl->warp_ok[par][2] & ctl->warp_ok[par][3]))
+        return false;
+    // The segment's sum goes to the buffer of its last step, where the fixups and the stores read
+    // it; then that buffer is released like the others.
+    const uint32_t t_sum = tmem_base + lanes + acc * TN;
 #pragma unroll
     for (int c = 0; c < TN / 32; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(run[c * 32 + i]);
-        tmem_st_32x32b_x32(t_run + c * 32, r);
+        tmem_st_32x32b_x32(t_sum + c * 32, r);
     }
     tmem_st_wait();
     tc_fence_after();
-    epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_run, ethread, ring,
-                                     bars + (2 * C::kStages + 4) * 8, last);
+    epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_sum, ethread, ring,
+                                     bars + C::kBarFold * 8, last);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + (C::kBarTempty + acc) * 8);
+    ++nstep;
     return true;
 }
 
@@ -921,7 +998,7 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     SegCursor cur;
     seg_init(plan, cta, cur);
     sk_segment_t seg;
-    int64_t nseg = 0, tau = 0;
+    int64_t nseg = 0, tau = 0, nblk = 0;
     while (true) {
         const bool dp = cur.dp_next >= 0;
         if (!seg_next(plan, cta, cur, seg)) break;
@@ -929,15 +1006,16 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             SegCursor ahead = cur;
             sk_segment_t next;
             const bool last = !seg_next(plan, cta, ahead, next);
-            if (!promote_segment<TN, CG, ST>(P, cta, seg, dp, tau, nseg, tmem_base, bars, ctl,
+            if (!promote_segment<TN, CG, ST>(P, cta, seg, dp, tau, nseg, nblk, tmem_base, bars, ctl,
                                              ring, warp, ethread, last))
                 break;
+            ++nblk;
             continue;
         }
         const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
-        const uint32_t tfull = bars + (2 * C::kStages + acc) * 8;
-        const uint32_t tempty = bars + (2 * C::kStages + 2 + acc) * 8;
+        const uint32_t tfull = bars + (C::kBarTfull + acc) * 8;
+        const uint32_t tempty = bars + (C::kBarTempty + acc) * 8;
         // One thread waits (bounded) and the verdict goes to all 128 epilogue threads through a
         // named barrier, so that every epilogue warp takes the same path and no barrier below
         // can be left short of arrivals.
@@ -976,7 +1054,7 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         sk_segment_t next;
         const bool last = !seg_next(plan, cta, ahead, next);
         epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ring,
-                                         bars + (2 * C::kStages + 4) * 8, last);
+                                         bars + C::kBarFold * 8, last);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -1004,8 +1082,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     static_assert(sizeof(SmemCtl) <= C::kCtlBytes, "control block");
     const uint32_t ring = smem_u32(smem);
     volatile SmemCtl* ctl =
-        reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes + C::kEpiStageBytes);
-    const uint32_t bars = ring + C::kRingBytes + C::kEpiStageBytes + C::kCtlBytes;
+        reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes);
+    const uint32_t bars = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes + C::kCtlBytes;
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const uint32_t ctl_addr = smem_u32(const_cast<SmemCtl*>(ctl));
@@ -1022,12 +1100,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
             mbar_init(bars + s * 8, 1);                    // full: producer arrive + tx bytes
             mbar_init(bars + (C::kStages + s) * 8, 1);     // empty: MMA commit
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(bars + (2 * C::kStages + a) * 8, 1);                   // accumulator full
-            mbar_init(bars + (2 * C::kStages + 2 + a) * 8, CG * kEpiThreads / 32);  // ... empty
+        for (int a = 0; a < C::kAccBars; ++a) {
+            mbar_init(bars + (C::kBarTfull + a) * 8, 1);                          // accumulator full
+            mbar_init(bars + (C::kBarTempty + a) * 8, CG * kEpiThreads / 32);     // ... empty
         }
         for (int f = 0; f < C::kFoldBufs; ++f)
-            mbar_init(bars + (2 * C::kStages + 4 + f) * 8, 1);   // owner's fold buffers
+            mbar_init(bars + (C::kBarFold + f) * 8, 1);   // owner's fold buffers
         fence_mbarrier_init();
         ctl->abort = 0;
         if (CG == 1) ctl->cta = static_cast<long long>(ticket);
@@ -1213,7 +1291,8 @@ static size_t smem_bytes_t() {
 }
 
 // (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); wgrad has no
-// pair form (the host rejects it first); the block-scaled fp8 GEMM has one 128 x 64 form.
+// pair form (the host rejects it first); the block-scaled fp8 GEMM has one form (5 stages, next to
+// its 32 KB store staging and its scale ring).
 #define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
     ((cg) == 2                                                                              \
          ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)                \
@@ -1224,7 +1303,7 @@ static size_t smem_bytes_t() {
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
      : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 6>(__VA_ARGS__)                            \
      : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 6>(__VA_ARGS__)                            \
-     : (op) == kOpFp8Block ? fn<kOpFp8Block, 64, 1, 8>(__VA_ARGS__)                           \
+     : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 1, 5>(__VA_ARGS__)                          \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
 size_t main_smem_bytes(int op, int cg, int tn, int st) {

@@ -12,7 +12,7 @@ namespace sk {
 
 enum OpKind : int {
     kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2, kOpFprop16 = 3, kOpDgrad16 = 4,
-    kOpFp8Block = 5   // fp8 with block scales: promoted per K step (128 x 64 tile)
+    kOpFp8Block = 5   // fp8 with block scales: each K step's partial promoted by the epilogue
 };
 
 // Forward convolution and data gradient fold conv groups into the output's columns (the output
@@ -68,7 +68,7 @@ struct KernelParams {
     int32_t c_dtype;
     int32_t c_tma;         // 1: a CTA's last complete tile is written with TMA stores (tmap_c)
     // kOpFp8Block: sa [M][nka] (A blocks of gka along K) and sb [ceil(N/gnb)][nkb] (B blocks of
-    // gnb x gkb), either may be null; gka, gkb multiples of 128, gnb a multiple of 64.
+    // gnb x gkb), either may be null; gka, gkb and gnb multiples of 128.
     const float* bsa;
     const float* bsb;
     int64_t nka, nkb;

@@ -44,9 +44,8 @@
  *    the control block and the scratch (and, for SK_ATOMIC, the output) on `stream` before every
  *    launch; partial tiles are never zeroed.
  *  - Concurrent calls that share one workspace must be ordered on one stream.
- *  - Tiles are 128 x 128 (M x N), or 256 x 128 / 256 x 256 for a CTA pair (sk_set_tile), and
- *    128 x 64 for the block-scaled fp8 GEMM; the reduction step is 64 elements for 16-bit inputs
- *    and 128 for fp8.
+ *  - Tiles are 128 x 128 (M x N), or 256 x 128 / 256 x 256 for a CTA pair (sk_set_tile); the
+ *    reduction step is 64 elements for 16-bit inputs and 128 for fp8.
  */
 #ifndef SKGEMM_H
 #define SKGEMM_H
@@ -167,9 +166,9 @@ int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, con
  *   sa: [M][ceil(K / a_group_k)] fp32, row-major, or NULL (aquant off: scale 1);
  *   sb: [ceil(N / b_group_n)][ceil(K / b_group_k)] fp32, row-major, or NULL (bquant off).
  *   a_group_k, b_group_k: multiples of 128 (one K step never straddles two blocks);
- *   b_group_n: a multiple of 64 (one 64-column tile never straddles two blocks). Group sizes of
- *   a NULL scale are ignored. Operands, layouts and limits otherwise as sk_gemm_rowcol_fp8
- *   (SK_ATOMIC rejected); the tile is 128 x 64 (sk_set_tile's pair settings are rejected).
+ *   b_group_n: a multiple of 128 (one 128-column tile never straddles two blocks). Group sizes
+ *   of a NULL scale are ignored. Operands, layouts and limits otherwise as sk_gemm_rowcol_fp8
+ *   (SK_ATOMIC rejected); the tile is 128 x 128 (sk_set_tile's pair settings are rejected).
  */
 int sk_gemm_blockscale_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
                            const float* sa, int64_t a_group_k, const float* sb, int64_t b_group_n,

@@ -163,8 +163,8 @@ def test_fp8_rejections():
     (dict(gka=64), "a_group_k"),
     (dict(gka=200), "a_group_k"),
     (dict(gkb=0), "b_group_k"),
-    (dict(gnb=32), "b_group_n"),
-    (dict(gnb=96), "b_group_n"),
+    (dict(gnb=64), "b_group_n"),
+    (dict(gnb=192), "b_group_n"),
     (dict(red=sk.ATOMIC), "atomic"),
     (dict(K=100), "multiple of 16"),
     (dict(ldc=32), "ldc"),

@@ -66,38 +66,38 @@ def test_blockscale_ragged(layout, mode, red):
     check_parity(C, ref, "bf16", 1040, kind="fp8", what=f"block {layout} {mode}/{red}")
 
 
-@pytest.mark.parametrize("gka,gnb,gkb", [(256, 64, 128), (512, 192, 384), (1024, 64, 1024)])
+@pytest.mark.parametrize("gka,gnb,gkb", [(256, 128, 128), (512, 256, 384), (1024, 384, 1024)])
 @pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("persistent", "tree"),
                                       ("splitk", "workspace")])
 def test_blockscale_group_sizes(gka, gnb, gkb, mode, red):
-    # groups spanning several K steps (and a B block of 3 column tiles); 24 K steps over 7 CTAs
-    # so that stream-K ranges start inside a block
+    # groups spanning several K steps and B blocks of 2 and 3 column tiles; 24 K steps over 7
+    # CTAs so that stream-K ranges start inside a block
     A, B, sa, sb, ref = case(384, 448, 3072, "abquant", gka, gnb, gkb, 2)
     C = run(A, B, sa, sb, gka, gnb, gkb, mode, red, 7)
     check_parity(C, ref, "bf16", 3072, kind="fp8", what=f"block groups {gka}/{gnb}/{gkb}")
 
 
-@pytest.mark.parametrize("shape", [(1, 8, 16), (129, 72, 144), (128, 64, 128)])
+@pytest.mark.parametrize("shape", [(1, 8, 16), (129, 136, 144), (128, 128, 128)])
 def test_blockscale_small_shapes(shape):
     M, N, K = shape
-    A, B, sa, sb, ref = case(M, N, K, "abquant", 128, 64, 128, 3)
+    A, B, sa, sb, ref = case(M, N, K, "abquant", 128, 128, 128, 3)
     for mode, red, ctas in [("dp_sk", "linear", -1), ("off", "linear", 1),
                             ("persistent", "workspace", 3)]:
-        C = run(A, B, sa, sb, 128, 64, 128, mode, red, ctas)
+        C = run(A, B, sa, sb, 128, 128, 128, mode, red, ctas)
         check_parity(C, ref, "bf16", K, kind="fp8", what=f"block {shape} {mode}/{red}")
 
 
 def test_blockscale_scales_matter():
     # The same operands with one A block scale doubled: exactly the outputs of that row and
     # block change, so the block index arithmetic cannot be off by one step.
-    M, N, K = 256, 128, 1024
-    A, B, sa, sb, ref = case(M, N, K, "abquant", 128, 64, 128, 4)
+    M, N, K = 256, 256, 1024
+    A, B, sa, sb, ref = case(M, N, K, "abquant", 128, 128, 128, 4)
     sa2 = sa.clone()
     sa2[5, 3] *= 2.0
-    ref2 = numerics.fp8_blockscale_rows(bits(A), bits(B), sa2.numpy(), 128, sb.numpy(), 64, 128)
-    C = run(A, B, sa2, sb, 128, 64, 128, "dp_sk", "linear", -1)
+    ref2 = numerics.fp8_blockscale_rows(bits(A), bits(B), sa2.numpy(), 128, sb.numpy(), 128, 128)
+    C = run(A, B, sa2, sb, 128, 128, 128, "dp_sk", "linear", -1)
     check_parity(C, ref2, "bf16", K, kind="fp8", what="block one scale doubled")
-    C0 = run(A, B, sa, sb, 128, 64, 128, "dp_sk", "linear", -1)
+    C0 = run(A, B, sa, sb, 128, 128, 128, "dp_sk", "linear", -1)
     changed = (C.float() != C0.float()).any(dim=1).nonzero().flatten().tolist()
     assert changed == [5]
 
@@ -108,7 +108,7 @@ def test_blockscale_4096_sampled(red):
     A, B, sa, sb = operands(M, N, K, "abquant", 128, 128, 128, 0)
     C = run(A, B, sa, sb, 128, 128, 128, "dp_sk", red, -1)
     assert torch.isfinite(C.float()).all(), "unwritten outputs"
-    ms, ns = sample_points(M, N, n_random=4096, tile=64)
+    ms, ns = sample_points(M, N, n_random=4096, tile=128)
     ref = numerics.fp8_blockscale_points(bits(A), bits(B), sa.numpy(), 128, sb.numpy(), 128, 128,
                                          ms, ns)
     out = C[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)]

@@ -229,7 +229,7 @@ def test_pair_tile_setting():
         sk.sk_set_tile(7)
 
 
-# ---- the block-scaled fp8 GEMM: 128 x 64 tiles, a 128-wide reduction step
+# ---- the block-scaled fp8 GEMM: 128 x 128 tiles, a 128-wide reduction step
 
 BLOCK_NAMED = [
     ("fp8 block 4096x4096x4096", (4096, 4096, 4096), -1),
@@ -240,7 +240,7 @@ BLOCK_NAMED = [
 
 def block_gemm(M, N, K):
     prob = sk.make_problem("fp8_block", ab_dtype="e4m3", c_dtype="bf16", M=M, N=N, K=K)
-    kw = dict(tiles_m=-(-M // 128), tiles_n=-(-N // 64), groups=1, kred=K, tm=128, tn=64, tk=128)
+    kw = dict(tiles_m=-(-M // 128), tiles_n=-(-N // 128), groups=1, kred=K, tm=128, tn=128, tk=128)
     return prob, kw
 
 
@@ -251,14 +251,14 @@ def test_block_scale_plans(name, shape, ctas, mode, red):
     prob, kw = block_gemm(*shape)
     big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
     cp = compare(prob, kw, mode, red, ctas, num_sms=152, check_ctas=big)
-    assert (cp.tm, cp.tn, cp.iters_per_tile) == (128, 64, -(-shape[2] // 128))
+    assert (cp.tm, cp.tn, cp.iters_per_tile) == (128, 128, -(-shape[2] // 128))
 
 
 def test_block_scale_tile_setting():
     prob, _ = block_gemm(4096, 4096, 4096)
     for t in ("auto", "128"):
         with sk.tile(t):
-            assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn == 64
+            assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn == 128
     for t in ("256_pair", "256x256_pair"):
         with sk.tile(t):
             with pytest.raises(sk.SkError, match="no CTA-pair tile"):

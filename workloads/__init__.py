@@ -97,7 +97,7 @@ def dgrad_operands(N, H, W, C, K, R, S, stride, pad, groups, dtype, dist, seed_o
 @dataclass
 class Workload:
     name: str
-    op: str                      # "gemm" | "wgrad" | "fp8" | "fprop" | "dgrad"
+    op: str                      # "gemm" | "wgrad" | "fp8" | "fp8_block" | "fprop" | "dgrad"
     ab: str                      # input storage type
     out: str                     # output type
     dist: str
@@ -108,6 +108,7 @@ class Workload:
     pool: int = -1
     modes: Tuple[str, ...] = ("dp_sk",)
     reductions: Tuple[str, ...] = ("linear",)
+    blocks: Optional[Tuple[int, int, int]] = None   # fp8_block: (a_group_k, b_group_n, b_group_k)
 
     def _conv_dims(self):
         c = self.conv
@@ -159,6 +160,9 @@ class Workload:
             dw = c["K"] * c["R"] * c["S"] * (c["C"] // c["groups"])
             return (x + dy) * sz[self.ab] + dw * sz[self.out]
         extra = 4 * (self.M + self.N) if self.op == "fp8" else 0
+        if self.op == "fp8_block":
+            gka, gnb, gkb = self.blocks
+            extra = 4 * (self.M * -(-self.K // gka) + -(-self.N // gnb) * -(-self.K // gkb))
         return (self.M + self.N) * self.K * sz[self.ab] + self.M * self.N * sz[self.out] + extra
 
 
@@ -179,6 +183,10 @@ WORKLOADS = {
                  pool=-1, modes=("dp_sk", "persistent"), reductions=("atomic", "workspace")),
         Workload("fp8_rowcol_8192x8192x8192", "fp8", "e4m3", "bf16", "n01", 8192, 8192, 8192,
                  pool=-1, modes=("dp_sk",), reductions=("linear", "tree", "workspace")),
+        # A scaled per row in blocks of 128 along K, B in 128 x 128 blocks.
+        Workload("fp8_blockscale_8192x8192x8192_a1x128_b128x128", "fp8_block", "e4m3", "bf16",
+                 "n01", 8192, 8192, 8192, pool=-1, modes=("dp_sk",),
+                 reductions=("linear", "workspace"), blocks=(128, 128, 128)),
         Workload("gemm_bf16_512x512x65536_pool148", "gemm", "bf16", "bf16", "n01", 512, 512, 65536,
                  pool=148, modes=("dp_sk", "persistent"),
                  reductions=("linear", "tree", "workspace")),
