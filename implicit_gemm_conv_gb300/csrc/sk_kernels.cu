@@ -417,8 +417,8 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
             ++total_commits;
             any = true;
             if constexpr (OP == kOpFp8Block) {
-                // One partial per K step: the epilogue scales it with that step's block scales.
-                tc_commit<CG>(tfull);
+                // One partial per K step: the epilogue scales it with that step's block scales. Its
+                // completion is the ring stage's commit (mma_stage), which the epilogue waits on.
                 ++nseg;
                 if (j + 1 < len) {
                     const uint32_t a2 = static_cast<uint32_t>(nseg % C::kAccBufs);
@@ -457,7 +457,7 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
             mbar_wait(bars + (C::kStages + st) * 8, ph, 10000000ull);
         }
     }
-    if (nseg > 0) {   // and the last accumulator commit
+    if (OP != kOpFp8Block && nseg > 0) {   // and the last accumulator commit
         const int64_t last = nseg - 1;
         mbar_wait(bars + (C::kBarTfull + last % C::kAccBufs) * 8,
                   static_cast<uint32_t>((last / C::kAccBufs) & 1), 10000000ull);
@@ -896,9 +896,13 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
         cp_async_commit();
     };
     for (int d = 0; d < D; ++d) fetch();
-    // Partial buffer and its phase for this CTA's nstep-th K step, advanced by counting.
+    // Partial buffer for this CTA's nstep-th K step, and the ring stage whose MMA commit marks that
+    // step's partial complete (and the phase of that commit), advanced by counting. The commit of
+    // a stage cannot complete a second phase before the epilogue has seen the first: the MMAs of
+    // the stage's next use wait for a partial buffer that the epilogue frees only after this step.
     uint32_t acc = static_cast<uint32_t>(nstep % C::kAccBufs);
-    uint32_t acc_phase = static_cast<uint32_t>((nstep / C::kAccBufs) & 1);
+    uint32_t rs = static_cast<uint32_t>(nstep % C::kStages);
+    uint32_t rs_phase = static_cast<uint32_t>((nstep / C::kStages) & 1);
     float run[TN];   // this thread's row of the running sum
 #pragma unroll
     for (int i = 0; i < TN; ++i) run[i] = 0.0f;
@@ -908,12 +912,12 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
     // warp takes the same path into the fixups.
     uint32_t ok = 1;
     for (int64_t j = 0; j < len; ++j) {
-        const uint32_t tfull = bars + (C::kBarTfull + acc) * 8;
+        const uint32_t done = bars + (C::kStages + rs) * 8;   // the stage's MMA commit
         const uint32_t tempty = bars + (C::kBarTempty + acc) * 8;
         if (ok) {
             uint32_t v = 0;
             if (lane == 0) {
-                v = (mbar_wait(tfull, acc_phase, P.mbar_timeout_ns) && !ctl->abort) ? 1u : 0u;
+                v = (mbar_wait(done, rs_phase, P.mbar_timeout_ns) && !ctl->abort) ? 1u : 0u;
                 if (!v) {
                     record_error(kErrPipeline, cta, seg.tile, 3);
                     ctl->abort = 1;
@@ -951,9 +955,10 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
             ++nstep;
-            if (++acc == C::kAccBufs) {
-                acc = 0;
-                acc_phase ^= 1u;
+            if (++acc == C::kAccBufs) acc = 0;
+            if (++rs == C::kStages) {
+                rs = 0;
+                rs_phase ^= 1u;
             }
         }
     }
@@ -1323,15 +1328,13 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
     const int cg = p.plan.tm == 2 * kTileM ? 2 : 1;
-    const int tn = p.plan.tn == 256 ? 256 : p.plan.tn == 64 ? 64 : 128;
+    const int tn = p.plan.tn == 256 ? 256 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
     if (cg == 2 && tn == 256)
         sk_stage2_kernel<256, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else if (cg == 2)
         sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
-    else if (tn == 64)
-        sk_stage2_kernel<64, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else
         sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
