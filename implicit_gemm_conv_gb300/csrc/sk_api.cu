@@ -220,12 +220,14 @@ struct TileCfg {
 };
 int tile_cfg(const View& v, TileCfg& t) {
     if (v.op_kind == sk::kOpFp8Block) {
-        // One 128 x 128 form: two 128-column partial buffers fill 256 TMEM columns (the running
-        // sum stays in the epilogue's registers); 5 ring stages beside the store staging and the
-        // scale ring.
-        if (g_tile == SK_TILE_256_PAIR || g_tile == SK_TILE_256x256_PAIR)
-            return fail(SK_ERR_UNSUPPORTED, "the block-scaled fp8 GEMM has no CTA-pair tile");
-        t = {1, 128, 5};
+        // Two 128-column partial buffers fill 256 TMEM columns (the running sum stays in the
+        // epilogue's registers), so the tile is 128 columns wide: 128 x 128 on one CTA (5 ring
+        // stages beside the store staging and the scale ring, the default), or 256 x 128 on a CTA
+        // pair (7 stages) on request. The pair's per-step hand-off of each partial between the two
+        // CTAs measured twice as slow as the one-CTA tile's, so it is not chosen by itself.
+        if (g_tile == SK_TILE_256x256_PAIR)
+            return fail(SK_ERR_UNSUPPORTED, "the block-scaled fp8 GEMM has no 256 x 256 tile");
+        t = g_tile == SK_TILE_256_PAIR ? TileCfg{2, 128, 7} : TileCfg{1, 128, 5};
         return SK_OK;
     }
     t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : 6};

@@ -65,7 +65,8 @@ constexpr uint32_t kEpiBarrier = 1;
 
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
-    static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8, "CTA pairs serve the GEMMs only");
+    static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8 || OP == kOpFp8Block,
+                  "CTA pairs serve the GEMMs only");
     static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
     static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
     static constexpr int kElem = kFp8 ? 1 : 2;
@@ -103,7 +104,9 @@ struct Cfg {
     // One CTA per SM with a 16-bit output (every op but wgrad): a dedicated 32 KB buffer where the
     // epilogue stages each complete 128 x 128 tile for its TMA stores, so that every tile, not only
     // a CTA's last, leaves that way while the producer already fills the ring for the next one.
-    static constexpr int kEpiStageBytes = (CG == 1 && OP != kOpWgrad16) ? kTileM * TN * 2 : 0;
+    // The block-scaled fp8 pair keeps one too (its ring is deep enough without the space).
+    static constexpr int kEpiStageBytes =
+        ((CG == 1 && OP != kOpWgrad16) || OP == kOpFp8Block) ? kTileM * TN * 2 : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (kBarFold + kFoldBufs) * 8;
     // Block-scaled fp8: each epilogue thread's ring of block scales (A and B) copied kScaleAhead
@@ -424,8 +427,10 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
                     const uint32_t a2 = static_cast<uint32_t>(nseg % C::kAccBufs);
                     const uint32_t ph2 = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
                     tfull = bars + (C::kBarTfull + a2) * 8;
-                    if (!mbar_wait(bars + (C::kBarTempty + a2) * 8, ph2 ^ 1, P.mbar_timeout_ns) ||
-                        ctl->abort) {
+                    const uint32_t te2 = bars + (C::kBarTempty + a2) * 8;
+                    const bool free2 = CG == 2 ? mbar_wait_cluster(te2, ph2 ^ 1, P.mbar_timeout_ns)
+                                               : mbar_wait(te2, ph2 ^ 1, P.mbar_timeout_ns);
+                    if (!free2 || ctl->abort) {
                         record_error(kErrPipeline, cta, seg.tile, 1);
                         ctl->abort = 1;
                         ok = false;
@@ -842,7 +847,7 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
                                 int64_t& tau, int64_t& nstep, int64_t seg_count, uint32_t tmem_base,
                                 uint32_t bars,
                                 volatile SmemCtl* ctl, uint32_t ring, int warp, int ethread,
-                                bool last) {
+                                bool last, uint32_t rank) {
     constexpr int OP = kOpFp8Block;
     using C = Cfg<OP, TN, CG, ST>;
     const sk_plan_t& plan = P.plan;
@@ -853,8 +858,8 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
     tile_coords(plan, seg.tile, g, mt, nt);
     EpiCtx e;
     e.row = row;
-    e.half = 0;
-    const int64_t m = mt * kTileM + row;
+    e.half = static_cast<int64_t>(rank);   // a pair's CTA holds rows rank*128 .. of the tile
+    const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
     e.row_ok = m < plan.gemm_m;
     e.out_row = m;
     e.n_base = nt * TN;
@@ -906,6 +911,13 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
     float run[TN];   // this thread's row of the running sum
 #pragma unroll
     for (int i = 0; i < TN; ++i) run[i] = 0.0f;
+    // A pair's partial-buffer barriers live in the even CTA, whose thread issues the MMAs.
+    auto release = [&](uint32_t bar) {
+        if (CG == 2 && rank != 0)
+            mbar_arrive_cluster(mapa_shared(bar, 0));
+        else
+            mbar_arrive(bar);
+    };
     // Each warp waits for the partials on its own (lane 0, bounded; the verdict is shuffled to the
     // warp), so that no barrier of all four warps is on the per-step path; after a failed wait a
     // warp only runs the loop out. The four verdicts meet at one barrier after the loop, so every
@@ -953,7 +965,7 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
         if (j + 1 < len) {   // the last step's buffer is kept: it takes the segment's sum below
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
+            if (lane == 0) release(tempty);
             ++nstep;
             if (++acc == C::kAccBufs) acc = 0;
             if (++rs == C::kStages) {
@@ -986,7 +998,7 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
                                      bars + C::kBarFold * 8, last);
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + (C::kBarTempty + acc) * 8);
+    if (lane == 0) release(bars + (C::kBarTempty + acc) * 8);
     ++nstep;
     return true;
 }
@@ -1012,7 +1024,7 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             sk_segment_t next;
             const bool last = !seg_next(plan, cta, ahead, next);
             if (!promote_segment<TN, CG, ST>(P, cta, seg, dp, tau, nseg, nblk, tmem_base, bars, ctl,
-                                             ring, warp, ethread, last))
+                                             ring, warp, ethread, last, rank))
                 break;
             ++nblk;
             continue;
@@ -1296,13 +1308,14 @@ static size_t smem_bytes_t() {
 }
 
 // (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); wgrad has no
-// pair form (the host rejects it first); the block-scaled fp8 GEMM has one form (5 stages, next to
-// its 32 KB store staging and its scale ring).
+// pair form (the host rejects it first); the block-scaled fp8 GEMM has a 128 x 128 form (5 stages
+// beside its 32 KB store staging and its scale ring) and a 256 x 128 pair form (7 stages).
 #define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
     ((cg) == 2                                                                              \
          ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)                \
                                           : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
                         : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \
+                           : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 2, 7>(__VA_ARGS__)    \
                                           : fn<kOpGemm16, 128, 2, 4>(__VA_ARGS__)))           \
      : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 6>(__VA_ARGS__)                              \
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
@@ -1320,7 +1333,8 @@ int main_ctas_per_sm(int op, int cg, int tn, int st) {
 }
 
 int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream) {
-    if (cg == 2 && op != kOpGemm16 && op != kOpFp8) return static_cast<int>(cudaErrorInvalidValue);
+    if (cg == 2 && op != kOpGemm16 && op != kOpFp8 && op != kOpFp8Block)
+        return static_cast<int>(cudaErrorInvalidValue);
     return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, stream);
 }
 

@@ -168,7 +168,8 @@ int sk_gemm_tensorquant_fp8(int64_t M, int64_t N, int64_t K, const void* A8, con
  *   a_group_k, b_group_k: multiples of 128 (one K step never straddles two blocks);
  *   b_group_n: a multiple of 128 (one 128-column tile never straddles two blocks). Group sizes
  *   of a NULL scale are ignored. Operands, layouts and limits otherwise as sk_gemm_rowcol_fp8
- *   (SK_ATOMIC rejected); the tile is 128 x 128 (sk_set_tile's pair settings are rejected).
+ *   (SK_ATOMIC rejected). Tile: 128 x 128; sk_set_tile(SK_TILE_256_PAIR) selects a 256 x 128
+ *   CTA-pair tile instead (SK_TILE_256x256_PAIR is rejected).
  */
 int sk_gemm_blockscale_fp8(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8,
                            const float* sa, int64_t a_group_k, const float* sb, int64_t b_group_n,

@@ -1,7 +1,8 @@
 """GPU parity of the block-scaled fp8 GEMM (sk_gemm_blockscale_fp8 through the C ABI) against the
-fp64 oracle: the three scale layouts (A blocks along K, B blocks along N and K, both), group sizes
-of one and several K steps, a ragged last K step, every mode x deterministic/workspace reduction,
-sampled outputs of a 4096^3 problem, bit-identical linear/tree hand-offs and the smallest shapes."""
+fp64 oracle, on the 128 x 128 one-CTA tile and the 256 x 128 CTA-pair tile: the three scale layouts
+(A blocks along K, B blocks along N and K, both), group sizes of one and several K steps, a ragged
+last K step, every mode x deterministic/workspace reduction, sampled outputs of a 4096^3 problem,
+bit-identical linear/tree hand-offs and the smallest shapes."""
 import pytest
 import torch
 
@@ -14,6 +15,13 @@ import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library
 from gpu_helpers import DEV, bits, check_parity, poisoned, sample_points  # noqa: E402
 
 MODES = ["off", "dp_sk", "persistent", "splitk"]
+
+
+@pytest.fixture(autouse=True, params=["128", "256_pair"])
+def block_tile(request):
+    with sk.tile(request.param):
+        yield request.param
+
 REDS = ["linear", "tree", "workspace"]
 LAYOUTS = ["aquant", "bquant", "abquant"]
 

@@ -238,28 +238,35 @@ BLOCK_NAMED = [
 ]
 
 
-def block_gemm(M, N, K):
+def block_gemm(M, N, K, tm=128):
     prob = sk.make_problem("fp8_block", ab_dtype="e4m3", c_dtype="bf16", M=M, N=N, K=K)
-    kw = dict(tiles_m=-(-M // 128), tiles_n=-(-N // 128), groups=1, kred=K, tm=128, tn=128, tk=128)
+    kw = dict(tiles_m=-(-M // tm), tiles_n=-(-N // 128), groups=1, kred=K, tm=tm, tn=128, tk=128)
     return prob, kw
 
 
+@pytest.mark.parametrize("tile,tm", [("128", 128), ("256_pair", 256)])
 @pytest.mark.parametrize("name,shape,ctas", BLOCK_NAMED, ids=[n[0] for n in BLOCK_NAMED])
 @pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
 @pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
-def test_block_scale_plans(name, shape, ctas, mode, red):
-    prob, kw = block_gemm(*shape)
+def test_block_scale_plans(tile, tm, name, shape, ctas, mode, red):
+    prob, kw = block_gemm(*shape, tm=tm)
     big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
-    cp = compare(prob, kw, mode, red, ctas, num_sms=152, check_ctas=big)
-    assert (cp.tm, cp.tn, cp.iters_per_tile) == (128, 128, -(-shape[2] // 128))
+    with sk.tile(tile):
+        cp = compare(prob, kw, mode, red, ctas, num_sms=152, check_ctas=big, cluster=tm // 128)
+    assert (cp.tm, cp.tn, cp.iters_per_tile) == (tm, 128, -(-shape[2] // 128))
 
 
 def test_block_scale_tile_setting():
     prob, _ = block_gemm(4096, 4096, 4096)
-    for t in ("auto", "128"):
-        with sk.tile(t):
-            assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn == 128
-    for t in ("256_pair", "256x256_pair"):
-        with sk.tile(t):
-            with pytest.raises(sk.SkError, match="no CTA-pair tile"):
-                sk.sk_plan(prob, "dp_sk", "linear", 148, 148)
+    small, _ = block_gemm(128, 4096, 4096)
+    with sk.tile("auto"):   # the one-CTA tile (the pair only on request)
+        assert (sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm,
+                sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn) == (128, 128)
+        assert sk.sk_plan(small, "dp_sk", "linear", 148, 148).tm == 128
+    with sk.tile("128"):
+        assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm == 128
+    with sk.tile("256_pair"):
+        assert sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tm == 256
+    with sk.tile("256x256_pair"):
+        with pytest.raises(sk.SkError, match="no 256 x 256 tile"):
+            sk.sk_plan(prob, "dp_sk", "linear", 148, 148)
