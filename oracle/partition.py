@@ -27,6 +27,11 @@ Readings where the pages are silent (each is listed in the design notes):
 * ``dp_sk``: logical ids ``[0, sk_ctas)`` are SK CTAs, the rest run one DP tile each.
   ``persistent``: grid = P; CTA ``c`` runs DP tiles ``sk_tiles + c + k*P`` and then its SK range.
   ``off``: one CTA per tile over the whole reduction.
+* ``hybrid`` (a variant of the pages' rule, which balances only the remainder): when the pool
+  does not divide the tiles and there is at least one full wave (``T >= P``, ``T mod P != 0``),
+  the stream-K region takes one full wave more, ``P + T mod P`` tiles, so that every SK CTA runs
+  between one and two tiles' worth of iterations; otherwise it is ``dp_sk``. Grid and CTA walk
+  as in ``dp_sk``.
 * Split-K comparator: ``s = clamp(P // T, 1, I)`` slices per tile, slice ``j`` covering
   iterations ``[j*I//s, (j+1)*I//s)``.
 * Flag table: one 32-bit flag per CTA that can publish, rounded up to 256 bytes. When a logical CTA
@@ -38,7 +43,7 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 from typing import List
 
-OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
+OFF, DP_SK, PERSISTENT, SPLITK, AUTO, HYBRID = 0, 1, 2, 3, 4, 5
 LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
 
 # Auto selection: "long reduction" once the tiles hold this many MAC iterations in total (the
@@ -118,8 +123,10 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
         p.grid = T * s
         p.publishers = T * s if s > 1 else 0
     else:
-        # 2. the remainder of whole waves is the stream-K part
+        # 2. the remainder of whole waves is the stream-K part (hybrid: plus one full wave)
         p.sk_tiles = T % P
+        if mode == HYBRID and T >= P and p.sk_tiles:
+            p.sk_tiles += P
         p.dp_tiles = T - p.sk_tiles
         # 3. its iterations; too few to give every pool CTA one -> all data-parallel
         p.sk_iters = p.sk_tiles * I
@@ -134,7 +141,7 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
         else:
             p.iters_per_sk_cta, p.extra = 1, 0
         # 6. grid
-        p.grid = p.sk_ctas + p.dp_tiles if mode == DP_SK else P
+        p.grid = p.sk_ctas + p.dp_tiles if mode in (DP_SK, HYBRID) else P
         p.publishers = p.sk_ctas
     # 7. contributors of the shared tiles
     mc = 1
@@ -269,7 +276,7 @@ def cta_segments(p: Plan, c: int) -> List[Segment]:
             return [full(t)]
         lo, hi = j * p.I // s, (j + 1) * p.I // s
         return [Segment(t, lo, hi, SEG_OWNER if j == 0 else SEG_PEER, j, s, t * s)]
-    if p.mode == DP_SK:
+    if p.mode in (DP_SK, HYBRID):
         if c < p.sk_ctas:
             return _sk_segments(p, c)
         t = p.sk_tiles + (c - p.sk_ctas)
@@ -322,7 +329,7 @@ def brute_force_assignment(p: Plan):
 def check_invariants(p: Plan) -> None:
     """Raise AssertionError on any violated invariant of the partition."""
     assert p.iters_per_sk_cta >= 1
-    if p.mode in (DP_SK, PERSISTENT):
+    if p.mode in (DP_SK, PERSISTENT, HYBRID):
         assert p.dp_tiles + p.sk_tiles == p.T
         if p.T % p.P == 0:
             assert p.sk_ctas == 0 and p.dp_tiles == p.T          # all-DP when tiles divide the pool
@@ -331,6 +338,8 @@ def check_invariants(p: Plan) -> None:
             assert len(owner) == p.sk_iters                      # complete coverage
             sizes = [sk_range(p, c)[1] - sk_range(p, c)[0] for c in range(p.sk_ctas)]
             assert max(sizes) - min(sizes) <= 1                  # balanced
+            if p.mode == HYBRID and p.T >= p.P:                  # one to two tiles per SK CTA
+                assert p.I <= min(sizes) and max(sizes) <= 2 * p.I
             for c in range(p.sk_ctas):
                 b, e = sk_range(p, c)
                 assert all(owner[i] == c for i in range(b, e))   # contiguous and disjoint

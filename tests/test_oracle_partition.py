@@ -11,7 +11,8 @@ from oracle import partition as P
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "partition_page_points.txt")
 RED = {"linear": P.LINEAR, "tree": P.TREE, "atomic": P.ATOMIC, "workspace": P.WORKSPACE}
-MODE = {"off": P.OFF, "dp_sk": P.DP_SK, "persistent": P.PERSISTENT, "splitk": P.SPLITK}
+MODE = {"off": P.OFF, "dp_sk": P.DP_SK, "persistent": P.PERSISTENT, "splitk": P.SPLITK,
+        "hybrid": P.HYBRID}
 
 
 def plan(T, I, Pool, mode=P.DP_SK, red=P.LINEAR, tm=128, tn=128, tk=64):
@@ -109,10 +110,46 @@ SWEEP = [(T, I, Pool) for T, I, Pool in itertools.product(
     [1, 2, 3, 4, 5, 7, 12, 13, 148, 149, 300], [1, 2, 3, 7, 64, 65], [1, 2, 3, 4, 5, 12, 148])]
 
 
-@pytest.mark.parametrize("mode", [P.OFF, P.DP_SK, P.PERSISTENT, P.SPLITK])
+@pytest.mark.parametrize("mode", [P.OFF, P.DP_SK, P.PERSISTENT, P.SPLITK, P.HYBRID])
 def test_invariants_sweep(mode):
     for T, I, Pool in SWEEP:
         P.check_invariants(plan(T, I, Pool, mode))
+
+
+def test_hybrid_worked_vector():
+    # 10 tiles of 8 iterations on a pool of 4, worked by hand: the remainder (2 tiles) plus one
+    # full wave (4) is stream-K, 48 iterations, 12 per CTA; tiles 6..9 run data-parallel
+    p = plan(10, 8, 4, P.HYBRID)
+    assert (p.sk_tiles, p.dp_tiles, p.sk_iters, p.sk_ctas) == (6, 4, 48, 4)
+    assert (p.iters_per_sk_cta, p.extra, p.grid) == (12, 0, 8)
+    seg = lambda c: [(s.tile, s.k_begin, s.k_end, s.kind) for s in P.cta_segments(p, c)]
+    # CTA 0: iterations 0..11 = all of tile 0, then the first half of tile 1, which it owns
+    assert seg(0) == [(0, 0, 8, P.SEG_FULL), (1, 0, 4, P.SEG_OWNER)]
+    # CTA 1: iterations 12..23 = the second half of tile 1 (handed to CTA 0), all of tile 2
+    assert seg(1) == [(1, 4, 8, P.SEG_PEER), (2, 0, 8, P.SEG_FULL)]
+    assert seg(4) == [(6, 0, 8, P.SEG_FULL)] and seg(7) == [(9, 0, 8, P.SEG_FULL)]
+    # dp_sk on the same problem balances only the remainder: half a tile per SK CTA
+    d = plan(10, 8, 4, P.DP_SK)
+    assert (d.sk_tiles, d.iters_per_sk_cta, d.grid) == (2, 4, 12)
+
+
+def test_hybrid_reduces_to_dp_sk():
+    # fewer tiles than the pool, or tiles that fill whole waves: the same plan as dp_sk
+    for T, I, Pool in [(3, 64, 4), (1, 1216, 148), (12, 33, 4), (296, 64, 148)]:
+        h, d = plan(T, I, Pool, P.HYBRID), plan(T, I, Pool, P.DP_SK)
+        assert (h.sk_tiles, h.dp_tiles, h.sk_ctas, h.iters_per_sk_cta, h.extra, h.grid) == \
+            (d.sk_tiles, d.dp_tiles, d.sk_ctas, d.iters_per_sk_cta, d.extra, d.grid)
+
+
+def test_planted_hybrid_with_two_extra_waves_is_caught():
+    # a stream-K region of two full waves plus the remainder gives every SK CTA 2.5 tiles
+    import dataclasses
+    p = plan(14, 8, 4, P.HYBRID)
+    P.check_invariants(p)
+    bad = dataclasses.replace(p, sk_tiles=10, dp_tiles=4, sk_iters=80, iters_per_sk_cta=20,
+                              grid=8)
+    with pytest.raises(AssertionError):
+        P.check_invariants(bad)
 
 
 def test_all_dp_when_tiles_divide_pool():
@@ -165,7 +202,7 @@ def test_forward_progress_simulation():
     cases = [(4, 64, 3), (5, 1568 // 16, 148 // 4), (7, 5, 6), (3, 40, 12)]
     cases += [(rng.randint(1, 30), rng.randint(1, 40), rng.randint(2, 24)) for _ in range(60)]
     for T, I, Pool in cases:
-        for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK):
+        for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK, P.HYBRID):
             for red in (P.LINEAR, P.TREE):
                 p = plan(T, I, Pool, mode, red)
                 # a blocked linear owner needs one more resident CTA to make progress; a tree
