@@ -217,7 +217,7 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
             A, B = A.to(dev), B.to(dev)
             variants = [(m, r) for m in w.modes for r in w.reductions]
             variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear"),
-                         ("persistent", "linear")]
+                         ("persistent", "linear"), ("hybrid", "linear")]
             for tile, pool in tiles(w):
                 with sk.tile(tile):
                     for mode, red in dict.fromkeys(variants):
@@ -248,7 +248,8 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
         elif w.op == "fp8_block":   # one tile shape (128 x 128)
             call = blockscale_call(torch, sk, w, dev, ws)
             variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]
+            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace"),
+                         ("hybrid", "linear")]
             for mode, red in dict.fromkeys(variants):
                 res[f"128:{mode}/{red}"] = rate(lambda: call(mode, red, w.pool), w.flops())
         else:
@@ -256,7 +257,8 @@ def extra_measurements(torch, sk, dev, flush, stream, steps):
             A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
             C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
             variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace")]
+            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace"),
+                         ("hybrid", "linear")]
             for tile, pool in tiles(w):
                 with sk.tile(tile):
                     for mode, red in variants:

@@ -23,13 +23,14 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 F16, BF16, F32, E4M3 = 0, 1, 2, 3
-OFF, DP_SK, PERSISTENT, SPLITK, AUTO = 0, 1, 2, 3, 4
+OFF, DP_SK, PERSISTENT, SPLITK, AUTO, HYBRID = 0, 1, 2, 3, 4, 5
 LINEAR, TREE, ATOMIC, WORKSPACE, REDUCTION_AUTO = 0, 1, 2, 3, 4
 OP_GEMM, OP_FP8_ROWCOL, OP_WGRAD, OP_FPROP, OP_DGRAD, OP_FP8_BLOCK = 0, 1, 2, 3, 4, 5
 SEG_FULL, SEG_OWNER, SEG_PEER = 0, 1, 2
 TILE_AUTO, TILE_128, TILE_256_PAIR, TILE_256x256_PAIR = 0, 1, 2, 3
 
-MODES = {"off": OFF, "dp_sk": DP_SK, "persistent": PERSISTENT, "splitk": SPLITK, "auto": AUTO}
+MODES = {"off": OFF, "dp_sk": DP_SK, "persistent": PERSISTENT, "splitk": SPLITK, "auto": AUTO,
+         "hybrid": HYBRID}
 REDUCTIONS = {"linear": LINEAR, "tree": TREE, "atomic": ATOMIC, "workspace": WORKSPACE,
               "auto": REDUCTION_AUTO}
 DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}

@@ -45,6 +45,7 @@ const char* mode_name(int m) {
         case SK_DP_SK: return "dp_sk";
         case SK_PERSISTENT: return "persistent";
         case SK_SPLITK: return "splitk";
+        case SK_HYBRID: return "hybrid";
         default: return "?";
     }
 }
@@ -277,7 +278,8 @@ int build_plan(const sk_problem& prob, int mode, int reduction, int ctas, int nu
 
 int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
                         int ctas_per_sm, sk_plan_t& p) {
-    if (mode < SK_OFF || mode > SK_SPLITK) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
+    if (mode < SK_OFF || mode > SK_HYBRID || mode == SK_AUTO)
+        return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
     if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
     View v;
@@ -325,6 +327,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
         p.publishers = s > 1 ? T * s : 0;
     } else {
         p.sk_tiles = T % P;
+        if (mode == SK_HYBRID && T >= P && p.sk_tiles > 0) p.sk_tiles += P;   // one wave more
         p.dp_tiles = T - p.sk_tiles;
         p.sk_iters = p.sk_tiles * I;
         if (p.sk_tiles == 0 || p.sk_iters < P) {   // too few iterations for the pool: all-DP
@@ -337,7 +340,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
             p.iters_per_sk_cta = sk::imax(1, p.sk_iters / p.sk_ctas);
             p.extra_iters = p.sk_iters % p.sk_ctas;
         }
-        p.grid = mode == SK_DP_SK ? p.sk_ctas + p.dp_tiles : P;
+        p.grid = (mode == SK_DP_SK || mode == SK_HYBRID) ? p.sk_ctas + p.dp_tiles : P;
         p.publishers = p.sk_ctas;
     }
     if (p.grid > 0x7fffffffLL) return fail(SK_ERR_UNSUPPORTED, "grid too large");
@@ -545,7 +548,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
 }
 
 int check_common(int mode, int reduction, int ctas, int c_dtype) {
-    if (mode < SK_OFF || mode > SK_AUTO) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
+    if (mode < SK_OFF || mode > SK_HYBRID) return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
     if (reduction < SK_LINEAR || reduction > SK_REDUCTION_AUTO)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk reduction %d", reduction);
     if (ctas == 0 || ctas < -1)

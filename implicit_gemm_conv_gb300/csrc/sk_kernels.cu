@@ -248,7 +248,7 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
 // `tau`, the stream-K iterations this CTA has run.
 __device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool dp,
                                                     const sk_segment_t& seg, int64_t& tau) {
-    if (dp || (plan.mode != SK_DP_SK && plan.mode != SK_PERSISTENT)) return 0;
+    if (dp || plan.mode == SK_OFF || plan.mode == SK_SPLITK) return 0;
     const int64_t len = seg.k_end - seg.k_begin;
     const int64_t rot = sk_segment_rotation(plan.iters_per_sk_cta, seg.k_begin, len, tau);
     tau += len;

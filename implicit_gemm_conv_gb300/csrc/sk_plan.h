@@ -103,7 +103,7 @@ SK_HD void seg_init(const sk_plan_t& p, int64_t cta, SegCursor& c) {
                 c.it_end = t * p.iters_per_tile + (j + 1) * p.iters_per_tile / p.splits;
             }
         }
-    } else if (p.mode == SK_DP_SK) {
+    } else if (p.mode == SK_DP_SK || p.mode == SK_HYBRID) {
         if (cta < p.sk_ctas) {
             c.it = sk_begin(p, cta);
             c.it_end = sk_end(p, cta);

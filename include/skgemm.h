@@ -31,6 +31,10 @@
  *    fill the pool (T < P) and the reduction is long (T * I >= 1024), and only if the plan the
  *    launch would use has stream-K CTAs; split-K otherwise (plain data-parallel when T >= P). The
  *    resolved mode is what sk_plan reports.
+ *    SK_HYBRID is SK_DP_SK with one full wave more in the stream-K region whenever the pool does
+ *    not divide the tiles and the tiles fill at least one wave: P + T mod P stream-K tiles, so
+ *    that every stream-K CTA runs between one and two tiles' worth of iterations (a variant of
+ *    [P2]'s remainder-only rule; otherwise the same plan as SK_DP_SK).
  *  - `reduction`: SK_LINEAR and SK_TREE are deterministic (bit-identical across launches with the
  *    same plan); SK_ATOMIC needs an fp32 output; SK_WORKSPACE adds into fp32 scratch and runs a
  *    second (Stage-2) kernel that writes the output. SK_REDUCTION_AUTO resolves to SK_WORKSPACE
@@ -58,7 +62,8 @@ extern "C" {
 #endif
 
 enum { SK_F16 = 0, SK_BF16 = 1, SK_F32 = 2, SK_E4M3 = 3 };                  /* element types */
-enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3, SK_AUTO = 4 };  /* streamk */
+enum { SK_OFF = 0, SK_DP_SK = 1, SK_PERSISTENT = 2, SK_SPLITK = 3, SK_AUTO = 4,
+       SK_HYBRID = 5 };                                                      /* streamk */
 enum { SK_LINEAR = 0, SK_TREE = 1, SK_ATOMIC = 2, SK_WORKSPACE = 3, SK_REDUCTION_AUTO = 4 };
                                                                              /* reduction    */
 enum { SK_OP_GEMM = 0, SK_OP_FP8_ROWCOL = 1, SK_OP_WGRAD = 2, SK_OP_FPROP = 3, SK_OP_DGRAD = 4,

@@ -38,7 +38,9 @@ def _repeat(launch, out, ws, n=20):
 @pytest.mark.parametrize("red", ["linear", "tree"])
 @pytest.mark.parametrize("mode,shape,ctas", [("persistent", (256, 256, 4096), 3),
                                              ("dp_sk", (3840, 4096, 4096), 148),
-                                             ("dp_sk", (512, 512, 65536), 148)])
+                                             ("dp_sk", (512, 512, 65536), 148),
+                                             ("hybrid", (3840, 4096, 4096), 148),
+                                             ("hybrid", (1280, 1152, 2048), 13)])
 def test_gemm_bit_identical(mode, shape, ctas, red):
     M, N, K = shape
     A, B = gemm_operands(M, N, K, "bf16", "n01")

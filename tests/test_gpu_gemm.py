@@ -21,7 +21,7 @@ def tile_128():
     with sk.tile("128"):
         yield
 
-MODES = ["off", "dp_sk", "persistent", "splitk"]
+MODES = ["off", "dp_sk", "persistent", "splitk", "hybrid"]
 REDS = ["linear", "tree", "atomic", "workspace"]
 TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 import implicit_gemm_conv_gb300 as sk  # noqa: E402  (no skip: a missing library must fail)
 from gpu_helpers import DEV, bits, check_parity, poisoned, sample_points  # noqa: E402
 
-MODES = ["off", "dp_sk", "persistent", "splitk"]
+MODES = ["off", "dp_sk", "persistent", "splitk", "hybrid"]
 REDS = ["linear", "tree", "atomic", "workspace"]
 TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 

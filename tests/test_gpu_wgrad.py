@@ -52,7 +52,7 @@ SHAPES = {
 
 
 @pytest.mark.parametrize("red", ["linear", "tree", "atomic", "workspace"])
-@pytest.mark.parametrize("mode", ["dp_sk", "persistent", "off", "splitk"])
+@pytest.mark.parametrize("mode", ["dp_sk", "persistent", "off", "splitk", "hybrid"])
 @pytest.mark.parametrize("name", list(SHAPES))
 def test_wgrad_shapes(name, mode, red):
     s = SHAPES[name]

@@ -16,7 +16,8 @@ def tile_128():
     with sk.tile("128"):
         yield
 
-MODES = [("off", P.OFF), ("dp_sk", P.DP_SK), ("persistent", P.PERSISTENT), ("splitk", P.SPLITK)]
+MODES = [("off", P.OFF), ("dp_sk", P.DP_SK), ("persistent", P.PERSISTENT), ("splitk", P.SPLITK),
+         ("hybrid", P.HYBRID)]
 REDS = [("linear", P.LINEAR), ("tree", P.TREE), ("atomic", P.ATOMIC), ("workspace", P.WORKSPACE)]
 
 FIELD_MAP = {  # C name -> oracle name
