@@ -89,6 +89,7 @@ _lib.sk_plan_cta_work.argtypes = [ctypes.POINTER(sk_plan_t), _i64, ctypes.POINTE
                                   _i32, ctypes.POINTER(_i32)]
 _lib.sk_default_pool.argtypes = [_i32, _i32, _i32, ctypes.POINTER(_i32)]
 _lib.sk_device_status.argtypes = [_p]
+_lib.sk_probe_flag_timeout.argtypes = [_i32, _p]
 _lib.sk_last_error.restype = ctypes.c_char_p
 _lib.sk_version.restype = _i32
 _lib.sk_gemm_rcr_static_ws.argtypes = [_i32, _i32, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
@@ -102,7 +103,7 @@ EXPORTS = ["sk_gemm_rcr", "sk_gemm_rowcol_fp8", "sk_conv2d_wgrad_nhwc", "sk_work
            "sk_plan", "sk_plan_cta_work", "sk_default_pool", "sk_device_status", "sk_last_error",
            "sk_version", "sk_timing_enable", "sk_timing_read", "sk_gemm_rcr_static_ws",
            "sk_set_tile", "sk_conv2d_fprop_nhwc", "sk_conv2d_dgrad_nhwc",
-           "sk_gemm_tensorquant_fp8", "sk_gemm_blockscale_fp8"]
+           "sk_gemm_tensorquant_fp8", "sk_gemm_blockscale_fp8", "sk_probe_flag_timeout"]
 
 
 class SkError(RuntimeError):
@@ -346,6 +347,12 @@ def sk_workspace_bytes(problem: sk_problem, streamk, reduction, ctas=-1) -> int:
 
 def sk_device_status(stream=None) -> int:
     return _check(_lib.sk_device_status(_stream_ptr(stream)))
+
+
+def sk_probe_flag_timeout(timeout_ms: int = 20, stream=None) -> int:
+    """Failure-detection self-test: a bounded flag wait that runs out after timeout_ms; the next
+    sk_device_status on the stream raises SkError(-1) with the hand-off timeout message."""
+    return _check(_lib.sk_probe_flag_timeout(int(timeout_ms), _stream_ptr(stream)))
 
 
 def sk_version() -> int:

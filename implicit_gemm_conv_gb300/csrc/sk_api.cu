@@ -1082,6 +1082,18 @@ int sk_device_status(void* stream) {
                 info[1], info[2]);
 }
 
+int sk_probe_flag_timeout(int timeout_ms, void* stream) {
+    if (timeout_ms < 1 || timeout_ms > 1000)
+        return fail(SK_ERR_UNSUPPORTED, "timeout_ms must be in [1, 1000], got %d", timeout_ms);
+    DevInfo dev;
+    int rc = check_arch(dev);
+    if (rc) return rc;
+    const int e = sk::launch_flag_timeout_probe(static_cast<uint64_t>(timeout_ms) * 1000000ull,
+                                                static_cast<cudaStream_t>(stream));
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "probe launch");
+    return SK_OK;
+}
+
 // ---- fixed-scratch variant (no device allocation) --------------------------------------------
 //
 // Workspace for callers that cannot allocate device memory at call time. The array lives in the

@@ -59,6 +59,30 @@ __device__ __noinline__ void record_error(unsigned long long code, long long cta
     }
 }
 
+// Bounded wait of a linear/tree receiver for a hand-off flag (acquire at gpu scope). `t0` is the
+// caller's deadline origin (0 = not started; set on the first miss), so that several receives can
+// share one deadline. False once `limit_ns` has passed since t0 without the flag.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint64_t& t0, uint64_t limit_ns) {
+    while (ld_acquire_gpu(f) != 1u) {
+        if (t0 == 0) t0 = globaltimer_ns();
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(128);
+    }
+    return true;
+}
+
+// A flag that nothing ever sets, for sk_probe_flag_timeout.
+__device__ uint32_t g_sk_unset_flag;
+
+// Failure-detection probe: one thread waits on g_sk_unset_flag with the receivers' own routine,
+// gives up after limit_ns and records the receivers' error (cta -1, tile -1, sender -1), exactly as
+// a lost hand-off would; the host reads it with take_device_error. Nothing faults or hangs.
+__global__ void sk_flag_timeout_probe_kernel(uint64_t limit_ns) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    uint64_t t0 = 0;
+    if (!wait_flag(&g_sk_unset_flag, t0, limit_ns)) record_error(kErrFlagWait, -1, -1, -1);
+}
+
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;
@@ -783,14 +807,9 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         bool late = false;
         for (int64_t i = 0; i < ns && !late; ++i) {
             const uint32_t* f = P.flags + (seg.first_cta + sender(i)) * CG + e.half;
-            while (ld_acquire_gpu(f) != 1u) {
-                if (t0 == 0) t0 = globaltimer_ns();
-                if (globaltimer_ns() - t0 > P.flag_timeout_ns) {
-                    record_error(kErrFlagWait, cta, seg.tile, seg.first_cta + sender(i));
-                    late = true;
-                    break;
-                }
-                __nanosleep(128);
+            if (!wait_flag(f, t0, P.flag_timeout_ns)) {
+                record_error(kErrFlagWait, cta, seg.tile, seg.first_cta + sender(i));
+                late = true;
             }
         }
     }
@@ -1353,6 +1372,11 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
         sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else
         sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_flag_timeout_probe(uint64_t limit_ns, cudaStream_t stream) {
+    sk_flag_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -101,5 +101,8 @@ int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStrea
 int launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Read and clear the device error record: returns the code (0 = none) and fills info[3].
 int take_device_error(cudaStream_t stream, long long info[3]);
+// Launch the failure-detection probe: a bounded flag wait that runs out after limit_ns and records
+// the hand-off timeout. Returns a cudaError_t value.
+int launch_flag_timeout_probe(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace sk

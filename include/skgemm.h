@@ -285,6 +285,16 @@ int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out);
  * call: 0 = no, -1 = yes (details in sk_last_error()); clears the record. */
 int sk_device_status(void* stream);
 
+/*
+ * Failure-detection self-test (no counterpart on the pages). Enqueues on `stream` one thread that
+ * waits, with the linear/tree receivers' own bounded routine, on a device flag that nothing ever
+ * sets; after `timeout_ms` (1..1000) it gives up and records the hand-off timeout exactly as a lost
+ * hand-off would (cta -1, tile -1, sender -1). The next sk_device_status on the stream then returns
+ * -1 with that message and clears it. Nothing faults or hangs, and the context stays usable.
+ * Returns 0 (enqueued), -1 (launch error) or -2 (bad timeout, or no sm_103a device).
+ */
+int sk_probe_flag_timeout(int timeout_ms, void* stream);
+
 /* Reason for the last -1 / -2 returned on this thread (never NULL). */
 const char* sk_last_error(void);
 

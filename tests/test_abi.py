@@ -188,6 +188,12 @@ def test_blockscale_group_sizes_of_a_missing_scale_are_ignored():
     assert rc == -2 and "group" not in sk.last_error()
 
 
+def test_flag_timeout_probe_gates():
+    lib = sk.library()
+    for bad in (0, -5, 1001):
+        assert lib.sk_probe_flag_timeout(bad, None) == -2 and "timeout_ms" in sk.last_error()
+
+
 def test_default_pool():
     assert sk.sk_default_pool("linear", 148, 1) == 148
     assert sk.sk_default_pool("tree", 148, 2) == 148
