@@ -701,8 +701,6 @@ int sk_gemm_rcr(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K, cons
 
 namespace {
 
-// The fp8 GEMM with either per-row / per-column scales (sa, sb) or per-tensor scales (sa == sb ==
-// null, `scale` = scale_a * scale_b).
 struct BlockScales {   // the block-scaled form; blocked == false for the other two
     bool blocked = false;
     const float* sa = nullptr;
@@ -710,6 +708,9 @@ struct BlockScales {   // the block-scaled form; blocked == false for the other 
     int64_t gka = 0, gnb = 0, gkb = 0;
 };
 
+// The fp8 GEMM with per-row / per-column scales (sa, sb), per-tensor scales (sa == sb == null,
+// `scale` = scale_a * scale_b), or block scales (`bs.blocked`; sa == sb == null here, the block
+// scales travel in `bs`).
 int fp8_gemm(int64_t M, int64_t N, int64_t K, const void* A8, const void* B8, const float* sa,
              const float* sb, float scale, void* C_bf16, int64_t ldc, int streamk, int reduction,
              int ctas, void* ws, size_t ws_bytes, void* stream, const BlockScales& bs = BlockScales()) {
