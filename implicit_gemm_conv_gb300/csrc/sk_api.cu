@@ -514,7 +514,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
                 if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
             }
         }
-        if (plan.reduction == SK_ATOMIC && plan.shared_tiles > 0) {
+        if (plan.reduction == SK_ATOMIC && plan.shared_tiles > 0 && out_rows > 0) {
             e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
             if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
         }
@@ -535,6 +535,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.scratch = kp.scratch;
             s2.c_dtype = kp.c_dtype;
             s2.op_kind = v.op_kind;
+            s2.rows = kp.conv.rows;
             le = sk::launch_stage2(s2, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
             if (g_timing.on) ++g_timing.all_launches;
@@ -557,6 +558,50 @@ int check_common(int mode, int reduction, int ctas, int c_dtype) {
         return fail(SK_ERR_UNSUPPORTED, "reduction 'atomic' needs an fp32 output, got %s",
                     dtype_name(c_dtype));
     return SK_OK;
+}
+
+// One output phase (a, b) of a data gradient with strides (sh, sw): the dx pixels
+// (sh*i + a, sw*j + b). Only the filter taps r = r0 + sh*t (t < Rt) reach them, with
+// dx[sh*i + a] = sum_t dy[i + q - t] * w[r0 + sh*t], q = (a + pad - r0) / sh: a stride-1
+// convolution of dy over an Hp x Wp grid with Rt x St taps and low padding Rt - 1 - q.
+struct DgradPhase {
+    int64_t Hp, Wp;   // phase pixels per image
+    int Rt, St;       // taps of the phase
+    int r0, s0;       // first filter tap of the phase
+    int padh, padw;   // traversal low padding
+    int a, b;         // offset of the phase in dx
+    bool live() const { return Hp > 0 && Wp > 0 && Rt > 0 && St > 0; }
+};
+
+void dgrad_phase_1d(int64_t X, int64_t R, int sigma, int pad, int a, int64_t& Xp, int& Rt, int& r0,
+                    int& padl) {
+    r0 = (a + pad) % sigma;
+    Rt = r0 < R ? static_cast<int>((R - 1 - r0) / sigma + 1) : 0;
+    const int q = (a + pad - r0) / sigma;
+    padl = Rt - 1 - q;
+    Xp = a < X ? (X - 1 - a) / sigma + 1 : 0;
+}
+
+// The plan-level problem of one phase: its pixel grid and taps as a stride-1 data gradient
+// (padding taps-1 only keeps the view's image-size check satisfied; the view uses n*h*w, c/groups
+// and r*s*k/groups).
+void set_phase_problem(sk_problem& prob, int64_t Hp, int64_t Wp, int Rt, int St) {
+    prob.h = Hp; prob.w = Wp; prob.r = Rt; prob.s = St;
+    prob.stride_h = 1; prob.stride_w = 1; prob.pad_h = Rt - 1; prob.pad_w = St - 1;
+}
+
+void dgrad_phases(int64_t H, int64_t W, int64_t R, int64_t S, int sh, int sw, int ph, int pw,
+                  std::vector<DgradPhase>& out) {
+    out.clear();
+    for (int a = 0; a < sh; ++a)
+        for (int b = 0; b < sw; ++b) {
+            DgradPhase p;
+            p.a = a;
+            p.b = b;
+            dgrad_phase_1d(H, R, sh, ph, a, p.Hp, p.Rt, p.r0, p.padh);
+            dgrad_phase_1d(W, S, sw, pw, b, p.Wp, p.St, p.s0, p.padw);
+            out.push_back(p);
+        }
 }
 
 }  // namespace
@@ -594,6 +639,9 @@ int sk_default_pool(int reduction, int num_sms, int ctas_per_sm, int* out) {
 
 int sk_plan(const sk_problem* p, int streamk, int reduction, int ctas, int num_sms, sk_plan_t* out) {
     if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
+    if (p->op == SK_OP_DGRAD && (p->stride_h > 1 || p->stride_w > 1))
+        return fail(SK_ERR_UNSUPPORTED, "a strided dgrad runs one plan per output phase; "
+                                        "sk_workspace_bytes covers them all");
     int per_sm = 1;
     if (ctas == -1 && num_sms <= 0) {
         DevInfo d;
@@ -628,6 +676,25 @@ int sk_plan_cta_work(const sk_plan_t* plan, int64_t cta, sk_segment_t* out, int 
 
 int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out) {
     if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
+    if (p->op == SK_OP_DGRAD && (p->stride_h > 1 || p->stride_w > 1)) {
+        // The largest workspace of the phases, which run one after another on one stream.
+        if (p->stride_h < 1 || p->stride_w < 1 || p->stride_h > 8 || p->stride_w > 8)
+            return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
+        std::vector<DgradPhase> phases;
+        dgrad_phases(p->h, p->w, p->r, p->s, p->stride_h, p->stride_w, p->pad_h, p->pad_w, phases);
+        size_t most = 0;
+        for (const DgradPhase& ph : phases) {
+            if (!ph.live()) continue;
+            sk_problem q = *p;
+            set_phase_problem(q, ph.Hp, ph.Wp, ph.Rt, ph.St);
+            sk_plan_t plan;
+            const int rc = sk_plan(&q, streamk, reduction, ctas, 0, &plan);
+            if (rc) return rc;
+            if (static_cast<size_t>(plan.ws_bytes) > most) most = static_cast<size_t>(plan.ws_bytes);
+        }
+        *out = most;
+        return SK_OK;
+    }
     sk_plan_t plan;
     int rc = sk_plan(p, streamk, reduction, ctas, 0, &plan);
     if (rc) return rc;
@@ -930,8 +997,6 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         return fail(SK_ERR_UNSUPPORTED, "groups must divide C and K");
     if (stride_h < 1 || stride_w < 1 || stride_h > 8 || stride_w > 8)
         return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
-    if (!fprop && (stride_h != 1 || stride_w != 1))
-        return fail(SK_ERR_UNSUPPORTED, "dgrad supports stride 1 only, got (%d, %d)", stride_h, stride_w);
     if (pad_h < 0 || pad_w < 0 || pad_h >= R || pad_w >= S)
         return fail(SK_ERR_UNSUPPORTED, "padding must be in [0, filter size)");
     if (R > 16 || S > 16) return fail(SK_ERR_UNSUPPORTED, "filter taps beyond 16 are not supported");
@@ -946,19 +1011,30 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
     const int64_t Wo = (W + 2 * pad_w - S) / stride_w + 1;
     if (H + 2 * pad_h < R || W + 2 * pad_w < S || Ho < 1 || Wo < 1)
         return fail(SK_ERR_UNSUPPORTED, "filter larger than the padded image");
-    // The activation read by im2col and the grid the traversal walks.
-    const int64_t AH = fprop ? H : Ho, AW = fprop ? W : Wo, AC = fprop ? C : K;
-    const int64_t TH = fprop ? Ho : H, TW = fprop ? Wo : W;
-    const int tsh = fprop ? stride_h : 1, tsw = fprop ? stride_w : 1;
-    const int tph = fprop ? pad_h : static_cast<int>(R - 1 - pad_h);
-    const int tpw = fprop ? pad_w : static_cast<int>(S - 1 - pad_w);
-    const int64_t up_w = (TW - 1) * tsw - tpw - (AW - 1);
-    const int64_t up_h = (TH - 1) * tsh - tph - (AH - 1);
-    if (up_w < -128 || up_h < -128 || up_w > 127 || up_h > 127 || -tpw < -128 || -tph < -128)
-        return fail(SK_ERR_UNSUPPORTED, "im2col bounding box outside the 4-D TMA range");
-    const int64_t pixels = N * TH * TW;
-    if (pixels + 128 >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
-        return fail(SK_ERR_UNSUPPORTED, "too many pixels (must stay below 2^31 - 128)");
+    const bool phased = !fprop && (stride_h > 1 || stride_w > 1);
+    std::vector<DgradPhase> phases;
+    if (phased) dgrad_phases(H, W, R, S, stride_h, stride_w, pad_h, pad_w, phases);
+    // Every launch's im2col bounding box and pixel count must fit the TMA and the 32-bit pixel
+    // index, checked before anything is enqueued.
+    auto box_ok = [&](int64_t AH, int64_t AW, int64_t TH, int64_t TW, int tsh, int tsw, int tph,
+                      int tpw) {
+        const int64_t up_w = (TW - 1) * tsw - tpw - (AW - 1);
+        const int64_t up_h = (TH - 1) * tsh - tph - (AH - 1);
+        return !(up_w < -128 || up_h < -128 || up_w > 127 || up_h > 127 || -tpw < -128 ||
+                 -tph < -128 || -tpw > 127 || -tph > 127) &&
+               N * TH * TW + 128 < (int64_t(1) << 31);
+    };
+    if (N >= (int64_t(1) << 31)) return fail(SK_ERR_UNSUPPORTED, "too many images");
+    if (!phased) {
+        const bool ok = fprop ? box_ok(H, W, Ho, Wo, stride_h, stride_w, pad_h, pad_w)
+                              : box_ok(Ho, Wo, H, W, 1, 1, static_cast<int>(R - 1 - pad_h),
+                                       static_cast<int>(S - 1 - pad_w));
+        if (!ok) return fail(SK_ERR_UNSUPPORTED, "im2col bounding box or pixel count outside the TMA range");
+    } else {
+        for (const DgradPhase& ph : phases)
+            if (ph.live() && !box_ok(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw))
+                return fail(SK_ERR_UNSUPPORTED, "im2col bounding box or pixel count outside the TMA range");
+    }
     if (!act || !wt || !out) return fail(SK_ERR_UNSUPPORTED, "NULL pointer");
     if (!aligned16(act) || !aligned16(wt) || !aligned16(out))
         return fail(SK_ERR_UNSUPPORTED, "activations, filter and output must be 16-byte aligned");
@@ -967,63 +1043,122 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
     if (N == 0) return SK_OK;   // no pixels: nothing to write
     rc = load_encoders();
     if (rc) return rc;
-    sk_problem prob;
-    memset(&prob, 0, sizeof(prob));
-    prob.op = op;
-    prob.ab_dtype = in_dtype;
-    prob.c_dtype = out_dtype;
-    prob.n = N; prob.h = H; prob.w = W; prob.c = C; prob.k = K; prob.r = R; prob.s = S;
-    prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
-    prob.groups = groups;
-    TileCfg tc;
-    rc = problem_tile(prob, tc);
-    if (rc) return rc;
-    sk::KernelParams kp;
-    memset(&kp, 0, sizeof(kp));
-    {   // A: im2col of the activation, 128 pixels x 64 channels per load (K-major)
-        const cuuint64_t dims[4] = {(cuuint64_t)AC, (cuuint64_t)AW, (cuuint64_t)AH, (cuuint64_t)N};
-        const cuuint64_t strides[3] = {(cuuint64_t)(AC * 2), (cuuint64_t)(AW * AC * 2),
-                                       (cuuint64_t)(AH * AW * AC * 2)};
-        const int lower[2] = {-tpw, -tph};
-        const int upper[2] = {static_cast<int>(up_w), static_cast<int>(up_h)};
-        const cuuint32_t estr[4] = {1, (cuuint32_t)tsw, (cuuint32_t)tsh, 1};
-        CUresult r = g_encode_im2col(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
-                                     const_cast<void*>(act), dims, strides, lower, upper, 64, 128,
-                                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
-    }
-    // B: the filter as [K][R*S*C/G]; fprop 64 x 128-row boxes (K-major), dgrad 64 x 64 boxes
-    // (two per step, MN-major).
-    const int64_t RSC = R * S * Cg;
-    rc = encode_2d(&kp.tmap_b, wt, 2, RSC, K, RSC * 2, 64, fprop ? 128 : 64);
-    if (rc) return rc;
     const int cs = dtype_size(out_dtype);
     const int64_t ldc = fprop ? K : C;
-    kp.c = out;
-    kp.ldc = ldc;
-    kp.c_dtype = out_dtype;
-    if (out_dtype != SK_F32 && groups == 1) {   // one group: complete tiles leave through TMA
-        rc = encode_2d(&kp.tmap_c, out, 2, ldc, pixels, ldc * 2, 64, 32);
-        if (rc) return rc;
-        kp.c_tma = 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // One implicit GEMM over a traversal grid TH x TW of the activation AH x AW (channels AC).
+    auto launch = [&](int64_t AH, int64_t AW, int64_t TH, int64_t TW, int tsh, int tsw, int tph,
+                      int tpw, int Rt, int St, int r0, int s0, const sk::RowMap& rows,
+                      bool zeroed) -> int {
+        const int64_t AC = fprop ? C : K;
+        sk_problem prob;
+        memset(&prob, 0, sizeof(prob));
+        prob.op = op;
+        prob.ab_dtype = in_dtype;
+        prob.c_dtype = out_dtype;
+        prob.n = N; prob.c = C; prob.k = K; prob.groups = groups;
+        if (rows.on) {   // a dgrad phase: its traversal grid and taps, as a stride-1 problem
+            set_phase_problem(prob, TH, TW, Rt, St);
+        } else {
+            prob.h = H; prob.w = W; prob.r = R; prob.s = S;
+            prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
+        }
+        sk::KernelParams kp;
+        memset(&kp, 0, sizeof(kp));
+        {   // A: im2col of the activation, 128 pixels x 64 channels per load (K-major)
+            const cuuint64_t dims[4] = {(cuuint64_t)AC, (cuuint64_t)AW, (cuuint64_t)AH, (cuuint64_t)N};
+            const cuuint64_t strides[3] = {(cuuint64_t)(AC * 2), (cuuint64_t)(AW * AC * 2),
+                                           (cuuint64_t)(AH * AW * AC * 2)};
+            const int lower[2] = {-tpw, -tph};
+            const int upper[2] = {static_cast<int>((TW - 1) * tsw - tpw - (AW - 1)),
+                                  static_cast<int>((TH - 1) * tsh - tph - (AH - 1))};
+            const cuuint32_t estr[4] = {1, (cuuint32_t)tsw, (cuuint32_t)tsh, 1};
+            CUresult r = g_encode_im2col(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                         const_cast<void*>(act), dims, strides, lower, upper, 64,
+                                         128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                         CU_TENSOR_MAP_SWIZZLE_128B,
+                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS)
+                return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeIm2col failed (%d)", (int)r);
+        }
+        // B: the filter as [K][R*S*C/G]; fprop 64 x 128-row boxes (K-major), dgrad 64 x 64 boxes
+        // (two per step, MN-major).
+        const int64_t Cg = C / groups;
+        const int64_t RSC = R * S * Cg;
+        int rc2 = encode_2d(&kp.tmap_b, wt, 2, RSC, K, RSC * 2, 64, fprop ? 128 : 64);
+        if (rc2) return rc2;
+        const int64_t pixels = N * TH * TW;
+        kp.c = out;
+        kp.ldc = ldc;
+        kp.c_dtype = out_dtype;
+        // One group and contiguous rows: complete tiles leave through TMA tile stores.
+        if (out_dtype != SK_F32 && groups == 1 && !rows.on) {
+            rc2 = encode_2d(&kp.tmap_c, out, 2, ldc, pixels, ldc * 2, 64, 32);
+            if (rc2) return rc2;
+            kp.c_tma = 1;
+        }
+        const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+        kp.idesc = sk::make_idesc(fmt, fmt, false, !fprop, 128, static_cast<uint32_t>(sk::kTileN));
+        kp.conv.HoWo = TH * TW;
+        kp.conv.Wo = static_cast<int32_t>(TW);
+        kp.conv.sh = tsh;
+        kp.conv.sw = tsw;
+        kp.conv.ph = tph;
+        kp.conv.pw = tpw;
+        kp.conv.R = Rt;
+        kp.conv.S = St;
+        kp.conv.r0 = r0;
+        kp.conv.s0 = s0;
+        kp.conv.dsh = rows.on ? stride_h : 1;
+        kp.conv.dsw = rows.on ? stride_w : 1;
+        kp.conv.Sf = static_cast<int32_t>(S);
+        kp.conv.Cg = static_cast<int32_t>(red_ch);
+        kp.conv.Kg = static_cast<int32_t>(Kg);
+        kp.conv.Cw = static_cast<int32_t>(Cg);
+        kp.conv.rows = rows;
+        // A dgrad phase writes scattered rows of dx, zeroed beforehand when needed: no per-launch
+        // zeroing of a row range (out_rows 0).
+        return run(prob, streamk, reduction, ctas, kp, out, ldc * cs, zeroed ? 0 : pixels, ldc * cs,
+                   ws, ws_bytes, st);
+    };
+
+    sk::RowMap identity;
+    memset(&identity, 0, sizeof(identity));
+    if (fprop)
+        return launch(H, W, Ho, Wo, stride_h, stride_w, pad_h, pad_w, static_cast<int>(R),
+                      static_cast<int>(S), 0, 0, identity, false);
+    if (!phased)   // stride 1: a stride-1 convolution of dy with the flipped filter, padding R-1-p
+        return launch(Ho, Wo, H, W, 1, 1, static_cast<int>(R - 1 - pad_h),
+                      static_cast<int>(S - 1 - pad_w), static_cast<int>(R), static_cast<int>(S), 0,
+                      0, identity, false);
+    // Strided: one launch per output phase. dx is zeroed first when a phase has no taps (its
+    // pixels receive nothing) or when the atomic reduction adds into it.
+    bool zero_first = reduction == SK_ATOMIC;
+    for (const DgradPhase& ph : phases) zero_first = zero_first || !ph.live();
+    if (zero_first) {
+        cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(N * H * W * ldc * cs), st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dx)");
     }
-    const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
-    kp.idesc = sk::make_idesc(fmt, fmt, false, !fprop, 128, static_cast<uint32_t>(sk::kTileN));
-    kp.conv.HoWo = TH * TW;
-    kp.conv.Wo = static_cast<int32_t>(TW);
-    kp.conv.sh = tsh;
-    kp.conv.sw = tsw;
-    kp.conv.ph = tph;
-    kp.conv.pw = tpw;
-    kp.conv.R = static_cast<int32_t>(R);
-    kp.conv.S = static_cast<int32_t>(S);
-    kp.conv.Cg = static_cast<int32_t>(red_ch);
-    kp.conv.Kg = static_cast<int32_t>(Kg);
-    kp.conv.Cw = static_cast<int32_t>(Cg);
-    return run(prob, streamk, reduction, ctas, kp, out, ldc * cs, pixels, ldc * cs, ws, ws_bytes,
-               static_cast<cudaStream_t>(stream));
+    for (const DgradPhase& ph : phases) {
+        if (!ph.live()) continue;
+        sk::RowMap rm;
+        memset(&rm, 0, sizeof(rm));
+        rm.on = 1;
+        rm.HoWo = ph.Hp * ph.Wp;
+        rm.Wo = static_cast<int32_t>(ph.Wp);
+        rm.Hd = static_cast<int32_t>(H);
+        rm.Wd = static_cast<int32_t>(W);
+        rm.dsh = stride_h;
+        rm.dsw = stride_w;
+        rm.ah = ph.a;
+        rm.aw = ph.b;
+        rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0, rm,
+                    true);
+        if (rc) return rc;
+    }
+    return SK_OK;
 }
 
 }  // namespace

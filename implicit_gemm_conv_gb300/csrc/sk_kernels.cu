@@ -224,8 +224,9 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
         } else {
             // B: the filter at the flipped tap, 64 output-gradient channels (rows of w) x 128 input
             // channels as two 64-channel slabs (MN-major).
-            const int32_t col = ((cg.R - 1 - r) * cg.S + (cg.S - 1 - s)) * cg.Cw +
-                                static_cast<int32_t>(nt * TN);
+            const int32_t fr = cg.r0 + cg.dsh * (cg.R - 1 - r);
+            const int32_t fs = cg.s0 + cg.dsw * (cg.S - 1 - s);
+            const int32_t col = (fr * cg.Sf + fs) * cg.Cw + static_cast<int32_t>(nt * TN);
 #pragma unroll
             for (int j = 0; j < TN / 64; ++j)
                 tma_load_2d(b_dst + j * (C::TK * 128), &P.tmap_b, bar, col + 64 * j,
@@ -1076,7 +1077,7 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
         e.row_ok = m < plan.gemm_m;
         if constexpr (folds_groups_into_columns(OP)) {
-            e.out_row = m;
+            e.out_row = map_row(P.conv.rows, m);
             e.n_base = g * plan.gemm_n + nt * TN;
             e.n_end = (g + 1) * plan.gemm_n;
         } else {
@@ -1239,7 +1240,7 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     const float* base = P.scratch + t * static_cast<int64_t>(kTileM * CG * TN);
     const float4 q = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4));
     float v[4] = {q.x, q.y, q.z, q.w};
-    const int64_t out_row = fold_cols ? m : g * plan.gemm_m + m;
+    const int64_t out_row = fold_cols ? map_row(P.rows, m) : g * plan.gemm_m + m;
     if (P.sa != nullptr) {
         const float rs = P.sa[out_row];
         for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);

@@ -37,11 +37,32 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
 // Geometry the convolution producers need to turn an iteration into im2col coordinates. The im2col
 // traversal runs over the pixels of one image grid: wgrad and fprop the output grid (Ho x Wo), dgrad
 // the input grid (H x W, stride 1, padding R-1-ph / S-1-pw with the taps flipped).
+// Output rows of one phase of a strided data gradient: traversal pixel m = (n, i, j) of an
+// HoWo = Hp*Wp grid (width Wo = Wp) is dx pixel (n, dsh*i + ah, dsw*j + aw) of an Hd x Wd image.
+// `on` = 0: the rows are the traversal pixels themselves.
+struct RowMap {
+    int64_t HoWo;
+    int32_t on, Wo, Hd, Wd, dsh, dsw, ah, aw;
+};
+
+__host__ __device__ __forceinline__ int64_t map_row(const RowMap& rm, int64_t m) {
+    if (!rm.on) return m;
+    const int64_t n = m / rm.HoWo;
+    const int64_t rem = m - n * rm.HoWo;
+    const int64_t i = rem / rm.Wo;
+    const int64_t j = rem - i * rm.Wo;
+    return (n * rm.Hd + rm.dsh * i + rm.ah) * rm.Wd + rm.dsw * j + rm.aw;
+}
+
 struct ConvGeom {
     int64_t HoWo;          // pixels per image of the traversal grid
     int32_t Wo;            // width of the traversal grid
     int32_t sh, sw, ph, pw;   // traversal stride and padding
-    int32_t R, S;
+    int32_t R, S;          // taps of the traversal window
+    // dgrad: traversal tap (r, s) reads filter tap (r0 + dsh*(R-1-r), s0 + dsw*(S-1-s)) of a
+    // filter Sf taps wide (stride 1: r0 = s0 = 0, dsh = dsw = 1, Sf = S: the flipped filter)
+    int32_t r0, s0, dsh, dsw, Sf;
+    RowMap rows;           // output rows (dgrad phases of a strided convolution)
     int32_t Cg, Kg;        // wgrad: channels and filters per group; fprop / dgrad: channels per
                            // group of the im2col'd tensor (x: C/G, dy: K/G) and filter rows per group
     int32_t Cw;            // fprop / dgrad: channels per group of the filter (C/G)
@@ -78,6 +99,7 @@ struct KernelParams {
 struct Stage2Params {
     sk_plan_t plan;
     int32_t op_kind;       // OpKind: where the group of a tile goes in the output
+    RowMap rows;           // output rows of the tile rows (identity unless a dgrad phase)
     void* c;
     int64_t ldc;
     const float* sa;

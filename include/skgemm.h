@@ -223,9 +223,13 @@ int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_
  *                         over the (ho, wo) with ho*sh-ph+r = h, wo*sw-pw+s = w
  *   dy: [N][Ho][Wo][K], w: [K][R][S][C/groups], dx: [N][H][W][C] (written whole).
  *   GEMM view per group: M = N*H*W input pixels, N = C/groups channels, reduction R*S*K/groups,
- *   computed as a stride-1 convolution of dy with the flipped filter.
- *   Supported: stride 1 (other strides return -2), (K/groups) a multiple of 64, C/groups a
- *   multiple of 8, dilation 1, R, S <= 16, padding < filter size. The 128 x 128 tile.
+ *   computed as a stride-1 convolution of dy with the flipped filter. With a stride above 1 it
+ *   runs one such convolution per output phase (the dx pixels h = sh*i + a, w = sw*j + b): only
+ *   the taps r = (a + ph) mod sh + sh*t reach them (likewise s), over an H/sh x W/sw grid;
+ *   phases that no tap reaches are zero. sk_workspace_bytes covers the largest phase; sk_plan
+ *   has no single plan for a strided call and returns -2.
+ *   Supported: strides 1..8, (K/groups) a multiple of 64, C/groups a multiple of 8, dilation 1,
+ *   R, S <= 16, padding < filter size. The 128 x 128 tile.
  */
 int sk_conv2d_dgrad_nhwc(int in_dtype, int dx_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
                          int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,

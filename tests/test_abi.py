@@ -134,9 +134,39 @@ def test_conv_rejections(fn, kw, reason):
     assert reason in msg, msg
 
 
-def test_dgrad_stride_and_fprop_tiles():
+def _phase_1d(X, R, sigma, pad, a):
+    """One dimension of an output phase of a strided data gradient, from its definition: the taps
+    r with (a + pad - r) divisible by sigma, and the pixels a, a + sigma, ... below X."""
+    taps = [r for r in range(R) if (a + pad - r) % sigma == 0]
+    return len(range(a, X, sigma)), len(taps)
+
+
+def test_strided_dgrad_gates_and_workspace():
     rc, msg = _conv("sk_conv2d_dgrad_nhwc", sh=2, sw=2)
-    assert rc == -2 and "stride 1" in msg
+    assert rc == -2 and "stride" not in msg          # past every argument gate (no device here)
+    rc, msg = _conv("sk_conv2d_dgrad_nhwc", sh=9, sw=1)
+    assert rc == -2 and "stride" in msg
+    # the workspace covers the largest phase plan, each recomputed by the oracle partitioner
+    N, H, W, C, K, R, S, sh, sw, ph, pw = 4, 17, 13, 64, 128, 3, 2, 2, 3, 1, 1
+    prob = sk.make_problem("dgrad", ab_dtype="bf16", c_dtype="bf16", n=N, h=H, w=W, c=C, k=K,
+                           r=R, s=S, stride_h=sh, stride_w=sw, pad_h=ph, pad_w=pw, groups=1)
+    with pytest.raises(sk.SkError, match="one plan per output phase"):
+        sk.sk_plan(prob, "dp_sk", "linear", 7, 148)
+    from oracle import partition as P
+    for mode, red, pm, pr in [("dp_sk", "linear", P.DP_SK, P.LINEAR),
+                              ("splitk", "workspace", P.SPLITK, P.WORKSPACE)]:
+        most = 0
+        for a in range(sh):
+            for b in range(sw):
+                hp, rt = _phase_1d(H, R, sh, ph, a)
+                wp, st = _phase_1d(W, S, sw, pw, b)
+                if not (hp and wp and rt and st):
+                    continue
+                plan = P.make_plan(tiles_m=-(-N * hp * wp // 128), tiles_n=1, groups=1,
+                                   kred=rt * st * K, tm=128, tn=128, tk=64, pool=7, mode=pm,
+                                   reduction=pr)
+                most = max(most, plan.ws_bytes)
+        assert sk.sk_workspace_bytes(prob, mode, red, 7) == most
     with sk.tile("256x256_pair"):
         rc, msg = _conv("sk_conv2d_fprop_nhwc", N=0)   # checked before any device work
     assert rc in (0, -2)

@@ -1,8 +1,8 @@
 """GPU parity of the forward convolution and the data gradient (sk_conv2d_fprop_nhwc and
 sk_conv2d_dgrad_nhwc through the C ABI) against the fp64 oracle: every mode x reduction on ragged
-shapes (pixel counts that leave partial tiles, partial channel tiles), groups, strides and padding,
-a 1x1 convolution, sampled tile-edge pixels of a 32x56x56 workload, and bit-identical linear/tree
-hand-offs."""
+shapes (pixel counts that leave partial tiles, partial channel tiles), groups, strides and padding
+(the strided data gradient runs one launch per output phase), a 1x1 convolution, sampled tile-edge
+pixels of a 32x56x56 workload, and bit-identical linear/tree hand-offs."""
 import numpy as np
 import pytest
 import torch
@@ -33,10 +33,10 @@ def run_fprop(x, w, out, stride, pad, groups, mode, red, ctas, ws=None):
     return y
 
 
-def run_dgrad(dy, w, H, W, C, out, pad, groups, mode, red, ctas, ws=None):
+def run_dgrad(dy, w, H, W, C, out, pad, groups, mode, red, ctas, ws=None, stride=(1, 1)):
     N = dy.shape[0]
     dx = poisoned((N, H, W, C), TD[out])
-    sk.sk_conv2d_dgrad_nhwc(dy.to(DEV), w.to(DEV), dx, (1, 1), pad, groups, mode, red, ctas, ws=ws)
+    sk.sk_conv2d_dgrad_nhwc(dy.to(DEV), w.to(DEV), dx, stride, pad, groups, mode, red, ctas, ws=ws)
     sk.sk_device_status()
     return dx
 
@@ -52,11 +52,11 @@ def fprop_case(N, H, W, C, K, R, S, stride, pad, groups, dt, off):
     return _REF[key]
 
 
-def dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, off):
-    key = ("d", N, H, W, C, K, R, S, pad, groups, dt, off)
+def dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, off, stride=(1, 1)):
+    key = ("d", N, H, W, C, K, R, S, pad, groups, dt, off, stride)
     if key not in _REF:
-        dy, w = dgrad_operands(N, H, W, C, K, R, S, (1, 1), pad, groups, dt, "u11", seed_offset=off)
-        _REF[key] = (dy, w, numerics.dgrad_nhwc(dt, bits(dy), bits(w), H, W, (1, 1), pad, groups))
+        dy, w = dgrad_operands(N, H, W, C, K, R, S, stride, pad, groups, dt, "u11", seed_offset=off)
+        _REF[key] = (dy, w, numerics.dgrad_nhwc(dt, bits(dy), bits(w), H, W, stride, pad, groups))
     return _REF[key]
 
 
@@ -175,5 +175,52 @@ def test_conv_bit_identical(op, red):
         assert torch.isfinite(o.float()).all()
         if first is None:
             first = b
+        else:
+            assert torch.equal(first, b), "result changed between launches"
+
+
+STRIDED = {
+    # N, H, W, C, K, R, S, stride, pad, groups, dtype
+    "s2_3x3_ragged": (2, 9, 11, 72, 64, 3, 3, (2, 2), (1, 1), 1, "f16"),
+    "s2x3_3x2_g2": (2, 10, 7, 64, 128, 3, 2, (2, 3), (1, 0), 2, "bf16"),
+    "s2_1x1": (3, 8, 8, 64, 64, 1, 1, (2, 2), (0, 0), 1, "f16"),       # 3 of 4 phases get no taps
+    "s3_3x3_pad2x1": (1, 13, 12, 64, 64, 3, 3, (3, 3), (2, 1), 1, "bf16"),   # negative padding
+}
+
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("persistent", "tree"), ("off", "linear"),
+                                      ("splitk", "workspace"), ("dp_sk", "atomic"),
+                                      ("hybrid", "linear")])
+@pytest.mark.parametrize("name", list(STRIDED))
+def test_dgrad_strided(name, mode, red):
+    N, H, W, C, K, R, S, stride, pad, groups, dt = STRIDED[name]
+    dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
+    out = "f32" if red == "atomic" else dt
+    dx = run_dgrad(dy, w, H, W, C, out, pad, groups, mode, red, 5, stride=stride)
+    check_parity(dx.reshape(-1, C), ref, out, R * S * K // groups,
+                 what=f"dgrad {name} {mode}/{red}")
+
+
+def test_dgrad_strided_caller_workspace_and_bit_identical():
+    # the caller's workspace, sized by sk_workspace_bytes for all phases; 10 launches, poisoned
+    N, H, W, C, K, R, S, stride, pad, groups, dt = STRIDED["s2_3x3_ragged"]
+    dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
+    prob = sk.make_problem("dgrad", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=C, k=K, r=R, s=S,
+                           stride_h=stride[0], stride_w=stride[1], pad_h=pad[0], pad_w=pad[1],
+                           groups=groups)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", "linear", 5), dtype=torch.uint8,
+                     device=DEV)
+    dyd, wd = dy.to(DEV), w.to(DEV)
+    dx = poisoned((N, H, W, C), TD[dt])
+    first = None
+    for _ in range(10):
+        ws.fill_(0xFF)
+        dx.view(torch.uint8).fill_(0xFF)
+        sk.sk_conv2d_dgrad_nhwc(dyd, wd, dx, stride, pad, groups, "dp_sk", "linear", 5, ws=ws)
+        sk.sk_device_status()
+        b = dx.view(torch.uint8).clone()
+        if first is None:
+            first = b
+            check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what="strided dgrad, caller ws")
         else:
             assert torch.equal(first, b), "result changed between launches"
