@@ -231,7 +231,10 @@ int tile_cfg(const View& v, TileCfg& t) {
         t = g_tile == SK_TILE_256_PAIR ? TileCfg{2, 128, 7} : TileCfg{1, 128, 5};
         return SK_OK;
     }
-    t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : 6};
+    // fprop / dgrad: 3 stages and no store staging, so that two CTAs share an SM (their reductions
+    // are short, and the other CTA's mainloop covers one's prologue and epilogue).
+    const bool conv_fwd = v.op_kind == sk::kOpFprop16 || v.op_kind == sk::kOpDgrad16;
+    t = {1, sk::kTileN, v.op_kind == sk::kOpWgrad16 ? 7 : conv_fwd ? 3 : 6};
     switch (g_tile) {
         case SK_TILE_128: return SK_OK;
         case SK_TILE_256_PAIR:

@@ -119,7 +119,8 @@ struct Cfg {
     // The owner's fold stages partial tiles through the (then idle) operand ring in units of
     // 128 rows x (32 x kFoldUnitChunks) fp32 columns, contiguous in the fragment-major layout:
     // 64 KB with one CTA per SM, 32 KB in the smaller ring of a pair.
-    static constexpr int kFoldUnitChunks = (CG == 1 && TN >= 128) ? 4 : 2;   // 32-column chunks per unit
+    static constexpr int kFoldUnitChunks =
+        (CG == 1 && TN >= 128 && ST * kStageBytes >= 128 * 1024) ? 4 : 2;   // 32-column chunks per unit
     static constexpr int kFoldUnitBytes = kTileM * 32 * 4 * kFoldUnitChunks;
     static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
@@ -129,8 +130,9 @@ struct Cfg {
     // epilogue stages each complete 128 x 128 tile for its TMA stores, so that every tile, not only
     // a CTA's last, leaves that way while the producer already fills the ring for the next one.
     // The block-scaled fp8 pair keeps one too (its ring is deep enough without the space).
+    // A 3-stage one-CTA ring (two CTAs per SM) has none: its last tile leaves through the ring.
     static constexpr int kEpiStageBytes =
-        ((CG == 1 && OP != kOpWgrad16) || OP == kOpFp8Block) ? kTileM * TN * 2 : 0;
+        ((CG == 1 && OP != kOpWgrad16 && ST > 3) || OP == kOpFp8Block) ? kTileM * TN * 2 : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (kBarFold + kFoldBufs) * 8;
     // Block-scaled fp8: each epilogue thread's ring of block scales (A and B) copied kScaleAhead
@@ -1341,8 +1343,8 @@ static size_t smem_bytes_t() {
                                           : fn<kOpGemm16, 128, 2, 4>(__VA_ARGS__)))           \
      : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 6>(__VA_ARGS__)                              \
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
-     : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 6>(__VA_ARGS__)                            \
-     : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 6>(__VA_ARGS__)                            \
+     : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 3>(__VA_ARGS__)                            \
+     : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 3>(__VA_ARGS__)                            \
      : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 1, 5>(__VA_ARGS__)                          \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
