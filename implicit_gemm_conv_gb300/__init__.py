@@ -290,7 +290,8 @@ def sk_conv2d_fprop_nhwc(x, w, y, stride=(1, 1), pad=(0, 0), groups=1, streamk="
 def sk_conv2d_dgrad_nhwc(dy, w, dx, stride=(1, 1), pad=(0, 0), groups=1, streamk="dp_sk",
                          reduction="linear", ctas=-1, ws=None, stream=None):
     """dx [N, H, W, C] = data gradient of a 2-D convolution, from NHWC dy [N, Ho, Wo, K] and the
-    KRSC filter w [K, R, S, C/groups]; dx's shape gives the input size."""
+    KRSC filter w [K, R, S, C/groups]; dx's shape gives the input size. Strides 1..8 (a stride
+    above 1 runs one launch per output phase)."""
     N, H, W, C = dx.shape
     K, R, S = w.shape[0], w.shape[1], w.shape[2]
     assert dy.is_contiguous() and w.is_contiguous() and dx.is_contiguous()

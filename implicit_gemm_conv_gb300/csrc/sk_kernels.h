@@ -34,9 +34,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// Geometry the convolution producers need to turn an iteration into im2col coordinates. The im2col
-// traversal runs over the pixels of one image grid: wgrad and fprop the output grid (Ho x Wo), dgrad
-// the input grid (H x W, stride 1, padding R-1-ph / S-1-pw with the taps flipped).
 // Output rows of one phase of a strided data gradient: traversal pixel m = (n, i, j) of an
 // HoWo = Hp*Wp grid (width Wo = Wp) is dx pixel (n, dsh*i + ah, dsw*j + aw) of an Hd x Wd image.
 // `on` = 0: the rows are the traversal pixels themselves.
@@ -54,6 +51,10 @@ __host__ __device__ __forceinline__ int64_t map_row(const RowMap& rm, int64_t m)
     return (n * rm.Hd + rm.dsh * i + rm.ah) * rm.Wd + rm.dsw * j + rm.aw;
 }
 
+// Geometry the convolution producers need to turn an iteration into im2col coordinates. The im2col
+// traversal runs over the pixels of one image grid: wgrad and fprop the output grid (Ho x Wo), dgrad
+// the input grid (H x W, stride 1, padding R-1-ph / S-1-pw with the taps flipped) or, for a strided
+// dgrad, the grid of one output phase.
 struct ConvGeom {
     int64_t HoWo;          // pixels per image of the traversal grid
     int32_t Wo;            // width of the traversal grid
