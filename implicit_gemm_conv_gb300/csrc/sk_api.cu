@@ -155,7 +155,63 @@ struct View {          // GEMM view of a problem
     int op_kind;       // sk::OpKind
 };
 
+// Geometry of the shifted-row wgrad (see wgrad_row_geom).
+struct RowGeom {
+    int64_t ho, wo, ho_pad;
+    int wseg, rows_per_step, qmax, sw;
+    int nq[2];
+};
+
+// The shifted-row wgrad serves groups of 64 channels and 64 filters with at most 3 column taps,
+// a column stride of 1 or 2, and output rows short enough that a row and the shifts' halo fit one
+// 64-position K step: wseg = the power of two >= Wo + qmax (at most 64), rows_per_step = 64/wseg
+// output rows per step, rows counted per image over Ho rounded up to rows_per_step. Column tap
+// s = sw*q + p (phase p < sw) reads x column sw*(wo + q) + p - pad, i.e. the x row of phase p read
+// at position wo + q: q <= qmax = ceil(S/sw) - 1. False when the problem does not fit.
+bool wgrad_row_geom(const sk_problem& p, RowGeom& g) {
+    if (p.op != SK_OP_WGRAD || p.groups < 1 || p.c % p.groups || p.k % p.groups) return false;
+    if (p.c / p.groups != 64 || p.k / p.groups != 64) return false;
+    if (p.s < 1 || p.s > 3 || p.r < 1 || p.stride_w < 1 || p.stride_w > 2 || p.stride_h < 1 ||
+        p.stride_h > 8)
+        return false;
+    g.sw = p.stride_w;
+    g.ho = (p.h + 2 * p.pad_h - p.r) / p.stride_h + 1;
+    g.wo = (p.w + 2 * p.pad_w - p.s) / p.stride_w + 1;
+    if (g.ho < 1 || g.wo < 1) return false;
+    g.nq[0] = static_cast<int>((p.s + g.sw - 1) / g.sw);
+    g.nq[1] = g.sw == 2 ? static_cast<int>(p.s / 2) : 0;
+    g.qmax = g.nq[0] - 1;
+    g.wseg = 1;
+    while (g.wseg < g.wo + g.qmax) g.wseg *= 2;
+    if (g.wseg > 64) return false;
+    g.rows_per_step = 64 / g.wseg;
+    if (static_cast<int64_t>(g.rows_per_step) * p.stride_h > 256) return false;   // TMA box rows
+    g.ho_pad = sk::round_up(g.ho, g.rows_per_step);
+    if (p.n * g.ho_pad >= (int64_t(1) << 31)) return false;   // 32-bit row index in the kernel
+    return true;
+}
+
+int problem_view_pages(const sk_problem& p, View& v);
+
+// The GEMM view of a problem under the calling thread's tile setting. Wgrad: the pages' view
+// (M = K/G filters, N = R*S*C/G, reduction over N*Ho*Wo output pixels), or with the automatic
+// tile, where it fits, the shifted-row view: M = (tap row r, channel) = R*64 in 128-row tiles (two
+// tap rows), N = (column tap s, filter) = S*64 in one 192-column tile, reduction over the padded
+// positions N*ho_pad*wseg.
 int problem_view(const sk_problem& p, View& v) {
+    int rc = problem_view_pages(p, v);
+    if (rc) return rc;
+    RowGeom g;
+    if (v.op_kind == sk::kOpWgrad16 && g_tile == SK_TILE_AUTO && wgrad_row_geom(p, g)) {
+        v.gemm_m = p.r * 64;
+        v.gemm_n = p.s * 64;
+        v.kred = p.n * g.ho_pad * g.wseg;
+        v.op_kind = g.sw == 1 ? sk::kOpWgradRow1 : sk::kOpWgradRow2;
+    }
+    return SK_OK;
+}
+
+int problem_view_pages(const sk_problem& p, View& v) {
     switch (p.op) {
         case SK_OP_GEMM:
         case SK_OP_FP8_ROWCOL:
@@ -220,6 +276,11 @@ struct TileCfg {
     int cg, tn, st;   // CTAs per logical CTA, tile N, operand-ring stages
 };
 int tile_cfg(const View& v, TileCfg& t) {
+    if (sk::is_wgrad_row(v.op_kind)) {
+        // 128 x 192 tile on one CTA: 8 stages of 25 KB (one x column phase) or 5 of 41 KB (two).
+        t = v.op_kind == sk::kOpWgradRow1 ? TileCfg{1, 192, 8} : TileCfg{1, 192, 5};
+        return SK_OK;
+    }
     if (v.op_kind == sk::kOpFp8Block) {
         // Two 128-column partial buffers fill 256 TMEM columns (the running sum stays in the
         // epilogue's registers), so the tile is 128 columns wide: 128 x 128 on one CTA (5 ring
@@ -347,6 +408,9 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
         p.publishers = p.sk_ctas;
     }
     if (p.grid > 0x7fffffffLL) return fail(SK_ERR_UNSUPPORTED, "grid too large");
+    // The kernels walk iterations, tiles and CTA ids with 32-bit arithmetic.
+    if (p.tiles * p.iters_per_tile > 0x7fffffffLL)
+        return fail(SK_ERR_UNSUPPORTED, "too many MAC iterations (tiles x iterations per tile >= 2^31)");
     int64_t maxc = 1, shared = 0;
     for (int64_t t = 0; t < sk::n_shared_candidates(p); ++t) {
         int64_t first, n;
@@ -503,26 +567,35 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
 
     rc = SK_OK;
     do {
-        // Flags, control block and (workspace reduction) scratch: one memset when they are
-        // contiguous, i.e. whenever there are no partial slots between them.
+        // One kernel zeroes the flags and the control block, the workspace reduction's scratch and,
+        // for the atomic reduction, the output; the main kernel is launched to overlap its tail and
+        // waits for its writes before it touches any of those words. With the library's timing
+        // on, an event sits between the two, so they run one after the other.
+        sk::ZeroParams z;
+        memset(&z, 0, sizeof(z));
         const int64_t head = plan.flag_bytes + sk::kControlBytes;
-        if (plan.partial_bytes == 0) {
-            e = cudaMemsetAsync(w, 0, static_cast<size_t>(head + plan.scratch_bytes), stream);
-            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags, scratch)"); break; }
+        if (plan.partial_bytes == 0) {   // flags, control and scratch are contiguous
+            z.ptr[z.nranges] = w;
+            z.bytes[z.nranges++] = head + plan.scratch_bytes;
         } else {
-            e = cudaMemsetAsync(w, 0, static_cast<size_t>(head), stream);
-            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(flags)"); break; }
+            z.ptr[z.nranges] = w;
+            z.bytes[z.nranges++] = head;
             if (plan.scratch_bytes > 0) {
-                e = cudaMemsetAsync(w + plan.scratch_offset, 0, static_cast<size_t>(plan.scratch_bytes), stream);
-                if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemsetAsync(scratch)"); break; }
+                z.ptr[z.nranges] = w + plan.scratch_offset;
+                z.bytes[z.nranges++] = plan.scratch_bytes;
             }
         }
         if (plan.reduction == SK_ATOMIC && plan.shared_tiles > 0 && out_rows > 0) {
-            e = cudaMemset2DAsync(out, out_pitch_bytes, 0, out_row_bytes, out_rows, stream);
-            if (e != cudaSuccess) { rc = cuda_fail(e, "cudaMemset2DAsync(output)"); break; }
+            z.out = out;
+            z.pitch = static_cast<int64_t>(out_pitch_bytes);
+            z.row_bytes = static_cast<int64_t>(out_row_bytes);
+            z.rows = static_cast<int64_t>(out_rows);
         }
+        int le = sk::launch_zero(z, stream);
+        if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "zeroing kernel launch"); break; }
+        if (g_timing.on) ++g_timing.all_launches;
         const int tslot = timing_start(stream);
-        int le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, stream);
+        le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, tslot < 0, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -539,6 +612,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.c_dtype = kp.c_dtype;
             s2.op_kind = v.op_kind;
             s2.rows = kp.conv.rows;
+            s2.conv = kp.conv;
             le = sk::launch_stage2(s2, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
             if (g_timing.on) ++g_timing.all_launches;
@@ -940,6 +1014,66 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     prob.groups = groups;
     sk::KernelParams kp;
     memset(&kp, 0, sizeof(kp));
+    const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+    View view;
+    rc = problem_view(prob, view);
+    if (rc) return rc;
+    RowGeom rg;
+    if (sk::is_wgrad_row(view.op_kind) && wgrad_row_geom(prob, rg)) {
+        // Shifted-row wgrad. A: x rows of 64 channels, `wseg` positions at column stride sw and
+        // `rows_per_step` rows at row stride sh (the traversal strides of the map), from any
+        // (column, row) start: outside the image reads zeros. B: dy rows of 64 filters.
+        {
+            const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+            const cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2),
+                                           (cuuint64_t)(H * W * C * 2)};
+            const cuuint32_t box[4] = {64, (cuuint32_t)(rg.wseg * stride_w),
+                                       (cuuint32_t)(rg.rows_per_step * stride_h), 1};
+            const cuuint32_t estr[4] = {1, (cuuint32_t)stride_w, (cuuint32_t)stride_h, 1};
+            CUresult r = g_encode_tiled(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                        const_cast<void*>(x), dims, strides, box, estr,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
+        }
+        {
+            const cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)N};
+            const cuuint64_t strides[3] = {(cuuint64_t)(K * 2), (cuuint64_t)(Wo * K * 2),
+                                           (cuuint64_t)(Ho * Wo * K * 2)};
+            const cuuint32_t box[4] = {64, (cuuint32_t)rg.wseg, (cuuint32_t)rg.rows_per_step, 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            CUresult r = g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                        const_cast<void*>(dy), dims, strides, box, estr,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(dy) failed (%d)", (int)r);
+        }
+        kp.c = dw;
+        kp.ldc = RSC;
+        kp.c_dtype = dw_dtype;
+        // M = 128 (two tap rows x 64 channels), both operands MN-major; the kernel sets N per
+        // column phase.
+        kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, static_cast<uint32_t>(64 * rg.nq[0]));
+        kp.conv.sh = stride_h;
+        kp.conv.sw = stride_w;
+        kp.conv.ph = pad_h;
+        kp.conv.pw = pad_w;
+        kp.conv.R = static_cast<int32_t>(R);
+        kp.conv.S = static_cast<int32_t>(S);
+        kp.conv.Cg = static_cast<int32_t>(Cg);
+        kp.conv.Kg = static_cast<int32_t>(Kg);
+        kp.conv.ho = static_cast<int32_t>(rg.ho);
+        kp.conv.ho_pad = static_cast<int32_t>(rg.ho_pad);
+        kp.conv.rows_per_step = rg.rows_per_step;
+        kp.conv.wseg = rg.wseg;
+        kp.conv.qmax = rg.qmax;
+        kp.conv.nq[0] = rg.nq[0];
+        kp.conv.nq[1] = rg.nq[1];
+        return run(prob, streamk, reduction, ctas, kp, dw, RSC * cs, K, RSC * cs, ws, ws_bytes,
+                   static_cast<cudaStream_t>(stream));
+    }
     // dy as a [N*Ho*Wo][K] matrix: 64-filter x 64-pixel boxes (MN-major operand)
     rc = encode_2d(&kp.tmap_a, dy, 2, K, N * Ho * Wo, K * 2, 64, 64);
     if (rc) return rc;
@@ -960,7 +1094,6 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
     kp.c = dw;
     kp.ldc = RSC;
     kp.c_dtype = dw_dtype;
-    const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
     kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, static_cast<uint32_t>(sk::kTileN));
     kp.conv.HoWo = Ho * Wo;
     kp.conv.Wo = static_cast<int32_t>(Wo);
@@ -1240,7 +1373,40 @@ int sk_probe_flag_timeout(int timeout_ms, void* stream) {
 static __device__ __align__(256) unsigned char g_sk_static_ws[SK_STATIC_WS_BYTES];
 
 static std::mutex g_static_ws_mu;
-static void* g_static_ws_ptr[64];
+
+// The array's address on each device, looked up once per device and CUDA context: a context that
+// was torn down and created again (cudaDeviceReset) loads the module again, so the address is
+// looked up again when the current context's id changes. Without the driver's context-id entry
+// points the address is looked up on every call.
+struct StaticWsAddr {
+    bool valid = false;
+    unsigned long long ctx_id = 0;
+    void* ptr = nullptr;
+};
+static StaticWsAddr g_static_ws_addr[64];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+static std::once_flag g_ctx_fn_once;
+static CtxGetCurrentFn g_ctx_get_current = nullptr;
+static CtxGetIdFn g_ctx_get_id = nullptr;
+
+static bool current_context_id(unsigned long long& id) {
+    std::call_once(g_ctx_fn_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    CUcontext ctx = nullptr;
+    return g_ctx_get_current && g_ctx_get_id && g_ctx_get_current(&ctx) == CUDA_SUCCESS &&
+           ctx != nullptr && g_ctx_get_id(ctx, &id) == CUDA_SUCCESS;
+}
 
 int sk_gemm_rcr_static_ws(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64_t K,
                           const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
@@ -1258,13 +1424,19 @@ int sk_gemm_rcr_static_ws(int ab_dtype, int c_dtype, int64_t M, int64_t N, int64
     void* ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_static_ws_mu);
-        if (g_static_ws_ptr[dev] == nullptr) {   // once per device, with that device current
+        StaticWsAddr& a = g_static_ws_addr[dev];
+        unsigned long long id = 0;
+        const bool have_id = current_context_id(id);
+        if (!have_id || !a.valid || a.ctx_id != id) {   // set-up, with this device current
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_sk_static_ws);
             if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
-            g_static_ws_ptr[dev] = p;
+            unsigned long long id2 = 0;
+            a.valid = current_context_id(id2);   // the lookup may have created the context
+            a.ctx_id = id2;
+            a.ptr = p;
         }
-        ws = g_static_ws_ptr[dev];
+        ws = a.ptr;
     }
     // Size the plan the call will use and refuse it up front if it does not fit.
     sk_problem prob;

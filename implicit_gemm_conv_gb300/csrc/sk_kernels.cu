@@ -91,14 +91,22 @@ template <int OP, int TN, int CG, int ST>
 struct Cfg {
     static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8 || OP == kOpFp8Block,
                   "CTA pairs serve the GEMMs only");
-    static_assert(CG == 2 || TN == 128, "one CTA computes 128 x 128 tiles");
+    static_assert(CG == 2 || TN == 128 || (is_wgrad_row(OP) && TN == 192),
+                  "one CTA computes 128 x 128 tiles (shifted-row wgrad: 128 x 192)");
     static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
+    static constexpr bool kWgRow = is_wgrad_row(OP);
+    static constexpr int kPhases = OP == kOpWgradRow2 ? 2 : 1;   // x column phases (W stride)
     static constexpr int kElem = kFp8 ? 1 : 2;
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
     static constexpr int kTileMAll = kTileM * CG;          // tile rows of the CTA (pair)
     static constexpr int kBRows = TN / CG;                 // B rows this CTA stages
-    static constexpr int kABytes = kTileM * 128;           // 16 KB
-    static constexpr int kBBytes = kBRows * 128;
+    // Shifted-row wgrad stage: per phase an x row of the tile's upper and of its lower tap row
+    // (64 positions x 64 channels, 8 KB each), then the dy rows (64 positions x 64 filters) with
+    // room for the shifts' overrun (at most 7 rows past the 64, kept zero), 9 KB.
+    static constexpr int kXRowBytes = 64 * 128;
+    static constexpr int kDyBytes = 9 * 1024;
+    static constexpr int kABytes = kWgRow ? kPhases * 2 * kXRowBytes : kTileM * 128;   // 16 KB
+    static constexpr int kBBytes = kWgRow ? kDyBytes : kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     // ST stages in the ring; two CTAs share an SM when the ring is at most 96 KB.
     static constexpr int kStages = ST;
@@ -107,8 +115,11 @@ struct Cfg {
     // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
     // Block-scaled fp8: the two buffers take one K step's partial each (the MMAs run up to two steps
     // ahead of the epilogue's promotion); the last step's buffer then holds the segment's sum.
-    static constexpr int kAccBufs = TN == 256 ? 1 : 2;
+    static constexpr int kAccBufs = (TN == 256 || kWgRow) ? 1 : 2;
     static constexpr int kTmemCols = kAccBufs * TN;
+    // The allocation is a power of two of at least 32 columns.
+    static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64
+                                      : kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
     // Barrier slots: [full x ST][empty x ST][acc full x kAccBars][acc empty x kAccBars][fold].
     static constexpr int kAccBars = kAccBufs < 2 ? 2 : kAccBufs;
     static constexpr int kBarTfull = 2 * kStages;
@@ -120,7 +131,7 @@ struct Cfg {
     // 128 rows x (32 x kFoldUnitChunks) fp32 columns, contiguous in the fragment-major layout:
     // 64 KB with one CTA per SM, 32 KB in the smaller ring of a pair.
     static constexpr int kFoldUnitChunks =
-        (CG == 1 && TN >= 128 && ST * kStageBytes >= 128 * 1024) ? 4 : 2;   // 32-column chunks per unit
+        (CG == 1 && (TN / 32) % 4 == 0 && ST * kStageBytes >= 128 * 1024) ? 4 : 2;   // 32-column chunks per unit
     static constexpr int kFoldUnitBytes = kTileM * 32 * 4 * kFoldUnitChunks;
     static constexpr int kFoldBufs = kStages * kStageBytes / kFoldUnitBytes;
     static_assert(kFoldBufs >= 2, "the fold needs two staging buffers");
@@ -132,7 +143,8 @@ struct Cfg {
     // The block-scaled fp8 pair keeps one too (its ring is deep enough without the space).
     // A 3-stage one-CTA ring (two CTAs per SM) has none: its last tile leaves through the ring.
     static constexpr int kEpiStageBytes =
-        ((CG == 1 && OP != kOpWgrad16 && ST > 3) || OP == kOpFp8Block) ? kTileM * TN * 2 : 0;
+        ((CG == 1 && OP != kOpWgrad16 && !kWgRow && ST > 3) || OP == kOpFp8Block) ? kTileM * TN * 2
+                                                                                   : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
     static constexpr int kBarBytes = (kBarFold + kFoldBufs) * 8;
     // Block-scaled fp8: each epilogue thread's ring of block scales (A and B) copied kScaleAhead
@@ -234,6 +246,27 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
                 tma_load_2d(b_dst + j * (C::TK * 128), &P.tmap_b, bar, col + 64 * j,
                             static_cast<int32_t>(g) * cg.Kg + c0);
         }
+    } else if constexpr (is_wgrad_row(OP)) {
+        // K step k: rows_per_step output rows of image n (rows counted per image over ho_pad), each
+        // a segment of wseg positions. B = dy from position -qmax, so that each segment starts with
+        // the zero halo that the shifted reads of its first positions take; A = per column phase the
+        // x rows of the tile's two tap rows, at traversal strides (sw, sh) from the tensor map.
+        const ConvGeom& cg = P.conv;
+        const uint32_t rr0 = static_cast<uint32_t>(k) * static_cast<uint32_t>(cg.rows_per_step);
+        const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
+        const uint32_t n_img = rr0 / hp;   // < 2^31 (checked on the host)
+        const int32_t ho0 = static_cast<int32_t>(rr0 - n_img * hp);
+        tma_load_4d(b_dst, &P.tmap_b, bar, static_cast<int32_t>(g) * cg.Kg, -cg.qmax, ho0,
+                    static_cast<int32_t>(n_img));
+        const int32_t r0 = 2 * static_cast<int32_t>(mt);
+#pragma unroll
+        for (int phs = 0; phs < C::kPhases; ++phs)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (r0 + j < cg.R)
+                    tma_load_4d(a_dst + (phs * 2 + j) * C::kXRowBytes, &P.tmap_a, bar,
+                                static_cast<int32_t>(g) * cg.Cg, phs - cg.pw,
+                                cg.sh * ho0 + r0 + j - cg.ph, static_cast<int32_t>(n_img));
     } else if constexpr (CG == 2) {
         // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
         const int32_t kx = static_cast<int32_t>(k * C::TK);
@@ -298,6 +331,13 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
+        // Bytes one stage receives: every box of a shifted-row wgrad step is 8 KB; the lower x row
+        // of a tile whose lower tap row lies past the filter is not loaded.
+        uint32_t stage_tx = C::kStageBytes;
+        if constexpr (C::kWgRow)
+            stage_tx = static_cast<uint32_t>(C::kXRowBytes) *
+                       (1u + static_cast<uint32_t>(C::kPhases) *
+                                 (2 * mt + 1 < P.conv.R ? 2u : 1u));
         WgradSlabs<TN> slabs;
         if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
         PixelStart ps{0, 0, 0};
@@ -321,7 +361,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
                 issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
                                             mapa_shared(full, 0), slabs, rank, ps);
             } else {
-                mbar_arrive_expect_tx(full, C::kStageBytes);
+                mbar_arrive_expect_tx(full, stage_tx);
                 issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes, full, slabs,
                                             rank, ps);
             }
@@ -381,6 +421,37 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
     tc_fence_after();
     const uint32_t a_addr = ring + stage * C::kStageBytes;
     const uint32_t b_addr = a_addr + C::kABytes;
+    if constexpr (C::kWgRow) {
+        // Per column phase: D[(tap row, channel)][(shift, filter)] over the step's 64 positions.
+        // A = the upper and lower x rows (two 64-channel blocks 8 KB apart); B = the dy rows read
+        // at the phase's nq shifts, one 64-filter block per shift, each block one row after the
+        // previous (LBO = 128): block b holds shift q = nq - 1 - b, its rows start at
+        // qmax - q. The phase's taps fill D columns [col0, col0 + 64 * nq).
+        const ConvGeom& cg = P.conv;
+        uint32_t col0 = 0;
+#pragma unroll
+        for (int phs = 0; phs < C::kPhases; ++phs) {
+            const uint32_t nq = static_cast<uint32_t>(cg.nq[phs]);
+            const uint32_t idesc = (P.idesc & ~(0x3Fu << 17)) | ((nq * 64u >> 3) << 17);
+            const uint32_t b0 = b_addr + static_cast<uint32_t>(cg.qmax + 1 - static_cast<int>(nq)) * 128u;
+            if (nq > 0) {
+#pragma unroll
+                for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a_addr + phs * 2 * C::kXRowBytes + kk * 2048,
+                                                        C::kXRowBytes, 1024);
+                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 128, 1024);
+                    mma_f16<CG>(d_tmem + col0, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+                }
+            }
+            col0 += nq * 64u;
+        }
+        tc_commit<CG>(empty);
+        if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+        }
+        return true;
+    }
 #pragma unroll
     for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
         uint64_t ad, bd;
@@ -514,11 +585,50 @@ struct EpiCtx {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
+// Shifted-row wgrad: the dW offset, relative to the thread's (group, tap row, channel) base, of
+// the first filter of the 32 D columns starting at `col` (a multiple of 32), or -1 past the tile's
+// taps. Consecutive columns are consecutive filters, `ldc` = R*S*C/G elements apart.
+__device__ __forceinline__ int64_t wgrow_col_offset(const ConvGeom& cg, int64_t ldc, int col) {
+    int cb = 0;
+#pragma unroll
+    for (int phs = 0; phs < 2; ++phs) {
+        const int nq = cg.nq[phs];
+        if (col < cb + nq * 64) {
+            const int b = (col - cb) >> 6, k0 = (col - cb) & 63;
+            const int s = cg.sw * (nq - 1 - b) + phs;
+            return static_cast<int64_t>(k0) * ldc + static_cast<int64_t>(s) * cg.Cg;
+        }
+        cb += nq * 64;
+    }
+    return -1;
+}
+
 // Store 32 consecutive columns (n_base + col0 ...) of this thread's row.
 template <int OP>
 __device__ __forceinline__ void store_out(const KernelParams& P, const EpiCtx& e, int col0,
                                           float (&v)[32]) {
     if (!e.row_ok) return;
+    if constexpr (is_wgrad_row(OP)) {
+        // 32 filters of one (tap, channel): a warp's lanes hold consecutive channels, so each
+        // filter's 32 values form one contiguous 128-byte (fp32) or 64-byte line.
+        const int64_t off = wgrow_col_offset(P.conv, P.ldc, col0);
+        if (off < 0) return;
+        const int64_t base = e.out_row + off;
+        if (P.c_dtype == SK_F32) {
+            float* dst = static_cast<float*>(P.c) + base;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dst[i * P.ldc] = v[i];
+        } else if (P.c_dtype == SK_BF16) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(P.c) + base;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dst[i * P.ldc] = __float2bfloat16_rn(v[i]);
+        } else {
+            __half* dst = static_cast<__half*>(P.c) + base;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dst[i * P.ldc] = __float2half_rn(v[i]);
+        }
+        return;
+    }
     const int64_t n0 = e.n_base + col0;
     const int64_t ncols = e.n_end;
     if (n0 >= ncols) return;
@@ -763,6 +873,17 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     if (red == SK_ATOMIC) {
         // tcgen05.ld is warp-collective (.sync.aligned): every lane loads, and only the lanes of
         // rows inside the output add.
+        if constexpr (is_wgrad_row(OP)) {
+            for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
+                if (!e.row_ok) return;
+                const int64_t off = wgrow_col_offset(P.conv, P.ldc, ch * 32);
+                if (off < 0) return;
+                float* dst = static_cast<float*>(P.c) + e.out_row + off;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) red_add_f32(dst + i * P.ldc, v[i]);
+            });
+            return;
+        }
         for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
             if (!e.row_ok) return;
             const int64_t n0 = e.n_base + ch * 32;
@@ -1082,6 +1203,13 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             e.out_row = map_row(P.conv.rows, m);
             e.n_base = g * plan.gemm_n + nt * TN;
             e.n_end = (g + 1) * plan.gemm_n;
+        } else if constexpr (is_wgrad_row(OP)) {
+            // Row m = (tap row r, channel c) of group g: dW[(g*Kg + k)][r][s][c] at
+            // out_row + k * ldc + s * Cg.
+            const int64_t r = m >> 6, c = m & 63;
+            e.out_row = e.row_ok ? (g * P.conv.Kg) * P.ldc + r * P.conv.S * P.conv.Cg + c : 0;
+            e.n_base = 0;
+            e.n_end = plan.gemm_n;
         } else {
             e.out_row = g * plan.gemm_m + m;
             e.n_base = nt * TN;
@@ -1131,9 +1259,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
 
     uint32_t ticket = 0;
     if (threadIdx.x == 0) {
-        // Take the ticket first: its round trip to L2 overlaps the barrier set-up below. A pair
-        // takes one ticket, in its even CTA.
-        if (rank == 0) ticket = atomicAdd(P.control, 1u);
+        tma_prefetch_desc(&P.tmap_a);
+        tma_prefetch_desc(&P.tmap_b);
         // The allocation below overwrites this; whatever a previous kernel left in shared memory
         // can never be taken for a TMEM address.
         ctl->tmem_base = kTmemSentinel;
@@ -1149,26 +1276,45 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
             mbar_init(bars + (C::kBarFold + f) * 8, 1);   // owner's fold buffers
         fence_mbarrier_init();
         ctl->abort = 0;
-        if (CG == 1) ctl->cta = static_cast<long long>(ticket);
-        tma_prefetch_desc(&P.tmap_a);
-        tma_prefetch_desc(&P.tmap_b);
     }
-    if constexpr (CG == 2) {
-        // Both CTAs of the pair have started and initialised their barriers; then the even CTA
-        // hands its ticket to both.
-        cluster_sync();
-        if (threadIdx.x == 0 && rank == 0) {
+    // Barriers and the sentinel are in place (and, for a pair, both CTAs have started) before the
+    // allocation writes the slot.
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tmem_alloc<CG>(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)),
+                       C::kTmemAlloc);
+        tmem_relinquish<CG>();
+    }
+    if constexpr (C::kWgRow) {
+        // The rows after the 64 dy rows of every stage, which the shifted reads of a step's last
+        // positions reach, hold zeros. No copy ever writes them (the owner's fold, which reuses the
+        // ring, comes after the CTA's last MMA), so every thread clears a part of them once; the
+        // fence makes the stores visible to the tensor cores, and the barrier below orders them
+        // before the first MMA.
+        constexpr int kPadBytes = C::kDyBytes - 64 * 128;
+        for (int i = static_cast<int>(threadIdx.x); i < C::kStages * kPadBytes / 16; i += kThreads) {
+            const int st = i / (kPadBytes / 16), b = i - st * (kPadBytes / 16);
+            st_shared_v4(ring + st * C::kStageBytes + C::kABytes + 64 * 128 + b * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
+    // The launch may overlap the tail of the kernel that zeroes the flags, the ticket counter and
+    // the scratch (a programmatic dependent launch): everything above touches only this CTA's
+    // shared memory, its TMEM and the tensor maps. Every thread waits for that kernel's writes
+    // before anything here can touch one of those words; a launch without that dependency passes
+    // straight through.
+    grid_dependency_wait();
+    if (threadIdx.x == 0 && rank == 0) {
+        // A pair takes one ticket, in its even CTA, and hands it to both (the barrier below
+        // publishes the stores).
+        ticket = atomicAdd(P.control, 1u);
+        if constexpr (CG == 2) {
             const uint32_t cta_off = ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, cta));
             st_shared_cluster_u64(mapa_shared(cta_off, 0), ticket);
             st_shared_cluster_u64(mapa_shared(cta_off, 1), ticket);
+        } else {
+            ctl->cta = static_cast<long long>(ticket);
         }
-    } else {
-        __syncthreads();   // the sentinel is in place before the allocation writes the slot
-    }
-    if (warp == 1) {
-        tmem_alloc<CG>(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)),
-                       C::kTmemCols);
-        tmem_relinquish<CG>();
     }
     tc_fence_before();
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
@@ -1179,17 +1325,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     // expected; it keeps a bad slot from ever reaching a TMEM access. A pair takes the verdict
     // of both its slots, so that both CTAs leave together.
     auto bad_slot = [](uint32_t t) {
-        return t == kTmemSentinel || (t >> 16) != 0 || (t & 0xFFFFu) + C::kTmemCols > 512u;
+        return t == kTmemSentinel || (t >> 16) != 0 || (t & 0xFFFFu) + C::kTmemAlloc > 512u;
     };
+    // `freeable`: the columns this CTA was granted can be handed back on the way out. A pair frees
+    // only when both slots are TMEM addresses, since its deallocation is issued by both CTAs.
     bool bad = bad_slot(tmem_base);
+    bool freeable = !bad;
     if constexpr (CG == 2) {
         const uint32_t peer = ld_shared_cluster_u32(
             mapa_shared(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)), rank ^ 1u));
+        freeable = freeable && !bad_slot(peer);
         bad = bad || bad_slot(peer) || peer != tmem_base;
         cluster_sync();   // the peer's slot has been read before either CTA can leave
     }
     if (bad) {
+        // Never expected. Nothing has touched TMEM yet; the columns are still released before the
+        // CTA leaves, so that a later CTA's allocation on this SM is not left waiting for them.
         if (threadIdx.x == 0) record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
+        tc_fence_before();
+        if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+        if (warp == 1 && freeable) {
+            tc_fence_after();
+            tmem_dealloc<CG>(tmem_base, C::kTmemAlloc);
+        }
         return;
     }
 
@@ -1209,7 +1367,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<CG>(tmem_base, C::kTmemCols);
+        tmem_dealloc<CG>(tmem_base, C::kTmemAlloc);
     }
 }
 
@@ -1249,6 +1407,22 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     } else if (P.tensor_scaled) {
         for (int j = 0; j < 4; ++j) v[j] *= P.scale;
     }
+    if (is_wgrad_row(P.op_kind)) {   // four consecutive filters of one (tap, channel)
+        const int64_t r = m >> 6, c = m & 63;
+        const int64_t coff = wgrow_col_offset(P.conv, P.ldc, static_cast<int>(n0 & ~int64_t(31)));
+        if (coff < 0) return;
+        const int64_t base = (g * P.conv.Kg) * P.ldc + r * P.conv.S * P.conv.Cg + c + coff +
+                             (n0 & 31) * P.ldc;
+        for (int j = 0; j < 4; ++j) {
+            if (P.c_dtype == SK_F32)
+                static_cast<float*>(P.c)[base + j * P.ldc] = v[j];
+            else if (P.c_dtype == SK_BF16)
+                static_cast<__nv_bfloat16*>(P.c)[base + j * P.ldc] = __float2bfloat16_rn(v[j]);
+            else
+                static_cast<__half*>(P.c)[base + j * P.ldc] = __float2half_rn(v[j]);
+        }
+        return;
+    }
     const int64_t off = out_row * P.ldc + col;
     const bool full = n0 + 4 <= plan.gemm_n;
     if (P.c_dtype == SK_F32) {
@@ -1285,44 +1459,60 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
 // ---------------------------------------------------------------------------------------------
 
 template <int OP, int TN, int CG, int ST>
-static int launch_main_t(const KernelParams& p, cudaStream_t stream) {
+static int launch_main_t(const KernelParams& p, bool after_zero, cudaStream_t stream) {
     using C = Cfg<OP, TN, CG, ST>;
     auto kern = sk_main_kernel<OP, TN, CG, ST>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmem));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    if (p.plan.grid <= 0) return 0;
-    if constexpr (CG == 1) {
-        kern<<<dim3(static_cast<unsigned>(p.plan.grid)), dim3(kThreads), C::kSmem, stream>>>(p);
-        return static_cast<int>(cudaGetLastError());
-    } else {
-        // One cluster of two CTAs per logical CTA.
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(p.plan.grid * CG));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = C::kSmem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return static_cast<int>(cudaLaunchKernelEx(&cfg, kern, p));
+    // Set once per device (the attribute belongs to the function in that device's context).
+    static unsigned long long smem_set = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+    if (dev < 0 || !(smem_set & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(C::kSmem));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        if (dev >= 0) smem_set |= 1ull << dev;
     }
+    if (p.plan.grid <= 0) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.plan.grid * CG));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CG == 2) {   // one cluster of two CTAs per logical CTA
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = CG;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (after_zero) {   // start while the zeroing kernel just before it finishes
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
 template <int OP, int TN, int CG, int ST>
 static int ctas_per_sm_t() {
     using C = Cfg<OP, TN, CG, ST>;
     auto kern = sk_main_kernel<OP, TN, CG, ST>;
+    // Queried once per device.
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+    if (dev >= 0 && cached[dev] > 0) return cached[dev];
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
         return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, C::kSmem) != cudaSuccess)
         return 0;
+    if (dev >= 0) cached[dev] = n;
     return n;
 }
 
@@ -1346,6 +1536,8 @@ static size_t smem_bytes_t() {
      : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 3>(__VA_ARGS__)                            \
      : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 3>(__VA_ARGS__)                            \
      : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 1, 5>(__VA_ARGS__)                          \
+     : (op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 1, 8>(__VA_ARGS__)                        \
+     : (op) == kOpWgradRow2 ? fn<kOpWgradRow2, 192, 1, 5>(__VA_ARGS__)                        \
                          : fn<kOpWgrad16, 128, 1, 7>(__VA_ARGS__))
 
 size_t main_smem_bytes(int op, int cg, int tn, int st) {
@@ -1356,10 +1548,11 @@ int main_ctas_per_sm(int op, int cg, int tn, int st) {
     return SK_DISPATCH(op, cg, tn, st, ctas_per_sm_t);
 }
 
-int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream) {
+int launch_main(const KernelParams& p, int op, int cg, int tn, int st, bool after_zero,
+                cudaStream_t stream) {
     if (cg == 2 && op != kOpGemm16 && op != kOpFp8 && op != kOpFp8Block)
         return static_cast<int>(cudaErrorInvalidValue);
-    return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, stream);
+    return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, after_zero, stream);
 }
 
 int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
@@ -1369,12 +1562,46 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int tn = p.plan.tn == 256 ? 256 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
-    if (cg == 2 && tn == 256)
+    if (p.plan.tn == 192)
+        sk_stage2_kernel<192, 1><<<dim3(static_cast<unsigned>(tiles), 128u * 192u / 4u / kStage2Threads),
+                                   dim3(kStage2Threads), 0, stream>>>(p);
+    else if (cg == 2 && tn == 256)
         sk_stage2_kernel<256, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else if (cg == 2)
         sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
     else
         sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+// Zeroes up to three 16-byte aligned ranges (flags + control block, scratch) and one strided
+// 2-D range of 4-byte words (the fp32 output of the atomic reduction) ahead of a main kernel.
+// Every CTA first lets the main kernel's launch begin, so that its start-up overlaps this kernel.
+__global__ void __launch_bounds__(256) sk_zero_kernel(const __grid_constant__ ZeroParams z) {
+    grid_launch_dependents();
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int r = 0; r < z.nranges; ++r) {
+        uint4* p = static_cast<uint4*>(z.ptr[r]);
+        const int64_t n = z.bytes[r] / 16;
+        for (int64_t i = tid; i < n; i += nthr) p[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (z.rows > 0) {
+        const int64_t words = z.row_bytes / 4;
+        const int64_t n = words * z.rows;
+        for (int64_t i = tid; i < n; i += nthr) {
+            const int64_t row = i / words, w = i - row * words;
+            reinterpret_cast<uint32_t*>(static_cast<char*>(z.out) + row * z.pitch)[w] = 0u;
+        }
+    }
+}
+
+int launch_zero(const ZeroParams& z, cudaStream_t stream) {
+    int64_t work = z.rows * (z.row_bytes / 4);
+    for (int r = 0; r < z.nranges; ++r) work += z.bytes[r] / 16;
+    if (work <= 0) return 0;
+    const int64_t blocks = imin(imax(ceil_div(work, 256 * 8), 1), 1184);
+    sk_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(z);
     return static_cast<int>(cudaGetLastError());
 }
 

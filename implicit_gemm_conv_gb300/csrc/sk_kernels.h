@@ -12,8 +12,15 @@ namespace sk {
 
 enum OpKind : int {
     kOpGemm16 = 0, kOpFp8 = 1, kOpWgrad16 = 2, kOpFprop16 = 3, kOpDgrad16 = 4,
-    kOpFp8Block = 5   // fp8 with block scales: each K step's partial promoted by the epilogue
+    kOpFp8Block = 5,   // fp8 with block scales: each K step's partial promoted by the epilogue
+    // Wgrad of 64-channel, 64-filter groups on shifted rows (one x row serves every column tap):
+    // W stride 1 (one phase of x columns) or 2 (even and odd columns).
+    kOpWgradRow1 = 6, kOpWgradRow2 = 7
 };
+
+__host__ __device__ constexpr bool is_wgrad_row(int op) {
+    return op == kOpWgradRow1 || op == kOpWgradRow2;
+}
 
 // Forward convolution and data gradient fold conv groups into the output's columns (the output
 // is [pixels][channels]); wgrad folds them into its rows.
@@ -67,11 +74,19 @@ struct ConvGeom {
     int32_t Cg, Kg;        // wgrad: channels and filters per group; fprop / dgrad: channels per
                            // group of the im2col'd tensor (x: C/G, dy: K/G) and filter rows per group
     int32_t Cw;            // fprop / dgrad: channels per group of the filter (C/G)
+    // Shifted-row wgrad (kOpWgradRow*): a K step is `rows_per_step` output rows of `wseg`
+    // positions (rows_per_step * wseg = 64) of image n, rows counted per image over ho_pad (Ho
+    // rounded up to rows_per_step). Column tap s = sw * q + phase reads the dy row shifted by q
+    // positions (q <= qmax); phase p holds nq[p] taps.
+    int32_t ho, ho_pad, rows_per_step, wseg, qmax;
+    int32_t nq[2];
 };
 
 struct KernelParams {
-    CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K]
-    CUtensorMap tmap_b;    // GEMM: B [N][K]; fp8: B8 [N][K]; wgrad: im2col view of x
+    CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K];
+                           // shifted-row wgrad: x [N][H][W][C], strided rows of 64 channels
+    CUtensorMap tmap_b;    // GEMM: B [N][K]; fp8: B8 [N][K]; wgrad: im2col view of x;
+                           // shifted-row wgrad: dy [N][Ho][Wo][K], rows of 64 filters
     CUtensorMap tmap_c;    // when c_tma: C [M][N] 16-bit, 64 x 32 boxes, 128-byte swizzle
     sk_plan_t plan;
     void* c;               // output
@@ -109,6 +124,18 @@ struct Stage2Params {
     int32_t tensor_scaled; // 1: multiply by `scale`
     const float* scratch;
     int32_t c_dtype;
+    ConvGeom conv;         // shifted-row wgrad: where a tile row and column go in dW
+};
+
+// Ranges a zeroing kernel clears ahead of a main kernel: up to three 16-byte aligned 1-D ranges
+// (sizes multiples of 16 bytes) and one 2-D range of `rows` rows of `row_bytes` (a multiple of 4)
+// at `pitch` bytes apart.
+struct ZeroParams {
+    void* ptr[3];
+    int64_t bytes[3];
+    int32_t nranges;
+    void* out;
+    int64_t pitch, row_bytes, rows;
 };
 
 // cg: 1 = one CTA per 128 x 128 tile (7 stages); 2 = a cluster of two CTAs per 256 x tn tile
@@ -118,8 +145,12 @@ size_t main_smem_bytes(int op, int cg, int tn, int st);
 // How many CTAs of the main kernel fit on one SM (0 if the device query fails).
 int main_ctas_per_sm(int op, int cg, int tn, int st);
 // Launch the main kernel: p.plan.grid logical CTAs, each one CTA (cg 1) or one cluster of two
-// (cg 2). Returns a cudaError_t value.
-int launch_main(const KernelParams& p, int op, int cg, int tn, int st, cudaStream_t stream);
+// (cg 2). `after_zero`: the launch directly follows launch_zero on `stream` and may overlap its
+// tail. Returns a cudaError_t value.
+int launch_main(const KernelParams& p, int op, int cg, int tn, int st, bool after_zero,
+                cudaStream_t stream);
+// Launch the zeroing kernel (nothing when every range is empty). Returns a cudaError_t value.
+int launch_zero(const ZeroParams& z, cudaStream_t stream);
 // Launch the Stage-2 reduce over the shared tiles of a workspace plan.
 int launch_stage2(const Stage2Params& p, cudaStream_t stream);
 // Read and clear the device error record: returns the code (0 = none) and fills info[3].

@@ -33,6 +33,18 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+
+// Wait until the grid this one was launched to overlap (programmatic stream serialization) has
+// finished and its writes are visible; a no-op for a launch without that dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the launch of the grid that depends on this one begin now.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier ------------------------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -147,6 +159,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Tiled load of a 4-D box at (x, y, z, w) (x innermost); the traversal strides are the tensor
+// map's. Coordinates outside the tensor read zeros.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
 
@@ -358,6 +381,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 //  K-major  : rows of 128 B along K, 8-row atoms 1024 B apart (SBO); LBO unused.
 //  MN-major : rows of 128 B along M/N (64 16-bit elements) per K index; 8 K-rows form a 1024 B
 //             atom; LBO = bytes between 64-element M/N blocks, SBO = bytes between 8-row K groups.
+// The base-offset field stays 0. With contiguous 8-row groups (SBO = 1024) the operand may start
+// at any 128-byte row of a buffer that TMA filled with the 128-byte swizzle, and LBO may be any
+// multiple of 128 (128: the next M/N block is the same rows one K row later): the unit reads the
+// rows TMA wrote at those addresses (measured on sm_103a through an identity operand).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);

@@ -251,10 +251,13 @@ int sk_conv2d_dgrad_nhwc(int in_dtype, int dx_dtype, int64_t N, int64_t H, int64
  * allocating library routine.
  *  - The first call on a device looks up that device's copy of the array (cudaGetSymbolAddress,
  *    which can load the library's GPU module); make that first call before any stream capture.
+ *    The address is kept per device and CUDA context: the first call after the device's context
+ *    was created again (e.g. after cudaDeviceReset) looks it up again.
  *  - A problem whose plan needs more than SK_STATIC_WS_BYTES of workspace is rejected with -2
  *    and a message giving both sizes (linear/tree need one fp32 tile per stream-K CTA, workspace
  *    one per shared tile: 64 KiB with the 128 x 128 tile, 256 KiB with the 256 x 256 pair tile,
- *    the default for GEMMs with M > 128; atomic and off need only the flag/control header).
+ *    which the automatic tile choice takes for GEMMs with M > 128 and at least 64 tiles of
+ *    256 x 256; atomic and off need only the flag/control header).
  *  - All calls share the one array and it keeps the previous call's contents: each call clears
  *    the flags, the control block and the scratch it reads before use, on `stream`. Calls that
  *    can overlap on the GPU (different streams, or several host threads) race on the array and

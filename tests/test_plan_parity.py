@@ -271,3 +271,88 @@ def test_block_scale_tile_setting():
     with sk.tile("256x256_pair"):
         with pytest.raises(sk.SkError, match="no 256 x 256 tile"):
             sk.sk_plan(prob, "dp_sk", "linear", 148, 148)
+
+
+# ---- shifted-row wgrad (automatic tile, 64-channel and 64-filter groups): GEMM view
+# M = (tap row, channel) in 128-row tiles of two tap rows, N = (column tap, filter) in one 192-wide
+# tile, reduction over the padded positions: 64 per K step, `64 / wseg` output rows of `wseg`
+# positions (the power of two >= Wo + shifts), rows counted per image over Ho rounded up.
+
+def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16"):
+    sh, sw = stride
+    ph, pw = pad
+    prob = sk.make_problem("wgrad", ab_dtype=dt, c_dtype="f32", n=N, h=H, w=W, c=C, k=K, r=R,
+                           s=S, stride_h=sh, stride_w=sw, pad_h=ph, pad_w=pw, groups=groups)
+    Ho = (H + 2 * ph - R) // sh + 1
+    Wo = (W + 2 * pw - S) // sw + 1
+    shifts = -(-S // sw) - 1
+    wseg = 1
+    while wseg < Wo + shifts:
+        wseg *= 2
+    rows = 64 // wseg
+    if rows == 0:   # rows too wide for one K step: not this view
+        return prob, None
+    ho_pad = -(-Ho // rows) * rows
+    kw = dict(tiles_m=-(-(R * 64) // 128), tiles_n=1, groups=groups, kred=N * ho_pad * wseg,
+              tm=128, tn=192, tk=64)
+    return prob, kw
+
+
+ROW_NAMED = [
+    ("wgrad 32x56x56x64", wgrad_row(32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), 1), -1),
+    ("wgrad 64x28x28x256 g4 s2", wgrad_row(64, 28, 28, 256, 256, 3, 3, (2, 2), (1, 1), 4), -1),
+    ("wgrad 2x9x13 r5 s3", wgrad_row(2, 9, 13, 64, 64, 5, 3, (1, 1), (2, 1), 1), 7),
+    ("wgrad 2x7x16 sw2", wgrad_row(2, 7, 16, 64, 64, 3, 3, (1, 2), (1, 1), 1), 7),
+]
+
+
+@pytest.mark.parametrize("name,pk,ctas", ROW_NAMED, ids=[n[0] for n in ROW_NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_row_wgrad_plans(name, pk, ctas, mode, red):
+    prob, kw = pk
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    with sk.tile("auto"):
+        cp = compare(prob, kw, mode, red, ctas, check_ctas=big)
+    assert (cp.tm, cp.tn, cp.tk) == (128, 192, 64)
+
+
+def test_row_wgrad_worked_vectors():
+    """32x56x56, 64 -> 64, 3x3: two tiles (tap rows {0,1} and {2}), 32*56 K steps of one
+    56-column row each (64 positions); 148 CTAs: 3584 steps, 24 each and one more for the first
+    32. Grouped stride 2 (4 groups of 64): 8 tiles, 14 output columns + 1 shift -> 16-position
+    rows, 4 rows per step, 14 rows per image padded to 16: 64*16/4 = 256 steps per tile."""
+    with sk.tile("auto"):
+        cp = sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", 148, 148)
+        assert (cp.tiles, cp.iters_per_tile, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
+                cp.extra_iters, cp.grid) == (2, 1792, 2, 3584, 24, 32, 148)
+        cp = sk.sk_plan(ROW_NAMED[1][1][0], "dp_sk", "atomic", 148, 148)
+        assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.iters_per_sk_cta, cp.extra_iters) == \
+            (8, 256, 148, 13, 124)
+
+
+def test_row_wgrad_sweep():
+    """Random shapes of the shifted-row kernel's domain (and some just outside it, which must keep
+    the 128 x 128 view) against the oracle's partition."""
+    rng = random.Random(29)
+    seen_row = seen_generic = 0
+    for _ in range(150):
+        R, S = rng.randint(1, 5), rng.randint(1, 3)
+        sh, sw = rng.randint(1, 3), rng.randint(1, 2)
+        ph, pw = rng.randint(0, R - 1), rng.randint(0, S - 1)
+        N, H, W = rng.randint(1, 4), rng.randint(R, 30), rng.randint(S, 80)
+        g = rng.randint(1, 3)
+        prob, kw = wgrad_row(N, H, W, 64 * g, 64 * g, R, S, (sh, sw), (ph, pw), g)
+        with sk.tile("auto"):
+            tn = sk.sk_plan(prob, "dp_sk", "atomic", 7, 148).tn
+        Wo = (W + 2 * pw - S) // sw + 1
+        fits = Wo + (-(-S // sw) - 1) <= 64
+        assert (tn == 192) == fits, (R, S, sh, sw, W, Wo)
+        if not fits:
+            seen_generic += 1
+            continue
+        seen_row += 1
+        with sk.tile("auto"):
+            compare(prob, kw, rng.choice(MODES), rng.choice(REDS), rng.choice([-1, 1, 3, 7, 148]),
+                    num_sms=rng.choice([148, 152, 8]))
+    assert seen_row > 50 and seen_generic > 5
