@@ -36,7 +36,18 @@ Readings where the pages are silent (each is listed in the design notes):
   iterations ``[j*I//s, (j+1)*I//s)``.
 * Flag table: one 32-bit flag per CTA that can publish, rounded up to 256 bytes. When a logical CTA
   is a cluster of ``cluster`` CTAs that each hand on their own rows of the tile, each of those CTAs
-  has its flag: ``4 * publishers * cluster`` bytes.
+  has its flag: ``4 * publishers * cluster`` bytes. A flag counts the partials its CTA has
+  published (a stream-K CTA shares at most two tiles: the tail of one and the head of the next).
+* Partial slots: one fp32 tile per contributor of every shared tile, so that every contributor can
+  hand its partial on: slot ``first(t) + t + j`` for contributor ``j`` of stream-K tile ``t`` (the
+  boundary CTA of two tiles contributes to both and has one slot in each), slot ``t*s + j`` for
+  slice ``j`` of split-K tile ``t``: ``sk_ctas + sk_tiles`` (stream-K) or ``T*s`` (split-K) slots.
+* Who adds the partials. The pages fix the order of the additions (linear: the owner's partial,
+  then the others in increasing contributor order; tree: the index-based rounds), not which CTA
+  performs them. Two ways reach the same sums: the owner (and in a tree each receiver) folds its
+  senders' partials, waiting only on higher ids; or every contributor publishes and then adds, in
+  that order, a share of the tile's elements from all the partials ("spread"), which waits on every
+  contributor of the tile and therefore needs all of the plan's publishing CTAs resident at once.
 """
 from __future__ import annotations
 
@@ -87,7 +98,8 @@ class Plan:
     extra: int = 0
     splits: int = 0
     grid: int = 0
-    publishers: int = 0          # CTAs that may publish a partial (flag + slot each)
+    publishers: int = 0          # CTAs that may publish a partial (one flag each)
+    slots: int = 0               # fp32 partial slots, one per contributor of a shared tile
     max_contrib: int = 1
     rounds: int = 0
     flag_bytes: int = 0
@@ -122,6 +134,7 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
         p.dp_tiles = T if s == 1 else 0
         p.grid = T * s
         p.publishers = T * s if s > 1 else 0
+        p.slots = p.publishers
     else:
         # 2. the remainder of whole waves is the stream-K part (hybrid: plus one full wave)
         p.sk_tiles = T % P
@@ -143,6 +156,7 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
         # 6. grid
         p.grid = p.sk_ctas + p.dp_tiles if mode in (DP_SK, HYBRID) else P
         p.publishers = p.sk_ctas
+        p.slots = p.sk_ctas + p.sk_tiles if p.sk_ctas else 0
     # 7. contributors of the shared tiles
     mc = 1
     shared = 0
@@ -159,7 +173,7 @@ def make_plan(*, tiles_m: int, tiles_n: int, groups: int, kred: int, tm: int, tn
     p.flag_bytes = round_up(4 * p.publishers * cluster, 256)
     tile_bytes = tm * tn * 4
     if reduction in (LINEAR, TREE):
-        p.partial_bytes = p.publishers * tile_bytes
+        p.partial_bytes = p.slots * tile_bytes
     if reduction == WORKSPACE:
         p.scratch_bytes = _n_sk_tiles(p) * tile_bytes
     p.ws_bytes = p.flag_bytes + CONTROL_BYTES + p.partial_bytes + p.scratch_bytes
@@ -307,6 +321,20 @@ def tree_senders(index: int, n: int, rounds: int) -> List[int]:
     return out
 
 
+def slot(p: Plan, t: int, j: int) -> int:
+    """Partial slot of contributor ``j`` of shared tile ``t``."""
+    if p.mode == SPLITK:
+        return t * p.splits + j
+    return contributors(p, t)[0] + t + j
+
+
+def publication(p: Plan, c: int, t: int) -> int:
+    """How many partials CTA ``c`` has published once it has handed on its partial of shared tile
+    ``t`` (its flag's value then): 2 for the second of its shared tiles, else 1."""
+    shared = [s.tile for s in cta_segments(p, c) if s.kind in (SEG_OWNER, SEG_PEER)]
+    return shared.index(t) + 1
+
+
 def linear_senders(index: int, n: int) -> List[int]:
     """Linear fixup: the owner takes every later contributor's partial, in increasing order."""
     return list(range(1, n)) if index == 0 else []
@@ -357,6 +385,13 @@ def check_invariants(p: Plan) -> None:
         rs.sort()
         assert rs[0][0] == 0 and rs[-1][1] == p.I
         assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+    # every contributor of every shared tile has its own partial slot inside the table
+    taken = set()
+    for t in _shared_tile_ids(p):
+        for j in range(len(contributors(p, t))):
+            k = slot(p, t, j)
+            assert 0 <= k < p.slots and k not in taken
+            taken.add(k)
     # waits only target higher logical ids
     for t in _shared_tile_ids(p):
         cs = contributors(p, t)
@@ -366,12 +401,18 @@ def check_invariants(p: Plan) -> None:
                 assert cs[snd] > cs[j]
 
 
-def simulate_progress(p: Plan, slots: int, reduction: int) -> bool:
+def simulate_progress(p: Plan, slots: int, reduction: int, fold: str = "owner") -> bool:
     """Discrete-event check that a pool of ``slots`` resident CTAs, started in logical-id order
-    (a ticket counter), always finishes. Each segment is one step; a receiving segment blocks until
-    every sender has published; a peer publishes when its own receives are done."""
+    (a ticket counter), always finishes.
+
+    ``fold="owner"``: each segment is one step; a receiving segment blocks until every sender has
+    published; a peer publishes when its own receives are done.
+    ``fold="spread"``: a CTA first runs all its segments, publishing every shared one without
+    waiting; then it blocks until every contributor of each of its shared tiles has published."""
     if reduction not in (LINEAR, TREE):
         return True
+    if fold == "spread":
+        return _simulate_spread(p, slots)
     work = {c: list(cta_segments(p, c)) for c in range(p.grid)}
     published = set()
     nxt = 0
@@ -401,4 +442,25 @@ def simulate_progress(p: Plan, slots: int, reduction: int) -> bool:
                 progressed = True
         if not progressed:
             return False
+    return True
+
+
+def _simulate_spread(p: Plan, slots: int) -> bool:
+    tiles_of = {c: [s.tile for s in cta_segments(p, c) if s.kind in (SEG_OWNER, SEG_PEER)]
+                for c in range(p.grid)}
+    published = set()   # (tile, cta)
+    nxt, running, done = 0, [], 0
+    while done < p.grid:
+        while len(running) < slots and nxt < p.grid:
+            for t in tiles_of[nxt]:   # a started CTA publishes all its shared segments
+                published.add((t, nxt))
+            running.append(nxt)
+            nxt += 1
+        finished = [c for c in running
+                    if all((t, d) in published for t in tiles_of[c] for d in contributors(p, t))]
+        if not finished:
+            return False
+        for c in finished:
+            running.remove(c)
+            done += 1
     return True

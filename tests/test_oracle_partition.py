@@ -168,9 +168,12 @@ def test_splitk_comparator():
 
 
 def test_workspace_layout():
+    # 4 tiles on 3 CTAs: one shared tile with 3 contributors; 3 + 1 partial slots of 64 KB
     p = plan(4, 64, 3, P.PERSISTENT, P.LINEAR)
-    assert p.flag_bytes == 256 and p.partial_bytes == 3 * 128 * 128 * 4
-    assert p.ws_bytes == 256 + P.CONTROL_BYTES + 3 * 65536
+    assert (p.publishers, p.slots) == (3, 4)
+    assert p.flag_bytes == 256 and p.partial_bytes == 4 * 128 * 128 * 4
+    assert p.ws_bytes == 256 + P.CONTROL_BYTES + 4 * 65536
+    assert [P.slot(p, 0, j) for j in range(3)] == [0, 1, 2]
     w = plan(4, 64, 3, P.PERSISTENT, P.WORKSPACE)
     assert w.partial_bytes == 0 and w.scratch_bytes == 1 * 65536
     a = plan(4, 64, 3, P.PERSISTENT, P.ATOMIC)
@@ -193,8 +196,8 @@ def test_flag_table_gives_every_cta_of_a_cluster_its_own_flag():
             # the partition itself does not depend on how many CTAs make a logical CTA
             assert (p2.sk_tiles, p2.sk_ctas, p2.iters_per_sk_cta, p2.extra, p2.grid) == \
                 (p.sk_tiles, p.sk_ctas, p.iters_per_sk_cta, p.extra, p.grid)
-            # one fp32 partial slot per CTA of each publisher: tm x tn x 4 bytes per publisher
-            assert p2.partial_bytes == p2.publishers * (128 * cluster) * 128 * 4
+            # one fp32 partial slot per contributor of a shared tile, tm x tn x 4 bytes each
+            assert p2.partial_bytes == p2.slots * (128 * cluster) * 128 * 4
 
 
 def test_forward_progress_simulation():
@@ -268,3 +271,53 @@ def test_planted_wrong_tree_direction_is_caught(monkeypatch):
                         lambda j, n, r: [j - 1] if j % 2 == 1 else [])   # waits on a lower id
     with pytest.raises(AssertionError):
         P.check_invariants(plan(4, 64, 3, P.PERSISTENT, P.TREE))
+
+
+def test_slot_worked_vector():
+    # 2 tiles of 3 iterations on 4 CTAs: ranges [0,2) [2,4) [4,5) [5,6); tile 0 is shared by CTAs
+    # 0 and 1, tile 1 by CTAs 1, 2 and 3; CTA 1 contributes to both and has a slot in each.
+    p = plan(2, 3, 4, P.DP_SK, P.LINEAR)
+    assert (p.sk_ctas, p.iters_per_sk_cta, p.extra, p.publishers, p.slots) == (4, 1, 2, 4, 6)
+    assert P.contributors(p, 0) == [0, 1] and P.contributors(p, 1) == [1, 2, 3]
+    assert [P.slot(p, 0, j) for j in range(2)] == [0, 1]
+    assert [P.slot(p, 1, j) for j in range(3)] == [2, 3, 4]
+    # CTA 1's flag reads 1 once its partial of tile 0 is out, 2 once that of tile 1 is too
+    assert (P.publication(p, 1, 0), P.publication(p, 1, 1), P.publication(p, 2, 1)) == (1, 2, 1)
+    assert p.partial_bytes == 6 * 128 * 128 * 4 and p.flag_bytes == 256
+    s = plan(2, 64, 8, P.SPLITK, P.LINEAR)     # 4 slices per tile
+    assert s.slots == 8 and [P.slot(s, 1, j) for j in range(4)] == [4, 5, 6, 7]
+
+
+def test_slots_distinct_over_sweep():
+    rng = random.Random(31)
+    for _ in range(300):
+        T, I, Pool = rng.randint(1, 40), rng.randint(1, 60), rng.randint(1, 160)
+        for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK, P.HYBRID):
+            p = plan(T, I, Pool, mode, P.LINEAR)
+            seen = set()
+            for t in P._shared_tile_ids(p):
+                for j in range(len(P.contributors(p, t))):
+                    k = P.slot(p, t, j)
+                    assert 0 <= k < p.slots and k not in seen, (T, I, Pool, mode, t, j)
+                    seen.add(k)
+
+
+def test_spread_fold_progress():
+    """With every publishing CTA resident at once, the spread fold (all contributors publish, then
+    each waits for every contributor of its tiles) always finishes; with fewer resident slots a
+    one-tile plan deadlocks, which the owner fold of the pages avoids."""
+    rng = random.Random(37)
+    cases = [(4, 64, 3), (2, 1792, 148), (8, 256, 148), (5, 1568 // 16, 148 // 4), (1, 400, 148)]
+    cases += [(rng.randint(1, 30), rng.randint(1, 40), rng.randint(2, 24)) for _ in range(60)]
+    for T, I, Pool in cases:
+        for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK, P.HYBRID):
+            for red in (P.LINEAR, P.TREE):
+                p = plan(T, I, Pool, mode, red)
+                publishing = p.grid if mode == P.SPLITK else p.sk_ctas
+                for extra in (0, 1, p.grid):
+                    assert P.simulate_progress(p, max(1, publishing) + extra, red, fold="spread"), \
+                        (T, I, Pool, mode, red)
+    one = plan(1, 400, 148, P.DP_SK, P.LINEAR)
+    assert one.sk_ctas == 148
+    assert not P.simulate_progress(one, 147, P.LINEAR, fold="spread")
+    assert P.simulate_progress(one, 2, P.LINEAR, fold="owner")
