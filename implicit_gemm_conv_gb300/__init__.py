@@ -53,7 +53,7 @@ PLAN_FIELDS = ["op", "mode", "reduction", "tm", "tn", "tk", "gemm_m", "gemm_n", 
                "sk_ctas", "sk_iters", "iters_per_sk_cta", "extra_iters", "splits", "grid",
                "publishers", "max_contributors", "tree_rounds", "shared_tiles", "flag_bytes",
                "control_offset", "partial_offset", "partial_bytes", "scratch_offset",
-               "scratch_bytes", "ws_bytes"]
+               "scratch_bytes", "ws_bytes", "partial_slots"]
 
 
 class sk_plan_t(ctypes.Structure):

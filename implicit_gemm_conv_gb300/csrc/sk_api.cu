@@ -269,6 +269,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
                         int ctas_per_sm, sk_plan_t& p);
 
 constexpr int64_t kAutoPairMinTiles = 64;   // SK_TILE_AUTO: pair tiles needed for the pair kernel
+constexpr int64_t kSpreadMinContributors = 8;   // linear / tree: contributors for the spread fold
 
 // The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
 // (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
@@ -428,7 +429,8 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
     p.flag_bytes = sk::round_up(4 * p.publishers * cg, 256);
     p.control_offset = p.flag_bytes;
     p.partial_offset = p.control_offset + sk::kControlBytes;
-    p.partial_bytes = (reduction == SK_LINEAR || reduction == SK_TREE) ? p.publishers * tile_bytes : 0;
+    p.partial_slots = mode == SK_SPLITK ? p.publishers : (p.sk_ctas > 0 ? p.sk_ctas + p.sk_tiles : 0);
+    p.partial_bytes = (reduction == SK_LINEAR || reduction == SK_TREE) ? p.partial_slots * tile_bytes : 0;
     p.scratch_offset = p.partial_offset + p.partial_bytes;
     p.scratch_bytes = reduction == SK_WORKSPACE ? sk::n_shared_candidates(p) * tile_bytes : 0;
     p.ws_bytes = p.scratch_offset + p.scratch_bytes;
@@ -564,6 +566,20 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
     kp.scratch = reinterpret_cast<float*>(w + plan.scratch_offset);
     kp.flag_timeout_ns = flag_timeout_ns();
     kp.mbar_timeout_ns = 2000000000ull;
+    // linear / tree: spread the additions over the contributors of a shared tile when a tile has
+    // many of them (the owner's fold grows with their count, a folder's share shrinks), all the
+    // CTAs that publish can be resident at once (each waits for all of its tiles' contributors),
+    // and a tree's binary counter of partial sums (8 levels) holds its contributors; otherwise
+    // the owner fold of the pages, whose waits target only later CTAs. Measured on GB300: with
+    // 4-5 contributors per tile (the 3840x4096x4096 GEMM on 74 CTA pairs) the owner fold is faster,
+    // with 19-74 (the wgrad workloads) the spread fold by 1.4-3x.
+    kp.spread = 0;
+    if ((plan.reduction == SK_LINEAR || plan.reduction == SK_TREE) && plan.shared_tiles > 0) {
+        const int64_t resident = static_cast<int64_t>(dev.sms / tc.cg) * (per_sm > 0 ? per_sm : 1);
+        kp.spread = plan.max_contributors >= kSpreadMinContributors &&
+                    plan.publishers <= resident &&
+                    (plan.reduction == SK_LINEAR || plan.max_contributors < 256);
+    }
 
     rc = SK_OK;
     do {

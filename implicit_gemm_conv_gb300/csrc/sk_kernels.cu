@@ -59,16 +59,53 @@ __device__ __noinline__ void record_error(unsigned long long code, long long cta
     }
 }
 
-// Bounded wait of a linear/tree receiver for a hand-off flag (acquire at gpu scope). `t0` is the
-// caller's deadline origin (0 = not started; set on the first miss), so that several receives can
-// share one deadline. False once `limit_ns` has passed since t0 without the flag.
-__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint64_t& t0, uint64_t limit_ns) {
-    while (ld_acquire_gpu(f) != 1u) {
+// Bounded wait of a linear/tree receiver until a hand-off flag reaches `need` (acquire at gpu
+// scope; a flag counts the partials its CTA has published). `t0` is the caller's deadline origin
+// (0 = not started; set on the first miss), so that several receives can share one deadline.
+// False once `limit_ns` has passed since t0 without the flag.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t need, uint64_t& t0,
+                                          uint64_t limit_ns) {
+    while (ld_acquire_gpu(f) < need) {
         if (t0 == 0) t0 = globaltimer_ns();
         if (globaltimer_ns() - t0 > limit_ns) return false;
         __nanosleep(128);
     }
     return true;
+}
+
+constexpr int kEpiThreadsWait = 128;       // the epilogue warps (warps 2-5)
+constexpr uint32_t kEpiBarrierWait = 2;    // their named barrier for the flag waits
+
+// All 128 epilogue threads wait together until the flags of `count` CTAs have reached their
+// values: thread i polls the flags of items i, i + 128, ... (acquire at gpu scope), and a barrier
+// reduction tells every thread when all are set, so the round trips to L2 overlap instead of
+// following one another. `item(k, cta_of_k, need_of_k)` names item k's CTA and flag value. One
+// deadline for all (`limit_ns`), decided collectively. Returns the CTA of a missing flag, or -1.
+template <typename Item>
+__device__ int64_t wait_flags_all(const uint32_t* flags, int cg, int64_t half, int64_t count,
+                                  int ethread, uint64_t limit_ns, Item&& item) {
+    uint64_t t0 = 0;
+    int64_t missing = -1;
+    while (true) {
+        bool mine = true;
+        for (int64_t k = ethread; k < count; k += kEpiThreadsWait) {
+            int64_t c;
+            uint32_t need;
+            item(k, c, need);
+            if (ld_acquire_gpu(flags + c * cg + half) < need) {
+                mine = false;
+                missing = c;
+            }
+        }
+        if (named_bar_and(kEpiBarrierWait, kEpiThreadsWait, mine)) {
+            __threadfence();   // every thread's later reads come after the flags polled above
+            return -1;
+        }
+        if (t0 == 0) t0 = globaltimer_ns();
+        const bool late = globaltimer_ns() - t0 > limit_ns;
+        if (named_bar_or(kEpiBarrierWait, kEpiThreadsWait, late)) return missing < 0 ? -2 : missing;
+        __nanosleep(64);
+    }
 }
 
 // A flag that nothing ever sets, for sk_probe_flag_timeout.
@@ -80,7 +117,7 @@ __device__ uint32_t g_sk_unset_flag;
 __global__ void sk_flag_timeout_probe_kernel(uint64_t limit_ns) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     uint64_t t0 = 0;
-    if (!wait_flag(&g_sk_unset_flag, t0, limit_ns)) record_error(kErrFlagWait, -1, -1, -1);
+    if (!wait_flag(&g_sk_unset_flag, 1u, t0, limit_ns)) record_error(kErrFlagWait, -1, -1, -1);
 }
 
 constexpr int kThreads = 192;
@@ -603,6 +640,80 @@ __device__ __forceinline__ int64_t wgrow_col_offset(const ConvGeom& cg, int64_t 
     return -1;
 }
 
+// Where an element of the tile goes: the output, its type and the op (which decides how tile rows
+// and columns map to output rows and columns), the fp8 scales (scale_mode 0: none; 1: sa[row] *
+// sb[column]; 2: the per-tensor product `scale`) and the convolution geometry.
+struct OutSpec {
+    void* c;
+    int64_t ldc;
+    int32_t c_dtype, op_kind;
+    const float* sa;
+    const float* sb;
+    float scale;
+    int32_t scale_mode;
+    const ConvGeom* conv;
+};
+
+// Scale, convert and store four consecutive GEMM-view columns n0..n0+3 of row m of group g
+// (columns past gemm_n are dropped; rows and columns outside the view are the caller's to skip).
+__device__ __forceinline__ void store4_out(const sk_plan_t& plan, const OutSpec& o, int64_t g,
+                                           int64_t m, int64_t n0, float (&v)[4]) {
+    const bool fold_cols = folds_groups_into_columns(o.op_kind);
+    const int64_t out_row = fold_cols ? map_row(o.conv->rows, m) : g * plan.gemm_m + m;
+    if (o.scale_mode == 1) {
+        const float rs = o.sa[out_row];
+        for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? o.sb[n0 + j] : 0.0f);
+    } else if (o.scale_mode == 2) {
+        for (int j = 0; j < 4; ++j) v[j] *= o.scale;
+    }
+    if (is_wgrad_row(o.op_kind)) {   // four consecutive filters of one (tap, channel)
+        const ConvGeom& cg = *o.conv;
+        const int64_t r = m >> 6, c = m & 63;
+        const int64_t coff = wgrow_col_offset(cg, o.ldc, static_cast<int>(n0 & ~int64_t(31)));
+        if (coff < 0) return;
+        const int64_t base = (g * cg.Kg) * o.ldc + r * cg.S * cg.Cg + c + coff + (n0 & 31) * o.ldc;
+        for (int j = 0; j < 4; ++j) {
+            if (o.c_dtype == SK_F32)
+                static_cast<float*>(o.c)[base + j * o.ldc] = v[j];
+            else if (o.c_dtype == SK_BF16)
+                static_cast<__nv_bfloat16*>(o.c)[base + j * o.ldc] = __float2bfloat16_rn(v[j]);
+            else
+                static_cast<__half*>(o.c)[base + j * o.ldc] = __float2half_rn(v[j]);
+        }
+        return;
+    }
+    const int64_t col = fold_cols ? g * plan.gemm_n + n0 : n0;
+    const int64_t off = out_row * o.ldc + col;
+    const bool full = n0 + 4 <= plan.gemm_n;
+    if (o.c_dtype == SK_F32) {
+        float* dst = static_cast<float*>(o.c) + off;
+        if (full) *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        else for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = v[j];
+    } else if (o.c_dtype == SK_BF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(o.c) + off;
+        if (full) {
+            __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&a);
+            w.y = *reinterpret_cast<uint32_t*>(&b);
+            *reinterpret_cast<uint2*>(dst) = w;
+        } else {
+            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2bfloat16_rn(v[j]);
+        }
+    } else {
+        __half* dst = static_cast<__half*>(o.c) + off;
+        if (full) {
+            __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&a);
+            w.y = *reinterpret_cast<uint32_t*>(&b);
+            *reinterpret_cast<uint2*>(dst) = w;
+        } else {
+            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2half_rn(v[j]);
+        }
+    }
+}
+
 // Store 32 consecutive columns (n_base + col0 ...) of this thread's row.
 template <int OP>
 __device__ __forceinline__ void store_out(const KernelParams& P, const EpiCtx& e, int col0,
@@ -795,10 +906,10 @@ __device__ void staged_fold(const KernelParams& P, int64_t cta, const sk_segment
     const int64_t units = ns * kUnitsPerSender;   // sender-major
     auto issue = [&](int64_t u) {
         const int64_t i = u / kUnitsPerSender, h = u - i * kUnitsPerSender;
-        const int64_t slot = seg.first_cta + sender(i);
+        const int64_t slot = partial_slot(P.plan, seg.tile, seg.first_cta, sender(i));
         const uint32_t buf = static_cast<uint32_t>(u % C::kFoldBufs);
         const uint32_t bar = fold_bars + buf * 8;
-        if (slot < 0 || slot >= P.plan.publishers) {   // never expected: record and skip
+        if (slot < 0 || slot >= P.plan.partial_slots) {   // never expected: record and skip
             record_error(kErrBounds, cta, seg.tile, slot);
             return;
         }
@@ -911,8 +1022,34 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         return;
     }
 
-    // linear / tree: the contributor indices this one receives from, in fold order. Linear:
-    // the owner takes 1, 2, ..., n-1. Tree: at most one sender per round.
+    // linear / tree. Every contributor's partial has its own slot; this CTA's flag counts the
+    // partials it has published.
+    const int64_t my_slot = partial_slot(plan, seg.tile, seg.first_cta, seg.index);
+    const bool slot_ok = my_slot >= 0 && my_slot < plan.partial_slots;
+    float* own = P.partials + (my_slot * CG + e.half) * static_cast<int64_t>(kTileM * TN);
+    if (P.spread) {
+        // Spread fold: hand the partial on now; the additions, a share of the tile for every
+        // contributor, follow in spread_fold once the CTA's last segment is out.
+        if (!slot_ok) {   // never expected: record and skip the stores
+            if (ethread == 0) record_error(kErrBounds, cta, seg.tile, my_slot);
+            return;
+        }
+        for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                __stcg(reinterpret_cast<float4*>(frag_ptr<TN>(own, ch * 32, i, e.row)),
+                       make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        });
+        // The barrier orders every epilogue thread's stores before the release below, which makes
+        // them visible (cumulatively) to a CTA that acquires the flag.
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (ethread == 0)
+            st_release_gpu(P.flags + cta * CG + e.half, publication(plan, cta, seg.tile));
+        return;
+    }
+
+    // Owner fold: the contributor indices this one receives from, in fold order. Linear: the
+    // owner takes 1, 2, ..., n-1. Tree: at most one sender per round.
     int32_t tree[32];
     int64_t ns = 0;
     const bool lin = red == SK_LINEAR;
@@ -924,21 +1061,16 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         });
     }
     auto sender = [&](int64_t i) -> int64_t { return lin ? i + 1 : tree[i]; };
-    if (ethread == 0) {
-        // One deadline for all of this segment's receives: a lost hand-off costs at most
-        // flag_timeout_ns, however many senders the segment has.
-        uint64_t t0 = 0;
-        bool late = false;
-        for (int64_t i = 0; i < ns && !late; ++i) {
-            const uint32_t* f = P.flags + (seg.first_cta + sender(i)) * CG + e.half;
-            if (!wait_flag(f, t0, P.flag_timeout_ns)) {
-                record_error(kErrFlagWait, cta, seg.tile, seg.first_cta + sender(i));
-                late = true;
-            }
-        }
+    if (ns > 0) {
+        // All senders' flags polled at once by the epilogue threads, one deadline for all: a lost
+        // hand-off costs at most flag_timeout_ns, however many senders the segment has.
+        const int64_t miss = wait_flags_all(P.flags, CG, e.half, ns, ethread, P.flag_timeout_ns,
+                                            [&](int64_t k, int64_t& c2, uint32_t& need) {
+                                                c2 = seg.first_cta + sender(k);
+                                                need = publication(plan, c2, seg.tile);
+                                            });
+        if (miss != -1 && ethread == 0) record_error(kErrFlagWait, cta, seg.tile, miss);
     }
-    named_bar_sync(kEpiBarrier, kEpiThreads);
-    if (ns > 0) (void)ld_acquire_gpu(P.flags + (seg.first_cta + sender(ns - 1)) * CG + e.half);
 
     if (seg.kind == SK_SEG_OWNER && ns > 0) {
         staged_fold<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ns, sender, ring, fold_bars);
@@ -946,15 +1078,15 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
     }
 
     bool publish = seg.kind == SK_SEG_PEER;
-    if (publish && cta >= plan.publishers) {   // never expected: record and skip the stores
+    if (publish && !slot_ok) {   // never expected: record and skip the stores
         if (ethread == 0) record_error(kErrBounds, cta, seg.tile, -2);
         publish = false;
     }
-    float* own = P.partials + (cta * CG + e.half) * static_cast<int64_t>(kTileM * TN);
     for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
         for (int64_t s = 0; s < ns; ++s) {
-            const float* src = P.partials + ((seg.first_cta + sender(s)) * CG + e.half) *
-                                                static_cast<int64_t>(kTileM * TN);
+            const float* src =
+                P.partials + (partial_slot(plan, seg.tile, seg.first_cta, sender(s)) * CG + e.half) *
+                                 static_cast<int64_t>(kTileM * TN);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 const float4 q = __ldcg(reinterpret_cast<const float4*>(
@@ -978,7 +1110,136 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         fence_proxy_async_global();   // a receiver may read this partial with bulk copies
         __threadfence();
         named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (ethread == 0) st_release_gpu(P.flags + cta * CG + e.half, 1u);
+        if (ethread == 0)
+            st_release_gpu(P.flags + cta * CG + e.half, publication(plan, cta, seg.tile));
+    }
+}
+
+// A shared tile whose additions this CTA takes part in under the spread fold.
+struct PendingFold {
+    int64_t tile, first, n, index;
+};
+
+// Spread fold of a shared tile (linear or tree): wait until every contributor has handed its partial
+// on, then add up this CTA's share of the tile's elements from all the partials, in the
+// reduction's own order (linear: contributor 0, then 1, 2, ...; tree: the index-based pairwise
+// rounds, kept as a binary counter of partial sums), and store them. The sums are the owner fold's,
+// bit for bit. The tile's F = 128 * TN / 4 float4s (fragment-major, per 128-row half) are split
+// evenly among its "folders": the contributors whose range lies in this one shared tile, or all of
+// them when none does (two contributors that each share a second tile); a contributor that shares
+// two tiles then folds none of the first. A share is contiguous in every slot, and a tile's slots
+// are consecutive (partial_slot(tile, first, j) = slot 0 + j): all threads copy the share's slices
+// of the n partials into the idle operand ring with coalesced loads (several in flight each), in
+// chunks that fit half of it, then every thread adds up its elements there.
+template <int OP, int TN, int CG, int ST>
+__device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFold& pd, int ethread,
+                            int64_t half, uint32_t ring) {
+    using C = Cfg<OP, TN, CG, ST>;
+    const sk_plan_t& plan = P.plan;
+    constexpr int kF4 = kTileM * TN / 4;
+    constexpr uint32_t kBufBytes = (C::kRingBytes / 2) & ~15u;
+    const int64_t n = pd.n;
+    // Folders: the contributors with a single shared tile. Only the first contributor (if this is
+    // its second shared tile) and the last (if its range runs on into a later shared tile) can
+    // share another; the others lie inside this tile.
+    auto shares_two = [&](int64_t j) {
+        if (plan.mode == SK_SPLITK) return false;
+        const int64_t c2 = pd.first + j;
+        if (j == 0) return publication(plan, c2, pd.tile) == 2;
+        if (j + 1 < n) return false;
+        const int64_t end = sk_end(plan, c2);
+        if (end - udiv31(end, plan.iters_per_tile) * plan.iters_per_tile == 0) return false;
+        int64_t f2, n2;
+        tile_contributors(plan, udiv31(end - 1, plan.iters_per_tile), f2, n2);
+        return udiv31(end - 1, plan.iters_per_tile) != pd.tile && n2 > 1;
+    };
+    const bool skip0 = shares_two(0), skip1 = n > 1 && shares_two(n - 1);
+    int64_t nfold = n - (skip0 ? 1 : 0) - (skip1 ? 1 : 0), me = pd.index - (skip0 ? 1 : 0);
+    if ((pd.index == 0 && skip0) || (pd.index == n - 1 && skip1)) me = -1;
+    if (nfold <= 0) {   // everyone folds
+        nfold = n;
+        me = pd.index;
+    }
+    if (me < 0) return;   // this CTA's part of the tile is its partial only
+    const int64_t miss = wait_flags_all(P.flags, CG, half, n, ethread, P.flag_timeout_ns,
+                                        [&](int64_t k, int64_t& c2, uint32_t& need) {
+                                            c2 = pd.first + k;
+                                            need = publication(plan, c2, pd.tile);
+                                        });
+    if (miss != -1) {
+        if (ethread == 0) record_error(kErrFlagWait, cta, pd.tile, miss);
+        return;
+    }
+    int64_t g, mt, nt;
+    tile_coords(plan, pd.tile, g, mt, nt);
+    const OutSpec o{P.c, P.ldc, P.c_dtype, OP, P.sa, P.sb, P.scale,
+                    OP == kOpFp8 ? (P.sa != nullptr ? 1 : 2) : 0, &P.conv};
+    const int64_t stride = static_cast<int64_t>(CG) * kTileM * TN;   // floats between slots
+    const float* base = P.partials + (partial_slot(plan, pd.tile, pd.first, 0) * CG + half) *
+                                         static_cast<int64_t>(kTileM * TN);
+    const int64_t b = me * kF4 / nfold, e = (me + 1) * kF4 / nfold;
+    const int64_t cap = imax(1, static_cast<int64_t>(kBufBytes) / (16 * n));   // float4s per chunk
+    const bool lin = plan.reduction == SK_LINEAR;
+    uint8_t* ring_ptr = nullptr;
+    asm volatile("cvta.shared.u64 %0, %1;" : "=l"(ring_ptr) : "l"(static_cast<uint64_t>(ring)));
+    float4* sbuf = reinterpret_cast<float4*>(ring_ptr);
+    auto add4 = [](const float4& x, const float4& y) {
+        return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+    };
+    for (int64_t c0 = b; c0 < e; c0 += cap) {
+        const int64_t len = imin(cap, e - c0);
+        // Copy the chunk's slices of all n partials, slot-major, with 16-byte asynchronous copies:
+        // every thread issues all of its own and waits once.
+        for (int64_t j = 0; j < n; ++j)
+            for (int64_t i = ethread; i < len; i += kEpiThreads)
+                cp_async_16(ring + static_cast<uint32_t>((j * len + i) * 16),
+                            base + j * stride + (c0 + i) * 4);
+        cp_async_commit();
+        cp_async_wait_all();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        for (int64_t i = ethread; i < len; i += kEpiThreads) {
+            auto part = [&](int64_t j) { return sbuf[j * len + i]; };
+            float4 v;
+            if (lin) {
+                v = part(0);
+                for (int64_t j = 1; j < n; ++j) v = add4(v, part(j));
+            } else {
+                // Tree: the pending block sums of the rounds form a binary counter. Contributor
+                // j's partial is added (on the right) to the block held at every level where j
+                // has a set bit, lowest first, and the result is held at the first clear bit; at
+                // the end the blocks of n's set bits are added right (low level) to left. acc[L]
+                // is a block of 2^L partials; n < 256 (the host takes the owner fold otherwise).
+                float4 acc[8];
+                for (int64_t j = 0; j < n; ++j) {
+                    float4 x = part(j);
+#pragma unroll
+                    for (int L = 0; L < 8; ++L) {
+                        if ((j >> L) & 1) {
+                            x = add4(acc[L], x);
+                        } else {
+                            acc[L] = x;
+                            break;
+                        }
+                    }
+                }
+                bool have = false;
+#pragma unroll
+                for (int L = 0; L < 8; ++L) {
+                    if ((n >> L) & 1) {
+                        v = have ? add4(acc[L], v) : acc[L];
+                        have = true;
+                    }
+                }
+            }
+            const int64_t idx = c0 + i;
+            const int row = static_cast<int>(idx % kTileM), q4 = static_cast<int>(idx / kTileM);
+            const int64_t m = mt * (kTileM * CG) + half * kTileM + row;
+            const int64_t n0 = nt * TN + q4 * 4;
+            if (m >= plan.gemm_m || n0 >= plan.gemm_n) continue;
+            float w[4] = {v.x, v.y, v.z, v.w};
+            store4_out(plan, o, g, m, n0, w);
+        }
+        named_bar_sync(kEpiBarrier, kEpiThreads);   // the buffer is free again
     }
 }
 
@@ -1161,6 +1422,15 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     seg_init(plan, cta, cur);
     sk_segment_t seg;
     int64_t nseg = 0, tau = 0, nblk = 0;
+    // Spread fold: the shared tiles of this CTA (at most two), folded once all its segments are out.
+    const bool spread = P.spread && (plan.reduction == SK_LINEAR || plan.reduction == SK_TREE);
+    PendingFold pend[2];
+    int npend = 0;
+    bool aborted = false;
+    auto note_shared = [&](const sk_segment_t& sg) {
+        if (spread && sg.kind != SK_SEG_FULL && npend < 2)
+            pend[npend++] = PendingFold{sg.tile, sg.first_cta, sg.n_contrib, sg.index};
+    };
     while (true) {
         const bool dp = cur.dp_next >= 0;
         if (!seg_next(plan, cta, cur, seg)) break;
@@ -1169,8 +1439,11 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             sk_segment_t next;
             const bool last = !seg_next(plan, cta, ahead, next);
             if (!promote_segment<TN, CG, ST>(P, cta, seg, dp, tau, nseg, nblk, tmem_base, bars, ctl,
-                                             ring, warp, ethread, last, rank))
+                                             ring, warp, ethread, last, rank)) {
+                aborted = true;
                 break;
+            }
+            note_shared(seg);
             ++nblk;
             continue;
         }
@@ -1190,7 +1463,10 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
             ctl->epi_ok[nseg & 1] = ready ? 1u : 0u;
         }
         named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (!ctl->epi_ok[nseg & 1]) break;
+        if (!ctl->epi_ok[nseg & 1]) {
+            aborted = true;
+            break;
+        }
         tc_fence_after();
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
@@ -1224,6 +1500,7 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         const bool last = !seg_next(plan, cta, ahead, next);
         epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ring,
                                          bars + C::kBarFold * 8, last);
+        note_shared(seg);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -1235,6 +1512,9 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         }
         ++nseg;
     }
+    if (!aborted)
+        for (int i = 0; i < npend; ++i)
+            spread_fold<OP, TN, CG, ST>(P, cta, pend[i], ethread, static_cast<int64_t>(rank), ring);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1395,63 +1675,12 @@ __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_
     const int64_t m = mt * (kTileM * CG) + half * kTileM + row;
     const int64_t n0 = nt * TN + q4 * 4;
     if (m >= plan.gemm_m || n0 >= plan.gemm_n) return;
-    const bool fold_cols = folds_groups_into_columns(static_cast<int>(P.op_kind));
-    const int64_t col = fold_cols ? g * plan.gemm_n + n0 : n0;   // output column of n0
     const float* base = P.scratch + t * static_cast<int64_t>(kTileM * CG * TN);
     const float4 q = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(idx) * 4));
     float v[4] = {q.x, q.y, q.z, q.w};
-    const int64_t out_row = fold_cols ? map_row(P.rows, m) : g * plan.gemm_m + m;
-    if (P.sa != nullptr) {
-        const float rs = P.sa[out_row];
-        for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? P.sb[n0 + j] : 0.0f);
-    } else if (P.tensor_scaled) {
-        for (int j = 0; j < 4; ++j) v[j] *= P.scale;
-    }
-    if (is_wgrad_row(P.op_kind)) {   // four consecutive filters of one (tap, channel)
-        const int64_t r = m >> 6, c = m & 63;
-        const int64_t coff = wgrow_col_offset(P.conv, P.ldc, static_cast<int>(n0 & ~int64_t(31)));
-        if (coff < 0) return;
-        const int64_t base = (g * P.conv.Kg) * P.ldc + r * P.conv.S * P.conv.Cg + c + coff +
-                             (n0 & 31) * P.ldc;
-        for (int j = 0; j < 4; ++j) {
-            if (P.c_dtype == SK_F32)
-                static_cast<float*>(P.c)[base + j * P.ldc] = v[j];
-            else if (P.c_dtype == SK_BF16)
-                static_cast<__nv_bfloat16*>(P.c)[base + j * P.ldc] = __float2bfloat16_rn(v[j]);
-            else
-                static_cast<__half*>(P.c)[base + j * P.ldc] = __float2half_rn(v[j]);
-        }
-        return;
-    }
-    const int64_t off = out_row * P.ldc + col;
-    const bool full = n0 + 4 <= plan.gemm_n;
-    if (P.c_dtype == SK_F32) {
-        float* dst = static_cast<float*>(P.c) + off;
-        if (full) *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-        else for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = v[j];
-    } else if (P.c_dtype == SK_BF16) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(P.c) + off;
-        if (full) {
-            __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
-            uint2 w;
-            w.x = *reinterpret_cast<uint32_t*>(&a);
-            w.y = *reinterpret_cast<uint32_t*>(&b);
-            *reinterpret_cast<uint2*>(dst) = w;
-        } else {
-            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2bfloat16_rn(v[j]);
-        }
-    } else {
-        __half* dst = static_cast<__half*>(P.c) + off;
-        if (full) {
-            __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
-            uint2 w;
-            w.x = *reinterpret_cast<uint32_t*>(&a);
-            w.y = *reinterpret_cast<uint32_t*>(&b);
-            *reinterpret_cast<uint2*>(dst) = w;
-        } else {
-            for (int j = 0; j < 4 && n0 + j < plan.gemm_n; ++j) dst[j] = __float2half_rn(v[j]);
-        }
-    }
+    const OutSpec o{P.c, P.ldc, P.c_dtype, P.op_kind, P.sa, P.sb, P.scale,
+                    P.sa != nullptr ? 1 : (P.tensor_scaled ? 2 : 0), &P.conv};
+    store4_out(plan, o, g, m, n0, v);
 }
 
 // ---------------------------------------------------------------------------------------------

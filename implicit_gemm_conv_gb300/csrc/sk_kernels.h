@@ -104,6 +104,10 @@ struct KernelParams {
     uint32_t idesc;
     int32_t c_dtype;
     int32_t c_tma;         // 1: a CTA's last complete tile is written with TMA stores (tmap_c)
+    // linear / tree: 1 = every contributor of a shared tile publishes its partial and adds a share
+    // of the tile (all publishing CTAs are resident at once); 0 = the owner (and each tree
+    // receiver) adds its senders' partials. The same sums either way.
+    int32_t spread;
     // kOpFp8Block: sa [M][nka] (A blocks of gka along K) and sb [ceil(N/gnb)][nkb] (B blocks of
     // gnb x gkb), either may be null; gka, gkb and gnb multiples of 128.
     const float* bsa;

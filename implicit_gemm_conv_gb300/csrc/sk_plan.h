@@ -74,6 +74,25 @@ SK_HD void tile_contributors(const sk_plan_t& p, int64_t t, int64_t& first, int6
     n = last - first + 1;
 }
 
+// Partial slot of contributor `index` of the shared tile of segment `s`: first + t + index for a
+// stream-K tile (the CTA at the boundary of two tiles has a slot in each), t*splits + index for
+// split-K (first = t*splits).
+SK_HD int64_t partial_slot(const sk_plan_t& p, int64_t tile, int64_t first, int64_t index) {
+    return first + index + (p.mode == SK_SPLITK ? 0 : tile);
+}
+
+// The value of CTA c's flag once it has handed on its partial of shared tile t: the number of
+// partials it has published by then. A stream-K CTA shares at most two tiles, the one its range
+// starts in (if it is shared) and the one its range ends in; the first is published first.
+SK_HD uint32_t publication(const sk_plan_t& p, int64_t c, int64_t t) {
+    if (p.mode == SK_SPLITK) return 1u;
+    const int64_t t0 = udiv31(sk_begin(p, c), p.iters_per_tile);
+    if (t == t0) return 1u;
+    int64_t first, n;
+    tile_contributors(p, t0, first, n);
+    return n > 1 ? 2u : 1u;
+}
+
 // Tree fixup, contributor `index` of `n`: in round r (stride s = 2^r) an index with
 // index mod 2s == s hands its sum to index - s and stops; one with index mod 2s == 0 and
 // index + s < n receives the sum of index + s. Calls f(sender_index) in round order.

@@ -106,15 +106,18 @@ typedef struct sk_plan_t {
     int64_t extra_iters;             /* the first extra_iters SK CTAs take one more iteration  */
     int64_t splits;                  /* SK_SPLITK only: K slices per tile                      */
     int64_t grid;                    /* CTAs launched                                           */
-    int64_t publishers;              /* CTAs owning a flag (and, linear/tree, a partial slot)  */
+    int64_t publishers;              /* CTAs owning a flag (it counts the partials they hand on) */
     int64_t max_contributors;        /* most CTAs sharing one tile                              */
     int64_t tree_rounds;             /* ceil(log2(max_contributors))                            */
     int64_t shared_tiles;            /* tiles with more than one contributor                   */
     int64_t flag_bytes;              /* round_up(4 * publishers * tm / 128, 256)                */
     int64_t control_offset;          /* = flag_bytes; 256-byte control block (ticket counter)  */
-    int64_t partial_offset, partial_bytes;   /* linear/tree: publishers * tm * tn * 4          */
+    int64_t partial_offset, partial_bytes;   /* linear/tree: partial_slots * tm * tn * 4       */
     int64_t scratch_offset, scratch_bytes;   /* workspace: (SK tiles) * tm * tn * 4            */
     int64_t ws_bytes;                /* total workspace bytes                                   */
+    int64_t partial_slots;           /* one per contributor of a shared tile: slot first+t+j for
+                                        contributor j of stream-K tile t (sk_ctas + sk_tiles in
+                                        all), t*splits+j for split-K                            */
 } sk_plan_t;
 
 /* One piece of a CTA's work: iterations [k_begin, k_end) of tile `tile`. */

@@ -26,6 +26,7 @@ FIELD_MAP = {  # C name -> oracle name
     "iters_per_sk_cta": "iters_per_sk_cta", "extra_iters": "extra", "grid": "grid",
     "publishers": "publishers", "max_contributors": "max_contrib", "tree_rounds": "rounds",
     "shared_tiles": "shared_tiles", "flag_bytes": "flag_bytes", "partial_bytes": "partial_bytes",
+    "partial_slots": "slots",
     "scratch_bytes": "scratch_bytes", "ws_bytes": "ws_bytes", "tiles_m": "tiles_m",
     "tiles_n": "tiles_n", "groups": "groups",
 }
