@@ -4,17 +4,22 @@
 
 Prints ONE JSON line (rank 0). The headline workload is the bf16 rcr GEMM 3840x4096x4096 on a
 148-SM pool, dp_sk mode, linear fixup, computed with the library's default tile for it: 240 tiles of
-256x256, each by a pair of CTAs on neighbouring SMs (the pool is 74 pairs). The same workload with
-the 128x128 tile (960 tiles, 148 CTAs) is reported under `extra`. A step is one sk_gemm_rcr call: the
-flag/control memset and the stream-K kernel (the linear fixup runs inside it). Inputs are resident
-in HBM; L2 is flushed (256 MB write) before every timed step and the flush is outside the timed
-events. `value` = algorithmic FLOP (2*M*N*K per step, all ranks) / summed step time.
+256x256, each by a pair of CTAs on neighbouring SMs (the pool is 74 pairs). A step is one
+sk_gemm_rcr call: the zeroing kernel (flags, ticket) and the stream-K kernel launched to overlap it
+(the linear fixup runs inside it). Inputs are resident in HBM; L2 is flushed (256 MB write) before
+every timed step and the flush is outside the timed events. `value` = algorithmic FLOP (2*M*N*K per
+step, all ranks) / summed step time of the K timed steps (their mean); the median and the
+10th/90th percentiles are reported beside it.
 
-Also reported: `roofline` (main kernel alone, timed with events the library records around it),
-`e2e` (same metric with pinned-host inputs copied in and the result copied out inside the timed
-region, every step; steps pipelined over copy-in / compute / copy-out streams), `cpu_baseline` (the CPU oracle on a bounded row sample of the same GEMM), `clocks`
-(nvidia-smi sampled during the timed region), and under `extra` the variants the comparison needs
-(DP-only, split-K, tree, persistent) and the other named workloads.
+Also reported: `roofline` (the main kernel alone, timed in a second pass with events the library
+records around it), `e2e` (same metric with pinned-host inputs copied in and the result copied out
+inside the timed region, every step; steps pipelined over copy-in / compute / copy-out streams),
+`cpu_baseline` (the CPU oracle on a bounded row sample of the same GEMM), `clocks` (nvidia-smi
+sampled during the timed region), and under `extra` every named workload: its stream-K variants
+next to the data-parallel-only and split-K plans of the same kernel, timed with the pages' A/B
+protocol (warm-up 50, 100 interleaved rounds, medians with 10th/90th percentiles, outliers beyond
+15% of the reference variant measured three times), each with its roofline fraction, plus the CPU
+oracle on a bounded sample of that workload.
 
 --impl reference times the CPU oracle (fp64, all host cores) as the reference arm on a bounded row
 sample per step of the same workload; under torchrun only rank 0 runs it.
@@ -151,15 +156,20 @@ def gemm_setup(torch, w, dev):
     return A, B
 
 
-def time_calls(torch, sk, call, steps, warmup, flush, stream):
+def time_calls(torch, sk, call, steps, warmup, flush, stream, kernel_timing=True):
     """Per step: flush L2 (untimed), then time one call with events on `stream`. Returns
-    (summed step ms, summed main-kernel ms, main launches, all launches)."""
+    (summed step ms, summed main-kernel ms, main launches, all launches, sorted step ms). With
+    kernel_timing the library records events around each main kernel, which then waits for the
+    zeroing kernel before it instead of overlapping it; the step times of such a pass are not the
+    library's own."""
     for _ in range(warmup):
         call()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    sk.sk_timing_enable(True)
+    sk.sk_timing_enable(True)   # counts the launches either way
+    if not kernel_timing:
+        sk.sk_timing_enable(False)
     with torch.cuda.stream(stream):
         for s, e in evs:
             flush.zero_()
@@ -167,10 +177,10 @@ def time_calls(torch, sk, call, steps, warmup, flush, stream):
             call()
             e.record(stream)
     torch.cuda.synchronize()
-    step_ms = sum(s.elapsed_time(e) for s, e in evs)
-    main_ms, n_main, n_all = sk.sk_timing_read()
+    ts = sorted(s.elapsed_time(e) for s, e in evs)
+    main_ms, n_main, n_all = sk.sk_timing_read() if kernel_timing else (0.0, 0, 0)
     sk.sk_timing_enable(False)
-    return step_ms, main_ms, n_main, n_all
+    return sum(ts), main_ms, n_main, n_all, ts
 
 
 def cpu_baseline_gemm(w, A, B, target_s=15.0):
@@ -193,96 +203,260 @@ def cpu_baseline_gemm(w, A, B, target_s=15.0):
                       f"({rows}/{w.M} of the work), fp64, {dt:.1f} s"}
 
 
-def extra_measurements(torch, sk, dev, flush, stream, steps):
-    """Variants of the headline and the other named workloads (fewer steps each). GEMM and fp8
-    workloads run with the 128x128 tile (their stated pool of CTAs) and with the 256x256 CTA-pair
-    tile (half as many pairs); keys are "tile:mode/reduction"."""
-    from workloads import WORKLOADS, fp8_operands, gemm_operands, wgrad_operands
+def peak_for(w, peaks):
+    """(dense tensor peak in TFLOP/s for the workload's input type, how it is obtained)."""
+    bf16 = peaks["bf16_tflops"]
+    if w.ab == "e4m3":
+        return 2.0 * bf16, (f"2 x the measured bf16 burst {bf16:.1f} TFLOP/s: the nominal dense "
+                            "fp8:bf16 ratio of GB300 (4.5 : 2.25 PFLOP/s); no fp8 peak is measured")
+    return bf16, "measured bf16 burst (cuBLAS 8192^3); fp16 has the bf16 dense rate"
+
+
+def roofline_of(w, peaks, t_us):
+    """The workload's roofline time (max of tensor and HBM time at the peaks) and the fraction of it
+    that a measured time t_us reaches."""
+    peak, src = peak_for(w, peaks)
+    t_tensor = w.flops() / (peak * 1e12) * 1e6
+    t_hbm = w.min_bytes() / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_roof = max(t_tensor, t_hbm)
+    return {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "roof_us": round(t_roof, 3),
+            "tensor_us": round(t_tensor, 3), "hbm_us": round(t_hbm, 3),
+            "frac": round(t_roof / t_us, 4) if t_us > 0 else None,
+            "peak_tflops": round(peak, 1), "peak_source": src, "hbm_gbs": peaks["hbm_gbs"],
+            "flop": w.flops(), "algorithmic_bytes": w.min_bytes()}
+
+
+def interleaved(torch, calls, flush, stream, warmup=50, repeat=100):
+    """The pages' A/B protocol: `warmup` rounds, then `repeat` rounds in which every variant runs
+    once in turn (L2 flushed before each step, outside its events). Per variant: median, 10th and
+    90th percentile of the step time (us)."""
+    names = list(calls)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for n in names:
+                calls[n]()
+    torch.cuda.synchronize()
+    evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(repeat)] for n in names}
+    with torch.cuda.stream(stream):
+        for r in range(repeat):
+            for n in names:
+                s, e = evs[n][r]
+                flush.zero_()
+                s.record(stream)
+                calls[n]()
+                e.record(stream)
+    torch.cuda.synchronize()
+    out = {}
+    for n in names:
+        ts = sorted(s.elapsed_time(e) * 1e3 for s, e in evs[n])
+        out[n] = {"med_us": statistics.median(ts), "p10_us": ts[len(ts) // 10],
+                  "p90_us": ts[(9 * len(ts)) // 10]}
+    return out
+
+
+def kernel_medians(torch, sk, calls, flush, stream, repeat=20):
+    """Median main-kernel time (us) of each variant: the library's events around the main kernel
+    (their presence makes the kernel wait for the zeroing kernel instead of overlapping it)."""
+    out = {}
+    for n, call in calls.items():
+        ts = []
+        for _ in range(repeat):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                sk.sk_timing_enable(True)
+                call()
+            ms, nm, _ = sk.sk_timing_read()
+            sk.sk_timing_enable(False)
+            if nm:
+                ts.append(ms / nm * 1e3)
+        out[n] = statistics.median(ts) if ts else None
+    return out
+
+
+def cpu_baseline_workload(w, host, target_s=3.0):
+    """The fp64 oracle as it stands, on the host's cores, timed on a bounded sample of the
+    workload (rows of a GEMM, filters of a wgrad, pixels of a convolution), scaled to its share of
+    the work."""
+    import numpy as np
+    from oracle import numerics
+    from workloads import conv_out
+    cores = numerics.threads()
+    bits = lambda t: t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+    def timed(f, lo, hi):
+        t0 = time.perf_counter()
+        f(lo, hi)
+        return time.perf_counter() - t0
+
+    if w.op == "gemm":
+        a, b = bits(host["A"]), bits(host["B"])
+        f = lambda lo, hi: numerics.gemm_rcr_rows(w.ab, a, b, lo, hi)
+        total, unit = w.M, "rows"
+    elif w.op == "fp8":
+        A8, B8 = host["A8"].view(__import__("torch").uint8).numpy(), host["B8"].view(__import__("torch").uint8).numpy()
+        sa, sb = host["sa"].numpy(), host["sb"].numpy()
+        f = lambda lo, hi: numerics.fp8_rowcol_rows(A8, B8, sa, sb, lo, hi)
+        total, unit = w.M, "rows"
+    elif w.op == "fp8_block":
+        A8, B8 = host["A8"].view(__import__("torch").uint8).numpy(), host["B8"].view(__import__("torch").uint8).numpy()
+        gka, gnb, gkb = w.blocks
+        sa, sb = host["sa"].numpy(), host["sb"].numpy()
+        f = lambda lo, hi: numerics.fp8_blockscale_rows(A8, B8, sa, gka, sb, gnb, gkb, lo, hi)
+        total, unit = w.M, "rows"
+    elif w.op == "wgrad":
+        c = w.conv
+        x, dy = bits(host["x"]), bits(host["dy"])
+        f = lambda lo, hi: numerics.wgrad_nhwc(w.ab, x, dy, c["R"], c["S"], c["stride"], c["pad"],
+                                               c["groups"], lo, hi)
+        total, unit = c["K"], "filters"
+    elif w.op == "fprop":
+        c = w.conv
+        x, wt = bits(host["x"]), bits(host["w"])
+        f = lambda lo, hi: numerics.fprop_nhwc(w.ab, x, wt, c["stride"], c["pad"], c["groups"], lo, hi)
+        total = c["N"] * conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0]) * \
+            conv_out(c["W"], c["S"], c["stride"][1], c["pad"][1])
+        unit = "output pixels"
+    else:   # dgrad
+        c = w.conv
+        dy, wt = bits(host["dy"]), bits(host["w"])
+        f = lambda lo, hi: numerics.dgrad_nhwc(w.ab, dy, wt, c["H"], c["W"], c["stride"], c["pad"],
+                                               c["groups"], lo, hi)
+        total, unit = c["N"] * c["H"] * c["W"], "input pixels"
+    probe = max(1, min(total, 2))
+    dt0 = timed(f, 0, probe)
+    n = int(max(1, min(total, round(probe * target_s / max(dt0, 1e-4)))))
+    dt = timed(f, 0, n)
+    frac = n / total
+    return {"value": w.flops() * frac / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": f"{n} of {total} {unit} ({frac:.3g} of the work), fp64, {dt:.2f} s"}
+
+
+def extra_measurements(torch, sk, dev, flush, stream, peaks, cpu=True):
+    """Every named workload: its stream-K variants next to the data-parallel-only (off) and split-K
+    plans of the same kernel, timed with the pages' A/B protocol (warm-up 50, then 100 interleaved
+    rounds; medians and 10th/90th percentiles; a variant whose median is more than 15% off the
+    workload's reference stream-K variant is measured twice more and reported as the median of
+    the three medians), each with its roofline fraction and main-kernel median, plus the CPU
+    oracle on a sample of the same workload. GEMM and fp8 workloads run with the 128x128 tile
+    they state (the pool they state) and with the 256x256 CTA-pair tile (half as many pairs);
+    keys are "tile:mode/reduction"."""
+    from workloads import (WORKLOADS, blockscale_scales, fp8_operands, gemm_operands,
+                           wgrad_operands)
     out = {}
     ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def rate(call, flops):
-        step_ms, main_ms, n_main, _ = time_calls(torch, sk, call, steps, 3, flush, stream)
-        return {"tflops": round(flops * steps / step_ms / 1e9, 1),
-                "us": round(step_ms / steps * 1e3, 1),
-                "main_us": round(main_ms / max(n_main, 1) * 1e3, 1)}
 
     def tiles(w):
         return [("128", w.pool), ("256x256_pair", w.pool // 2 if w.pool > 0 else -1)]
 
+    def tiled(tile, f):
+        def call():
+            with sk.tile(tile):
+                f()
+        return call
+
     for name, w in WORKLOADS.items():
-        res = {}
+        calls, host = {}, {}
+        sk_variants = [(m, r) for m in w.modes for r in w.reductions]
+        fp32_out = w.out == "f32"
+        comparators = [("off", "linear"), ("splitk", "workspace"),
+                       ("splitk", "atomic" if fp32_out else "linear")]
         if w.op == "gemm":
             A, B = gemm_operands(w.M, w.N, w.K, w.ab, w.dist)
+            host.update(A=A, B=B)
             A, B = A.to(dev), B.to(dev)
-            variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear"),
-                         ("persistent", "linear"), ("hybrid", "linear")]
+            C16 = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
+            C32 = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
             for tile, pool in tiles(w):
-                with sk.tile(tile):
-                    for mode, red in dict.fromkeys(variants):
-                        out_dt = torch.float32 if red == "atomic" else A.dtype
-                        C = torch.empty(w.M, w.N, dtype=out_dt, device=dev)
-                        res[f"{tile}:{mode}/{red}"] = rate(
-                            lambda: sk.sk_gemm_rcr(A, B, C, mode, red, pool, ws=ws), w.flops())
+                for mode, red in dict.fromkeys(sk_variants + comparators):
+                    Cx = C32 if red == "atomic" else C16
+                    calls[f"{tile}:{mode}/{red}"] = tiled(tile, lambda mode=mode, red=red, Cx=Cx, pool=pool:
+                                                          sk.sk_gemm_rcr(A, B, Cx, mode, red, pool, ws=ws))
         elif w.op in ("fprop", "dgrad"):
-            call, _ = conv_call(torch, sk, w, dev, ws)
-            variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "linear")]
-            for mode, red in variants:
-                res[f"128:{mode}/{red}"] = rate(lambda: call(mode, red, w.pool), w.flops())
+            call, _ = conv_call(torch, sk, w, dev, ws, host)
+            for mode, red in dict.fromkeys(sk_variants + comparators):
+                calls[f"128:{mode}/{red}"] = lambda mode=mode, red=red: call(mode, red, w.pool)
         elif w.op == "wgrad":
             c = w.conv
             x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
                                    c["stride"], c["pad"], w.ab, w.dist)
+            host.update(x=x, dy=dy)
             x, dy = x.to(dev), dy.to(dev)
             dw = torch.empty(c["K"], c["R"], c["S"], c["C"] // c["groups"], dtype=torch.float32,
                              device=dev)
-            variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("off", "linear"), ("splitk", "workspace"), ("splitk", "atomic")]
-            for mode, red in variants:
-                res[f"128:{mode}/{red}"] = rate(
-                    lambda: sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"],
-                                                    c["pad"], c["groups"], mode, red, w.pool,
-                                                    ws=ws), w.flops())
-        elif w.op == "fp8_block":   # one tile shape (128 x 128)
-            call = blockscale_call(torch, sk, w, dev, ws)
-            variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace"),
-                         ("hybrid", "linear")]
-            for mode, red in dict.fromkeys(variants):
-                res[f"128:{mode}/{red}"] = rate(lambda: call(mode, red, w.pool), w.flops())
+            for tile in ("auto", "128"):
+                for mode, red in dict.fromkeys(sk_variants + comparators):
+                    calls[f"{tile}:{mode}/{red}"] = tiled(tile, lambda mode=mode, red=red:
+                        sk.sk_conv2d_wgrad_nhwc(x, dy, dw, c["R"], c["S"], c["stride"], c["pad"],
+                                                c["groups"], mode, red, w.pool, ws=ws))
+        elif w.op == "fp8_block":
+            call = blockscale_call(torch, sk, w, dev, ws, host)
+            for mode, red in dict.fromkeys(sk_variants + comparators + [("persistent", "linear")]):
+                calls[f"128:{mode}/{red}"] = lambda mode=mode, red=red: call(mode, red, w.pool)
         else:
             A8, B8, sa, sb = fp8_operands(w.M, w.N, w.K)
+            host.update(A8=A8, B8=B8, sa=sa, sb=sb)
             A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
             C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
-            variants = [(m, r) for m in w.modes for r in w.reductions]
-            variants += [("persistent", "linear"), ("off", "linear"), ("splitk", "workspace"),
-                         ("hybrid", "linear")]
             for tile, pool in tiles(w):
-                with sk.tile(tile):
-                    for mode, red in variants:
-                        res[f"{tile}:{mode}/{red}"] = rate(
-                            lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, pool,
-                                                          ws=ws), w.flops())
+                for mode, red in dict.fromkeys(sk_variants + comparators + [("persistent", "linear")]):
+                    calls[f"{tile}:{mode}/{red}"] = tiled(tile, lambda mode=mode, red=red, pool=pool:
+                        sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, pool, ws=ws))
+        first_tile = next(iter(calls)).split(":")[0]
+        ref = f"{first_tile}:{sk_variants[0][0]}/{sk_variants[0][1]}"
+        stats = interleaved(torch, calls, flush, stream)
+        for n in calls:   # the pages' outlier rule against the reference variant
+            if n != ref and abs(stats[n]["med_us"] / stats[ref]["med_us"] - 1.0) > 0.15:
+                meds = [stats[n]["med_us"]]
+                for _ in range(2):
+                    meds.append(interleaved(torch, {ref: calls[ref], n: calls[n]}, flush, stream,
+                                            warmup=10)[n]["med_us"])
+                stats[n]["remeasured_us"] = [round(m, 2) for m in meds]
+                stats[n]["med_us"] = statistics.median(meds)
+        kern = kernel_medians(torch, sk, calls, flush, stream)
+        res = {"reference_variant": ref, "variants": {}}
+        for n, st in stats.items():
+            entry = {"step_med_us": round(st["med_us"], 2), "p10_us": round(st["p10_us"], 2),
+                     "p90_us": round(st["p90_us"], 2),
+                     "tflops": round(w.flops() / st["med_us"] / 1e6, 1),
+                     "frac_step": roofline_of(w, peaks, st["med_us"])["frac"]}
+            if kern.get(n):
+                entry["kernel_med_us"] = round(kern[n], 2)
+                entry["frac_kernel"] = roofline_of(w, peaks, kern[n])["frac"]
+            if "remeasured_us" in st:
+                entry["remeasured_us"] = st["remeasured_us"]
+            res["variants"][n] = entry
+        v = res["variants"]
+        pick = lambda pred: min((k for k in v if pred(k)), key=lambda k: v[k]["step_med_us"],
+                                default=None)
+        best = {"stream_k": pick(lambda k: k.split(":")[1].split("/")[0] not in ("off", "splitk")),
+                "dp_only": pick(lambda k: ":off/" in k), "split_k": pick(lambda k: ":splitk/" in k)}
+        res["best"] = {kind: ({"variant": k, **v[k]} if k else None) for kind, k in best.items()}
+        res["roofline"] = roofline_of(w, peaks, v[best["stream_k"]]["step_med_us"])
+        if cpu:
+            res["cpu_baseline"] = cpu_baseline_workload(w, host)
         out[name] = res
     return out
 
 
-def blockscale_call(torch, sk, w, dev, ws):
-    """A launcher for a block-scaled fp8 workload: call(mode, red, pool)."""
+def blockscale_call(torch, sk, w, dev, ws, host=None):
+    """A launcher for a block-scaled fp8 workload: call(mode, red, pool). `host` receives the CPU
+    operands."""
     from workloads import blockscale_scales, fp8_operands
     gka, gnb, gkb = w.blocks
     A8, B8, _, _ = fp8_operands(w.M, w.N, w.K)
     sa, sb = blockscale_scales(w.M, w.N, w.K, gka, gnb, gkb)
+    if host is not None:
+        host.update(A8=A8, B8=B8, sa=sa, sb=sb)
     A8, B8, sa, sb = A8.to(dev), B8.to(dev), sa.to(dev), sb.to(dev)
     C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
     return lambda mode, red, pool: sk.sk_gemm_blockscale_fp8(A8, B8, sa, gka, sb, gnb, gkb, C, mode,
                                                              red, pool, ws=ws)
 
 
-def conv_call(torch, sk, w, dev, ws):
-    """A launcher for a forward-convolution or data-gradient workload: call(mode, red, pool)."""
+def conv_call(torch, sk, w, dev, ws, host=None):
+    """A launcher for a forward-convolution or data-gradient workload: call(mode, red, pool).
+    `host` receives the CPU operands."""
     from workloads import TORCH_DTYPE, conv_out, dgrad_operands, fprop_operands
     c = w.conv
     Ho = conv_out(c["H"], c["R"], c["stride"][0], c["pad"][0])
@@ -290,12 +464,16 @@ def conv_call(torch, sk, w, dev, ws):
     if w.op == "fprop":
         x, f = fprop_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["groups"],
                               w.ab, w.dist)
+        if host is not None:
+            host.update(x=x, w=f)
         x, f = x.to(dev), f.to(dev)
         y = torch.empty(c["N"], Ho, Wo, c["K"], dtype=TORCH_DTYPE[w.out], device=dev)
         return (lambda mode, red, pool: sk.sk_conv2d_fprop_nhwc(
             x, f, y, c["stride"], c["pad"], c["groups"], mode, red, pool, ws=ws)), y
     dy, f = dgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"], c["stride"],
                            c["pad"], c["groups"], w.ab, w.dist)
+    if host is not None:
+        host.update(dy=dy, w=f)
     dy, f = dy.to(dev), f.to(dev)
     dx = torch.empty(c["N"], c["H"], c["W"], c["C"], dtype=TORCH_DTYPE[w.out], device=dev)
     return (lambda mode, red, pool: sk.sk_conv2d_dgrad_nhwc(
@@ -339,8 +517,8 @@ def run_variant(args, dev):
         C = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
         call = lambda: sk.sk_gemm_rowcol_fp8(A8, B8, sa, sb, C, mode, red, pool, ws=ws)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    step_ms, main_ms, n_main, n_all = time_calls(torch, sk, call, args.steps, args.warmup, flush,
-                                                 torch.cuda.current_stream())
+    step_ms, main_ms, n_main, n_all, _ = time_calls(torch, sk, call, args.steps, args.warmup,
+                                                    flush, torch.cuda.current_stream())
     sk.sk_device_status()
     return {"variant": args.variant, "pool": pool, "steps": args.steps, "step_us": step_ms / args.steps * 1e3,
             "main_us": main_ms / max(n_main, 1) * 1e3, "tflops": w.flops() * args.steps / step_ms / 1e9,
@@ -366,7 +544,7 @@ def run_ours(args, rank, world, dev):
     stream = torch.cuda.current_stream()
     call = lambda: sk.sk_gemm_rcr(Ad, Bd, C, mode, red, pool, ws=ws)
 
-    # ---- the timed region ----
+    # ---- the timed region: the library as a caller runs it (no events of its own) ----
     for _ in range(args.warmup):
         call()
     barrier(world)
@@ -374,12 +552,17 @@ def run_ours(args, rank, world, dev):
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        step_ms, main_ms, n_main, n_all = time_calls(torch, sk, call, args.steps, 0, flush, stream)
+        step_ms, _, _, _, step_sorted = time_calls(torch, sk, call, args.steps, 0, flush, stream,
+                                                   kernel_timing=False)
         torch.cuda.synchronize()
         barrier(world)
     sk.sk_device_status()
     step_ms = max_over_ranks(torch, world, step_ms, dev)
+    # ---- the main kernel alone (library events around it), for the roofline ----
+    kern_steps = max(20, min(args.steps, 400))
+    _, main_ms, n_main, n_all, _ = time_calls(torch, sk, call, kern_steps, 3, flush, stream)
     main_ms = max_over_ranks(torch, world, main_ms, dev)
+    n_all = n_all * args.steps // kern_steps   # launches per timed step, scaled to the timed steps
     flops_step = w.flops()
     value = whole_job_tflops(flops_step, args.steps, world, step_ms)
     main_avg_s = main_ms / max(n_main, 1) / 1e3
@@ -454,6 +637,10 @@ def run_ours(args, rank, world, dev):
                    "inputs": "bf16 N(0,1), seeds A=1 B=2", "out": "bf16",
                    "l2": "flushed (256 MB write) before every timed step, outside the events",
                    "parallelism": f"replicas x{world} (independent problems)"},
+        "ms_per_step_median": round(statistics.median(step_sorted), 5),
+        "ms_per_step_p10_p90": [round(step_sorted[len(step_sorted) // 10], 5),
+                                round(step_sorted[(9 * len(step_sorted)) // 10], 5)],
+        "main_kernel_ms": round(main_avg_s * 1e3, 5),
         "pct_of_peak": round(100.0 * value / world / peak, 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -469,7 +656,8 @@ def run_ours(args, rank, world, dev):
         line["cpu_baseline"] = cpu_baseline_gemm(w, A, B)
     sk.sk_set_tile("auto")
     if rank == 0 and not args.no_extra:
-        line["extra"] = extra_measurements(torch, sk, dev, flush, stream, args.extra_steps)
+        line["extra"] = extra_measurements(torch, sk, dev, flush, stream, peaks,
+                                           cpu=not args.no_cpu_baseline)
     return line
 
 
@@ -543,7 +731,6 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--extra-steps", type=int, default=50)
     ap.add_argument("--reference-rows", type=int, default=4)
     ap.add_argument("--variant", default=None,
                     help="WORKLOAD:MODE/REDUCTION - time only this variant (for profiling)")
