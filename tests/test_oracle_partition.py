@@ -321,3 +321,70 @@ def test_spread_fold_progress():
     assert one.sk_ctas == 148
     assert not P.simulate_progress(one, 147, P.LINEAR, fold="spread")
     assert P.simulate_progress(one, 2, P.LINEAR, fold="owner")
+
+
+# --- forward progress at the scale the pages checked it ---------------------------------------
+
+FULL_PLANS = [   # (name, make_plan keywords) of the named workloads' whole partitions
+    ("gemm 3840x4096x4096 128x128 P=148",
+     dict(tiles_m=30, tiles_n=32, groups=1, kred=4096, tm=128, tn=128, tk=64, pool=148)),
+    ("gemm 3840x4096x4096 256x256 pairs P=74",
+     dict(tiles_m=15, tiles_n=16, groups=1, kred=4096, tm=256, tn=256, tk=64, pool=74, cluster=2)),
+    ("gemm 3840x4096x4096 128x128 P=152",
+     dict(tiles_m=30, tiles_n=32, groups=1, kred=4096, tm=128, tn=128, tk=64, pool=152)),
+    ("gemm 512x512x65536 P=148",
+     dict(tiles_m=4, tiles_n=4, groups=1, kred=65536, tm=128, tn=128, tk=64, pool=148)),
+    ("gemm 512x512x65536 P=152",
+     dict(tiles_m=4, tiles_n=4, groups=1, kred=65536, tm=128, tn=128, tk=64, pool=152)),
+    ("fp8 8192^3 256x256 pairs P=76",
+     dict(tiles_m=32, tiles_n=32, groups=1, kred=8192, tm=256, tn=256, tk=128, pool=76, cluster=2)),
+    ("wgrad 32x56x56x64 rows P=148",
+     dict(tiles_m=2, tiles_n=1, groups=1, kred=32 * 56 * 64, tm=128, tn=192, tk=64, pool=148)),
+    ("wgrad 32x56x56x64 rows P=152",
+     dict(tiles_m=2, tiles_n=1, groups=1, kred=32 * 56 * 64, tm=128, tn=192, tk=64, pool=152)),
+    ("wgrad 64x28x28x256 g4 s2 rows P=148",
+     dict(tiles_m=2, tiles_n=1, groups=4, kred=64 * 16 * 16, tm=128, tn=192, tk=64, pool=148)),
+    ("wgrad 32x56x56x64 128x128 P=152",
+     dict(tiles_m=1, tiles_n=5, groups=1, kred=32 * 56 * 56, tm=128, tn=128, tk=64, pool=152)),
+]
+
+
+def _need(p, red):
+    # resident slots the owner fold needs: a blocked linear owner waits on one later CTA; a tree
+    # blocks at most `rounds` CTAs at a time
+    return 2 if red == P.LINEAR else p.rounds + 1
+
+
+def test_forward_progress_5280_partitions():
+    """The review thread on forward progress simulated the hand-off on 5280 partitions: here
+    24 tile counts x 11 reduction lengths x 20 pool sizes = 5280 stream-K partitions, each run
+    under both deterministic reductions with only the resident slots the owner fold needs, and
+    under the spread fold with exactly its publishers resident."""
+    Ts = list(range(1, 25))
+    Is = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144]
+    Pools = [2, 3, 4, 5, 6, 7, 8, 12, 16, 24, 32, 37, 48, 64, 74, 96, 128, 148, 152, 304]
+    n = 0
+    for T in Ts:
+        for I in Is:
+            for Pool in Pools:
+                n += 1
+                for red in (P.LINEAR, P.TREE):
+                    p = plan(T, I, Pool, P.DP_SK, red)
+                    assert P.simulate_progress(p, _need(p, red), red), (T, I, Pool, red)
+                    if red == P.LINEAR:
+                        assert P.simulate_progress(p, max(1, p.sk_ctas), red, fold="spread"), \
+                            (T, I, Pool)
+    assert n == 5280
+
+
+@pytest.mark.parametrize("name,kw", FULL_PLANS, ids=[f[0] for f in FULL_PLANS])
+def test_forward_progress_named_full_plans(name, kw):
+    """The named workloads' whole partitions, every mode, with the fewest resident slots each
+    fold needs (owner: one or `rounds` more than the blocked CTAs; spread: every publisher)."""
+    for mode in (P.DP_SK, P.PERSISTENT, P.SPLITK, P.HYBRID):
+        for red in (P.LINEAR, P.TREE):
+            p = P.make_plan(mode=mode, reduction=red, **kw)
+            P.check_invariants(p)
+            assert P.simulate_progress(p, _need(p, red), red), (name, mode, red)
+            publishing = p.grid if mode == P.SPLITK else p.sk_ctas
+            assert P.simulate_progress(p, max(1, publishing), red, fold="spread"), (name, mode, red)
