@@ -573,13 +573,23 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
     // the owner fold of the pages, whose waits target only later CTAs. Measured on GB300: with
     // 4-5 contributors per tile (the 3840x4096x4096 GEMM on 74 CTA pairs) the owner fold is faster,
     // with 19-74 (the wgrad workloads) the spread fold by 1.4-3x.
+    // The spread fold's arrival counters (one per shared-tile candidate and CTA of a pair) fill the
+    // control block's words after the ticket.
+    const int64_t resident = static_cast<int64_t>(dev.sms / tc.cg) * (per_sm > 0 ? per_sm : 1);
+    const int64_t candidates = plan.mode == SK_SPLITK ? (plan.splits > 1 ? plan.tiles : 0)
+                                                      : plan.sk_tiles;
     kp.spread = 0;
     if ((plan.reduction == SK_LINEAR || plan.reduction == SK_TREE) && plan.shared_tiles > 0) {
-        const int64_t resident = static_cast<int64_t>(dev.sms / tc.cg) * (per_sm > 0 ? per_sm : 1);
         kp.spread = plan.max_contributors >= kSpreadMinContributors &&
                     plan.publishers <= resident &&
+                    candidates * tc.cg <= sk::kControlBytes / 4 - 1 &&
                     (plan.reduction == SK_LINEAR || plan.max_contributors < 256);
     }
+    // A ticket orders the logical ids by start time where a CTA may wait on a later one that is
+    // not yet resident; with no waits (atomic, workspace, data-parallel) or the whole grid
+    // resident at once, the block index serves.
+    kp.ticket = (plan.reduction == SK_LINEAR || plan.reduction == SK_TREE) &&
+                plan.shared_tiles > 0 && plan.grid > resident;
 
     rc = SK_OK;
     do {

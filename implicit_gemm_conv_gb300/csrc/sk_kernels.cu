@@ -812,10 +812,12 @@ __device__ __forceinline__ float* frag_ptr(float* tile_base, int col0, int i, in
 // chunks are read per TMEM round trip (two loads, one wait): the epilogue is bound by these round
 // trips, not by the arithmetic between them.
 template <int kChunks, typename F>
-__device__ __forceinline__ void for_each_chunk(uint32_t t_acc, F&& f) {
+__device__ __forceinline__ void for_each_chunk(uint32_t t_acc, F&& f, int first_pair = 0) {
     static_assert(kChunks % 2 == 0, "chunks are read in pairs");
+    constexpr int kPairs = kChunks / 2;
 #pragma unroll 1
-    for (int ch = 0; ch < kChunks; ch += 2) {
+    for (int i = 0; i < kPairs; ++i) {
+        const int ch = 2 * (first_pair + i < kPairs ? first_pair + i : first_pair + i - kPairs);
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(t_acc + ch * 32, r0);
         tmem_ld_32x32b_x32(t_acc + (ch + 1) * 32, r1);
@@ -981,6 +983,10 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
                                 [&](int ch, float (&v)[32]) { store_out<OP>(P, e, ch * 32, v); });
         return;
     }
+    // The contributors of a tile add into the same words at about the same time; each starts at
+    // its own pair of 32-column chunks (by CTA id), so that at any moment they spread over the
+    // tile's columns instead of queueing on the same L2 lines.
+    const int first_pair = static_cast<int>(cta % (kChunks / 2));
     if (red == SK_ATOMIC) {
         // tcgen05.ld is warp-collective (.sync.aligned): every lane loads, and only the lanes of
         // rows inside the output add.
@@ -992,7 +998,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
                 float* dst = static_cast<float*>(P.c) + e.out_row + off;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) red_add_f32(dst + i * P.ldc, v[i]);
-            });
+            }, first_pair);
             return;
         }
         for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
@@ -1008,7 +1014,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
                         if (n0 + i + j < e.n_end) red_add_f32(dst + i + j, v[i + j]);
                 }
             }
-        });
+        }, first_pair);
         return;
     }
     if (red == SK_WORKSPACE) {
@@ -1018,7 +1024,7 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
             for (int i = 0; i < 32; i += 4)
                 red_add_v4(frag_ptr<TN>(base, ch * 32, i, e.row), v[i], v[i + 1], v[i + 2],
                            v[i + 3]);
-        });
+        }, first_pair);
         return;
     }
 
@@ -1040,11 +1046,14 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
                 __stcg(reinterpret_cast<float4*>(frag_ptr<TN>(own, ch * 32, i, e.row)),
                        make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         });
-        // The barrier orders every epilogue thread's stores before the release below, which makes
-        // them visible (cumulatively) to a CTA that acquires the flag.
+        // The barrier orders every epilogue thread's stores before the releases below, which make
+        // them visible (cumulatively) to a CTA that acquires the flag or the tile's arrival
+        // counter (control block word 1 + tile * CG + half), which the folders poll.
         named_bar_sync(kEpiBarrier, kEpiThreads);
-        if (ethread == 0)
+        if (ethread == 0) {
             st_release_gpu(P.flags + cta * CG + e.half, publication(plan, cta, seg.tile));
+            red_release_gpu_add(P.control + 1 + seg.tile * CG + e.half, 1u);
+        }
         return;
     }
 
@@ -1161,15 +1170,21 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
         me = pd.index;
     }
     if (me < 0) return;   // this CTA's part of the tile is its partial only
-    const int64_t miss = wait_flags_all(P.flags, CG, half, n, ethread, P.flag_timeout_ns,
-                                        [&](int64_t k, int64_t& c2, uint32_t& need) {
-                                            c2 = pd.first + k;
-                                            need = publication(plan, c2, pd.tile);
-                                        });
-    if (miss != -1) {
-        if (ethread == 0) record_error(kErrFlagWait, cta, pd.tile, miss);
+    // One thread polls the tile's arrival counter until all n contributors have counted their
+    // partials (bounded); one word per tile keeps the polling off the flag table, which every
+    // folder of a tile would otherwise read whole on each round. The verdict goes to all epilogue
+    // threads through a barrier reduction, and each fences before its reads of the partials.
+    bool arrived = true;
+    if (ethread == 0) {
+        uint64_t t0 = 0;
+        arrived = wait_flag(P.control + 1 + pd.tile * CG + half, static_cast<uint32_t>(n), t0,
+                            P.flag_timeout_ns);
+    }
+    if (!named_bar_and(kEpiBarrierWait, kEpiThreadsWait, arrived)) {
+        if (ethread == 0) record_error(kErrFlagWait, cta, pd.tile, -3);
         return;
     }
+    __threadfence();
     int64_t g, mt, nt;
     tile_coords(plan, pd.tile, g, mt, nt);
     const OutSpec o{P.c, P.ldc, P.c_dtype, OP, P.sa, P.sb, P.scale,
@@ -1422,6 +1437,9 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     seg_init(plan, cta, cur);
     sk_segment_t seg;
     int64_t nseg = 0, tau = 0, nblk = 0;
+    // Without a ticket the zeroing kernel may still be running: the epilogue's first write (output,
+    // scratch, partials, flags or counters) comes after its writes.
+    if (!P.ticket) grid_dependency_wait();
     // Spread fold: the shared tiles of this CTA (at most two), folded once all its segments are out.
     const bool spread = P.spread && (plan.reduction == SK_LINEAR || plan.reduction == SK_TREE);
     PendingFold pend[2];
@@ -1578,23 +1596,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         }
         fence_proxy_async_smem();
     }
-    // The launch may overlap the tail of the kernel that zeroes the flags, the ticket counter and
-    // the scratch (a programmatic dependent launch): everything above touches only this CTA's
-    // shared memory, its TMEM and the tensor maps. Every thread waits for that kernel's writes
-    // before anything here can touch one of those words; a launch without that dependency passes
-    // straight through.
-    grid_dependency_wait();
-    if (threadIdx.x == 0 && rank == 0) {
-        // A pair takes one ticket, in its even CTA, and hands it to both (the barrier below
-        // publishes the stores).
-        ticket = atomicAdd(P.control, 1u);
-        if constexpr (CG == 2) {
-            const uint32_t cta_off = ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, cta));
-            st_shared_cluster_u64(mapa_shared(cta_off, 0), ticket);
-            st_shared_cluster_u64(mapa_shared(cta_off, 1), ticket);
-        } else {
-            ctl->cta = static_cast<long long>(ticket);
+    // The launch may overlap the tail of the kernel that zeroes the flags, the control block (the
+    // ticket and arrival counters), the scratch and, for the atomic reduction, the output (a
+    // programmatic dependent launch): everything above touches only this CTA's shared memory, its
+    // TMEM and the tensor maps. A launch without that dependency passes straight through the waits.
+    if (P.ticket) {
+        // Logical ids in start order: every thread waits for the zeroed counter first. A pair
+        // takes one ticket, in its even CTA, and hands it to both (the barrier below publishes
+        // the stores).
+        grid_dependency_wait();
+        if (threadIdx.x == 0 && rank == 0) {
+            ticket = atomicAdd(P.control, 1u);
+            if constexpr (CG == 2) {
+                const uint32_t cta_off = ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, cta));
+                st_shared_cluster_u64(mapa_shared(cta_off, 0), ticket);
+                st_shared_cluster_u64(mapa_shared(cta_off, 1), ticket);
+            } else {
+                ctl->cta = static_cast<long long>(ticket);
+            }
         }
+    } else if (threadIdx.x == 0) {
+        // No CTA waits on one that may not have started (no waits at all, or every CTA of the
+        // grid resident at once): the block index, one per CTA pair (clusters of two consecutive
+        // blocks). Only the epilogue writes zeroed words; its threads wait for them there.
+        ctl->cta = static_cast<long long>(CG == 2 ? (blockIdx.x >> 1) : blockIdx.x);
     }
     tc_fence_before();
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();

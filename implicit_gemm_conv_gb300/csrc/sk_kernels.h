@@ -104,10 +104,17 @@ struct KernelParams {
     uint32_t idesc;
     int32_t c_dtype;
     int32_t c_tma;         // 1: a CTA's last complete tile is written with TMA stores (tmap_c)
-    // linear / tree: 1 = every contributor of a shared tile publishes its partial and adds a share
-    // of the tile (all publishing CTAs are resident at once); 0 = the owner (and each tree
-    // receiver) adds its senders' partials. The same sums either way.
+    // linear / tree: 1 = every contributor of a shared tile publishes its partial, counts it in the
+    // tile's arrival counter (control block word 1 + tile * CG + half) and adds a share of the tile
+    // once the counter has reached the tile's contributors (all publishing CTAs are resident at
+    // once); 0 = the owner (and each tree receiver) adds its senders' partials. The same sums
+    // either way.
     int32_t spread;
+    // 1: logical CTA ids come from a ticket counter in the control block, taken in start order
+    // (linear/tree with more CTAs than can be resident at once, where a CTA may wait on a later
+    // one); 0: the block (cluster) index, and the wait for the zeroing kernel's writes moves from
+    // the prologue to the first access of the zeroed words.
+    int32_t ticket;
     // kOpFp8Block: sa [M][nka] (A blocks of gka along K) and sb [ceil(N/gnb)][nkb] (B blocks of
     // gnb x gkb), either may be null; gka, gkb and gnb multiples of 128.
     const float* bsa;

@@ -111,7 +111,8 @@ typedef struct sk_plan_t {
     int64_t tree_rounds;             /* ceil(log2(max_contributors))                            */
     int64_t shared_tiles;            /* tiles with more than one contributor                   */
     int64_t flag_bytes;              /* round_up(4 * publishers * tm / 128, 256)                */
-    int64_t control_offset;          /* = flag_bytes; 256-byte control block (ticket counter)  */
+    int64_t control_offset;          /* = flag_bytes; 256-byte control block: ticket and       */
+                                     /* spread-fold arrival counters                          */
     int64_t partial_offset, partial_bytes;   /* linear/tree: partial_slots * tm * tn * 4       */
     int64_t scratch_offset, scratch_bytes;   /* workspace: (SK tiles) * tm * tn * 4            */
     int64_t ws_bytes;                /* total workspace bytes                                   */
