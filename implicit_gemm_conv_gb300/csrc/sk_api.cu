@@ -278,8 +278,15 @@ struct TileCfg {
 };
 int tile_cfg(const View& v, TileCfg& t) {
     if (sk::is_wgrad_row(v.op_kind)) {
-        // 128 x 192 tile on one CTA: 8 stages of 25 KB (one x column phase) or 5 of 41 KB (two).
-        t = v.op_kind == sk::kOpWgradRow1 ? TileCfg{1, 192, 8} : TileCfg{1, 192, 5};
+        // Three or four tap rows (M = 192 or 256): a 256 x 192 tile on a CTA pair, each CTA
+        // holding two tap rows and half the filters, so that every tensor core reads only half of
+        // B from its shared memory (10 stages of 21 KB, or 6 of 37 KB with two x column phases).
+        // Otherwise a 128 x 192 tile on one CTA: 8 stages of 25 KB or 5 of 41 KB.
+        const bool pair = v.gemm_m == 3 * 64 || v.gemm_m == 4 * 64;
+        if (v.op_kind == sk::kOpWgradRow1)
+            t = pair ? TileCfg{2, 192, 10} : TileCfg{1, 192, 8};
+        else
+            t = pair ? TileCfg{2, 192, 6} : TileCfg{1, 192, 5};
         return SK_OK;
     }
     if (v.op_kind == sk::kOpFp8Block) {
@@ -1063,15 +1070,22 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
         }
+        TileCfg tc;
+        rc = tile_cfg(view, tc);
+        if (rc) return rc;
         {
+            // A CTA pair splits the filters: each CTA reads rows of 32 (64 bytes, 64-byte swizzle).
             const cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)N};
             const cuuint64_t strides[3] = {(cuuint64_t)(K * 2), (cuuint64_t)(Wo * K * 2),
                                            (cuuint64_t)(Ho * Wo * K * 2)};
-            const cuuint32_t box[4] = {64, (cuuint32_t)rg.wseg, (cuuint32_t)rg.rows_per_step, 1};
+            const cuuint32_t box[4] = {(cuuint32_t)(64 / tc.cg), (cuuint32_t)rg.wseg,
+                                       (cuuint32_t)rg.rows_per_step, 1};
             const cuuint32_t estr[4] = {1, 1, 1, 1};
             CUresult r = g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                                         const_cast<void*>(dy), dims, strides, box, estr,
-                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                        tc.cg == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_128B,
                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(dy) failed (%d)", (int)r);
@@ -1079,9 +1093,11 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
         kp.c = dw;
         kp.ldc = RSC;
         kp.c_dtype = dw_dtype;
-        // M = 128 (two tap rows x 64 channels), both operands MN-major; the kernel sets N per
-        // column phase.
-        kp.idesc = sk::make_idesc(fmt, fmt, true, true, 128, static_cast<uint32_t>(64 * rg.nq[0]));
+        // M = 128 per CTA (two tap rows x 64 channels; 256 for a pair), both operands MN-major; the
+        // kernel sets N per column phase.
+        kp.idesc = sk::make_idesc(fmt, fmt, true, true, static_cast<uint32_t>(128 * tc.cg),
+                                  static_cast<uint32_t>(64 * rg.nq[0]));
+        kp.conv.fsplit = tc.cg;
         kp.conv.sh = stride_h;
         kp.conv.sw = stride_w;
         kp.conv.ph = pad_h;

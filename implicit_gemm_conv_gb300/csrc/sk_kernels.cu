@@ -126,8 +126,9 @@ constexpr uint32_t kEpiBarrier = 1;
 
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
-    static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8 || OP == kOpFp8Block,
-                  "CTA pairs serve the GEMMs only");
+    static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8 || OP == kOpFp8Block ||
+                      is_wgrad_row(OP),
+                  "CTA pairs serve the GEMMs and the shifted-row wgrad");
     static_assert(CG == 2 || TN == 128 || (is_wgrad_row(OP) && TN == 192),
                   "one CTA computes 128 x 128 tiles (shifted-row wgrad: 128 x 192)");
     static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
@@ -137,11 +138,14 @@ struct Cfg {
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
     static constexpr int kTileMAll = kTileM * CG;          // tile rows of the CTA (pair)
     static constexpr int kBRows = TN / CG;                 // B rows this CTA stages
-    // Shifted-row wgrad stage: per phase an x row of the tile's upper and of its lower tap row
-    // (64 positions x 64 channels, 8 KB each), then the dy rows (64 positions x 64 filters) with
-    // room for the shifts' overrun (at most 7 rows past the 64, kept zero), 9 KB.
+    // Shifted-row wgrad stage: per phase an x row of the CTA's upper and of its lower tap row
+    // (64 positions x 64 channels, 8 KB each), then the dy rows (64 positions x the CTA's filters:
+    // 64, or 32 in each CTA of a pair) with room for the shifts' overrun (at most 7 rows past the
+    // 64, kept zero): 72 rows of 128 bytes (9 KB), or 80 of 64 bytes for a pair (5 KB, so that
+    // every stage starts 1024-byte aligned).
     static constexpr int kXRowBytes = 64 * 128;
-    static constexpr int kDyBytes = 9 * 1024;
+    static constexpr int kDyRowBytes = 128 / CG;
+    static constexpr int kDyBytes = CG == 1 ? 9 * 1024 : 5 * 1024;
     static constexpr int kABytes = kWgRow ? kPhases * 2 * kXRowBytes : kTileM * 128;   // 16 KB
     static constexpr int kBBytes = kWgRow ? kDyBytes : kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -293,17 +297,25 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
         const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
         const uint32_t n_img = rr0 / hp;   // < 2^31 (checked on the host)
         const int32_t ho0 = static_cast<int32_t>(rr0 - n_img * hp);
-        tma_load_4d(b_dst, &P.tmap_b, bar, static_cast<int32_t>(g) * cg.Kg, -cg.qmax, ho0,
-                    static_cast<int32_t>(n_img));
-        const int32_t r0 = 2 * static_cast<int32_t>(mt);
+        // A CTA pair splits the filters: this CTA's 32 of them. Its tap rows are the pair tile's
+        // 128-row half of (tap row, channel): rows 2 * (mt * CG + rank) and the next.
+        auto load4 = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
+            if constexpr (CG == 2)
+                tma_load_4d_pair(dst, m, bar, x, y, z, static_cast<int32_t>(n_img));
+            else
+                tma_load_4d(dst, m, bar, x, y, z, static_cast<int32_t>(n_img));
+        };
+        load4(b_dst, &P.tmap_b,
+              static_cast<int32_t>(g) * cg.Kg + static_cast<int32_t>(rank) * (64 / CG), -cg.qmax,
+              ho0);
+        const int32_t r0 = 2 * (static_cast<int32_t>(mt) * CG + static_cast<int32_t>(rank));
 #pragma unroll
         for (int phs = 0; phs < C::kPhases; ++phs)
 #pragma unroll
             for (int j = 0; j < 2; ++j)
                 if (r0 + j < cg.R)
-                    tma_load_4d(a_dst + (phs * 2 + j) * C::kXRowBytes, &P.tmap_a, bar,
-                                static_cast<int32_t>(g) * cg.Cg, phs - cg.pw,
-                                cg.sh * ho0 + r0 + j - cg.ph, static_cast<int32_t>(n_img));
+                    load4(a_dst + (phs * 2 + j) * C::kXRowBytes, &P.tmap_a,
+                          static_cast<int32_t>(g) * cg.Cg, phs - cg.pw, cg.sh * ho0 + r0 + j - cg.ph);
     } else if constexpr (CG == 2) {
         // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
         const int32_t kx = static_cast<int32_t>(k * C::TK);
@@ -368,13 +380,19 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
-        // Bytes one stage receives: every box of a shifted-row wgrad step is 8 KB; the lower x row
-        // of a tile whose lower tap row lies past the filter is not loaded.
-        uint32_t stage_tx = C::kStageBytes;
-        if constexpr (C::kWgRow)
-            stage_tx = static_cast<uint32_t>(C::kXRowBytes) *
-                       (1u + static_cast<uint32_t>(C::kPhases) *
-                                 (2 * mt + 1 < P.conv.R ? 2u : 1u));
+        // Bytes one stage receives (of both CTAs of a pair): a shifted-row wgrad step loads 64 dy
+        // positions of each CTA's filters (8 KB in all) and per phase an 8 KB x row for each of
+        // the tile's tap rows inside the filter (rows past it are not loaded).
+        uint32_t stage_tx = CG * C::kStageBytes;
+        if constexpr (C::kWgRow) {
+            uint32_t xrows = 0;
+            for (int c = 0; c < CG; ++c) {
+                const int64_t r0 = 2 * (mt * CG + c);
+                xrows += r0 + 1 < P.conv.R ? 2u : (r0 < P.conv.R ? 1u : 0u);
+            }
+            stage_tx = static_cast<uint32_t>(CG * 64 * C::kDyRowBytes) +
+                       static_cast<uint32_t>(C::kXRowBytes * C::kPhases) * xrows;
+        }
         WgradSlabs<TN> slabs;
         if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
         PixelStart ps{0, 0, 0};
@@ -394,7 +412,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
             const uint32_t a_dst = ring + stage * C::kStageBytes;
             if constexpr (CG == 2) {
                 // Both CTAs' bytes are counted on the even CTA's barrier, which expects them all.
-                if (rank == 0) mbar_arrive_expect_tx(full, CG * C::kStageBytes);
+                if (rank == 0) mbar_arrive_expect_tx(full, stage_tx);
                 issue_loads<OP, TN, CG, ST>(P, g, mt, nt, k, a_dst, a_dst + C::kABytes,
                                             mapa_shared(full, 0), slabs, rank, ps);
             } else {
@@ -461,22 +479,28 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
     if constexpr (C::kWgRow) {
         // Per column phase: D[(tap row, channel)][(shift, filter)] over the step's 64 positions.
         // A = the upper and lower x rows (two 64-channel blocks 8 KB apart); B = the dy rows read
-        // at the phase's nq shifts, one 64-filter block per shift, each block one row after the
-        // previous (LBO = 128): block b holds shift q = nq - 1 - b, its rows start at
-        // qmax - q. The phase's taps fill D columns [col0, col0 + 64 * nq).
+        // at the phase's nq shifts, one block of the CTA's filters per shift, each block one row
+        // after the previous (LBO = one dy row): block b holds shift q = nq - 1 - b, its rows
+        // start at qmax - q. The phase's taps fill D columns [col0, col0 + 64 * nq); a CTA pair
+        // (M = 256: four tap rows) takes the first half of them from the even CTA's 32 filters
+        // and the second half from the odd CTA's, in 64-byte swizzled rows.
         const ConvGeom& cg = P.conv;
         uint32_t col0 = 0;
 #pragma unroll
         for (int phs = 0; phs < C::kPhases; ++phs) {
             const uint32_t nq = static_cast<uint32_t>(cg.nq[phs]);
             const uint32_t idesc = (P.idesc & ~(0x3Fu << 17)) | ((nq * 64u >> 3) << 17);
-            const uint32_t b0 = b_addr + static_cast<uint32_t>(cg.qmax + 1 - static_cast<int>(nq)) * 128u;
+            const uint32_t b0 = b_addr + static_cast<uint32_t>(cg.qmax + 1 - static_cast<int>(nq)) *
+                                             static_cast<uint32_t>(C::kDyRowBytes);
             if (nq > 0) {
 #pragma unroll
                 for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
                     const uint64_t ad = smem_desc_sw128(a_addr + phs * 2 * C::kXRowBytes + kk * 2048,
                                                         C::kXRowBytes, 1024);
-                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 128, 1024);
+                    const uint64_t bd =
+                        CG == 1 ? smem_desc_sw128(b0 + kk * 2048, 128, 1024)
+                                : smem_desc_sw64(b0 + kk * 16 * C::kDyRowBytes, C::kDyRowBytes,
+                                                 8 * C::kDyRowBytes);
                     mma_f16<CG>(d_tmem + col0, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
                 }
             }
@@ -624,14 +648,19 @@ __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
 // Shifted-row wgrad: the dW offset, relative to the thread's (group, tap row, channel) base, of
 // the first filter of the 32 D columns starting at `col` (a multiple of 32), or -1 past the tile's
-// taps. Consecutive columns are consecutive filters, `ldc` = R*S*C/G elements apart.
+// taps. A phase's columns are cg.fsplit halves (one per CTA of the filter split), each nq blocks of
+// 64 / fsplit consecutive filters (`ldc` = R*S*C/G elements apart), block b for shift
+// q = nq - 1 - b.
 __device__ __forceinline__ int64_t wgrow_col_offset(const ConvGeom& cg, int64_t ldc, int col) {
+    const int fw = 64 / cg.fsplit;   // filters per block
     int cb = 0;
 #pragma unroll
     for (int phs = 0; phs < 2; ++phs) {
         const int nq = cg.nq[phs];
         if (col < cb + nq * 64) {
-            const int b = (col - cb) >> 6, k0 = (col - cb) & 63;
+            const int local = col - cb;
+            const int h = local / (nq * fw), rem = local - h * nq * fw;
+            const int b = rem / fw, k0 = h * fw + (rem - b * fw);
             const int s = cg.sw * (nq - 1 - b) + phs;
             return static_cast<int64_t>(k0) * ldc + static_cast<int64_t>(s) * cg.Cg;
         }
@@ -1048,7 +1077,9 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
         });
         // The barrier orders every epilogue thread's stores before the releases below, which make
         // them visible (cumulatively) to a CTA that acquires the flag or the tile's arrival
-        // counter (control block word 1 + tile * CG + half), which the folders poll.
+        // counter (control block word 1 + tile * CG + half), which the folders poll; the folders
+        // read the partials with bulk copies (the async proxy).
+        fence_proxy_async_global();
         named_bar_sync(kEpiBarrier, kEpiThreads);
         if (ethread == 0) {
             st_release_gpu(P.flags + cta * CG + e.half, publication(plan, cta, seg.tile));
@@ -1142,7 +1173,7 @@ struct PendingFold {
 // chunks that fit half of it, then every thread adds up its elements there.
 template <int OP, int TN, int CG, int ST>
 __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFold& pd, int ethread,
-                            int64_t half, uint32_t ring) {
+                            int64_t half, uint32_t ring, uint32_t fold_bar, uint32_t& fold_phase) {
     using C = Cfg<OP, TN, CG, ST>;
     const sk_plan_t& plan = P.plan;
     constexpr int kF4 = kTileM * TN / 4;
@@ -1203,15 +1234,26 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
     };
     for (int64_t c0 = b; c0 < e; c0 += cap) {
         const int64_t len = imin(cap, e - c0);
-        // Copy the chunk's slices of all n partials, slot-major, with 16-byte asynchronous copies:
-        // every thread issues all of its own and waits once.
-        for (int64_t j = 0; j < n; ++j)
-            for (int64_t i = ethread; i < len; i += kEpiThreads)
-                cp_async_16(ring + static_cast<uint32_t>((j * len + i) * 16),
-                            base + j * stride + (c0 + i) * 4);
-        cp_async_commit();
-        cp_async_wait_all();
-        named_bar_sync(kEpiBarrier, kEpiThreads);
+        const uint32_t bytes = static_cast<uint32_t>(len * 16);
+        // The chunk's slices of all n partials, slot-major, each one contiguous run of `bytes`:
+        // one bulk copy per partial, issued by the lanes of the first epilogue warp and counted on
+        // the fold barrier, whose single arrival (lane 0) expects them all.
+        if (ethread < 32) {
+            fence_proxy_async_global();   // the acquired partials are read by the async proxy
+            if (ethread == 0) mbar_arrive_expect_tx(fold_bar, static_cast<uint32_t>(n) * bytes);
+            __syncwarp();
+            for (int64_t j = ethread; j < n; j += 32)
+                bulk_copy_g2s(ring + static_cast<uint32_t>(j) * bytes, base + j * stride + c0 * 4,
+                              bytes, fold_bar);
+        }
+        const bool landed = mbar_wait(fold_bar, fold_phase, P.mbar_timeout_ns);
+        fold_phase ^= 1u;
+        if (!named_bar_and(kEpiBarrierWait, kEpiThreadsWait, landed)) {
+            // Never expected (a copy outstanding for the barrier's whole time limit): the error is
+            // recorded for the host and the CTA stops folding.
+            if (ethread == 0) record_error(kErrPipeline, cta, pd.tile, 5);
+            return;
+        }
         for (int64_t i = ethread; i < len; i += kEpiThreads) {
             auto part = [&](int64_t j) { return sbuf[j * len + i]; };
             float4 v;
@@ -1530,9 +1572,12 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         }
         ++nseg;
     }
+    // The fold barrier is free here: the owner fold, its other user, never runs in a spread plan.
+    uint32_t fold_phase = 0;
     if (!aborted)
         for (int i = 0; i < npend; ++i)
-            spread_fold<OP, TN, CG, ST>(P, cta, pend[i], ethread, static_cast<int64_t>(rank), ring);
+            spread_fold<OP, TN, CG, ST>(P, cta, pend[i], ethread, static_cast<int64_t>(rank), ring,
+                                        bars + C::kBarFold * 8, fold_phase);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1589,10 +1634,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         // ring, comes after the CTA's last MMA), so every thread clears a part of them once; the
         // fence makes the stores visible to the tensor cores, and the barrier below orders them
         // before the first MMA.
-        constexpr int kPadBytes = C::kDyBytes - 64 * 128;
+        constexpr int kDyLoaded = 64 * C::kDyRowBytes;
+        constexpr int kPadBytes = C::kDyBytes - kDyLoaded;
         for (int i = static_cast<int>(threadIdx.x); i < C::kStages * kPadBytes / 16; i += kThreads) {
             const int st = i / (kPadBytes / 16), b = i - st * (kPadBytes / 16);
-            st_shared_v4(ring + st * C::kStageBytes + C::kABytes + 64 * 128 + b * 16, 0u, 0u, 0u, 0u);
+            st_shared_v4(ring + st * C::kStageBytes + C::kABytes + kDyLoaded + b * 16, 0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
     }
@@ -1775,12 +1821,16 @@ static size_t smem_bytes_t() {
     return Cfg<OP, TN, CG, ST>::kSmem;
 }
 
-// (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); wgrad has no
-// pair form (the host rejects it first); the block-scaled fp8 GEMM has a 128 x 128 form (5 stages
-// beside its 32 KB store staging and its scale ring) and a 256 x 128 pair form (7 stages).
+// (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); the
+// im2col wgrad has no pair form (the host rejects it first); the shifted-row wgrad has a one-CTA
+// 128 x 192 form and a 256 x 192 pair form (10 stages of 21 KB, or 6 of 37 KB with two column
+// phases); the block-scaled fp8 GEMM has a 128 x 128 form (5 stages beside its 32 KB store staging
+// and its scale ring) and a 256 x 128 pair form (7 stages).
 #define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
     ((cg) == 2                                                                              \
-         ? ((tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)                \
+         ? ((op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 2, 10>(__VA_ARGS__)                 \
+            : (op) == kOpWgradRow2 ? fn<kOpWgradRow2, 192, 2, 6>(__VA_ARGS__)                \
+            : (tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)             \
                                           : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
                         : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \
                            : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 2, 7>(__VA_ARGS__)    \
@@ -1804,7 +1854,7 @@ int main_ctas_per_sm(int op, int cg, int tn, int st) {
 
 int launch_main(const KernelParams& p, int op, int cg, int tn, int st, bool after_zero,
                 cudaStream_t stream) {
-    if (cg == 2 && op != kOpGemm16 && op != kOpFp8 && op != kOpFp8Block)
+    if (cg == 2 && op != kOpGemm16 && op != kOpFp8 && op != kOpFp8Block && !is_wgrad_row(op))
         return static_cast<int>(cudaErrorInvalidValue);
     return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, after_zero, stream);
 }
@@ -1816,7 +1866,10 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int tn = p.plan.tn == 256 ? 256 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
-    if (p.plan.tn == 192)
+    if (p.plan.tn == 192 && cg == 2)
+        sk_stage2_kernel<192, 2><<<dim3(static_cast<unsigned>(tiles), 256u * 192u / 4u / kStage2Threads),
+                                   dim3(kStage2Threads), 0, stream>>>(p);
+    else if (p.plan.tn == 192)
         sk_stage2_kernel<192, 1><<<dim3(static_cast<unsigned>(tiles), 128u * 192u / 4u / kStage2Threads),
                                    dim3(kStage2Threads), 0, stream>>>(p);
     else if (cg == 2 && tn == 256)

@@ -80,13 +80,18 @@ struct ConvGeom {
     // positions (q <= qmax); phase p holds nq[p] taps.
     int32_t ho, ho_pad, rows_per_step, wseg, qmax;
     int32_t nq[2];
+    // Shifted-row wgrad: CTAs the 64 filters are split over (1, or 2 for a CTA pair, each holding
+    // 32 of them). A phase's D columns are fsplit halves, each nq blocks of 64/fsplit filters, one
+    // block per shift q = nq - 1 - block.
+    int32_t fsplit;
 };
 
 struct KernelParams {
     CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K];
                            // shifted-row wgrad: x [N][H][W][C], strided rows of 64 channels
     CUtensorMap tmap_b;    // GEMM: B [N][K]; fp8: B8 [N][K]; wgrad: im2col view of x;
-                           // shifted-row wgrad: dy [N][Ho][Wo][K], rows of 64 filters
+                           // shifted-row wgrad: dy [N][Ho][Wo][K], rows of 64 filters (128-byte
+                           // swizzle), or of 32 for a CTA pair (64-byte swizzle)
     CUtensorMap tmap_c;    // when c_tma: C [M][N] 16-bit, 64 x 32 boxes, 128-byte swizzle
     sk_plan_t plan;
     void* c;               // output
@@ -95,7 +100,7 @@ struct KernelParams {
     const float* sb;       // fp8 column scales; null for the per-tensor scaling below
     float scale;           // fp8 with sa == sb == null: the product of the two tensor scales
     uint32_t* flags;       // per-publisher flags (linear/tree)
-    uint32_t* control;     // [0] ticket counter
+    uint32_t* control;     // [0] ticket counter; [1 + tile * CG + half] spread-fold arrival counters
     float* partials;       // linear/tree partial tiles, one slot per publisher
     float* scratch;        // workspace reduction scratch, one tile per shared-tile candidate
     ConvGeom conv;

@@ -173,6 +173,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// The same into this CTA's shared memory, completing on the barrier of the even CTA of its pair
+// (a shared::cluster address): the CTA-pair form.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // im2col load of a 4-D NHWC tensor: start pixel (w, h, n) of the traversal, channel c,
 // filter-tap offsets (off_w, off_h).
 __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap* m,
@@ -396,6 +408,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// The same for the 64-byte swizzle (atoms of 64-byte rows, the pattern repeating every 8 rows):
+// MN-major with 32 16-bit elements per row. Measured on GB300: an atom may start at any 64-byte
+// row (the swizzle follows the absolute address, base offset 0), so LBO = 64 gives atoms one row
+// apart, and an M = 128, N = 192 MMA reading such a B runs at the full rate.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
     return d;
 }
 

@@ -1,9 +1,9 @@
 """GPU parity of the implicit-GEMM conv wgrad (sk_conv2d_wgrad_nhwc through the C ABI) against the
 fp64 direct-loop oracle: every launch mode x four reductions on dense, strided and grouped shapes
 with a partial last M tile and a ragged pixel tail, under both wgrad kernels (the automatic tile,
-which takes the shifted-row kernel for 64-channel, 64-filter groups, and the 128 x 128 tile of the
-pages' GEMM view), shapes that reach the shifted-row kernel's edges (one, two, four and five tap
-rows; one to three column taps; column stride 2; rows packed several to a K step with a ragged
+which takes the shifted-row kernel for 64-channel, 64-filter groups, on a CTA pair for three or
+four tap rows, and the 128 x 128 tile of the pages' GEMM view), shapes that reach the shifted-row
+kernel's edges (one to five tap rows; one to three column taps; column stride 2; rows packed several to a K step with a ragged
 last step; the widest rows it takes), and the two named wgrad workloads in full."""
 import numpy as np
 import pytest
@@ -40,14 +40,19 @@ def run(x, dy, K, R, S, stride, pad, groups, out, mode, red, ctas, tile="auto"):
     return dw
 
 
-def row_kernel(s) -> bool:
-    """Whether the automatic tile runs this shape on the shifted-row kernel (its 192-wide tile)."""
+def row_plan(s):
+    """The automatic tile's plan of this shape."""
     N, H, W, C, K, R, S = s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"]
     prob = sk.make_problem("wgrad", ab_dtype=s["dt"], c_dtype="f32", n=N, h=H, w=W, c=C, k=K,
                            r=R, s=S, stride_h=s["stride"][0], stride_w=s["stride"][1],
                            pad_h=s["pad"][0], pad_w=s["pad"][1], groups=s["groups"])
     with sk.tile("auto"):
-        return sk.sk_plan(prob, "dp_sk", "atomic", 7, 148).tn == 192
+        return sk.sk_plan(prob, "dp_sk", "atomic", 7, 148)
+
+
+def row_kernel(s) -> bool:
+    """Whether the automatic tile runs this shape on the shifted-row kernel (its 192-wide tile)."""
+    return row_plan(s).tn == 192
 
 
 SHAPES = {
@@ -87,6 +92,9 @@ ROW_SHAPES = {
     # stride 2 both ways with 2x2 taps: one tap per column phase, no shift, 16 rows per K step
     "row_s2_2x2": dict(dt="bf16", N=2, H=9, W=9, C=64, K=64, R=2, S=2, stride=(2, 2),
                        pad=(0, 0), groups=1),
+    # four tap rows (the CTA pair's 256 rows all used), two groups, row padding only
+    "row_r4s2_g2": dict(dt="bf16", N=2, H=8, W=10, C=128, K=128, R=4, S=2, stride=(1, 1),
+                        pad=(1, 0), groups=2),
     # the widest rows the kernel takes: 62 output columns + 2 shifts = 64 positions
     "row_wide": dict(dt="f16", N=1, H=3, W=62, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
                      groups=1),
@@ -106,6 +114,8 @@ def test_row_kernel_takes_its_shapes():
     too wide for a K step fall back too."""
     for name, s in ROW_SHAPES.items():
         assert row_kernel(s), name
+        # three or four tap rows: one 256-row tile on a CTA pair
+        assert row_plan(s).tm == (256 if s["R"] in (3, 4) else 128), name
     assert row_kernel(SHAPES["dense_3x3"]) and row_kernel(SHAPES["grouped_s2"])
     assert not row_kernel(SHAPES["pointwise"]) and not row_kernel(SHAPES["asym"])
     too_wide = dict(ROW_SHAPES["row_wide"], W=63)

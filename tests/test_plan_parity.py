@@ -33,6 +33,8 @@ FIELD_MAP = {  # C name -> oracle name
 
 
 def compare(prob, oracle_kw, mode, red, ctas, num_sms=148, check_ctas=None, cluster=1):
+    oracle_kw = dict(oracle_kw)
+    cluster = oracle_kw.pop("cluster", cluster)
     cp = sk.sk_plan(prob, mode[0], red[0], ctas, num_sms)
     # a pair kernel's default pool is resolved over SM pairs
     pool = ctas if ctas > 0 else P.default_pool(red[1], num_sms // cluster, 1)
@@ -275,9 +277,10 @@ def test_block_scale_tile_setting():
 
 
 # ---- shifted-row wgrad (automatic tile, 64-channel and 64-filter groups): GEMM view
-# M = (tap row, channel) in 128-row tiles of two tap rows, N = (column tap, filter) in one 192-wide
-# tile, reduction over the padded positions: 64 per K step, `64 / wseg` output rows of `wseg`
-# positions (the power of two >= Wo + shifts), rows counted per image over Ho rounded up.
+# M = (tap row, channel) in 128-row tiles of two tap rows (three or four tap rows: one 256-row tile
+# on a CTA pair), N = (column tap, filter) in one 192-wide tile, reduction over the padded
+# positions: 64 per K step, `64 / wseg` output rows of `wseg` positions (the power of two
+# >= Wo + shifts), rows counted per image over Ho rounded up.
 
 def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16"):
     sh, sw = stride
@@ -294,8 +297,9 @@ def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16"):
     if rows == 0:   # rows too wide for one K step: not this view
         return prob, None
     ho_pad = -(-Ho // rows) * rows
-    kw = dict(tiles_m=-(-(R * 64) // 128), tiles_n=1, groups=groups, kred=N * ho_pad * wseg,
-              tm=128, tn=192, tk=64)
+    tm = 256 if R in (3, 4) else 128
+    kw = dict(tiles_m=-(-(R * 64) // tm), tiles_n=1, groups=groups, kred=N * ho_pad * wseg,
+              tm=tm, tn=192, tk=64, cluster=tm // 128)
     return prob, kw
 
 
@@ -315,21 +319,25 @@ def test_row_wgrad_plans(name, pk, ctas, mode, red):
     big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
     with sk.tile("auto"):
         cp = compare(prob, kw, mode, red, ctas, check_ctas=big)
-    assert (cp.tm, cp.tn, cp.tk) == (128, 192, 64)
+    assert (cp.tm, cp.tn, cp.tk) == (kw["tm"], 192, 64)
 
 
 def test_row_wgrad_worked_vectors():
-    """32x56x56, 64 -> 64, 3x3: two tiles (tap rows {0,1} and {2}), 32*56 K steps of one
-    56-column row each (64 positions); 148 CTAs: 3584 steps, 24 each and one more for the first
-    32. Grouped stride 2 (4 groups of 64): 8 tiles, 14 output columns + 1 shift -> 16-position
-    rows, 4 rows per step, 14 rows per image padded to 16: 64*16/4 = 256 steps per tile."""
+    """32x56x56, 64 -> 64, 3x3: one 256 x 192 pair tile (tap rows 0-2), 32*56 K steps of one
+    56-column row each (64 positions); 74 CTA pairs: 1792 steps, 24 each and one more for the
+    first 16. Grouped stride 2 (4 groups of 64): 4 tiles, 14 output columns + 1 shift ->
+    16-position rows, 4 rows per step, 14 rows per image padded to 16: 64*16/4 = 256 steps per
+    tile; 1024 steps on 74 pairs: 13 each and one more for the first 62. Five tap rows stay on the
+    one-CTA 128 x 192 tile (three tiles)."""
     with sk.tile("auto"):
-        cp = sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", 148, 148)
-        assert (cp.tiles, cp.iters_per_tile, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
-                cp.extra_iters, cp.grid) == (2, 1792, 2, 3584, 24, 32, 148)
-        cp = sk.sk_plan(ROW_NAMED[1][1][0], "dp_sk", "atomic", 148, 148)
+        cp = sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", 74, 148)
+        assert (cp.tm, cp.tiles, cp.iters_per_tile, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
+                cp.extra_iters, cp.grid) == (256, 1, 1792, 1, 1792, 24, 16, 74)
+        cp = sk.sk_plan(ROW_NAMED[1][1][0], "dp_sk", "atomic", 74, 148)
         assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.iters_per_sk_cta, cp.extra_iters) == \
-            (8, 256, 148, 13, 124)
+            (4, 256, 74, 13, 62)
+        cp = sk.sk_plan(ROW_NAMED[2][1][0], "dp_sk", "atomic", 7, 148)
+        assert (cp.tm, cp.tiles_m) == (128, 3)
 
 
 def test_row_wgrad_sweep():
