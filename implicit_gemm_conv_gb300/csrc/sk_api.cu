@@ -202,7 +202,8 @@ int problem_view(const sk_problem& p, View& v) {
     int rc = problem_view_pages(p, v);
     if (rc) return rc;
     RowGeom g;
-    if (v.op_kind == sk::kOpWgrad16 && g_tile == SK_TILE_AUTO && wgrad_row_geom(p, g)) {
+    if (v.op_kind == sk::kOpWgrad16 && (g_tile == SK_TILE_AUTO || g_tile == SK_TILE_256_PAIR) &&
+        wgrad_row_geom(p, g)) {
         v.gemm_m = p.r * 64;
         v.gemm_n = p.s * 64;
         v.kred = p.n * g.ho_pad * g.wseg;
@@ -270,6 +271,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
 
 constexpr int64_t kAutoPairMinTiles = 64;   // SK_TILE_AUTO: pair tiles needed for the pair kernel
 constexpr int64_t kSpreadMinContributors = 8;   // linear / tree: contributors for the spread fold
+constexpr int64_t kRowPairMinSteps = 128 * 148;  // shifted-row wgrad: K steps for the pair kernel
 
 // The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
 // (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
@@ -278,15 +280,17 @@ struct TileCfg {
 };
 int tile_cfg(const View& v, TileCfg& t) {
     if (sk::is_wgrad_row(v.op_kind)) {
-        // Three or four tap rows (M = 192 or 256): a 256 x 192 tile on a CTA pair, each CTA
-        // holding two tap rows and half the filters, so that every tensor core reads only half of
-        // B from its shared memory (10 stages of 21 KB, or 6 of 37 KB with two x column phases).
-        // Otherwise a 128 x 192 tile on one CTA: 8 stages of 25 KB or 5 of 41 KB.
-        const bool pair = v.gemm_m == 3 * 64 || v.gemm_m == 4 * 64;
-        if (v.op_kind == sk::kOpWgradRow1)
-            t = pair ? TileCfg{2, 192, 10} : TileCfg{1, 192, 8};
-        else
-            t = pair ? TileCfg{2, 192, 6} : TileCfg{1, 192, 5};
+        // Three or four tap rows (M = 192 or 256) over a long reduction (at least
+        // kRowPairMinSteps K steps of 128-row tiles in all, about 128 per SM): a 256 x 192 tile
+        // on a CTA pair, each CTA holding two tap rows and half the filters, with several K steps
+        // per ring stage. Otherwise a 128 x 192 tile on one CTA with one-step stages: with a
+        // few dozen steps per CTA its deeper ring ramps up faster (measured on the 32x56x56 and
+        // grouped 64x28x28 wgrad, 20.1 against 21.2-24.3 us).
+        // SK_TILE_256_PAIR asks for the pair kernel whatever the size.
+        const int64_t steps = v.groups * sk::ceil_div(v.gemm_m, sk::kTileM) * (v.kred / 64);
+        const bool pair = g_tile == SK_TILE_256_PAIR ||
+                          ((v.gemm_m == 3 * 64 || v.gemm_m == 4 * 64) && steps >= kRowPairMinSteps);
+        t = TileCfg{pair ? 2 : 1, 192, sk::wgrow_stages(v.op_kind, pair ? 2 : 1)};
         return SK_OK;
     }
     if (v.op_kind == sk::kOpFp8Block) {
@@ -309,7 +313,7 @@ int tile_cfg(const View& v, TileCfg& t) {
         case SK_TILE_256_PAIR:
         case SK_TILE_256x256_PAIR:
             if (v.op_kind != sk::kOpGemm16 && v.op_kind != sk::kOpFp8)
-                return fail(SK_ERR_UNSUPPORTED, "the CTA-pair tiles serve the GEMMs only");
+                return fail(SK_ERR_UNSUPPORTED, "the CTA-pair tiles serve the GEMMs and the shifted-row wgrad only");
             // Rings of about 96 KB, so that two CTAs share an SM and one's epilogue overlaps the
             // other's mainloop (measured faster than one CTA per SM with twice the stages).
             t = g_tile == SK_TILE_256_PAIR ? TileCfg{2, 128, 4} : TileCfg{2, 256, 3};
@@ -1056,12 +1060,46 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
         // Shifted-row wgrad. A: x rows of 64 channels, `wseg` positions at column stride sw and
         // `rows_per_step` rows at row stride sh (the traversal strides of the map), from any
         // (column, row) start: outside the image reads zeros. B: dy rows of 64 filters.
+        TileCfg tc;
+        rc = tile_cfg(view, tc);
+        if (rc) return rc;
+        // Ring stage: the most K steps (at most 8, at most one image's) whose boxes fit the stage:
+        // per column phase the x rows (a CTA pair with sh = 1: one box of T * rows_per_step + 1
+        // rows holding both tap rows; else one box of T * rows_per_step rows per tap row), then
+        // the dy rows with 16 zero rows after them; every box 1024-byte aligned.
+        const int64_t dy_row = 128 / tc.cg;
+        const int64_t cap = sk::wgrow_stage_bytes(view.op_kind, tc.cg);
+        const int64_t steps_per_image = rg.ho_pad / rg.rows_per_step;
+        int64_t T = 0, x_phase = 0;
+        // The one-CTA kernel keeps a box per tap row (measured faster there than one box of
+        // both: 0.27 against 0.44 us per step on the 32x56x56 wgrad).
+        const bool shared_box = stride_h == 1 && tc.cg == 2;
+        for (int64_t t = sk::imin(8, steps_per_image); t >= 1 && T == 0; --t) {
+            const int64_t rows = t * rg.rows_per_step;
+            if (rows + 1 > 256 || rows * stride_h > 256) continue;   // TMA box dimensions
+            const int64_t xp = shared_box ? sk::round_up((rows + 1) * rg.wseg * 128, 1024)
+                                          : 2 * t * 8192;
+            const int64_t dy = sk::round_up((t * 64 + 16) * dy_row, 1024);
+            if (stride_w * xp + dy <= cap) {
+                T = t;
+                x_phase = xp;
+            }
+        }
+        if (T == 0) return fail(SK_ERR_UNSUPPORTED, "shifted-row wgrad stage does not fit");
+        kp.conv.stage_steps = static_cast<int32_t>(T);
+        kp.conv.x_lbo = static_cast<int32_t>(shared_box ? rg.wseg * 128 : T * 8192);
+        kp.conv.x_shared_box = shared_box ? 1 : 0;
+        kp.conv.x_phase_bytes = static_cast<int32_t>(x_phase);
+        kp.conv.dy_off = static_cast<int32_t>(stride_w * x_phase);
         {
             const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
             const cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2),
                                            (cuuint64_t)(H * W * C * 2)};
+            // The box spans sh image rows per loaded row (the traversal stride takes every sh-th).
             const cuuint32_t box[4] = {64, (cuuint32_t)(rg.wseg * stride_w),
-                                       (cuuint32_t)(rg.rows_per_step * stride_h), 1};
+                                       (cuuint32_t)(shared_box ? T * rg.rows_per_step + 1
+                                                               : T * rg.rows_per_step * stride_h),
+                                       1};
             const cuuint32_t estr[4] = {1, (cuuint32_t)stride_w, (cuuint32_t)stride_h, 1};
             CUresult r = g_encode_tiled(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                                         const_cast<void*>(x), dims, strides, box, estr,
@@ -1070,16 +1108,13 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
         }
-        TileCfg tc;
-        rc = tile_cfg(view, tc);
-        if (rc) return rc;
         {
             // A CTA pair splits the filters: each CTA reads rows of 32 (64 bytes, 64-byte swizzle).
             const cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)N};
             const cuuint64_t strides[3] = {(cuuint64_t)(K * 2), (cuuint64_t)(Wo * K * 2),
                                            (cuuint64_t)(Ho * Wo * K * 2)};
             const cuuint32_t box[4] = {(cuuint32_t)(64 / tc.cg), (cuuint32_t)rg.wseg,
-                                       (cuuint32_t)rg.rows_per_step, 1};
+                                       (cuuint32_t)(T * rg.rows_per_step), 1};
             const cuuint32_t estr[4] = {1, 1, 1, 1};
             CUresult r = g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                                         const_cast<void*>(dy), dims, strides, box, estr,

@@ -138,16 +138,15 @@ struct Cfg {
     static constexpr int TK = 128 / kElem;                 // one 128-byte swizzle row per K step
     static constexpr int kTileMAll = kTileM * CG;          // tile rows of the CTA (pair)
     static constexpr int kBRows = TN / CG;                 // B rows this CTA stages
-    // Shifted-row wgrad stage: per phase an x row of the CTA's upper and of its lower tap row
-    // (64 positions x 64 channels, 8 KB each), then the dy rows (64 positions x the CTA's filters:
-    // 64, or 32 in each CTA of a pair) with room for the shifts' overrun (at most 7 rows past the
-    // 64, kept zero): 72 rows of 128 bytes (9 KB), or 80 of 64 bytes for a pair (5 KB, so that
-    // every stage starts 1024-byte aligned).
-    static constexpr int kXRowBytes = 64 * 128;
+    // Shifted-row wgrad stage: a fixed capacity laid out at run time (ConvGeom stage_steps,
+    // x_phase_bytes, x_lbo, dy_off): per x column phase the CTA's x rows of up to stage_steps K
+    // steps (8 KB of 64 positions x 64 channels per step and tap row), then their dy rows (64
+    // positions x the CTA's filters per step: 128-byte rows, or 64-byte rows of 32 filters in each
+    // CTA of a pair) and 16 zero rows for the shifts' overrun.
     static constexpr int kDyRowBytes = 128 / CG;
-    static constexpr int kDyBytes = CG == 1 ? 9 * 1024 : 5 * 1024;
-    static constexpr int kABytes = kWgRow ? kPhases * 2 * kXRowBytes : kTileM * 128;   // 16 KB
-    static constexpr int kBBytes = kWgRow ? kDyBytes : kBRows * 128;
+    static constexpr int kDyPadRows = 16;
+    static constexpr int kABytes = kWgRow ? wgrow_stage_bytes(OP, CG) : kTileM * 128;   // 16 KB
+    static constexpr int kBBytes = kWgRow ? 0 : kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     // ST stages in the ring; two CTAs share an SM when the ring is at most 96 KB.
     static constexpr int kStages = ST;
@@ -255,6 +254,27 @@ __device__ __forceinline__ void pixel_start(const ConvGeom& cg, int64_t mt, Pixe
     ps.n = static_cast<int32_t>(n_img);
 }
 
+// Shifted-row wgrad stage layout: the one-CTA kernel's is fixed (one step: per phase the two tap
+// rows' x boxes, 8 KB apart, then the dy rows); the pair's comes from the host (ConvGeom).
+template <int CG, int PHASES>
+struct RowLayout {
+    uint32_t x_lbo, x_phase, dy_off;
+    bool shared_box;
+    __device__ __forceinline__ explicit RowLayout(const ConvGeom& cg) {
+        if constexpr (CG == 1) {
+            x_lbo = 8192u;
+            x_phase = 16384u;
+            dy_off = PHASES * 16384u;
+            shared_box = false;
+        } else {
+            x_lbo = static_cast<uint32_t>(cg.x_lbo);
+            x_phase = static_cast<uint32_t>(cg.x_phase_bytes);
+            dy_off = static_cast<uint32_t>(cg.dy_off);
+            shared_box = cg.x_shared_box != 0;
+        }
+    }
+};
+
 template <int OP, int TN, int CG, int ST>
 __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, int64_t mt,
                                             int64_t nt, int64_t k, uint32_t a_dst, uint32_t b_dst,
@@ -288,34 +308,45 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
                             static_cast<int32_t>(g) * cg.Kg + c0);
         }
     } else if constexpr (is_wgrad_row(OP)) {
-        // K step k: rows_per_step output rows of image n (rows counted per image over ho_pad), each
-        // a segment of wseg positions. B = dy from position -qmax, so that each segment starts with
-        // the zero halo that the shifted reads of its first positions take; A = per column phase the
-        // x rows of the tile's two tap rows, at traversal strides (sw, sh) from the tensor map.
+        // A stage from K step k on: rows_per_step output rows of image n per step (rows counted
+        // per image over ho_pad), each a segment of wseg positions. B = dy from position -qmax, so
+        // that each segment starts with the zero halo that the shifted reads of its first
+        // positions take (and the last step's overrun reads the next row's); A = per column phase
+        // the x rows of the CTA's two tap rows, at traversal strides (sw, sh) from the tensor map.
+        // A CTA pair splits the filters: this CTA's 32 of them; its tap rows are the pair tile's
+        // 128-row half of (tap row, channel): rows 2 * (mt * CG + rank) and the next.
         const ConvGeom& cg = P.conv;
         const uint32_t rr0 = static_cast<uint32_t>(k) * static_cast<uint32_t>(cg.rows_per_step);
         const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
         const uint32_t n_img = rr0 / hp;   // < 2^31 (checked on the host)
         const int32_t ho0 = static_cast<int32_t>(rr0 - n_img * hp);
-        // A CTA pair splits the filters: this CTA's 32 of them. Its tap rows are the pair tile's
-        // 128-row half of (tap row, channel): rows 2 * (mt * CG + rank) and the next.
         auto load4 = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
             if constexpr (CG == 2)
                 tma_load_4d_pair(dst, m, bar, x, y, z, static_cast<int32_t>(n_img));
             else
                 tma_load_4d(dst, m, bar, x, y, z, static_cast<int32_t>(n_img));
         };
-        load4(b_dst, &P.tmap_b,
+        const RowLayout<CG, C::kPhases> lay(cg);
+        load4(a_dst + lay.dy_off, &P.tmap_b,
               static_cast<int32_t>(g) * cg.Kg + static_cast<int32_t>(rank) * (64 / CG), -cg.qmax,
               ho0);
         const int32_t r0 = 2 * (static_cast<int32_t>(mt) * CG + static_cast<int32_t>(rank));
 #pragma unroll
-        for (int phs = 0; phs < C::kPhases; ++phs)
+        for (int phs = 0; phs < C::kPhases; ++phs) {
+            const uint32_t xd = a_dst + phs * lay.x_phase;
+            if (lay.shared_box) {   // both tap rows in one box of stage_steps * rows_per_step + 1 rows
+                if (r0 < cg.R)
+                    load4(xd, &P.tmap_a, static_cast<int32_t>(g) * cg.Cg, phs - cg.pw,
+                          ho0 + r0 - cg.ph);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                if (r0 + j < cg.R)
-                    load4(a_dst + (phs * 2 + j) * C::kXRowBytes, &P.tmap_a,
-                          static_cast<int32_t>(g) * cg.Cg, phs - cg.pw, cg.sh * ho0 + r0 + j - cg.ph);
+                for (int j = 0; j < 2; ++j)
+                    if (r0 + j < cg.R)
+                        load4(xd + j * lay.x_lbo, &P.tmap_a,
+                              static_cast<int32_t>(g) * cg.Cg, phs - cg.pw,
+                              cg.sh * ho0 + r0 + j - cg.ph);
+            }
+        }
     } else if constexpr (CG == 2) {
         // This CTA's rows of the pair tile: A rows [128*rank, +128), B rows [TN/2*rank, +TN/2).
         const int32_t kx = static_cast<int32_t>(k * C::TK);
@@ -364,6 +395,32 @@ __device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool 
     return rot;
 }
 
+// K steps in the ring stage at position j of a segment's rotated order: one, or for the
+// shifted-row wgrad up to stage_steps consecutive steps of one image before the order wraps or the
+// segment ends. The producer and the MMA issuer walk the same stages.
+template <int OP, int CG>
+__device__ __forceinline__ int64_t stage_step_count(const ConvGeom& cg, const sk_segment_t& seg,
+                                                    int64_t rot, int64_t j) {
+    if constexpr (!is_wgrad_row(OP) || CG == 1) {   // the one-CTA row kernel: one step per stage
+        return 1;
+    } else {
+        const int64_t len = seg.k_end - seg.k_begin;
+        int64_t k = seg.k_begin + rot + j;
+        int64_t run;
+        if (k >= seg.k_end) {
+            k -= len;
+            run = seg.k_begin + rot - k;   // up to the wrap point
+        } else {
+            run = seg.k_end - k;
+        }
+        const uint32_t rr0 = static_cast<uint32_t>(k) * static_cast<uint32_t>(cg.rows_per_step);
+        const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
+        const uint32_t ho0 = rr0 - (rr0 / hp) * hp;
+        const int64_t img = static_cast<int64_t>((hp - ho0) / static_cast<uint32_t>(cg.rows_per_step));
+        return imin(imin(static_cast<int64_t>(cg.stage_steps), run), img);
+    }
+}
+
 template <int OP, int TN, int CG, int ST>
 __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, uint32_t bars,
                              volatile SmemCtl* ctl, uint32_t rank) {
@@ -380,18 +437,28 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
         int64_t g, mt, nt;
         tile_coords(plan, seg.tile, g, mt, nt);
-        // Bytes one stage receives (of both CTAs of a pair): a shifted-row wgrad step loads 64 dy
-        // positions of each CTA's filters (8 KB in all) and per phase an 8 KB x row for each of
-        // the tile's tap rows inside the filter (rows past it are not loaded).
+        // Bytes one stage receives (of both CTAs of a pair). A shifted-row wgrad stage is whole
+        // boxes whatever its steps: each CTA's dy box (64 positions of its filters per step) and
+        // per phase its x box(es): a shared box of stage_steps * rows_per_step + 1 rows when its
+        // upper tap row is inside the filter, else one box of stage_steps * 8 KB per tap row
+        // inside it.
         uint32_t stage_tx = CG * C::kStageBytes;
         if constexpr (C::kWgRow) {
-            uint32_t xrows = 0;
+            const ConvGeom& cg = P.conv;
+            const uint32_t T = CG == 1 ? 1u : static_cast<uint32_t>(cg.stage_steps);
+            const RowLayout<CG, C::kPhases> lay(cg);
+            uint32_t x = 0;
             for (int c = 0; c < CG; ++c) {
                 const int64_t r0 = 2 * (mt * CG + c);
-                xrows += r0 + 1 < P.conv.R ? 2u : (r0 < P.conv.R ? 1u : 0u);
+                if (lay.shared_box)
+                    x += r0 < cg.R ? (T * static_cast<uint32_t>(cg.rows_per_step) + 1u) *
+                                         static_cast<uint32_t>(cg.wseg) * 128u
+                                   : 0u;
+                else
+                    x += (r0 + 1 < cg.R ? 2u : (r0 < cg.R ? 1u : 0u)) * T * 8192u;
             }
-            stage_tx = static_cast<uint32_t>(CG * 64 * C::kDyRowBytes) +
-                       static_cast<uint32_t>(C::kXRowBytes * C::kPhases) * xrows;
+            stage_tx = static_cast<uint32_t>(CG) * T * 64u * static_cast<uint32_t>(C::kDyRowBytes) +
+                       static_cast<uint32_t>(C::kPhases) * x;
         }
         WgradSlabs<TN> slabs;
         if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
@@ -399,7 +466,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if constexpr (folds_groups_into_columns(OP)) pixel_start(P.conv, mt, ps);
         const int64_t len = seg.k_end - seg.k_begin;
         const int64_t rot = segment_rotation(plan, dp, seg, tau);
-        for (int64_t j = 0; j < len; ++j) {
+        for (int64_t j = 0; j < len; j += stage_step_count<OP, CG>(P.conv, seg, rot, j)) {
             int64_t k = seg.k_begin + rot + j;
             if (k >= seg.k_end) k -= len;
             const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
@@ -462,9 +529,68 @@ template <int OP, int TN, int CG, int ST>
 __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
                                           const sk_segment_t& seg, uint32_t ring, uint32_t bars,
                                           volatile SmemCtl* ctl, uint32_t d_tmem, bool accumulate,
-                                          uint32_t& stage, uint32_t& phase) {
+                                          uint32_t& stage, uint32_t& phase, int64_t steps) {
     using C = Cfg<OP, TN, CG, ST>;
+    static_assert(C::kMmasPerStage == 4, "a K step is four MMAs");
     const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
+    const uint32_t a_addr = ring + stage * C::kStageBytes;
+    const uint32_t b_addr = a_addr + C::kABytes;
+    // The stage's descriptors go into registers before its data is awaited, and its MMAs then
+    // leave back to back (mma_x4): the issuing thread stalls while the tensor pipe runs the
+    // previous MMA, so work between two MMAs would leave the pipe idle.
+    uint64_t ad[C::kPhases][4], bd[C::kPhases][4];
+    uint32_t idesc[C::kPhases], col0[C::kPhases];
+    bool live[C::kPhases];
+    if constexpr (C::kWgRow) {
+        // Per K step and column phase: D[(tap row, channel)][(shift, filter)] over the step's 64
+        // positions. A = the CTA's upper and lower tap-row x rows of the step (8 KB per step
+        // along the box, the lower one x_lbo bytes after the upper); B = the step's dy rows read
+        // at the phase's nq shifts, one block of the CTA's filters per shift, each block one row
+        // after the previous (LBO = one dy row): block b holds shift q = nq - 1 - b, its rows
+        // start at qmax - q. The phase's taps fill D columns [col0, col0 + 64 * nq); a CTA pair
+        // (M = 256: four tap rows) takes the first half of them from the even CTA's 32 filters
+        // and the second half from the odd CTA's, in 64-byte swizzled rows. The descriptors here
+        // are the stage's first step; step t adds t * 8 KB (A) and t * 64 dy rows (B).
+        const ConvGeom& cg = P.conv;
+        const RowLayout<CG, C::kPhases> lay(cg);
+        uint32_t c0 = 0;
+#pragma unroll
+        for (int phs = 0; phs < C::kPhases; ++phs) {
+            const uint32_t nq = static_cast<uint32_t>(cg.nq[phs]);
+            idesc[phs] = (P.idesc & ~(0x3Fu << 17)) | ((nq * 64u >> 3) << 17);
+            col0[phs] = c0;
+            live[phs] = nq > 0;
+            const uint32_t xa = a_addr + phs * lay.x_phase;
+            const uint32_t b0 = a_addr + lay.dy_off +
+                                static_cast<uint32_t>(cg.qmax + 1 - static_cast<int>(nq)) *
+                                    static_cast<uint32_t>(C::kDyRowBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                ad[phs][kk] = smem_desc_sw128(xa + kk * 2048, lay.x_lbo, 1024);
+                bd[phs][kk] = CG == 1 ? smem_desc_sw128(b0 + kk * 2048, 128, 1024)
+                                      : smem_desc_sw64(b0 + kk * 16 * C::kDyRowBytes,
+                                                       C::kDyRowBytes, 8 * C::kDyRowBytes);
+            }
+            c0 += nq * 64u;
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
+            // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
+            if constexpr (OP == kOpWgrad16)
+                ad[0][kk] = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
+            else
+                ad[0][kk] = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            if constexpr (OP == kOpWgrad16 || OP == kOpDgrad16)
+                bd[0][kk] = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
+            else
+                bd[0][kk] = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+        }
+        idesc[0] = P.idesc;
+        col0[0] = 0;
+        live[0] = true;
+    }
     // The abort flag is read here only for the block-scaled op: elsewhere the read on every step
     // measured slower (128x128 tile: 1012 against 1064 TFLOP/s), and a stalled producer still ends
     // the wait at its time limit.
@@ -474,63 +600,27 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
         return false;
     }
     tc_fence_after();
-    const uint32_t a_addr = ring + stage * C::kStageBytes;
-    const uint32_t b_addr = a_addr + C::kABytes;
+    const uint32_t acc = accumulate ? 1u : 0u;
     if constexpr (C::kWgRow) {
-        // Per column phase: D[(tap row, channel)][(shift, filter)] over the step's 64 positions.
-        // A = the upper and lower x rows (two 64-channel blocks 8 KB apart); B = the dy rows read
-        // at the phase's nq shifts, one block of the CTA's filters per shift, each block one row
-        // after the previous (LBO = one dy row): block b holds shift q = nq - 1 - b, its rows
-        // start at qmax - q. The phase's taps fill D columns [col0, col0 + 64 * nq); a CTA pair
-        // (M = 256: four tap rows) takes the first half of them from the even CTA's 32 filters
-        // and the second half from the odd CTA's, in 64-byte swizzled rows.
-        const ConvGeom& cg = P.conv;
-        uint32_t col0 = 0;
+        // Descriptor address fields count 16-byte units.
+        constexpr uint64_t kStepA = 8192 >> 4, kStepB = (64 * C::kDyRowBytes) >> 4;
+        const int64_t nsteps = CG == 1 ? 1 : steps;
+        for (int64_t t = 0; t < nsteps; ++t) {
 #pragma unroll
-        for (int phs = 0; phs < C::kPhases; ++phs) {
-            const uint32_t nq = static_cast<uint32_t>(cg.nq[phs]);
-            const uint32_t idesc = (P.idesc & ~(0x3Fu << 17)) | ((nq * 64u >> 3) << 17);
-            const uint32_t b0 = b_addr + static_cast<uint32_t>(cg.qmax + 1 - static_cast<int>(nq)) *
-                                             static_cast<uint32_t>(C::kDyRowBytes);
-            if (nq > 0) {
+            for (int phs = 0; phs < C::kPhases; ++phs) {
+                if (!live[phs]) continue;
+                uint64_t a[4], b[4];
 #pragma unroll
-                for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a_addr + phs * 2 * C::kXRowBytes + kk * 2048,
-                                                        C::kXRowBytes, 1024);
-                    const uint64_t bd =
-                        CG == 1 ? smem_desc_sw128(b0 + kk * 2048, 128, 1024)
-                                : smem_desc_sw64(b0 + kk * 16 * C::kDyRowBytes, C::kDyRowBytes,
-                                                 8 * C::kDyRowBytes);
-                    mma_f16<CG>(d_tmem + col0, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) {
+                    a[kk] = ad[phs][kk] + static_cast<uint64_t>(t) * kStepA;
+                    b[kk] = bd[phs][kk] + static_cast<uint64_t>(t) * kStepB;
                 }
+                mma_x4<CG, false>(d_tmem + col0[phs], a, b, idesc[phs], t > 0 ? 1u : acc);
             }
-            col0 += nq * 64u;
         }
-        tc_commit<CG>(empty);
-        if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1;
-        }
-        return true;
-    }
-#pragma unroll
-    for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
-        uint64_t ad, bd;
-        // MN-major: 16 K-rows of 128 B per MMA; 64-element slabs TK*128 B apart.
-        // K-major: advance 32 B (one MMA's K) inside the 128-byte swizzle row.
-        if constexpr (OP == kOpWgrad16)
-            ad = smem_desc_sw128(a_addr + kk * 2048, C::TK * 128, 1024);
-        else
-            ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-        if constexpr (OP == kOpWgrad16 || OP == kOpDgrad16)
-            bd = smem_desc_sw128(b_addr + kk * 2048, C::TK * 128, 1024);
-        else
-            bd = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-        const uint32_t acc_in = (accumulate || kk > 0) ? 1u : 0u;
-        if constexpr (C::kFp8)
-            mma_f8<CG>(d_tmem, ad, bd, P.idesc, acc_in);
-        else
-            mma_f16<CG>(d_tmem, ad, bd, P.idesc, acc_in);
+    } else {
+        (void)steps;
+        mma_x4<CG, C::kFp8>(d_tmem + col0[0], ad[0], bd[0], idesc[0], acc);
     }
     tc_commit<CG>(empty);
     if (++stage == C::kStages) {
@@ -549,13 +639,12 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
     seg_init(plan, cta, cur);
     sk_segment_t seg;
     uint32_t stage = 0, phase = 0;
-    int64_t nseg = 0;
+    int64_t nseg = 0, tau = 0;
     int64_t total_commits = 0;
     bool any = false, ok = true;
     while (true) {
         const bool dp = cur.dp_next >= 0;
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
-        (void)dp;
         const int64_t len = seg.k_end - seg.k_begin;
         const uint32_t acc = static_cast<uint32_t>(nseg % C::kAccBufs);
         const uint32_t acc_phase = static_cast<uint32_t>((nseg / C::kAccBufs) & 1);
@@ -571,11 +660,14 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         }
         tc_fence_after();
         uint32_t d_tmem = tmem_base + acc * TN;
-        for (int64_t j = 0; j < len; ++j) {
+        // The shifted-row wgrad groups K steps into stages as the producer does (same rotation).
+        const int64_t rot = is_wgrad_row(OP) ? segment_rotation(plan, dp, seg, tau) : 0;
+        for (int64_t j = 0, steps = 1; j < len; j += steps) {
+            steps = stage_step_count<OP, CG>(P.conv, seg, rot, j);
             // Block scales: every K step starts a fresh partial.
             const bool accumulate = OP == kOpFp8Block ? false : j > 0;
             if (!mma_stage<OP, TN, CG, ST>(P, cta, seg, ring, bars, ctl, d_tmem, accumulate, stage,
-                                           phase)) {
+                                           phase, steps)) {
                 ok = false;
                 break;
             }
@@ -1629,16 +1721,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         tmem_relinquish<CG>();
     }
     if constexpr (C::kWgRow) {
-        // The rows after the 64 dy rows of every stage, which the shifted reads of a step's last
-        // positions reach, hold zeros. No copy ever writes them (the owner's fold, which reuses the
-        // ring, comes after the CTA's last MMA), so every thread clears a part of them once; the
-        // fence makes the stores visible to the tensor cores, and the barrier below orders them
-        // before the first MMA.
-        constexpr int kDyLoaded = 64 * C::kDyRowBytes;
-        constexpr int kPadBytes = C::kDyBytes - kDyLoaded;
+        // The 16 rows after the dy rows of every stage, which the shifted reads of a stage's last
+        // positions reach, hold zeros. No copy ever writes them (the fold, which reuses the ring,
+        // comes after the CTA's last MMA), so every thread clears a part of them once; the fence
+        // makes the stores visible to the tensor cores, and the barrier below orders them before
+        // the first MMA.
+        const uint32_t pad0 = RowLayout<CG, C::kPhases>(P.conv).dy_off +
+                              (CG == 1 ? 1u : static_cast<uint32_t>(P.conv.stage_steps)) * 64u *
+                                  C::kDyRowBytes;
+        constexpr int kPadBytes = C::kDyPadRows * C::kDyRowBytes;
         for (int i = static_cast<int>(threadIdx.x); i < C::kStages * kPadBytes / 16; i += kThreads) {
             const int st = i / (kPadBytes / 16), b = i - st * (kPadBytes / 16);
-            st_shared_v4(ring + st * C::kStageBytes + C::kABytes + kDyLoaded + b * 16, 0u, 0u, 0u, 0u);
+            st_shared_v4(ring + st * C::kStageBytes + pad0 + b * 16, 0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
     }
@@ -1823,13 +1917,14 @@ static size_t smem_bytes_t() {
 
 // (op, cg, tn, stages) -> the kernel instantiation (the stages follow from cg and tn); the
 // im2col wgrad has no pair form (the host rejects it first); the shifted-row wgrad has a one-CTA
-// 128 x 192 form and a 256 x 192 pair form (10 stages of 21 KB, or 6 of 37 KB with two column
-// phases); the block-scaled fp8 GEMM has a 128 x 128 form (5 stages beside its 32 KB store staging
+// 128 x 192 form with one-step stages (8 of 26 KB, or 5 of 42 KB with two x column phases) and a
+// 256 x 192 pair form with several steps per stage (4 of 48 KB, or 3 of 73 KB); the block-scaled
+// fp8 GEMM has a 128 x 128 form (5 stages beside its 32 KB store staging
 // and its scale ring) and a 256 x 128 pair form (7 stages).
 #define SK_DISPATCH(op, cg, tn, st, fn, ...)                                                \
     ((cg) == 2                                                                              \
-         ? ((op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 2, 10>(__VA_ARGS__)                 \
-            : (op) == kOpWgradRow2 ? fn<kOpWgradRow2, 192, 2, 6>(__VA_ARGS__)                \
+         ? ((op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 2, 4>(__VA_ARGS__)                  \
+            : (op) == kOpWgradRow2 ? fn<kOpWgradRow2, 192, 2, 3>(__VA_ARGS__)                \
             : (tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)             \
                                           : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
                         : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \

@@ -84,7 +84,25 @@ struct ConvGeom {
     // 32 of them). A phase's D columns are fsplit halves, each nq blocks of 64/fsplit filters, one
     // block per shift q = nq - 1 - block.
     int32_t fsplit;
+    // Shifted-row wgrad ring stage: up to stage_steps consecutive K steps of one image. Per column
+    // phase (x_phase_bytes apart) the x rows of the CTA's tap rows for all of them: with
+    // x_shared_box one box of stage_steps * rows_per_step + 1 rows (sh = 1: the lower tap row is
+    // the next row, x_lbo = wseg * 128 bytes on), else one box per tap row (x_lbo = stage_steps *
+    // 8 KB apart); then the dy rows of all of them at dy_off.
+    int32_t stage_steps, x_lbo, x_phase_bytes, dy_off, x_shared_box;
 };
+
+// Shifted-row wgrad ring: stage capacity (bytes) and stage count of each instance (one x column
+// phase, or two). One CTA: deep rings of one-step stages (8 x 26 KB, 5 x 42 KB), for reductions
+// short per CTA, where the ramp and the tail dominate; a CTA pair: several steps per stage
+// (4 x 48 KB, 3 x 73 KB: fewer, larger copies and x rows shared by the steps), for long ones.
+constexpr int wgrow_stage_bytes(int op, int cg) {
+    return cg == 1 ? (op == kOpWgradRow1 ? 26 * 1024 : 42 * 1024)
+                   : (op == kOpWgradRow1 ? 48 * 1024 : 73 * 1024);
+}
+constexpr int wgrow_stages(int op, int cg) {
+    return cg == 1 ? (op == kOpWgradRow1 ? 8 : 5) : (op == kOpWgradRow1 ? 4 : 3);
+}
 
 struct KernelParams {
     CUtensorMap tmap_a;    // GEMM: A [M][K]; fp8: A8 [M][K]; wgrad: dy as [N*Ho*Wo][K];
@@ -154,8 +172,8 @@ struct ZeroParams {
     int64_t pitch, row_bytes, rows;
 };
 
-// cg: 1 = one CTA per 128 x 128 tile (7 stages); 2 = a cluster of two CTAs per 256 x tn tile
-// (GEMMs only): tn 128 with 4 stages, tn 256 with 3. st: stages of the operand ring.
+// cg: 1 = one CTA per tile; 2 = a cluster of two CTAs per 256 x tn tile (GEMMs: tn 128 with 4
+// stages, tn 256 with 3; shifted-row wgrad: tn 192). st: stages of the operand ring.
 // Dynamic shared memory of one CTA of the main kernel.
 size_t main_smem_bytes(int op, int cg, int tn, int st);
 // How many CTAs of the main kernel fit on one SM (0 if the device query fails).

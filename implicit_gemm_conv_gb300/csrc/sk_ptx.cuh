@@ -342,6 +342,31 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
             : "memory");
 }
+// Four MMAs into one accumulator from one asm block, nothing between them: the thread that issues
+// a tcgen05.mma waits while the tensor pipe works through the previous one (measured on GB300:
+// any instruction between two MMAs adds its latency to the pipe's time), so a stage's MMAs are
+// issued back to back once their descriptors are in registers. The first MMA accumulates when
+// `accumulate` is nonzero, the other three always. F8 selects kind::f8f6f4, else kind::f16.
+template <int CG, bool F8>
+__device__ __forceinline__ void mma_x4(uint32_t d_tmem, const uint64_t (&a)[4],
+                                       const uint64_t (&b)[4], uint32_t idesc,
+                                       uint32_t accumulate) {
+#define SK_MMA4_ASM(GROUP, KIND)                                                                \
+    asm volatile(                                                                               \
+        "{\n .reg .pred p, t;\n setp.ne.b32 p, %9, 0;\n setp.eq.b32 t, %9, %9;\n"                \
+        " tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %5, %10, p;\n"                \
+        " tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %2, %6, %10, t;\n"                \
+        " tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %3, %7, %10, t;\n"                \
+        " tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %4, %8, %10, t;\n}\n" ::"r"(d_tmem), \
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),  \
+        "r"(accumulate), "r"(idesc)                                                            \
+        : "memory")
+    if constexpr (CG == 1 && !F8) SK_MMA4_ASM("1", "f16");
+    else if constexpr (CG == 1) SK_MMA4_ASM("1", "f8f6f4");
+    else if constexpr (!F8) SK_MMA4_ASM("2", "f16");
+    else SK_MMA4_ASM("2", "f8f6f4");
+#undef SK_MMA4_ASM
+}
 // Same with 8-bit float inputs (E4M3 / E5M2 per idesc).
 template <int CG>
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

@@ -316,9 +316,14 @@ int sk_version(void);
  * Tile shape for the later calls of the calling thread, planning calls included. (No counterpart on
  * the pages, whose tiles are one workgroup's; this is a GB300 kernel choice.)
  *  SK_TILE_AUTO (the default): SK_TILE_256x256_PAIR for the GEMM and fp8 GEMM when M > 128 and
- *    the output has at least 64 tiles of 256 x 256; SK_TILE_128 otherwise (and always for wgrad,
- *    whose GEMM M per group is K / groups). Few large tiles over a long reduction would be shared
- *    by many CTAs each; the 128 x 128 tile keeps those fixups smaller.
+ *    the output has at least 64 tiles of 256 x 256; SK_TILE_128 otherwise. Few large tiles over a
+ *    long reduction would be shared by many CTAs each; the 128 x 128 tile keeps those fixups
+ *    smaller. Wgrad with 64-channel, 64-filter groups, at most 3 column taps and a column stride
+ *    of 1 or 2 (and output rows of at most 64 positions with the taps' shifts) takes the
+ *    shifted-row view: M = (tap row, channel), N = (column tap, filter), reduction over the
+ *    output rows padded to 64 positions per K step; a 128 x 192 tile on one CTA, or, for three or
+ *    four tap rows over a long reduction (about 128 K steps per SM or more), a 256 x 192 tile on a
+ *    CTA pair. Other wgrad shapes use the 128 x 128 tile of the pages' view.
  *  SK_TILE_128: one CTA computes each 128 x 128 output tile.
  *  SK_TILE_256_PAIR: a cluster of two CTAs on neighbouring SMs computes each 256 x 128 tile with the
  *    two-SM tensor-core instruction; each CTA stages its 128 rows of A and 64 of the 128 rows of B,
@@ -326,8 +331,9 @@ int sk_version(void);
  *  SK_TILE_256x256_PAIR: the same with 256 x 256 tiles; each CTA stages 128 rows of A and 128 of B,
  *    half the bytes per MMA of the 128 x 128 tile.
  *  For the pair tiles the stream-K partition is the same algorithm over the pair tiles, and its CTA
- *  pool `ctas` counts pairs (the default pool is resolved over SMs / 2). GEMM and fp8 GEMM only:
- *  the wgrad call returns -2.
+ *  pool `ctas` counts pairs (the default pool is resolved over SMs / 2). SK_TILE_256_PAIR also
+ *  selects the shifted-row wgrad's 256 x 192 pair tile for the shapes it takes (whatever their
+ *  size); the other wgrad shapes, fprop and dgrad return -2 under the pair tiles.
  * Returns the previous setting, or -2 for an unknown value.
  */
 enum { SK_TILE_AUTO = 0, SK_TILE_128 = 1, SK_TILE_256_PAIR = 2, SK_TILE_256x256_PAIR = 3 };

@@ -173,7 +173,7 @@ def test_strided_dgrad_gates_and_workspace():
     prob = sk.make_problem("fprop", ab_dtype="bf16", c_dtype="bf16", n=8, h=28, w=28, c=128,
                            k=128, r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
     with sk.tile("256x256_pair"):
-        with pytest.raises(sk.SkError, match="GEMMs only"):
+        with pytest.raises(sk.SkError, match="GEMMs and the shifted-row wgrad only"):
             sk.sk_plan(prob, "dp_sk", "linear", 148, 148)
     plan = sk.sk_plan(prob, "dp_sk", "linear", 148, 148)   # auto: the 128x128 tile
     assert (plan.tm, plan.gemm_m, plan.gemm_n, plan.kred) == (128, 8 * 28 * 28, 128, 9 * 128)

@@ -58,7 +58,7 @@ WGRAD = {   # (N, H, W, C, K, R, S, stride, pad, groups)
 
 
 @pytest.mark.parametrize("red", ["linear", "tree"])
-@pytest.mark.parametrize("tile", ["128", "auto"])   # auto: the shifted-row kernel for these shapes
+@pytest.mark.parametrize("tile", ["128", "auto", "256_pair"])   # auto / 256_pair: shifted rows
 @pytest.mark.parametrize("name", list(WGRAD))
 def test_wgrad_bit_identical(name, tile, red):
     N, H, W, C, K, R, S, st, pd, g = WGRAD[name]

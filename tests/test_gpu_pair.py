@@ -169,14 +169,16 @@ def test_pair_agrees_with_single_tile():
     assert (C2 - C1).abs().max().item() <= 1e-3 * max(1.0, C1.abs().max().item())
 
 
-def test_pair_rejects_wgrad():
-    x = torch.zeros((1, 8, 8, 64), dtype=torch.float16, device=DEV)
+def test_pair_rejects_wgrad_outside_the_row_view():
+    """Under the pair tiles a wgrad of 128-channel groups (the pages' view) is refused; the
+    shifted-row shapes run on the row kernel's pair tile (tests/test_gpu_wgrad.py)."""
+    x = torch.zeros((1, 8, 8, 128), dtype=torch.float16, device=DEV)
     dy = torch.zeros((1, 8, 8, 64), dtype=torch.float16, device=DEV)
-    dw = torch.zeros((64, 1, 1, 64), dtype=torch.float32, device=DEV)
+    dw = torch.zeros((64, 1, 1, 128), dtype=torch.float32, device=DEV)
     with pytest.raises(sk.SkError) as e:
         sk.sk_conv2d_wgrad_nhwc(x, dy, dw, 1, 1, (1, 1), (0, 0), 1, streamk="dp_sk",
                                 reduction="linear", ctas=-1)
-    assert e.value.code == -2 and "GEMMs only" in str(e.value)
+    assert e.value.code == -2 and "GEMMs and the shifted-row wgrad only" in str(e.value)
 
 
 @pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("off", "linear"), ("dp_sk", "tree"),

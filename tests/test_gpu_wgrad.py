@@ -1,8 +1,8 @@
 """GPU parity of the implicit-GEMM conv wgrad (sk_conv2d_wgrad_nhwc through the C ABI) against the
 fp64 direct-loop oracle: every launch mode x four reductions on dense, strided and grouped shapes
 with a partial last M tile and a ragged pixel tail, under both wgrad kernels (the automatic tile,
-which takes the shifted-row kernel for 64-channel, 64-filter groups, on a CTA pair for three or
-four tap rows, and the 128 x 128 tile of the pages' GEMM view), shapes that reach the shifted-row
+which takes the shifted-row kernel for 64-channel, 64-filter groups, its CTA-pair form with several
+K steps per ring stage on request, and the 128 x 128 tile of the pages' GEMM view), shapes that reach the shifted-row
 kernel's edges (one to five tap rows; one to three column taps; column stride 2; rows packed several to a K step with a ragged
 last step; the widest rows it takes), and the two named wgrad workloads in full."""
 import numpy as np
@@ -40,13 +40,13 @@ def run(x, dy, K, R, S, stride, pad, groups, out, mode, red, ctas, tile="auto"):
     return dw
 
 
-def row_plan(s):
-    """The automatic tile's plan of this shape."""
+def row_plan(s, tile="auto"):
+    """The plan of this shape under a tile setting."""
     N, H, W, C, K, R, S = s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"]
     prob = sk.make_problem("wgrad", ab_dtype=s["dt"], c_dtype="f32", n=N, h=H, w=W, c=C, k=K,
                            r=R, s=S, stride_h=s["stride"][0], stride_w=s["stride"][1],
                            pad_h=s["pad"][0], pad_w=s["pad"][1], groups=s["groups"])
-    with sk.tile("auto"):
+    with sk.tile(tile):
         return sk.sk_plan(prob, "dp_sk", "atomic", 7, 148)
 
 
@@ -114,8 +114,9 @@ def test_row_kernel_takes_its_shapes():
     too wide for a K step fall back too."""
     for name, s in ROW_SHAPES.items():
         assert row_kernel(s), name
-        # three or four tap rows: one 256-row tile on a CTA pair
-        assert row_plan(s).tm == (256 if s["R"] in (3, 4) else 128), name
+        # at these sizes the one-CTA 128 x 192 tile; the pair tile on request
+        assert row_plan(s).tm == 128, name
+        assert row_plan(s, "256_pair").tm == 256, name
     assert row_kernel(SHAPES["dense_3x3"]) and row_kernel(SHAPES["grouped_s2"])
     assert not row_kernel(SHAPES["pointwise"]) and not row_kernel(SHAPES["asym"])
     too_wide = dict(ROW_SHAPES["row_wide"], W=63)
@@ -124,12 +125,16 @@ def test_row_kernel_takes_its_shapes():
 
 @pytest.mark.parametrize("red", ["linear", "tree", "atomic", "workspace"])
 @pytest.mark.parametrize("mode", ["dp_sk", "persistent", "off", "splitk", "hybrid"])
-@pytest.mark.parametrize("tile", ["auto", "128"])
+@pytest.mark.parametrize("tile", ["auto", "128", "256_pair"])
 @pytest.mark.parametrize("name", list(ALL_SHAPES))
 def test_wgrad_shapes(name, tile, mode, red):
+    """auto: the one-CTA shifted-row kernel on these sizes; 256_pair: its CTA-pair form (several
+    K steps per ring stage); 128: the pages' view."""
     s = ALL_SHAPES[name]
     if tile == "128" and name in ROW_SHAPES and mode not in ("dp_sk", "off"):
         pytest.skip("the 128 x 128 tile's modes are covered on the first four shapes")
+    if tile == "256_pair" and not row_kernel(s):
+        pytest.skip("the pair tile serves the shifted-row view only")
     x, dy, ref = case(s["dt"], s["N"], s["H"], s["W"], s["C"], s["K"], s["R"], s["S"], s["stride"],
                       s["pad"], s["groups"])
     Ho, Wo = conv_out(s["H"], s["R"], s["stride"][0], s["pad"][0]), \

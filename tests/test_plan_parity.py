@@ -224,9 +224,13 @@ def test_pair_tile_setting():
     with sk.tile("256_pair"):
         assert (sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tm,
                 sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn) == (256, 128)
+        # a shifted-row wgrad shape: its 256 x 192 pair tile; another wgrad shape: refused
         w, _ = wgrad(32, 56, 56, 64, 64, 3, 3, 1, 1, 1)
-        with pytest.raises(sk.SkError, match="GEMMs only"):
-            sk.sk_plan(w, "dp_sk", "linear", -1, 148)
+        assert (sk.sk_plan(w, "dp_sk", "linear", -1, 148).tm,
+                sk.sk_plan(w, "dp_sk", "linear", -1, 148).tn) == (256, 192)
+        w2, _ = wgrad(2, 9, 9, 128, 192, 1, 1, 1, 0, 1)
+        with pytest.raises(sk.SkError, match="GEMMs and the shifted-row wgrad only"):
+            sk.sk_plan(w2, "dp_sk", "linear", -1, 148)
     with sk.tile("256x256_pair"):
         assert sk.sk_plan(prob, "dp_sk", "linear", 148, 148).tn == 256
     with pytest.raises(sk.SkError, match="tile setting"):
@@ -277,12 +281,12 @@ def test_block_scale_tile_setting():
 
 
 # ---- shifted-row wgrad (automatic tile, 64-channel and 64-filter groups): GEMM view
-# M = (tap row, channel) in 128-row tiles of two tap rows (three or four tap rows: one 256-row tile
-# on a CTA pair), N = (column tap, filter) in one 192-wide tile, reduction over the padded
-# positions: 64 per K step, `64 / wseg` output rows of `wseg` positions (the power of two
-# >= Wo + shifts), rows counted per image over Ho rounded up.
+# M = (tap row, channel) in 128-row tiles of two tap rows (on request, 256-row tiles of four on a
+# CTA pair), N = (column tap, filter) in one 192-wide tile, reduction over the padded positions: 64
+# per K step, `64 / wseg` output rows of `wseg` positions (the power of two >= Wo + shifts), rows
+# counted per image over Ho rounded up.
 
-def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16"):
+def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16", pair=False):
     sh, sw = stride
     ph, pw = pad
     prob = sk.make_problem("wgrad", ab_dtype=dt, c_dtype="f32", n=N, h=H, w=W, c=C, k=K, r=R,
@@ -297,7 +301,7 @@ def wgrad_row(N, H, W, C, K, R, S, stride, pad, groups, dt="bf16"):
     if rows == 0:   # rows too wide for one K step: not this view
         return prob, None
     ho_pad = -(-Ho // rows) * rows
-    tm = 256 if R in (3, 4) else 128
+    tm = 256 if pair else 128
     kw = dict(tiles_m=-(-(R * 64) // tm), tiles_n=1, groups=groups, kred=N * ho_pad * wseg,
               tm=tm, tn=192, tk=64, cluster=tm // 128)
     return prob, kw
@@ -322,22 +326,56 @@ def test_row_wgrad_plans(name, pk, ctas, mode, red):
     assert (cp.tm, cp.tn, cp.tk) == (kw["tm"], 192, 64)
 
 
+ROW_PAIR_NAMED = [
+    ("wgrad 32x56x56x64 pair", wgrad_row(32, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), 1, pair=True), -1),
+    ("wgrad 64x28x28x256 g4 s2 pair",
+     wgrad_row(64, 28, 28, 256, 256, 3, 3, (2, 2), (1, 1), 4, pair=True), -1),
+    ("wgrad 2x9x13 r5 s3 pair", wgrad_row(2, 9, 13, 64, 64, 5, 3, (1, 1), (2, 1), 1, pair=True), 7),
+]
+
+
+@pytest.mark.parametrize("name,pk,ctas", ROW_PAIR_NAMED, ids=[n[0] for n in ROW_PAIR_NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_row_wgrad_pair_plans(name, pk, ctas, mode, red):
+    prob, kw = pk
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    with sk.tile("256_pair"):
+        cp = compare(prob, kw, mode, red, ctas, num_sms=152, check_ctas=big)
+    assert (cp.tm, cp.tn, cp.tk) == (256, 192, 64)
+
+
 def test_row_wgrad_worked_vectors():
-    """32x56x56, 64 -> 64, 3x3: one 256 x 192 pair tile (tap rows 0-2), 32*56 K steps of one
-    56-column row each (64 positions); 74 CTA pairs: 1792 steps, 24 each and one more for the
-    first 16. Grouped stride 2 (4 groups of 64): 4 tiles, 14 output columns + 1 shift ->
-    16-position rows, 4 rows per step, 14 rows per image padded to 16: 64*16/4 = 256 steps per
-    tile; 1024 steps on 74 pairs: 13 each and one more for the first 62. Five tap rows stay on the
-    one-CTA 128 x 192 tile (three tiles)."""
+    """32x56x56, 64 -> 64, 3x3: two tiles (tap rows {0,1} and {2}), 32*56 K steps of one
+    56-column row each (64 positions); 148 CTAs: 3584 steps, 24 each and one more for the first
+    32. Grouped stride 2 (4 groups of 64): 8 tiles, 14 output columns + 1 shift -> 16-position
+    rows, 4 rows per step, 14 rows per image padded to 16: 64*16/4 = 256 steps per tile. On the
+    CTA pair (on request): one 256 x 192 tile (tap rows 0-2) of 1792 steps on 74 pairs, 24 each
+    and one more for the first 16; grouped: 4 tiles, 1024 steps, 13 each and one more for the
+    first 62."""
     with sk.tile("auto"):
+        cp = sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", 148, 148)
+        assert (cp.tm, cp.tiles, cp.iters_per_tile, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
+                cp.extra_iters, cp.grid) == (128, 2, 1792, 2, 3584, 24, 32, 148)
+        cp = sk.sk_plan(ROW_NAMED[1][1][0], "dp_sk", "atomic", 148, 148)
+        assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.iters_per_sk_cta, cp.extra_iters) == \
+            (8, 256, 148, 13, 124)
+    with sk.tile("256_pair"):
         cp = sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", 74, 148)
         assert (cp.tm, cp.tiles, cp.iters_per_tile, cp.sk_tiles, cp.sk_iters, cp.iters_per_sk_cta,
                 cp.extra_iters, cp.grid) == (256, 1, 1792, 1, 1792, 24, 16, 74)
         cp = sk.sk_plan(ROW_NAMED[1][1][0], "dp_sk", "atomic", 74, 148)
         assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.iters_per_sk_cta, cp.extra_iters) == \
             (4, 256, 74, 13, 62)
-        cp = sk.sk_plan(ROW_NAMED[2][1][0], "dp_sk", "atomic", 7, 148)
-        assert (cp.tm, cp.tiles_m) == (128, 3)
+
+
+def test_row_wgrad_pair_only_for_long_reductions():
+    """The automatic tile takes the CTA pair for three tap rows once the reduction is long
+    (about 128 K steps per SM): 32x56x56 stays on one CTA, 192x56x56 goes to the pair."""
+    with sk.tile("auto"):
+        assert sk.sk_plan(ROW_NAMED[0][1][0], "dp_sk", "atomic", -1, 148).tm == 128
+        big = wgrad_row(192, 56, 56, 64, 64, 3, 3, (1, 1), (1, 1), 1)[0]
+        assert sk.sk_plan(big, "dp_sk", "atomic", -1, 148).tm == 256
 
 
 def test_row_wgrad_sweep():
