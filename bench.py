@@ -347,7 +347,12 @@ def extra_measurements(torch, sk, dev, flush, stream, peaks, cpu=True):
     ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def tiles(w):
-        return [("128", w.pool), ("256x256_pair", w.pool // 2 if w.pool > 0 else -1)]
+        # the automatic tile too where it is neither of the other two (the deep-ring pair of few
+        # tiles over a long reduction)
+        t = [("128", w.pool), ("256x256_pair", w.pool // 2 if w.pool > 0 else -1)]
+        if w.op == "gemm" and w.K // 64 >= 512 and -(-w.M // 256) * -(-w.N // 256) < 64:
+            t.append(("auto", w.pool // 2 if w.pool > 0 else -1))
+        return t
 
     def tiled(tile, f):
         def call():

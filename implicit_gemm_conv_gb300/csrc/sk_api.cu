@@ -272,6 +272,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
 constexpr int64_t kAutoPairMinTiles = 64;   // SK_TILE_AUTO: pair tiles needed for the pair kernel
 constexpr int64_t kSpreadMinContributors = 8;   // linear / tree: contributors for the spread fold
 constexpr int64_t kRowPairMinSteps = 128 * 148;  // shifted-row wgrad: K steps for the pair kernel
+constexpr int64_t kAutoLongReductionSteps = 512;  // SK_TILE_AUTO: K steps for the deep-ring pair
 
 // The kernel shape for a problem under the calling thread's tile setting: cg CTAs per logical CTA
 // (1, or 2 for a CTA pair) and the tile's N; the tile's M is 128 * cg.
@@ -326,6 +327,13 @@ int tile_cfg(const View& v, TileCfg& t) {
             if ((v.op_kind == sk::kOpGemm16 || v.op_kind == sk::kOpFp8) && v.gemm_m > sk::kTileM &&
                 pair_tiles >= kAutoPairMinTiles)
                 t = TileCfg{2, 256, 3};
+            // Few tiles over a long 16-bit reduction (the 512 x 512 x 65536 GEMM): each SM takes in
+            // the operands of its share of the MMAs through its copy engine, at about 115 GB/s, so
+            // the 256 x 256 pair tile's half bytes per FLOP matter most; one CTA per SM with a
+            // 6-stage ring keeps its copies in flight.
+            else if (v.op_kind == sk::kOpGemm16 && v.gemm_m > sk::kTileM && v.gemm_n > 128 &&
+                     v.kred / 64 >= kAutoLongReductionSteps)
+                t = TileCfg{2, 256, 6};
             return SK_OK;
         }
     }

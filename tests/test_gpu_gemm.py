@@ -161,3 +161,27 @@ def test_gemm_strided_16bit_output(mode, red):
     sk.sk_device_status()
     check_parity(C, ref, "bf16", 520, what=f"strided 16-bit C {mode}/{red}")
     assert torch.isnan(Cbig[:, N:].float()).all(), "wrote outside the [M, N] window"
+
+
+# ---- the automatic tile's deep-ring 256x256 CTA pair for few tiles over a long 16-bit reduction
+
+@pytest.mark.parametrize("mode,red", [("dp_sk", "linear"), ("dp_sk", "tree"), ("dp_sk", "workspace"),
+                                      ("splitk", "workspace"), ("persistent", "linear")])
+def test_gemm_512x512x65536_auto_pair_sampled(mode, red):
+    with sk.tile("auto"):
+        prob = sk.make_problem("gemm", ab_dtype="bf16", c_dtype="bf16", M=512, N=512, K=65536)
+        assert (sk.sk_plan(prob, mode, red, 74).tm, sk.sk_plan(prob, mode, red, 74).tn) == (256, 256)
+        _sampled("bf16", 512, 512, 65536, "n01", mode, red, 74)
+
+
+@pytest.mark.parametrize("red", ["linear", "atomic", "workspace"])
+def test_gemm_ragged_long_k_auto_pair(red):
+    """Partial M and N pair tiles and a ragged K tail (K = 33000) on the deep-ring pair."""
+    M, N, K = 300, 392, 33000
+    with sk.tile("auto"):
+        prob = sk.make_problem("gemm", ab_dtype="bf16", c_dtype="bf16", M=M, N=N, K=K)
+        assert sk.sk_plan(prob, "dp_sk", red, 5).tm == 256
+        A, B, ref = ref_full("bf16", M, N, K, "u11", 21)
+        out = "f32" if red == "atomic" else "bf16"
+        C = run_gemm(A, B, out, "dp_sk", red, 5)
+    check_parity(C, ref, out, K, what=f"ragged long-K pair {red}")

@@ -212,10 +212,12 @@ def test_pair_tile_random_sweep(tile, tn):
 
 def test_pair_tile_setting():
     prob, _ = gemm(3840, 4096, 4096, "bf16")
-    with sk.tile("auto"):   # 240 pair tiles: the pair; 4 pair tiles or 128 rows: one CTA per tile
+    with sk.tile("auto"):   # 240 pair tiles: the pair; few pair tiles or 128 rows: one CTA per tile
         assert (sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tm,
                 sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tn) == (256, 256)
-        assert sk.sk_plan(gemm(512, 512, 65536, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
+        # 4 pair tiles over 1024 K steps: the deep-ring pair (one CTA per SM, 6 stages)
+        assert sk.sk_plan(gemm(512, 512, 65536, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 256
+        assert sk.sk_plan(gemm(512, 512, 4096, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
         assert sk.sk_plan(gemm(128, 8192, 4096, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
         assert sk.sk_plan(gemm(2048, 2048, 4096, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 256
         assert sk.sk_plan(gemm(2048, 1792, 4096, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 128
