@@ -379,8 +379,12 @@ def extra_measurements(torch, sk, dev, flush, stream, peaks, cpu=True):
                                                           sk.sk_gemm_rcr(A, B, Cx, mode, red, pool, ws=ws))
         elif w.op in ("fprop", "dgrad"):
             call, _ = conv_call(torch, sk, w, dev, ws, host)
-            for mode, red in dict.fromkeys(sk_variants + comparators):
-                calls[f"128:{mode}/{red}"] = lambda mode=mode, red=red: call(mode, red, w.pool)
+            # fprop: the automatic tile (the shifted-row kernel where the layer fits it) and the
+            # pages' im2col view on the 128 x 128 tile
+            for tile in (("auto", "128") if w.op == "fprop" else ("128",)):
+                for mode, red in dict.fromkeys(sk_variants + comparators):
+                    calls[f"{tile}:{mode}/{red}"] = tiled(tile, lambda mode=mode, red=red:
+                                                          call(mode, red, w.pool))
         elif w.op == "wgrad":
             c = w.conv
             x, dy = wgrad_operands(c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
@@ -434,10 +438,14 @@ def extra_measurements(torch, sk, dev, flush, stream, peaks, cpu=True):
         v = res["variants"]
         pick = lambda pred: min((k for k in v if pred(k)), key=lambda k: v[k]["step_med_us"],
                                 default=None)
-        best = {"stream_k": pick(lambda k: k.split(":")[1].split("/")[0] not in ("off", "splitk")),
+        mode_of = lambda k: k.split(":")[1].split("/")[0]
+        best = {"stream_k": pick(lambda k: mode_of(k) in ("dp_sk", "persistent", "hybrid")),
+                "auto": pick(lambda k: mode_of(k) == "auto"),
                 "dp_only": pick(lambda k: ":off/" in k), "split_k": pick(lambda k: ":splitk/" in k)}
         res["best"] = {kind: ({"variant": k, **v[k]} if k else None) for kind, k in best.items()}
-        res["roofline"] = roofline_of(w, peaks, v[best["stream_k"]]["step_med_us"])
+        # the roofline of the best schedule the library offers (stream-K or the automatic choice)
+        lib_best = pick(lambda k: mode_of(k) not in ("off", "splitk"))
+        res["roofline"] = roofline_of(w, peaks, v[lib_best]["step_med_us"])
         if cpu:
             res["cpu_baseline"] = cpu_baseline_workload(w, host)
         out[name] = res

@@ -193,6 +193,20 @@ bool wgrad_row_geom(const sk_problem& p, RowGeom& g) {
 
 int problem_view_pages(const sk_problem& p, View& v);
 
+// The shifted-row forward convolution serves stride 1, one group of 64 channels and 64 filters, at
+// most 3 x 3 taps and output rows of at most 64 positions with the column taps' overrun
+// (Wo + S - 1 <= 64): a tile is two output rows of 64 positions (rows counted per image over Ho
+// rounded up to even), its reduction the taps (64 channels each).
+bool fprop_row_geom(const sk_problem& p, int64_t& ho, int64_t& wo, int64_t& ho_pad) {
+    if (p.op != SK_OP_FPROP || p.groups != 1 || p.c != 64 || p.k != 64) return false;
+    if (p.stride_h != 1 || p.stride_w != 1 || p.r < 1 || p.r > 3 || p.s < 1 || p.s > 3) return false;
+    ho = p.h + 2 * p.pad_h - p.r + 1;
+    wo = p.w + 2 * p.pad_w - p.s + 1;
+    if (ho < 1 || wo < 1 || wo + p.s - 1 > 64) return false;
+    ho_pad = sk::round_up(ho, 2);
+    return p.n * ho_pad * 64 < (int64_t(1) << 31);
+}
+
 // The GEMM view of a problem under the calling thread's tile setting. Wgrad: the pages' view
 // (M = K/G filters, N = R*S*C/G, reduction over N*Ho*Wo output pixels), or with the automatic
 // tile, where it fits, the shifted-row view: M = (tap row r, channel) = R*64 in 128-row tiles (two
@@ -201,6 +215,14 @@ int problem_view_pages(const sk_problem& p, View& v);
 int problem_view(const sk_problem& p, View& v) {
     int rc = problem_view_pages(p, v);
     if (rc) return rc;
+    int64_t fho, fwo, fho_pad;
+    if (v.op_kind == sk::kOpFprop16 && g_tile == SK_TILE_AUTO && fprop_row_geom(p, fho, fwo, fho_pad)) {
+        v.gemm_m = p.n * fho_pad * 64;
+        v.gemm_n = 64;
+        v.kred = p.r * p.s * 64;
+        v.op_kind = sk::kOpFpropRow;
+        return SK_OK;
+    }
     RowGeom g;
     if (v.op_kind == sk::kOpWgrad16 && (g_tile == SK_TILE_AUTO || g_tile == SK_TILE_256_PAIR) &&
         wgrad_row_geom(p, g)) {
@@ -267,7 +289,7 @@ int problem_view_pages(const sk_problem& p, View& v) {
 }
 
 int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
-                        int ctas_per_sm, sk_plan_t& p);
+                        int ctas_per_sm, sk_plan_t& p, bool all_dp = false);
 
 constexpr int64_t kAutoPairMinTiles = 64;   // SK_TILE_AUTO: pair tiles needed for the pair kernel
 constexpr int64_t kSpreadMinContributors = 8;   // linear / tree: contributors for the spread fold
@@ -280,6 +302,10 @@ struct TileCfg {
     int cg, tn, st;   // CTAs per logical CTA, tile N, operand-ring stages
 };
 int tile_cfg(const View& v, TileCfg& t) {
+    if (v.op_kind == sk::kOpFpropRow) {   // 128 x 64 tile, 4 stages of 33 KB + the 72 KB filter
+        t = TileCfg{1, 64, 4};
+        return SK_OK;
+    }
     if (sk::is_wgrad_row(v.op_kind)) {
         // Three or four tap rows (M = 192 or 256) over a long reduction (at least
         // kRowPairMinSteps K steps of 128-row tiles in all, about 128 per SM): a 256 x 192 tile
@@ -357,11 +383,21 @@ int build_plan(const sk_problem& prob, int mode, int reduction, int ctas, int nu
     if (rc) return rc;
     if (p.tiles < p.pool && p.tiles * p.iters_per_tile >= kAutoMinIterations && p.sk_ctas > 0)
         return SK_OK;
+    // The shifted-row fprop keeps its filter resident: with more tiles than CTAs each CTA loads
+    // it once and runs its tiles in turn (persistent) instead of one CTA per tile. Its tiles are
+    // short (one K step per tap), so a stream-K wave's fixups cost more than the last wave's idle
+    // CTAs: every tile stays data-parallel.
+    View v;
+    if (p.tiles > p.pool && problem_view(prob, v) == SK_OK && v.op_kind == sk::kOpFpropRow)
+        return build_plan_resolved(prob, SK_PERSISTENT, reduction, ctas, num_sms, ctas_per_sm, p,
+                                   true);
     return build_plan_resolved(prob, SK_SPLITK, reduction, ctas, num_sms, ctas_per_sm, p);
 }
 
+// all_dp: no stream-K region whatever the tile count (SK_PERSISTENT: every CTA runs tiles
+// cta, cta + pool, ...).
 int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int ctas, int num_sms,
-                        int ctas_per_sm, sk_plan_t& p) {
+                        int ctas_per_sm, sk_plan_t& p, bool all_dp) {
     if (mode < SK_OFF || mode > SK_HYBRID || mode == SK_AUTO)
         return fail(SK_ERR_UNSUPPORTED, "unknown streamk mode %d", mode);
     if (reduction < SK_LINEAR || reduction > SK_WORKSPACE)
@@ -414,7 +450,7 @@ int build_plan_resolved(const sk_problem& prob, int mode, int reduction, int cta
         if (mode == SK_HYBRID && T >= P && p.sk_tiles > 0) p.sk_tiles += P;   // one wave more
         p.dp_tiles = T - p.sk_tiles;
         p.sk_iters = p.sk_tiles * I;
-        if (p.sk_tiles == 0 || p.sk_iters < P) {   // too few iterations for the pool: all-DP
+        if (all_dp || p.sk_tiles == 0 || p.sk_iters < P) {   // too few iterations for the pool: all-DP
             p.sk_tiles = 0;
             p.dp_tiles = T;
             p.sk_iters = 0;
@@ -636,11 +672,17 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             z.row_bytes = static_cast<int64_t>(out_row_bytes);
             z.rows = static_cast<int64_t>(out_rows);
         }
-        int le = sk::launch_zero(z, stream);
-        if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "zeroing kernel launch"); break; }
-        if (g_timing.on) ++g_timing.all_launches;
+        // Nothing to zero when no tile is shared and no ticket is drawn (the data-parallel plans):
+        // the main kernel then runs alone, without overlapping what came before it.
+        const bool zero = plan.shared_tiles > 0 || kp.ticket || z.out != nullptr;
+        int le = 0;
+        if (zero) {
+            le = sk::launch_zero(z, stream);
+            if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "zeroing kernel launch"); break; }
+            if (g_timing.on) ++g_timing.all_launches;
+        }
         const int tslot = timing_start(stream);
-        le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, tslot < 0, stream);
+        le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, zero && tslot < 0, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -1347,9 +1389,107 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
 
     sk::RowMap identity;
     memset(&identity, 0, sizeof(identity));
-    if (fprop)
+    if (fprop) {
+        sk_problem prob;
+        memset(&prob, 0, sizeof(prob));
+        prob.op = op;
+        prob.ab_dtype = in_dtype;
+        prob.c_dtype = out_dtype;
+        prob.n = N; prob.h = H; prob.w = W; prob.c = C; prob.k = K; prob.r = R; prob.s = S;
+        prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
+        prob.groups = groups;
+        int64_t fho, fwo, fho_pad;
+        if (g_tile == SK_TILE_AUTO && fprop_row_geom(prob, fho, fwo, fho_pad)) {
+            // Shifted rows. A: x boxes of 64 channels x 64 positions (from column -pw) x R + 1
+            // rows (from row ho0 - ph); outside the image reads zeros. B: the filter as
+            // [K][R*S*C], one 64 x 64 box per tap.
+            sk::KernelParams kp;
+            memset(&kp, 0, sizeof(kp));
+            {
+                const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+                const cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2),
+                                               (cuuint64_t)(H * W * C * 2)};
+                const cuuint32_t box[4] = {64, 64, (cuuint32_t)(R + 1), 1};
+                const cuuint32_t estr[4] = {1, 1, 1, 1};
+                CUresult r = g_encode_tiled(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                            const_cast<void*>(act), dims, strides, box, estr,
+                                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_128B,
+                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS)
+                    return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
+            }
+            // The filter as one box: [tap][filter][channel] over w[K][R][S][C] (strides: a
+            // filter RSC * 2 bytes, a tap 128 bytes), else one [K][RSC] box per tap.
+            const int64_t RSC = R * S * C;
+            {
+                const cuuint64_t dims[3] = {64, 64, (cuuint64_t)(R * S)};
+                const cuuint64_t strides[2] = {(cuuint64_t)(RSC * 2), 128};
+                const cuuint32_t box[3] = {64, 64, (cuuint32_t)(R * S)};
+                const cuuint32_t estr[3] = {1, 1, 1};
+                kp.conv.filter_box =
+                    g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                                   const_cast<void*>(wt), dims, strides, box, estr,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            }
+            if (!kp.conv.filter_box) {
+                rc = encode_2d(&kp.tmap_b, wt, 2, RSC, K, RSC * 2, 64, 64);
+                if (rc) return rc;
+            }
+            kp.c = out;
+            kp.ldc = K;
+            kp.c_dtype = out_dtype;
+            // A 16-bit y leaves through TMA tile stores: y as [N][Ho][Wo][64], boxes of 32
+            // positions x 64 filters; the map clips the positions past Wo.
+            if (out_dtype != SK_F32) {
+                const cuuint64_t dims[4] = {64, (cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)N};
+                const cuuint64_t strides[3] = {128, (cuuint64_t)(Wo * 128),
+                                               (cuuint64_t)(Ho * Wo * 128)};
+                const cuuint32_t box[4] = {64, 32, 1, 1};
+                const cuuint32_t estr[4] = {1, 1, 1, 1};
+                CUresult r = g_encode_tiled(&kp.tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, out,
+                                            dims, strides, box, estr,
+                                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_128B,
+                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS)
+                    return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(y) failed (%d)", (int)r);
+                kp.c_tma = 1;
+            }
+            const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+            kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, 64);
+            kp.conv.ph = pad_h;
+            kp.conv.pw = pad_w;
+            kp.conv.sh = 1;
+            kp.conv.sw = 1;
+            kp.conv.R = static_cast<int32_t>(R);
+            kp.conv.S = static_cast<int32_t>(S);
+            kp.conv.Cg = 64;
+            kp.conv.Kg = 64;
+            kp.conv.Cw = 64;
+            kp.conv.ho = static_cast<int32_t>(fho);
+            kp.conv.ho_pad = static_cast<int32_t>(fho_pad);
+            // Tile rows are (image, row over ho_pad, position over 64): output pixel when the
+            // row is below Ho and the position below Wo.
+            kp.conv.rows.on = 1;
+            kp.conv.rows.HoWo = fho_pad * 64;
+            kp.conv.rows.Wo = 64;
+            kp.conv.rows.Hd = static_cast<int32_t>(Ho);
+            kp.conv.rows.Wd = static_cast<int32_t>(Wo);
+            kp.conv.rows.dsh = 1;
+            kp.conv.rows.dsw = 1;
+            kp.conv.rows.vh = static_cast<int32_t>(Ho);
+            kp.conv.rows.vw = static_cast<int32_t>(Wo);
+            return run(prob, streamk, reduction, ctas, kp, out, K * cs, N * Ho * Wo, K * cs, ws,
+                       ws_bytes, st);
+        }
         return launch(H, W, Ho, Wo, stride_h, stride_w, pad_h, pad_w, static_cast<int>(R),
                       static_cast<int>(S), 0, 0, identity, false);
+    }
     if (!phased)   // stride 1: a stride-1 convolution of dy with the flipped filter, padding R-1-p
         return launch(Ho, Wo, H, W, 1, 1, static_cast<int>(R - 1 - pad_h),
                       static_cast<int>(S - 1 - pad_w), static_cast<int>(R), static_cast<int>(S), 0,

@@ -129,8 +129,11 @@ struct Cfg {
     static_assert(CG == 1 || OP == kOpGemm16 || OP == kOpFp8 || OP == kOpFp8Block ||
                       is_wgrad_row(OP),
                   "CTA pairs serve the GEMMs and the shifted-row wgrad");
-    static_assert(CG == 2 || TN == 128 || (is_wgrad_row(OP) && TN == 192),
-                  "one CTA computes 128 x 128 tiles (shifted-row wgrad: 128 x 192)");
+    static_assert(CG == 2 || TN == 128 || (is_wgrad_row(OP) && TN == 192) ||
+                      (OP == kOpFpropRow && TN == 64),
+                  "one CTA computes 128 x 128 tiles (shifted-row wgrad: 128 x 192; shifted-row "
+                  "fprop: 128 x 64)");
+    static constexpr bool kFpRow = OP == kOpFpropRow;
     static constexpr bool kFp8 = OP == kOpFp8 || OP == kOpFp8Block;
     static constexpr bool kWgRow = is_wgrad_row(OP);
     static constexpr int kPhases = OP == kOpWgradRow2 ? 2 : 1;   // x column phases (W stride)
@@ -145,17 +148,24 @@ struct Cfg {
     // CTA of a pair) and 16 zero rows for the shifts' overrun.
     static constexpr int kDyRowBytes = 128 / CG;
     static constexpr int kDyPadRows = 16;
-    static constexpr int kABytes = kWgRow ? wgrow_stage_bytes(OP, CG) : kTileM * 128;   // 16 KB
-    static constexpr int kBBytes = kWgRow ? 0 : kBRows * 128;
+    // Shifted-row fprop stage: the x box of a tile's two output rows for every tap row (at most
+    // four rows of 64 positions x 64 channels, 32 KB) and 1 KB for the column taps' overrun; its
+    // filter (at most 9 taps of 64 x 64) stays in its own 72 KB region for the whole kernel.
+    static constexpr int kABytes = kWgRow ? wgrow_stage_bytes(OP, CG)
+                                   : kFpRow ? 33 * 1024 : kTileM * 128;   // 16 KB
+    static constexpr int kBBytes = (kWgRow || kFpRow) ? 0 : kBRows * 128;
+    static constexpr int kResBytes = kFpRow ? 9 * 8192 : 0;
     static constexpr int kStageBytes = kABytes + kBBytes;
     // ST stages in the ring; two CTAs share an SM when the ring is at most 96 KB.
     static constexpr int kStages = ST;
     static constexpr int kMinBlocks = ST * kStageBytes <= 96 * 1024 ? 2 : 1;
     // fp32 accumulator buffers in TMEM: two (the epilogue of one segment overlaps the MMAs of the
-    // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one.
+    // next), except for the 256-column accumulator of a 256 x 256 pair, which keeps one, and the
+    // shifted-row fprop, whose tiles take about as long to store as to compute: four of 64
+    // columns, so that the MMAs never wait for an epilogue.
     // Block-scaled fp8: the two buffers take one K step's partial each (the MMAs run up to two steps
     // ahead of the epilogue's promotion); the last step's buffer then holds the segment's sum.
-    static constexpr int kAccBufs = (TN == 256 || kWgRow) ? 1 : 2;
+    static constexpr int kAccBufs = (TN == 256 || kWgRow) ? 1 : kFpRow ? 4 : 2;
     static constexpr int kTmemCols = kAccBufs * TN;
     // The allocation is a power of two of at least 32 columns.
     static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64
@@ -182,17 +192,21 @@ struct Cfg {
     // a CTA's last, leaves that way while the producer already fills the ring for the next one.
     // The block-scaled fp8 pair keeps one too (its ring is deep enough without the space).
     // A 3-stage one-CTA ring (two CTAs per SM) has none: its last tile leaves through the ring.
+    // The shifted-row fprop stages its 128 x 64 tiles (16 KB) the same way.
     static constexpr int kEpiStageBytes =
-        ((CG == 1 && OP != kOpWgrad16 && !kWgRow && ST > 3) || OP == kOpFp8Block) ? kTileM * TN * 2
-                                                                                   : 0;
+        ((CG == 1 && OP != kOpWgrad16 && !kWgRow && ST > 3) || OP == kOpFp8Block)
+            ? kTileM * TN * 2
+            : 0;
     static constexpr int kCtlBytes = 64;                         // SmemCtl, 1024-aligned
-    static constexpr int kBarBytes = (kBarFold + kFoldBufs) * 8;
+    static constexpr int kBarRes = kBarFold + kFoldBufs;   // shifted-row fprop: filter loaded
+    static constexpr int kBarBytes = (kBarRes + 1) * 8;
     // Block-scaled fp8: each epilogue thread's ring of block scales (A and B) copied kScaleAhead
     // K steps ahead of their use, so that their global-memory latency stays off the per-step path.
     static constexpr int kScaleAhead = OP == kOpFp8Block ? 8 : 0;
     static constexpr int kScaleBytes = kScaleAhead * kEpiThreads * 2 * 4;
     static constexpr size_t kSmem =
-        1024 + size_t(kRingBytes) + kEpiStageBytes + kScaleBytes + kCtlBytes + kBarBytes;
+        1024 + size_t(kRingBytes) + kEpiStageBytes + kScaleBytes + kResBytes + kCtlBytes +
+        kBarBytes;
 };
 
 // Per-CTA control words. The block starts right after the operand ring, so tmem_base (written by
@@ -281,7 +295,20 @@ __device__ __forceinline__ void issue_loads(const KernelParams& P, int64_t g, in
                                             uint32_t bar, const WgradSlabs<TN>& sl, uint32_t rank,
                                             const PixelStart& ps) {
     using C = Cfg<OP, TN, CG, ST>;
-    if constexpr (folds_groups_into_columns(OP)) {
+    if constexpr (OP == kOpFpropRow) {
+        // Tile mt: output rows 2*mt and 2*mt+1 of the images' rows counted over ho_pad (even), 64
+        // positions each from column 0. One box: the x rows ho0 - ph ... ho0 - ph + R of image n,
+        // 64 positions from column -pw (outside the image reads zeros), 64 channels.
+        const ConvGeom& cg = P.conv;
+        const uint32_t t0 = 2u * static_cast<uint32_t>(mt);
+        const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
+        const uint32_t n_img = t0 / hp;
+        const int32_t ho0 = static_cast<int32_t>(t0 - n_img * hp);
+        tma_load_4d(a_dst, &P.tmap_a, bar, static_cast<int32_t>(g) * cg.Cg, -cg.pw, ho0 - cg.ph,
+                    static_cast<int32_t>(n_img));
+        (void)k;
+        (void)b_dst;
+    } else if constexpr (folds_groups_into_columns(OP)) {
         // Reduction index k*64 = (tap, channel block) with the channels fastest.
         const ConvGeom& cg = P.conv;
         const int32_t kk = static_cast<int32_t>(k) * C::TK;
@@ -401,7 +428,12 @@ __device__ __forceinline__ int64_t segment_rotation(const sk_plan_t& plan, bool 
 template <int OP, int CG>
 __device__ __forceinline__ int64_t stage_step_count(const ConvGeom& cg, const sk_segment_t& seg,
                                                     int64_t rot, int64_t j) {
-    if constexpr (!is_wgrad_row(OP) || CG == 1) {   // the one-CTA row kernel: one step per stage
+    if constexpr (OP == kOpFpropRow) {
+        // every tap of the segment reads the tile's one x box
+        (void)cg;
+        (void)rot;
+        return (seg.k_end - seg.k_begin) - j;
+    } else if constexpr (!is_wgrad_row(OP) || CG == 1) {   // one-CTA row wgrad: one step per stage
         return 1;
     } else {
         const int64_t len = seg.k_end - seg.k_begin;
@@ -432,6 +464,20 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0, tau = 0;
     bool ok = true;
+    bool res_pending = false;   // shifted-row fprop: filter copies in flight (drained at the end)
+    if constexpr (C::kFpRow) {
+        // The filter, tap (r, s) = w[0..63][r][s][0..63] (64 filters x 64 channels, K-major), 8 KB
+        // apart in the resident region, once for the CTA's whole work.
+        const uint32_t res = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes;
+        const uint32_t bar = bars + C::kBarRes * 8;
+        const int taps = P.conv.R * P.conv.S;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(taps) * 8192u);
+        if (P.conv.filter_box)
+            tma_load_3d(res, &P.tmap_b, bar, 0, 0, 0);
+        else
+            for (int t = 0; t < taps; ++t) tma_load_2d(res + t * 8192, &P.tmap_b, bar, t * 64, 0);
+        res_pending = true;
+    }
     while (true) {
         const bool dp = cur.dp_next >= 0;
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
@@ -443,6 +489,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         // upper tap row is inside the filter, else one box of stage_steps * 8 KB per tap row
         // inside it.
         uint32_t stage_tx = CG * C::kStageBytes;
+        if constexpr (C::kFpRow) stage_tx = static_cast<uint32_t>(P.conv.R + 1) * 8192u;
         if constexpr (C::kWgRow) {
             const ConvGeom& cg = P.conv;
             const uint32_t T = CG == 1 ? 1u : static_cast<uint32_t>(cg.stage_steps);
@@ -463,7 +510,7 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         WgradSlabs<TN> slabs;
         if constexpr (OP == kOpWgrad16) wgrad_slabs<TN>(P.conv, g, nt, slabs);
         PixelStart ps{0, 0, 0};
-        if constexpr (folds_groups_into_columns(OP)) pixel_start(P.conv, mt, ps);
+        if constexpr (folds_groups_into_columns(OP) && !C::kFpRow) pixel_start(P.conv, mt, ps);
         const int64_t len = seg.k_end - seg.k_begin;
         const int64_t rot = segment_rotation(plan, dp, seg, tau);
         for (int64_t j = 0; j < len; j += stage_step_count<OP, CG>(P.conv, seg, rot, j)) {
@@ -494,6 +541,8 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
             }
         }
     }
+    // The filter's copies land before the CTA can exit, even if it had no work.
+    if (res_pending) mbar_wait(bars + C::kBarRes * 8, 0u, 10000000ull);
     if constexpr (CG == 2) {
         // The copies of a pair complete on the even CTA's barriers, so this CTA waits until the
         // MMAs have consumed its last stages (their commits arrive here too): then nothing is
@@ -529,7 +578,8 @@ template <int OP, int TN, int CG, int ST>
 __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
                                           const sk_segment_t& seg, uint32_t ring, uint32_t bars,
                                           volatile SmemCtl* ctl, uint32_t d_tmem, bool accumulate,
-                                          uint32_t& stage, uint32_t& phase, int64_t steps) {
+                                          uint32_t& stage, uint32_t& phase, int64_t steps,
+                                          int64_t k0) {
     using C = Cfg<OP, TN, CG, ST>;
     static_assert(C::kMmasPerStage == 4, "a K step is four MMAs");
     const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
@@ -601,7 +651,42 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
     }
     tc_fence_after();
     const uint32_t acc = accumulate ? 1u : 0u;
-    if constexpr (C::kWgRow) {
+    if constexpr (C::kFpRow) {
+        // Step k = tap (r, s) of the reduction (64 channels each). D[(output row, position)][filter]
+        // += x[row + r][position + s][c] * w[filter][r][s][c]: A = the box's rows from row r,
+        // position s on (128 consecutive 128-byte rows, K-major: any row may start the 128-byte
+        // swizzle pattern); B = the resident filter tap (K-major). Steps in the segment's order,
+        // which wraps at k_end.
+        // Descriptors: the base ones plus the tap's offset in 16-byte units (addresses stay
+        // below 2^18, so the sums never leave the 14-bit address field); (r, s) advance with the
+        // tap, no division per step.
+        const uint32_t res = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes;
+        const uint64_t a_base = smem_desc_sw128(a_addr, 16, 1024);
+        const uint64_t b_base = smem_desc_sw128(res, 16, 1024);
+        const int S = P.conv.S;
+        int tap = static_cast<int>(k0);
+        int r = tap / S, s_ = tap - r * S;
+        for (int64_t t = 0; t < steps; ++t) {
+            const uint64_t ao = static_cast<uint64_t>((r * 64 + s_) * 8);
+            const uint64_t bo = static_cast<uint64_t>(tap * 512);
+            uint64_t a[4], b[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                a[kk] = a_base + ao + 2 * kk;
+                b[kk] = b_base + bo + 2 * kk;
+            }
+            mma_x4<CG, false>(d_tmem, a, b, P.idesc, t > 0 ? 1u : acc);
+            // next tap in the segment's order, which wraps from k_end - 1 to k_begin
+            if (++tap == seg.k_end) {
+                tap = static_cast<int>(seg.k_begin);
+                r = tap / S;
+                s_ = tap - r * S;
+            } else if (++s_ == S) {
+                s_ = 0;
+                ++r;
+            }
+        }
+    } else if constexpr (C::kWgRow) {
         // Descriptor address fields count 16-byte units.
         constexpr uint64_t kStepA = 8192 >> 4, kStepB = (64 * C::kDyRowBytes) >> 4;
         const int64_t nsteps = CG == 1 ? 1 : steps;
@@ -620,6 +705,7 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
         }
     } else {
         (void)steps;
+        (void)k0;
         mma_x4<CG, C::kFp8>(d_tmem + col0[0], ad[0], bd[0], idesc[0], acc);
     }
     tc_commit<CG>(empty);
@@ -642,6 +728,14 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
     int64_t nseg = 0, tau = 0;
     int64_t total_commits = 0;
     bool any = false, ok = true;
+    if constexpr (C::kFpRow) {   // the resident filter, loaded once by the producer
+        if (!mbar_wait(bars + C::kBarRes * 8, 0u, P.mbar_timeout_ns)) {
+            record_error(kErrPipeline, cta, -1, 6);
+            ctl->abort = 1;
+            ok = false;
+        }
+        tc_fence_after();
+    }
     while (true) {
         const bool dp = cur.dp_next >= 0;
         if (!ok || !seg_next(plan, cta, cur, seg)) break;
@@ -660,14 +754,17 @@ __device__ void run_mma(const KernelParams& P, int64_t cta, uint32_t ring, uint3
         }
         tc_fence_after();
         uint32_t d_tmem = tmem_base + acc * TN;
-        // The shifted-row wgrad groups K steps into stages as the producer does (same rotation).
-        const int64_t rot = is_wgrad_row(OP) ? segment_rotation(plan, dp, seg, tau) : 0;
+        // The shifted-row kernels group K steps into stages as the producer does (same rotation).
+        const int64_t rot = (is_wgrad_row(OP) || OP == kOpFpropRow)
+                                ? segment_rotation(plan, dp, seg, tau) : 0;
         for (int64_t j = 0, steps = 1; j < len; j += steps) {
             steps = stage_step_count<OP, CG>(P.conv, seg, rot, j);
+            int64_t k0 = seg.k_begin + rot + j;
+            if (k0 >= seg.k_end) k0 -= len;
             // Block scales: every K step starts a fresh partial.
             const bool accumulate = OP == kOpFp8Block ? false : j > 0;
             if (!mma_stage<OP, TN, CG, ST>(P, cta, seg, ring, bars, ctl, d_tmem, accumulate, stage,
-                                           phase, steps)) {
+                                           phase, steps, k0)) {
                 ok = false;
                 break;
             }
@@ -733,6 +830,7 @@ struct EpiCtx {
     int64_t n_end;         // output columns of this tile's group end here (exclusive)
     int row;               // accumulator row 0..127
     int64_t half;          // CG = 2: rank of this CTA in its pair (which 128 rows of the tile); else 0
+    int64_t mt;            // the tile's row block (shifted-row fprop: output rows 2*mt, 2*mt + 1)
     float row_scale;       // fp8: sa[out_row] (per-tensor: the scale product); else 1
 };
 
@@ -781,6 +879,7 @@ __device__ __forceinline__ void store4_out(const sk_plan_t& plan, const OutSpec&
                                            int64_t m, int64_t n0, float (&v)[4]) {
     const bool fold_cols = folds_groups_into_columns(o.op_kind);
     const int64_t out_row = fold_cols ? map_row(o.conv->rows, m) : g * plan.gemm_m + m;
+    if (out_row < 0) return;   // a padded position (shifted-row fprop)
     if (o.scale_mode == 1) {
         const float rs = o.sa[out_row];
         for (int j = 0; j < 4; ++j) v[j] *= rs * (n0 + j < plan.gemm_n ? o.sb[n0 + j] : 0.0f);
@@ -968,6 +1067,12 @@ __device__ void store_tile_tma(const KernelParams& P, const EpiCtx& e, uint32_t 
     const int64_t ncols = P.plan.gemm_n;
     const bool bf16 = P.c_dtype == SK_BF16;
     const int32_t y0 = static_cast<int32_t>(e.out_row - lane);   // the warp's first row
+    if constexpr (OP == kOpFpropRow) {
+        // The shifted-row fprop's staging buffer is its own: the previous tile's store has to be
+        // out of it before it is written again (waited here, not after each store).
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+    }
 #pragma unroll 1
     for (int sl = 0; sl < kSlabs; ++sl) {
         uint32_t r[2][32];
@@ -1004,12 +1109,25 @@ __device__ void store_tile_tma(const KernelParams& P, const EpiCtx& e, uint32_t 
                          packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0)
-            tma_store_2d(&P.tmap_c, buf, static_cast<int32_t>(e.n_base + sl * 64), y0);
+        if constexpr (OP == kOpFpropRow) {
+            // The warp's 32 rows: positions (quarter & 1) * 32 ... of output row 2*mt + quarter / 2
+            // (rows counted per image over ho_pad); C is [N][Ho][Wo][64] and the map clips
+            // positions past Wo. A padding row (past Ho) or a box wholly past Wo is not stored.
+            const uint32_t hp = static_cast<uint32_t>(P.conv.ho_pad);
+            const uint32_t t0 = 2u * static_cast<uint32_t>(e.mt);
+            const uint32_t n_img = t0 / hp;
+            const int32_t ho = static_cast<int32_t>(t0 - n_img * hp) + (quarter >> 1);
+            const int32_t wo0 = (quarter & 1) * 32;
+            if (lane == 0 && ho < P.conv.ho && wo0 < P.conv.rows.vw)
+                tma_store_4d(&P.tmap_c, buf, 0, wo0, ho, static_cast<int32_t>(n_img));
+        } else {
+            if (lane == 0)
+                tma_store_2d(&P.tmap_c, buf, static_cast<int32_t>(e.n_base + sl * 64), y0);
+        }
     }
     if (lane == 0) {
         bulk_commit_group();
-        bulk_wait_group_read0();
+        if constexpr (OP != kOpFpropRow) bulk_wait_group_read0();
     }
     __syncwarp();
 }
@@ -1414,6 +1532,7 @@ __device__ bool promote_segment(const KernelParams& P, int64_t cta, const sk_seg
     EpiCtx e;
     e.row = row;
     e.half = static_cast<int64_t>(rank);   // a pair's CTA holds rows rank*128 .. of the tile
+    e.mt = mt;
     const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
     e.row_ok = m < plan.gemm_m;
     e.out_row = m;
@@ -1625,9 +1744,24 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         EpiCtx e;
         e.row = row;
         e.half = static_cast<int64_t>(rank);
+        e.mt = mt;
         const int64_t m = mt * C::kTileMAll + static_cast<int64_t>(rank) * kTileM + row;
         e.row_ok = m < plan.gemm_m;
-        if constexpr (folds_groups_into_columns(OP)) {
+        if constexpr (OP == kOpFpropRow) {
+            // Row (output row 2*mt + row / 64, position row % 64) of the image's rows counted over
+            // ho_pad: an output pixel when the row is below Ho and the position below Wo (what
+            // map_row gives, in 32-bit arithmetic: n * ho_pad * 64 < 2^31).
+            const uint32_t hp = static_cast<uint32_t>(P.conv.ho_pad);
+            const uint32_t t0 = 2u * static_cast<uint32_t>(mt);
+            const uint32_t n_img = t0 / hp;
+            const int32_t ho = static_cast<int32_t>(t0 - n_img * hp) + (row >> 6);
+            const int32_t wo = row & 63;
+            const int32_t Wo = P.conv.rows.vw;
+            e.row_ok = ho < P.conv.ho && wo < Wo;
+            e.out_row = e.row_ok ? (static_cast<int64_t>(n_img) * P.conv.ho + ho) * Wo + wo : 0;
+            e.n_base = 0;
+            e.n_end = plan.gemm_n;
+        } else if constexpr (folds_groups_into_columns(OP)) {
             e.out_row = map_row(P.conv.rows, m);
             e.n_base = g * plan.gemm_n + nt * TN;
             e.n_end = (g + 1) * plan.gemm_n;
@@ -1670,6 +1804,10 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         for (int i = 0; i < npend; ++i)
             spread_fold<OP, TN, CG, ST>(P, cta, pend[i], ethread, static_cast<int64_t>(rank), ring,
                                         bars + C::kBarFold * 8, fold_phase);
+    if constexpr (OP == kOpFpropRow) {   // the last tile store has read its staging buffer
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1686,8 +1824,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     static_assert(sizeof(SmemCtl) <= C::kCtlBytes, "control block");
     const uint32_t ring = smem_u32(smem);
     volatile SmemCtl* ctl =
-        reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes);
-    const uint32_t bars = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes + C::kCtlBytes;
+        reinterpret_cast<volatile SmemCtl*>(smem + C::kRingBytes + C::kEpiStageBytes +
+                                            C::kScaleBytes + C::kResBytes);
+    const uint32_t bars = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes +
+                          C::kResBytes + C::kCtlBytes;
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const uint32_t ctl_addr = smem_u32(const_cast<SmemCtl*>(ctl));
@@ -1709,6 +1849,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         }
         for (int f = 0; f < C::kFoldBufs; ++f)
             mbar_init(bars + (C::kBarFold + f) * 8, 1);   // owner's fold buffers
+        mbar_init(bars + C::kBarRes * 8, 1);              // shifted-row fprop: filter loaded
         fence_mbarrier_init();
         ctl->abort = 0;
     }
@@ -1934,6 +2075,7 @@ static size_t smem_bytes_t() {
      : (op) == kOpGemm16 ? fn<kOpGemm16, 128, 1, 6>(__VA_ARGS__)                              \
      : (op) == kOpFp8    ? fn<kOpFp8, 128, 1, 6>(__VA_ARGS__)                                 \
      : (op) == kOpFprop16 ? fn<kOpFprop16, 128, 1, 3>(__VA_ARGS__)                            \
+     : (op) == kOpFpropRow ? fn<kOpFpropRow, 64, 1, 4>(__VA_ARGS__)                           \
      : (op) == kOpDgrad16 ? fn<kOpDgrad16, 128, 1, 3>(__VA_ARGS__)                            \
      : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 1, 5>(__VA_ARGS__)                          \
      : (op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 1, 8>(__VA_ARGS__)                        \
@@ -1959,10 +2101,12 @@ int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
     const int cg = p.plan.tm == 2 * kTileM ? 2 : 1;
-    const int tn = p.plan.tn == 256 ? 256 : 128;
+    const int tn = p.plan.tn == 256 ? 256 : p.plan.tn == 64 ? 64 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
-    if (p.plan.tn == 192 && cg == 2)
+    if (tn == 64)
+        sk_stage2_kernel<64, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
+    else if (p.plan.tn == 192 && cg == 2)
         sk_stage2_kernel<192, 2><<<dim3(static_cast<unsigned>(tiles), 256u * 192u / 4u / kStage2Threads),
                                    dim3(kStage2Threads), 0, stream>>>(p);
     else if (p.plan.tn == 192)

@@ -15,7 +15,11 @@ enum OpKind : int {
     kOpFp8Block = 5,   // fp8 with block scales: each K step's partial promoted by the epilogue
     // Wgrad of 64-channel, 64-filter groups on shifted rows (one x row serves every column tap):
     // W stride 1 (one phase of x columns) or 2 (even and odd columns).
-    kOpWgradRow1 = 6, kOpWgradRow2 = 7
+    kOpWgradRow1 = 6, kOpWgradRow2 = 7,
+    // Forward convolution (stride 1, 64 channels, 64 filters, at most 3 x 3 taps) on shifted rows:
+    // a tile is two output rows of 64 positions, the x rows for all taps come in one box and the
+    // filter stays in shared memory.
+    kOpFpropRow = 8
 };
 
 __host__ __device__ constexpr bool is_wgrad_row(int op) {
@@ -25,7 +29,7 @@ __host__ __device__ constexpr bool is_wgrad_row(int op) {
 // Forward convolution and data gradient fold conv groups into the output's columns (the output
 // is [pixels][channels]); wgrad folds them into its rows.
 __host__ __device__ constexpr bool folds_groups_into_columns(int op) {
-    return op == kOpFprop16 || op == kOpDgrad16;
+    return op == kOpFprop16 || op == kOpDgrad16 || op == kOpFpropRow;
 }
 
 constexpr int kTileM = 128;
@@ -44,9 +48,12 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
 // Output rows of one phase of a strided data gradient: traversal pixel m = (n, i, j) of an
 // HoWo = Hp*Wp grid (width Wo = Wp) is dx pixel (n, dsh*i + ah, dsw*j + aw) of an Hd x Wd image.
 // `on` = 0: the rows are the traversal pixels themselves.
+// `vh` > 0: only grid positions i < vh, j < vw are output pixels (the shifted-row fprop pads rows
+// to 64 positions and images to an even row count); map_row gives -1 for the others.
 struct RowMap {
     int64_t HoWo;
     int32_t on, Wo, Hd, Wd, dsh, dsw, ah, aw;
+    int32_t vh, vw;
 };
 
 __host__ __device__ __forceinline__ int64_t map_row(const RowMap& rm, int64_t m) {
@@ -55,6 +62,7 @@ __host__ __device__ __forceinline__ int64_t map_row(const RowMap& rm, int64_t m)
     const int64_t rem = m - n * rm.HoWo;
     const int64_t i = rem / rm.Wo;
     const int64_t j = rem - i * rm.Wo;
+    if (rm.vh > 0 && (i >= rm.vh || j >= rm.vw)) return -1;
     return (n * rm.Hd + rm.dsh * i + rm.ah) * rm.Wd + rm.dsw * j + rm.aw;
 }
 
@@ -90,6 +98,9 @@ struct ConvGeom {
     // the next row, x_lbo = wseg * 128 bytes on), else one box per tap row (x_lbo = stage_steps *
     // 8 KB apart); then the dy rows of all of them at dy_off.
     int32_t stage_steps, x_lbo, x_phase_bytes, dy_off, x_shared_box;
+    // Shifted-row fprop: the filter's taps arrive as one 3-D box (64 channels x 64 filters x R*S
+    // taps, tap-major in shared memory) instead of one 2-D box per tap.
+    int32_t filter_box;
 };
 
 // Shifted-row wgrad ring: stage capacity (bytes) and stage count of each instance (one x column

@@ -29,8 +29,9 @@
  *    defaults to auto" and the review fix "auto builds the launch partition, requires sk_ctas > 0";
  *    this selection was later reverted from the pages' dispatcher): stream-K when the tiles do not
  *    fill the pool (T < P) and the reduction is long (T * I >= 1024), and only if the plan the
- *    launch would use has stream-K CTAs; split-K otherwise (plain data-parallel when T >= P). The
- *    resolved mode is what sk_plan reports.
+ *    launch would use has stream-K CTAs; split-K otherwise (plain data-parallel when T >= P),
+ *    except that the shifted-row forward convolution (whose CTAs keep the filter resident) with
+ *    more tiles than CTAs runs SK_PERSISTENT. The resolved mode is what sk_plan reports.
  *    SK_HYBRID is SK_DP_SK with one full wave more in the stream-K region whenever the pool does
  *    not divide the tiles and the tiles fill at least one wave: P + T mod P stream-K tiles, so
  *    that every stream-K CTA runs between one and two tiles' worth of iterations (a variant of

@@ -119,12 +119,14 @@ def _pixel_ranges(P):
     return [(0, 300), (P // 2 - 130, P // 2 + 130), (P - 300, P)]
 
 
+@pytest.mark.parametrize("tile", ["auto", "128"])   # auto: the shifted-row kernel
 @pytest.mark.parametrize("red", ["linear", "atomic"])
-def test_fprop_32x56x56_sampled(red):
+def test_fprop_32x56x56_sampled(red, tile):
     N, H, W, C, K = 32, 56, 56, 64, 64
     x, w = fprop_operands(N, H, W, C, K, 3, 3, 1, "f16", "u11")
     out = "f32" if red == "atomic" else "f16"
-    y = run_fprop(x, w, out, (1, 1), (1, 1), 1, "dp_sk", red, -1).reshape(-1, K)
+    with sk.tile(tile):
+        y = run_fprop(x, w, out, (1, 1), (1, 1), 1, "dp_sk", red, -1).reshape(-1, K)
     assert torch.isfinite(y.float()).all(), "unwritten outputs"
     for p0, p1 in _pixel_ranges(N * H * W):
         ref = numerics.fprop_nhwc("f16", bits(x), bits(w), (1, 1), (1, 1), 1, p0=p0, p1=p1)
@@ -222,5 +224,78 @@ def test_dgrad_strided_caller_workspace_and_bit_identical():
         if first is None:
             first = b
             check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what="strided dgrad, caller ws")
+        else:
+            assert torch.equal(first, b), "result changed between launches"
+
+
+# ---- the shifted-row forward convolution (stride 1, 64 channels -> 64 filters, <= 3x3 taps)
+
+ROW_FPROP = {   # (N, H, W, R, S, pad, dtype)
+    # odd Ho (the last tile's second row is padding), 11 of 64 positions per row
+    "ragged_3x3": (2, 9, 11, 3, 3, (1, 1), "f16"),
+    # the widest rows it takes: 62 output columns + 2 column taps = 64 positions
+    "wide_3x3": (1, 5, 62, 3, 3, (1, 1), "bf16"),
+    # 2x2 taps, padding on one side only
+    "2x2_pad01": (3, 7, 7, 2, 2, (0, 1), "f16"),
+    # 1x1
+    "1x1": (2, 6, 20, 1, 1, (0, 0), "bf16"),
+    # three tap rows, one column tap, row padding 2
+    "3x1_pad2": (1, 4, 30, 3, 1, (2, 0), "f16"),
+}
+
+
+def row_fprop_plan(N, H, W, R, S, pad, dt, tile="auto"):
+    prob = sk.make_problem("fprop", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=64, k=64, r=R, s=S,
+                           stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    with sk.tile(tile):
+        return sk.sk_plan(prob, "dp_sk", "linear", 5, 148)
+
+
+def test_fprop_row_kernel_takes_its_shapes():
+    """The automatic tile runs these shapes on the shifted-row kernel (a 128 x 64 tile, a K step
+    per tap); the 128 x 128 tile keeps the pages' im2col view; other shapes keep the im2col view."""
+    for name, (N, H, W, R, S, pad, dt) in ROW_FPROP.items():
+        p = row_fprop_plan(N, H, W, R, S, pad, dt)
+        ho = H + 2 * pad[0] - R + 1
+        assert (p.tn, p.iters_per_tile, p.gemm_m) == (64, R * S, N * (ho + ho % 2) * 64), name
+        assert row_fprop_plan(N, H, W, R, S, pad, dt, tile="128").tn == 128, name
+    # 72 filters, or rows too wide for a 64-position segment: the im2col view
+    prob = sk.make_problem("fprop", ab_dtype="f16", c_dtype="f16", n=2, h=9, w=11, c=64, k=72, r=3,
+                           s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    assert sk.sk_plan(prob, "dp_sk", "linear", 5, 148).tn == 128
+    assert row_fprop_plan(1, 5, 63, 3, 3, (1, 1), "f16").tn == 128
+
+
+@pytest.mark.parametrize("red", REDS)
+@pytest.mark.parametrize("mode", MODES + ["hybrid"])
+@pytest.mark.parametrize("name", list(ROW_FPROP))
+def test_fprop_row_shapes(name, mode, red):
+    N, H, W, R, S, pad, dt = ROW_FPROP[name]
+    x, w, ref = fprop_case(N, H, W, 64, 64, R, S, (1, 1), pad, 1, dt, 31)
+    out = "f32" if red == "atomic" else dt
+    y = run_fprop(x, w, out, (1, 1), pad, 1, mode, red, 5)
+    check_parity(y.reshape(-1, 64), ref, out, R * S * 64, what=f"fprop row {name} {mode}/{red}")
+
+
+@pytest.mark.parametrize("red", ["linear", "tree"])
+def test_fprop_row_bit_identical(red):
+    """20 launches, workspace and output poisoned before each; pool 5 so that tiles are shared."""
+    N, H, W, R, S, pad, dt = ROW_FPROP["ragged_3x3"]
+    x, w, _ = fprop_case(N, H, W, 64, 64, R, S, (1, 1), pad, 1, dt, 31)
+    xd, wd = x.to(DEV), w.to(DEV)
+    prob = sk.make_problem("fprop", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=64, k=64, r=R, s=S,
+                           stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", red, 5), dtype=torch.uint8, device=DEV)
+    y = poisoned((N, 9, 11, 64), TD[dt])
+    first = None
+    for _ in range(20):
+        ws.fill_(0xFF)
+        y.view(torch.uint8).fill_(0xFF)
+        sk.sk_conv2d_fprop_nhwc(xd, wd, y, (1, 1), pad, 1, "dp_sk", red, 5, ws=ws)
+        sk.sk_device_status()
+        b = y.view(torch.uint8).clone()
+        assert torch.isfinite(y.float()).all()
+        if first is None:
+            first = b
         else:
             assert torch.equal(first, b), "result changed between launches"

@@ -405,3 +405,71 @@ def test_row_wgrad_sweep():
             compare(prob, kw, rng.choice(MODES), rng.choice(REDS), rng.choice([-1, 1, 3, 7, 148]),
                     num_sms=rng.choice([148, 152, 8]))
     assert seen_row > 50 and seen_generic > 5
+
+
+
+# ---- shifted-row forward convolution (automatic tile; stride 1, 64 channels, 64 filters, <= 3x3):
+# M = positions, 64 per output row, rows counted per image over Ho rounded up to even, in 128-row
+# tiles (two output rows); N = 64 filters; one K step per tap.
+
+def fprop_row(N, H, W, R, S, pad):
+    prob = sk.make_problem("fprop", ab_dtype="f16", c_dtype="f16", n=N, h=H, w=W, c=64, k=64, r=R,
+                           s=S, stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    ho = H + 2 * pad[0] - R + 1
+    ho_pad = ho + ho % 2
+    kw = dict(tiles_m=N * ho_pad * 64 // 128, tiles_n=1, groups=1, kred=R * S * 64, tm=128, tn=64,
+              tk=64)
+    return prob, kw
+
+
+FPROP_ROW_NAMED = [
+    ("fprop 32x56x56 3x3", fprop_row(32, 56, 56, 3, 3, (1, 1)), -1),
+    ("fprop 2x9x11 3x3", fprop_row(2, 9, 11, 3, 3, (1, 1)), 5),
+    ("fprop 3x7x7 2x2", fprop_row(3, 7, 7, 2, 2, (0, 1)), 7),
+]
+
+
+@pytest.mark.parametrize("name,pk,ctas", FPROP_ROW_NAMED, ids=[n[0] for n in FPROP_ROW_NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_fprop_row_plans(name, pk, ctas, mode, red):
+    prob, kw = pk
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    with sk.tile("auto"):
+        cp = compare(prob, kw, mode, red, ctas, check_ctas=big)
+    assert (cp.tm, cp.tn, cp.tk, cp.iters_per_tile) == (128, 64, 64, kw["kred"] // 64)
+
+
+def test_fprop_row_worked_vector():
+    """32x56x56, 64 -> 64, 3x3: 32 images x 56 rows / 2 = 896 tiles of 9 taps; 148 CTAs: 888
+    tiles in six data-parallel waves, 8 left over (72 iterations, fewer than the pool: all
+    data-parallel)."""
+    with sk.tile("auto"):
+        cp = sk.sk_plan(FPROP_ROW_NAMED[0][1][0], "dp_sk", "linear", 148, 148)
+    assert (cp.tiles, cp.iters_per_tile, cp.sk_ctas, cp.dp_tiles, cp.grid) == (896, 9, 0, 896, 896)
+
+
+def test_fprop_row_auto_mode_is_persistent():
+    """The automatic mode runs the shifted-row fprop persistently when its tiles outnumber the CTAs
+    (every CTA keeps the filter resident over its tiles), all tiles data-parallel (a stream-K wave's
+    fixups cost more than one short tile): CTA c runs tiles c, c + pool, ... With fewer tiles than
+    CTAs it keeps the pages' rule."""
+    prob, kw = FPROP_ROW_NAMED[0][1]
+    with sk.tile("auto"):
+        for ctas, sms in ((-1, 152), (-1, 148), (300, 152)):
+            cp = sk.sk_plan(prob, "auto", "linear", ctas, sms)
+            pool = ctas if ctas > 0 else sms
+            assert (cp.mode, cp.pool, cp.grid, cp.sk_tiles, cp.sk_ctas, cp.dp_tiles) == (
+                P.PERSISTENT, pool, pool, 0, 0, 896)
+            assert cp.ws_bytes <= 256 * 1024   # no partials: flags and the control block at most
+            seen = []
+            for c in range(pool):
+                segs = sk.sk_plan_cta_work(cp, c)
+                assert [s.tile for s in segs] == list(range(c, 896, pool))
+                assert all((s.k_begin, s.k_end) == (0, 9) for s in segs)
+                seen += [s.tile for s in segs]
+            assert sorted(seen) == list(range(896))
+        small, skw = fprop_row(1, 4, 8, 3, 3, (1, 1))   # 2 tiles, fewer than the pool
+        cp = sk.sk_plan(small, "auto", "linear", -1, 152)
+        op = P.make_auto_plan(pool=P.default_pool(P.LINEAR, 152, 1), reduction=P.LINEAR, **skw)
+        assert cp.mode == op.mode != P.PERSISTENT

@@ -191,10 +191,11 @@ WORKLOADS = {
                  pool=148, modes=("dp_sk", "persistent"),
                  reductions=("linear", "tree", "workspace")),
         # The same 3x3 layer as the wgrad workload, forward and data gradient.
+        # The automatic mode runs the shifted-row kernel persistently (all tiles data-parallel).
         Workload("fprop_f16_n32_56x56_c64_k64_3x3", "fprop", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
                            groups=1),
-                 pool=-1, modes=("dp_sk",), reductions=("linear", "tree")),
+                 pool=-1, modes=("dp_sk", "auto"), reductions=("linear", "tree")),
         Workload("dgrad_f16_n32_56x56_c64_k64_3x3", "dgrad", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
                            groups=1),
