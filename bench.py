@@ -379,9 +379,10 @@ def extra_measurements(torch, sk, dev, flush, stream, peaks, cpu=True):
                                                           sk.sk_gemm_rcr(A, B, Cx, mode, red, pool, ws=ws))
         elif w.op in ("fprop", "dgrad"):
             call, _ = conv_call(torch, sk, w, dev, ws, host)
-            # fprop: the automatic tile (the shifted-row kernel where the layer fits it) and the
-            # pages' im2col view on the 128 x 128 tile
-            for tile in (("auto", "128") if w.op == "fprop" else ("128",)):
+            # stride 1: the automatic tile (the shifted-row kernel where the layer fits it) and the
+            # pages' im2col view on the 128 x 128 tile; a strided dgrad has the latter only
+            stride1 = tuple(w.conv["stride"]) == (1, 1)
+            for tile in (("auto", "128") if stride1 else ("128",)):
                 for mode, red in dict.fromkeys(sk_variants + comparators):
                     calls[f"{tile}:{mode}/{red}"] = tiled(tile, lambda mode=mode, red=red:
                                                           call(mode, red, w.pool))

@@ -27,6 +27,13 @@ namespace {
 thread_local char g_err[512] = "";
 thread_local int g_tile = SK_TILE_AUTO;   // sk_set_tile
 
+// Sets the calling thread's tile setting for a scope.
+struct TileGuard {
+    int prev;
+    explicit TileGuard(int tile) : prev(g_tile) { g_tile = tile; }
+    ~TileGuard() { g_tile = prev; }
+};
+
 int fail(int code, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -193,18 +200,24 @@ bool wgrad_row_geom(const sk_problem& p, RowGeom& g) {
 
 int problem_view_pages(const sk_problem& p, View& v);
 
-// The shifted-row forward convolution serves stride 1, one group of 64 channels and 64 filters, at
+// The shifted-row kernel serves stride-1 convolutions of one group of 64 channels into 64, at
 // most 3 x 3 taps and output rows of at most 64 positions with the column taps' overrun
-// (Wo + S - 1 <= 64): a tile is two output rows of 64 positions (rows counted per image over Ho
-// rounded up to even), its reduction the taps (64 channels each).
-bool fprop_row_geom(const sk_problem& p, int64_t& ho, int64_t& wo, int64_t& ho_pad) {
-    if (p.op != SK_OP_FPROP || p.groups != 1 || p.c != 64 || p.k != 64) return false;
+// (width + S - 1 <= 64): the forward convolution (x -> y, Ho x Wo), and the data gradient as the
+// stride-1 convolution of dy with the flipped filter, padding R - 1 - p (dy -> dx, H x W). A tile is
+// two output rows of 64 positions (rows counted per image over the height rounded up to even),
+// its reduction the taps (64 channels each). th x tw: the output grid of that traversal.
+bool conv_row_geom(const sk_problem& p, int64_t& th, int64_t& tw, int64_t& th_pad) {
+    if ((p.op != SK_OP_FPROP && p.op != SK_OP_DGRAD) || p.groups != 1 || p.c != 64 || p.k != 64)
+        return false;
     if (p.stride_h != 1 || p.stride_w != 1 || p.r < 1 || p.r > 3 || p.s < 1 || p.s > 3) return false;
-    ho = p.h + 2 * p.pad_h - p.r + 1;
-    wo = p.w + 2 * p.pad_w - p.s + 1;
-    if (ho < 1 || wo < 1 || wo + p.s - 1 > 64) return false;
-    ho_pad = sk::round_up(ho, 2);
-    return p.n * ho_pad * 64 < (int64_t(1) << 31);
+    if (p.pad_h < 0 || p.pad_w < 0 || p.pad_h >= p.r || p.pad_w >= p.s) return false;
+    const int64_t ho = p.h + 2 * p.pad_h - p.r + 1, wo = p.w + 2 * p.pad_w - p.s + 1;
+    if (ho < 1 || wo < 1) return false;
+    th = p.op == SK_OP_FPROP ? ho : p.h;
+    tw = p.op == SK_OP_FPROP ? wo : p.w;
+    if (tw + p.s - 1 > 64) return false;
+    th_pad = sk::round_up(th, 2);
+    return p.n * th_pad * 64 < (int64_t(1) << 31);
 }
 
 // The GEMM view of a problem under the calling thread's tile setting. Wgrad: the pages' view
@@ -216,7 +229,8 @@ int problem_view(const sk_problem& p, View& v) {
     int rc = problem_view_pages(p, v);
     if (rc) return rc;
     int64_t fho, fwo, fho_pad;
-    if (v.op_kind == sk::kOpFprop16 && g_tile == SK_TILE_AUTO && fprop_row_geom(p, fho, fwo, fho_pad)) {
+    if ((v.op_kind == sk::kOpFprop16 || v.op_kind == sk::kOpDgrad16) && g_tile == SK_TILE_AUTO &&
+        conv_row_geom(p, fho, fwo, fho_pad)) {
         v.gemm_m = p.n * fho_pad * 64;
         v.gemm_n = 64;
         v.kred = p.r * p.s * 64;
@@ -841,7 +855,9 @@ int sk_plan_cta_work(const sk_plan_t* plan, int64_t cta, sk_segment_t* out, int 
 int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out) {
     if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
     if (p->op == SK_OP_DGRAD && (p->stride_h > 1 || p->stride_w > 1)) {
-        // The largest workspace of the phases, which run one after another on one stream.
+        // The largest workspace of the phases, which run one after another on one stream, in
+        // the pages' view as their launches take it.
+        const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
         if (p->stride_h < 1 || p->stride_w < 1 || p->stride_h > 8 || p->stride_w > 8)
             return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
         std::vector<DgradPhase> phases;
@@ -1314,6 +1330,9 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
     auto launch = [&](int64_t AH, int64_t AW, int64_t TH, int64_t TW, int tsh, int tsw, int tph,
                       int tpw, int Rt, int St, int r0, int s0, const sk::RowMap& rows,
                       bool zeroed) -> int {
+        // The im2col kernel serves the pages' view: a dgrad phase problem that fits the shifted-row
+        // view keeps the 128 x 128 tile (the automatic tile's choice for the pages' view).
+        const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
         const int64_t AC = fprop ? C : K;
         sk_problem prob;
         memset(&prob, 0, sizeof(prob));
@@ -1387,109 +1406,115 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
                    ws, ws_bytes, st);
     };
 
+    // The shifted-row kernel over the activation (AH x AW, 64 channels) into the TH x TW output
+    // (64 channels) with padding (tph, tpw). A: boxes of 64 channels x 64 positions (from column
+    // -tpw) x R + 1 rows (from row ho0 - tph); outside the activation reads zeros. B: the filter's
+    // taps [tap][filter][channel] of w[K][R][S][C]: for fprop (output channel = filter) K-major,
+    // for dgrad (output channel = channel, the taps flipped) MN-major.
+    auto row_launch = [&](const sk_problem& prob, int64_t AH, int64_t AW, int64_t TH, int64_t TW,
+                          int tph, int tpw, bool flip) -> int {
+        sk::KernelParams kp;
+        memset(&kp, 0, sizeof(kp));
+        {
+            const cuuint64_t dims[4] = {64, (cuuint64_t)AW, (cuuint64_t)AH, (cuuint64_t)N};
+            const cuuint64_t strides[3] = {128, (cuuint64_t)(AW * 128), (cuuint64_t)(AH * AW * 128)};
+            const cuuint32_t box[4] = {64, 64, (cuuint32_t)(R + 1), 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            CUresult r = g_encode_tiled(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                                        const_cast<void*>(act), dims, strides, box, estr,
+                                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS)
+                return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(activation) failed (%d)", (int)r);
+        }
+        // The filter as one box (strides: a filter R*S*64 * 2 bytes, a tap 128 bytes), else one
+        // [K][R*S*64] box per tap.
+        const int64_t RSC = R * S * 64;
+        {
+            const cuuint64_t dims[3] = {64, 64, (cuuint64_t)(R * S)};
+            const cuuint64_t strides[2] = {(cuuint64_t)(RSC * 2), 128};
+            const cuuint32_t box[3] = {64, 64, (cuuint32_t)(R * S)};
+            const cuuint32_t estr[3] = {1, 1, 1};
+            kp.conv.filter_box =
+                g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(wt),
+                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        if (!kp.conv.filter_box) {
+            int rc2 = encode_2d(&kp.tmap_b, wt, 2, RSC, 64, RSC * 2, 64, 64);
+            if (rc2) return rc2;
+        }
+        kp.c = out;
+        kp.ldc = 64;
+        kp.c_dtype = out_dtype;
+        // A 16-bit output leaves through TMA tile stores: [N][TH][TW][64], boxes of 32 positions x
+        // 64 channels; the map clips the positions past TW.
+        if (out_dtype != SK_F32) {
+            const cuuint64_t dims[4] = {64, (cuuint64_t)TW, (cuuint64_t)TH, (cuuint64_t)N};
+            const cuuint64_t strides[3] = {128, (cuuint64_t)(TW * 128), (cuuint64_t)(TH * TW * 128)};
+            const cuuint32_t box[4] = {64, 32, 1, 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            CUresult r = g_encode_tiled(&kp.tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, out, dims,
+                                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                        CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS)
+                return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(output) failed (%d)", (int)r);
+            kp.c_tma = 1;
+        }
+        const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
+        kp.idesc = sk::make_idesc(fmt, fmt, false, flip, 128, 64);
+        kp.conv.row_flip = flip ? 1 : 0;
+        kp.conv.ph = tph;
+        kp.conv.pw = tpw;
+        kp.conv.sh = 1;
+        kp.conv.sw = 1;
+        kp.conv.R = static_cast<int32_t>(R);
+        kp.conv.S = static_cast<int32_t>(S);
+        kp.conv.Cg = 64;
+        kp.conv.Kg = 64;
+        kp.conv.Cw = 64;
+        const int64_t th_pad = sk::round_up(TH, 2);
+        kp.conv.ho = static_cast<int32_t>(TH);
+        kp.conv.ho_pad = static_cast<int32_t>(th_pad);
+        // Tile rows are (image, row over th_pad, position over 64): an output pixel when the row
+        // is below TH and the position below TW.
+        kp.conv.rows.on = 1;
+        kp.conv.rows.HoWo = th_pad * 64;
+        kp.conv.rows.Wo = 64;
+        kp.conv.rows.Hd = static_cast<int32_t>(TH);
+        kp.conv.rows.Wd = static_cast<int32_t>(TW);
+        kp.conv.rows.dsh = 1;
+        kp.conv.rows.dsw = 1;
+        kp.conv.rows.vh = static_cast<int32_t>(TH);
+        kp.conv.rows.vw = static_cast<int32_t>(TW);
+        return run(prob, streamk, reduction, ctas, kp, out, 64 * cs, N * TH * TW, 64 * cs, ws,
+                   ws_bytes, st);
+    };
+
     sk::RowMap identity;
     memset(&identity, 0, sizeof(identity));
-    if (fprop) {
-        sk_problem prob;
-        memset(&prob, 0, sizeof(prob));
-        prob.op = op;
-        prob.ab_dtype = in_dtype;
-        prob.c_dtype = out_dtype;
-        prob.n = N; prob.h = H; prob.w = W; prob.c = C; prob.k = K; prob.r = R; prob.s = S;
-        prob.stride_h = stride_h; prob.stride_w = stride_w; prob.pad_h = pad_h; prob.pad_w = pad_w;
-        prob.groups = groups;
-        int64_t fho, fwo, fho_pad;
-        if (g_tile == SK_TILE_AUTO && fprop_row_geom(prob, fho, fwo, fho_pad)) {
-            // Shifted rows. A: x boxes of 64 channels x 64 positions (from column -pw) x R + 1
-            // rows (from row ho0 - ph); outside the image reads zeros. B: the filter as
-            // [K][R*S*C], one 64 x 64 box per tap.
-            sk::KernelParams kp;
-            memset(&kp, 0, sizeof(kp));
-            {
-                const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
-                const cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2),
-                                               (cuuint64_t)(H * W * C * 2)};
-                const cuuint32_t box[4] = {64, 64, (cuuint32_t)(R + 1), 1};
-                const cuuint32_t estr[4] = {1, 1, 1, 1};
-                CUresult r = g_encode_tiled(&kp.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
-                                            const_cast<void*>(act), dims, strides, box, estr,
-                                            CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                            CU_TENSOR_MAP_SWIZZLE_128B,
-                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                if (r != CUDA_SUCCESS)
-                    return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(x) failed (%d)", (int)r);
-            }
-            // The filter as one box: [tap][filter][channel] over w[K][R][S][C] (strides: a
-            // filter RSC * 2 bytes, a tap 128 bytes), else one [K][RSC] box per tap.
-            const int64_t RSC = R * S * C;
-            {
-                const cuuint64_t dims[3] = {64, 64, (cuuint64_t)(R * S)};
-                const cuuint64_t strides[2] = {(cuuint64_t)(RSC * 2), 128};
-                const cuuint32_t box[3] = {64, 64, (cuuint32_t)(R * S)};
-                const cuuint32_t estr[3] = {1, 1, 1};
-                kp.conv.filter_box =
-                    g_encode_tiled(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
-                                   const_cast<void*>(wt), dims, strides, box, estr,
-                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-            }
-            if (!kp.conv.filter_box) {
-                rc = encode_2d(&kp.tmap_b, wt, 2, RSC, K, RSC * 2, 64, 64);
-                if (rc) return rc;
-            }
-            kp.c = out;
-            kp.ldc = K;
-            kp.c_dtype = out_dtype;
-            // A 16-bit y leaves through TMA tile stores: y as [N][Ho][Wo][64], boxes of 32
-            // positions x 64 filters; the map clips the positions past Wo.
-            if (out_dtype != SK_F32) {
-                const cuuint64_t dims[4] = {64, (cuuint64_t)Wo, (cuuint64_t)Ho, (cuuint64_t)N};
-                const cuuint64_t strides[3] = {128, (cuuint64_t)(Wo * 128),
-                                               (cuuint64_t)(Ho * Wo * 128)};
-                const cuuint32_t box[4] = {64, 32, 1, 1};
-                const cuuint32_t estr[4] = {1, 1, 1, 1};
-                CUresult r = g_encode_tiled(&kp.tmap_c, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, out,
-                                            dims, strides, box, estr,
-                                            CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                            CU_TENSOR_MAP_SWIZZLE_128B,
-                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                if (r != CUDA_SUCCESS)
-                    return fail(SK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(y) failed (%d)", (int)r);
-                kp.c_tma = 1;
-            }
-            const uint32_t fmt = in_dtype == SK_BF16 ? 1u : 0u;
-            kp.idesc = sk::make_idesc(fmt, fmt, false, false, 128, 64);
-            kp.conv.ph = pad_h;
-            kp.conv.pw = pad_w;
-            kp.conv.sh = 1;
-            kp.conv.sw = 1;
-            kp.conv.R = static_cast<int32_t>(R);
-            kp.conv.S = static_cast<int32_t>(S);
-            kp.conv.Cg = 64;
-            kp.conv.Kg = 64;
-            kp.conv.Cw = 64;
-            kp.conv.ho = static_cast<int32_t>(fho);
-            kp.conv.ho_pad = static_cast<int32_t>(fho_pad);
-            // Tile rows are (image, row over ho_pad, position over 64): output pixel when the
-            // row is below Ho and the position below Wo.
-            kp.conv.rows.on = 1;
-            kp.conv.rows.HoWo = fho_pad * 64;
-            kp.conv.rows.Wo = 64;
-            kp.conv.rows.Hd = static_cast<int32_t>(Ho);
-            kp.conv.rows.Wd = static_cast<int32_t>(Wo);
-            kp.conv.rows.dsh = 1;
-            kp.conv.rows.dsw = 1;
-            kp.conv.rows.vh = static_cast<int32_t>(Ho);
-            kp.conv.rows.vw = static_cast<int32_t>(Wo);
-            return run(prob, streamk, reduction, ctas, kp, out, K * cs, N * Ho * Wo, K * cs, ws,
-                       ws_bytes, st);
-        }
+    {
+        sk_problem whole;
+        memset(&whole, 0, sizeof(whole));
+        whole.op = op;
+        whole.ab_dtype = in_dtype;
+        whole.c_dtype = out_dtype;
+        whole.n = N; whole.h = H; whole.w = W; whole.c = C; whole.k = K; whole.r = R; whole.s = S;
+        whole.stride_h = stride_h; whole.stride_w = stride_w; whole.pad_h = pad_h; whole.pad_w = pad_w;
+        whole.groups = groups;
+        int64_t th, tw, th_pad;
+        if (g_tile == SK_TILE_AUTO && conv_row_geom(whole, th, tw, th_pad))
+            return fprop ? row_launch(whole, H, W, Ho, Wo, pad_h, pad_w, false)
+                         : row_launch(whole, Ho, Wo, H, W, static_cast<int>(R - 1 - pad_h),
+                                      static_cast<int>(S - 1 - pad_w), true);
+    }
+    if (fprop)
         return launch(H, W, Ho, Wo, stride_h, stride_w, pad_h, pad_w, static_cast<int>(R),
                       static_cast<int>(S), 0, 0, identity, false);
-    }
     if (!phased)   // stride 1: a stride-1 convolution of dy with the flipped filter, padding R-1-p
         return launch(Ho, Wo, H, W, 1, 1, static_cast<int>(R - 1 - pad_h),
                       static_cast<int>(S - 1 - pad_w), static_cast<int>(R), static_cast<int>(S), 0,

@@ -660,20 +660,24 @@ __device__ __forceinline__ bool mma_stage(const KernelParams& P, int64_t cta,
         // Descriptors: the base ones plus the tap's offset in 16-byte units (addresses stay
         // below 2^18, so the sums never leave the 14-bit address field); (r, s) advance with the
         // tap, no division per step.
+        // As a data gradient (row_flip) B is the flipped tap, MN-major: 16 of its 128-byte rows
+        // (filters) per MMA, 8-row atoms 1024 bytes apart.
         const uint32_t res = ring + C::kRingBytes + C::kEpiStageBytes + C::kScaleBytes;
+        const bool flip = P.conv.row_flip != 0;
         const uint64_t a_base = smem_desc_sw128(a_addr, 16, 1024);
-        const uint64_t b_base = smem_desc_sw128(res, 16, 1024);
-        const int S = P.conv.S;
+        const uint64_t b_base = smem_desc_sw128(res, flip ? 8192 : 16, 1024);
+        const uint64_t b_kstep = flip ? 128 : 2;
+        const int S = P.conv.S, taps_1 = P.conv.R * P.conv.S - 1;
         int tap = static_cast<int>(k0);
         int r = tap / S, s_ = tap - r * S;
         for (int64_t t = 0; t < steps; ++t) {
             const uint64_t ao = static_cast<uint64_t>((r * 64 + s_) * 8);
-            const uint64_t bo = static_cast<uint64_t>(tap * 512);
+            const uint64_t bo = static_cast<uint64_t>((flip ? taps_1 - tap : tap) * 512);
             uint64_t a[4], b[4];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 a[kk] = a_base + ao + 2 * kk;
-                b[kk] = b_base + bo + 2 * kk;
+                b[kk] = b_base + bo + b_kstep * kk;
             }
             mma_x4<CG, false>(d_tmem, a, b, P.idesc, t > 0 ? 1u : acc);
             // next tap in the segment's order, which wraps from k_end - 1 to k_begin

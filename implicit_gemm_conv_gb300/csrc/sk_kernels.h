@@ -101,6 +101,9 @@ struct ConvGeom {
     // Shifted-row fprop: the filter's taps arrive as one 3-D box (64 channels x 64 filters x R*S
     // taps, tap-major in shared memory) instead of one 2-D box per tap.
     int32_t filter_box;
+    // Shifted-row kernel run as a data gradient: the filter's taps flipped (traversal tap t reads
+    // filter tap R*S - 1 - t) and B MN-major (the output channels are the filter's contiguous ones).
+    int32_t row_flip;
 };
 
 // Shifted-row wgrad ring: stage capacity (bytes) and stage count of each instance (one x column

@@ -133,11 +133,13 @@ def test_fprop_32x56x56_sampled(red, tile):
         check_parity(y[p0:p1], ref, out, 9 * C, what=f"fprop 32x56x56 {red} pixels {p0}..{p1}")
 
 
+@pytest.mark.parametrize("tile", ["auto", "128"])   # auto: the shifted-row kernel
 @pytest.mark.parametrize("red", ["linear", "workspace"])
-def test_dgrad_32x56x56_sampled(red):
+def test_dgrad_32x56x56_sampled(red, tile):
     N, H, W, C, K = 32, 56, 56, 64, 64
     dy, w = dgrad_operands(N, H, W, C, K, 3, 3, (1, 1), (1, 1), 1, "f16", "u11")
-    dx = run_dgrad(dy, w, H, W, C, "f16", (1, 1), 1, "dp_sk", red, -1).reshape(-1, C)
+    with sk.tile(tile):
+        dx = run_dgrad(dy, w, H, W, C, "f16", (1, 1), 1, "dp_sk", red, -1).reshape(-1, C)
     assert torch.isfinite(dx.float()).all(), "unwritten outputs"
     for p0, p1 in _pixel_ranges(N * H * W):
         ref = numerics.dgrad_nhwc("f16", bits(dy), bits(w), H, W, (1, 1), (1, 1), 1, p0=p0, p1=p1)
@@ -299,3 +301,86 @@ def test_fprop_row_bit_identical(red):
             first = b
         else:
             assert torch.equal(first, b), "result changed between launches"
+
+
+# ---- the shifted-row data gradient (stride 1, 64 filters -> 64 channels, <= 3x3 taps): the
+# stride-1 convolution of dy with the flipped filter on the same kernel
+
+ROW_DGRAD = {   # (N, H, W, R, S, pad, dtype): dx is N x H x W x 64
+    "ragged_3x3": (2, 9, 11, 3, 3, (1, 1), "f16"),
+    "wide_3x3": (1, 5, 62, 3, 3, (1, 1), "bf16"),
+    "2x2_pad01": (3, 7, 7, 2, 2, (0, 1), "f16"),
+    "1x1": (2, 6, 20, 1, 1, (0, 0), "bf16"),
+    "3x1_pad2": (1, 4, 30, 3, 1, (2, 0), "f16"),
+    "3x3_unpadded": (2, 8, 10, 3, 3, (0, 0), "f16"),   # the traversal pads by 2 on every side
+}
+
+
+def row_dgrad_plan(N, H, W, R, S, pad, dt, tile="auto"):
+    prob = sk.make_problem("dgrad", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=64, k=64, r=R, s=S,
+                           stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    with sk.tile(tile):
+        return sk.sk_plan(prob, "dp_sk", "linear", 5, 148)
+
+
+def test_dgrad_row_kernel_takes_its_shapes():
+    for name, (N, H, W, R, S, pad, dt) in ROW_DGRAD.items():
+        p = row_dgrad_plan(N, H, W, R, S, pad, dt)
+        assert (p.tn, p.iters_per_tile, p.gemm_m) == (64, R * S, N * (H + H % 2) * 64), name
+        assert row_dgrad_plan(N, H, W, R, S, pad, dt, tile="128").tn == 128, name
+    # 72 channels, or rows too wide: the im2col view
+    prob = sk.make_problem("dgrad", ab_dtype="f16", c_dtype="f16", n=2, h=9, w=11, c=72, k=64,
+                           r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1, groups=1)
+    assert sk.sk_plan(prob, "dp_sk", "linear", 5, 148).tn == 128
+    assert row_dgrad_plan(1, 5, 63, 3, 3, (1, 1), "f16").tn == 128
+
+
+@pytest.mark.parametrize("red", REDS)
+@pytest.mark.parametrize("mode", MODES + ["hybrid"])
+@pytest.mark.parametrize("name", list(ROW_DGRAD))
+def test_dgrad_row_shapes(name, mode, red):
+    N, H, W, R, S, pad, dt = ROW_DGRAD[name]
+    dy, w, ref = dgrad_case(N, H, W, 64, 64, R, S, pad, 1, dt, 33)
+    out = "f32" if red == "atomic" else dt
+    dx = run_dgrad(dy, w, H, W, 64, out, pad, 1, mode, red, 5)
+    check_parity(dx.reshape(-1, 64), ref, out, R * S * 64, what=f"dgrad row {name} {mode}/{red}")
+
+
+@pytest.mark.parametrize("red", ["linear", "tree"])
+def test_dgrad_row_bit_identical(red):
+    """20 launches, workspace and output poisoned before each; pool 5 so that tiles are shared."""
+    N, H, W, R, S, pad, dt = ROW_DGRAD["ragged_3x3"]
+    dy, w, _ = dgrad_case(N, H, W, 64, 64, R, S, pad, 1, dt, 33)
+    dyd, wd = dy.to(DEV), w.to(DEV)
+    prob = sk.make_problem("dgrad", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=64, k=64, r=R, s=S,
+                           stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", red, 5), dtype=torch.uint8, device=DEV)
+    dx = poisoned((N, H, W, 64), TD[dt])
+    first = None
+    for _ in range(20):
+        ws.fill_(0xFF)
+        dx.view(torch.uint8).fill_(0xFF)
+        sk.sk_conv2d_dgrad_nhwc(dyd, wd, dx, (1, 1), pad, 1, "dp_sk", red, 5, ws=ws)
+        sk.sk_device_status()
+        b = dx.view(torch.uint8).clone()
+        assert torch.isfinite(dx.float()).all()
+        if first is None:
+            first = b
+        else:
+            assert torch.equal(first, b), "result changed between launches"
+
+
+def test_dgrad_strided_phases_keep_the_im2col_view():
+    """A stride-2 dgrad of 64 -> 64 channels: its phase problems fit the shifted-row shape, but the
+    phases run the im2col kernel; the workspace query sizes them the same way."""
+    N, H, W, C, K, R, S, stride, pad, groups, dt = STRIDED["s2_1x1"]
+    prob = sk.make_problem("dgrad", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=C, k=K, r=R, s=S,
+                           stride_h=2, stride_w=2, pad_h=0, pad_w=0, groups=1)
+    ws = torch.empty(sk.sk_workspace_bytes(prob, "dp_sk", "linear", 5), dtype=torch.uint8,
+                     device=DEV)
+    dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
+    dx = poisoned((N, H, W, C), TD[dt])
+    sk.sk_conv2d_dgrad_nhwc(dy.to(DEV), w.to(DEV), dx, stride, pad, groups, "dp_sk", "linear", 5,
+                            ws=ws)
+    sk.sk_device_status()
+    check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what="strided dgrad phases, auto tile")

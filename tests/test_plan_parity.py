@@ -473,3 +473,54 @@ def test_fprop_row_auto_mode_is_persistent():
         cp = sk.sk_plan(small, "auto", "linear", -1, 152)
         op = P.make_auto_plan(pool=P.default_pool(P.LINEAR, 152, 1), reduction=P.LINEAR, **skw)
         assert cp.mode == op.mode != P.PERSISTENT
+
+
+# ---- shifted-row data gradient (automatic tile; stride 1, 64 filters -> 64 channels, <= 3x3): the
+# stride-1 convolution of dy with the flipped filter over the dx grid, in the same view.
+
+def dgrad_row(N, H, W, R, S, pad):
+    prob = sk.make_problem("dgrad", ab_dtype="f16", c_dtype="f16", n=N, h=H, w=W, c=64, k=64, r=R,
+                           s=S, stride_h=1, stride_w=1, pad_h=pad[0], pad_w=pad[1], groups=1)
+    kw = dict(tiles_m=N * (H + H % 2) * 64 // 128, tiles_n=1, groups=1, kred=R * S * 64, tm=128,
+              tn=64, tk=64)
+    return prob, kw
+
+
+DGRAD_ROW_NAMED = [
+    ("dgrad 32x56x56 3x3", dgrad_row(32, 56, 56, 3, 3, (1, 1)), -1),
+    ("dgrad 2x9x11 3x3", dgrad_row(2, 9, 11, 3, 3, (1, 1)), 5),
+    ("dgrad 2x8x10 3x3 unpadded", dgrad_row(2, 8, 10, 3, 3, (0, 0)), 7),
+]
+
+
+@pytest.mark.parametrize("name,pk,ctas", DGRAD_ROW_NAMED, ids=[n[0] for n in DGRAD_ROW_NAMED])
+@pytest.mark.parametrize("mode", MODES, ids=[m[0] for m in MODES])
+@pytest.mark.parametrize("red", REDS, ids=[r[0] for r in REDS])
+def test_dgrad_row_plans(name, pk, ctas, mode, red):
+    prob, kw = pk
+    big = lambda g: sorted(set(list(range(min(g, 200))) + list(range(max(0, g - 50), g))))
+    with sk.tile("auto"):
+        cp = compare(prob, kw, mode, red, ctas, check_ctas=big)
+    assert (cp.tm, cp.tn, cp.tk, cp.iters_per_tile) == (128, 64, 64, kw["kred"] // 64)
+
+
+def test_row_views_need_their_shape():
+    """The shifted-row view only for one group of 64 -> 64 channels, stride 1, at most 3 x 3 taps
+    and rows of at most 64 positions with the column taps; the pages' im2col view otherwise, and
+    always under the 128 x 128 tile."""
+    def tn(op, tile="auto", **kw):
+        a = dict(n=2, h=9, w=11, c=64, k=64, r=3, s=3, stride_h=1, stride_w=1, pad_h=1, pad_w=1,
+                 groups=1)
+        a.update(kw)
+        with sk.tile(tile):
+            return sk.sk_plan(sk.make_problem(op, ab_dtype="f16", c_dtype="f16", **a), "dp_sk",
+                              "linear", 5, 148).tn
+    for op in ("fprop", "dgrad"):
+        assert tn(op) == 64
+        assert tn(op, tile="128") == 128
+        assert tn(op, c=128, k=128) == 128
+        assert tn(op, r=5, s=5, pad_h=2, pad_w=2) == 128
+        assert tn(op, groups=2, c=128, k=128) == 128
+    assert tn("fprop", stride_h=2) == 128
+    assert tn("fprop", w=63) == 128 and tn("fprop", w=62) == 64    # Wo + S - 1 = 64 fits
+    assert tn("dgrad", w=63) == 128 and tn("dgrad", w=62) == 64    # W + S - 1 = 64 fits
