@@ -213,7 +213,10 @@ int sk_conv2d_wgrad_nhwc(int in_dtype, int dw_dtype, int64_t N, int64_t H, int64
  *   GEMM view per group: M = N*Ho*Wo output pixels, N = K/groups filters, reduction R*S*C/groups.
  *   in_dtype: SK_F16 or SK_BF16; y_dtype: in_dtype or SK_F32 (SK_ATOMIC needs SK_F32).
  *   Supported: (C/groups) a multiple of 64, K a multiple of 8, dilation 1, R, S <= 16, padding
- *   < filter size. The 128 x 128 tile (sk_set_tile's pair tiles return -2).
+ *   < filter size. The 128 x 128 tile (sk_set_tile's pair tiles return -2). Under SK_TILE_AUTO a
+ *   layer of one group of 64 channels into 64 filters, stride 1, R, S <= 3 and Wo + S - 1 <= 64
+ *   takes the shifted-row view instead (see sk_set_tile): the same sums, M = output positions in
+ *   pairs of output rows of 64, N = 64, one reduction step per tap.
  */
 int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
                          int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
@@ -234,7 +237,9 @@ int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_
  *   phases that no tap reaches are zero. sk_workspace_bytes covers the largest phase; sk_plan
  *   has no single plan for a strided call and returns -2.
  *   Supported: strides 1..8, (K/groups) a multiple of 64, C/groups a multiple of 8, dilation 1,
- *   R, S <= 16, padding < filter size. The 128 x 128 tile.
+ *   R, S <= 16, padding < filter size. The 128 x 128 tile; under SK_TILE_AUTO a stride-1 layer of
+ *   one group of 64 filters into 64 channels with R, S <= 3 and W + S - 1 <= 64 takes the
+ *   shifted-row view (see sk_set_tile). A strided call's phases always take the 128 x 128 tile.
  */
 int sk_conv2d_dgrad_nhwc(int in_dtype, int dx_dtype, int64_t N, int64_t H, int64_t W, int64_t C,
                          int64_t K, int64_t R, int64_t S, int stride_h, int stride_w, int pad_h,
@@ -324,7 +329,13 @@ int sk_version(void);
  *    shifted-row view: M = (tap row, channel), N = (column tap, filter), reduction over the
  *    output rows padded to 64 positions per K step; a 128 x 192 tile on one CTA, or, for three or
  *    four tap rows over a long reduction (about 128 K steps per SM or more), a 256 x 192 tile on a
- *    CTA pair. Other wgrad shapes use the 128 x 128 tile of the pages' view.
+ *    CTA pair. Other wgrad shapes use the 128 x 128 tile of the pages' view. The forward
+ *    convolution and the stride-1 data gradient of one group of 64 channels into 64 with at most
+ *    3 x 3 taps and output rows of at most 64 positions with the column taps take the shifted-row
+ *    convolution view: a 128 x 64 tile of two output rows, one reduction step per tap, computed
+ *    from one box of R + 1 input rows read at each tap's row shift, the filter kept in shared
+ *    memory for all of a CTA's tiles (with SK_AUTO and more tiles than CTAs, SK_PERSISTENT with
+ *    every tile data-parallel).
  *  SK_TILE_128: one CTA computes each 128 x 128 output tile.
  *  SK_TILE_256_PAIR: a cluster of two CTAs on neighbouring SMs computes each 256 x 128 tile with the
  *    two-SM tensor-core instruction; each CTA stages its 128 rows of A and 64 of the 128 rows of B,
