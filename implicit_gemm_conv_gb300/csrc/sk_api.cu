@@ -696,7 +696,11 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             if (g_timing.on) ++g_timing.all_launches;
         }
         const int tslot = timing_start(stream);
-        le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st, zero && tslot < 0, stream);
+        // A chained launch (kp.pdl_chain bit 0, set by the caller) overlaps the previous kernel
+        // only when nothing is zeroed for it and no timing event sits between the two.
+        if (zero || tslot >= 0) kp.pdl_chain &= ~1;
+        le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st,
+                             (zero && tslot < 0) || (kp.pdl_chain & 1) != 0, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
         if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "main kernel launch"); break; }
         if (g_timing.on) { ++g_timing.main_launches; ++g_timing.all_launches; }
@@ -1329,7 +1333,7 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
     // One implicit GEMM over a traversal grid TH x TW of the activation AH x AW (channels AC).
     auto launch = [&](int64_t AH, int64_t AW, int64_t TH, int64_t TW, int tsh, int tsw, int tph,
                       int tpw, int Rt, int St, int r0, int s0, const sk::RowMap& rows,
-                      bool zeroed) -> int {
+                      bool zeroed, int chain = 0) -> int {
         // The im2col kernel serves the pages' view: a dgrad phase problem that fits the shifted-row
         // view keeps the 128 x 128 tile (the automatic tile's choice for the pages' view).
         const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
@@ -1400,6 +1404,7 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         kp.conv.Kg = static_cast<int32_t>(Kg);
         kp.conv.Cw = static_cast<int32_t>(Cg);
         kp.conv.rows = rows;
+        kp.pdl_chain = chain;
         // A dgrad phase writes scattered rows of dx, zeroed beforehand when needed: no per-launch
         // zeroing of a row range (out_rows 0).
         return run(prob, streamk, reduction, ctas, kp, out, ldc * cs, zeroed ? 0 : pixels, ldc * cs,
@@ -1527,8 +1532,30 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(N * H * W * ldc * cs), st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dx)");
     }
-    for (const DgradPhase& ph : phases) {
-        if (!ph.live()) continue;
+    // The phases write disjoint pixels of dx and read only dy and w, so a phase whose plan shares
+    // no tile (nothing zeroed, no workspace words) starts while the previous one is still running
+    // (a programmatic dependent launch that waits for nothing of it); the others follow in order.
+    std::vector<const DgradPhase*> live;
+    for (const DgradPhase& ph : phases)
+        if (ph.live()) live.push_back(&ph);
+    std::vector<char> solo(live.size(), 0);
+    {
+        const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
+        for (size_t i = 0; i < live.size(); ++i) {
+            sk_problem q;
+            memset(&q, 0, sizeof(q));
+            q.op = op; q.ab_dtype = in_dtype; q.c_dtype = out_dtype;
+            q.n = N; q.c = C; q.k = K; q.groups = groups;
+            set_phase_problem(q, live[i]->Hp, live[i]->Wp, live[i]->Rt, live[i]->St);
+            sk_plan_t pl;
+            rc = sk_plan(&q, streamk, reduction, ctas, 0, &pl);
+            if (rc) return rc;
+            solo[i] = pl.shared_tiles == 0 ? 1 : 0;
+        }
+    }
+    for (size_t i = 0; i < live.size(); ++i) {
+        const DgradPhase& ph = *live[i];
+        const int chain = (i > 0 && solo[i] ? 1 : 0) | (i + 1 < live.size() && solo[i + 1] ? 2 : 0);
         sk::RowMap rm;
         memset(&rm, 0, sizeof(rm));
         rm.on = 1;
@@ -1541,7 +1568,7 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         rm.ah = ph.a;
         rm.aw = ph.b;
         rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0, rm,
-                    true);
+                    true, chain);
         if (rc) return rc;
     }
     return SK_OK;

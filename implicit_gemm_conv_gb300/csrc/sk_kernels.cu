@@ -1695,8 +1695,9 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
     sk_segment_t seg;
     int64_t nseg = 0, tau = 0, nblk = 0;
     // Without a ticket the zeroing kernel may still be running: the epilogue's first write (output,
-    // scratch, partials, flags or counters) comes after its writes.
-    if (!P.ticket) grid_dependency_wait();
+    // scratch, partials, flags or counters) comes after its writes. A chained launch has no such
+    // predecessor (its previous kernel writes other pixels and no word it reads).
+    if (!P.ticket && !(P.pdl_chain & 1)) grid_dependency_wait();
     // Spread fold: the shared tiles of this CTA (at most two), folded once all its segments are out.
     const bool spread = P.spread && (plan.reduction == SK_LINEAR || plan.reduction == SK_TREE);
     PendingFold pend[2];
@@ -1838,6 +1839,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
 
     uint32_t ticket = 0;
     if (threadIdx.x == 0) {
+        if (P.pdl_chain & 2) grid_launch_dependents();   // the next launch of the call may start
         tma_prefetch_desc(&P.tmap_a);
         tma_prefetch_desc(&P.tmap_b);
         // The allocation below overwrites this; whatever a previous kernel left in shared memory

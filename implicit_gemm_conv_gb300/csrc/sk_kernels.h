@@ -152,6 +152,11 @@ struct KernelParams {
     // one); 0: the block (cluster) index, and the wait for the zeroing kernel's writes moves from
     // the prologue to the first access of the zeroed words.
     int32_t ticket;
+    // Launches of one call that do not read each other's results (the phases of a strided data
+    // gradient, each writing its own pixels, with no shared tile): bit 0 = this kernel was
+    // launched to overlap the previous one and waits for nothing of it; bit 1 = it lets the next
+    // one start as soon as all its CTAs have started.
+    int32_t pdl_chain;
     // kOpFp8Block: sa [M][nka] (A blocks of gka along K) and sb [ceil(N/gnb)][nkb] (B blocks of
     // gnb x gkb), either may be null; gka, gkb and gnb multiples of 128.
     const float* bsa;

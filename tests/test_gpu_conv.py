@@ -384,3 +384,22 @@ def test_dgrad_strided_phases_keep_the_im2col_view():
                             ws=ws)
     sk.sk_device_status()
     check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what="strided dgrad phases, auto tile")
+
+
+@pytest.mark.parametrize("mode", ["off", "dp_sk"])
+def test_dgrad_strided_phases_finish_before_the_next_work(mode):
+    """The phases of a strided data gradient may overlap one another (programmatic dependent
+    launches where a phase shares no tile); work queued after the call on the same stream still
+    sees every phase's pixels: a copy of dx enqueued right after the call, with no host
+    synchronisation, equals dx read after synchronising, 20 times over, and matches the oracle."""
+    N, H, W, C, K, R, S, stride, pad, groups, dt = STRIDED["s3_3x3_pad2x1"]
+    dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
+    dyd, wd = dy.to(DEV), w.to(DEV)
+    dx = poisoned((N, H, W, C), TD[dt])
+    for _ in range(20):
+        dx.view(torch.uint8).fill_(0xFF)
+        sk.sk_conv2d_dgrad_nhwc(dyd, wd, dx, stride, pad, groups, mode, "linear", 5)
+        early = dx.clone()   # same stream, no synchronisation in between
+        sk.sk_device_status()
+        assert torch.equal(early.view(torch.uint8), dx.view(torch.uint8)), "a phase was still running"
+    check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what=f"strided dgrad {mode}, chained phases")

@@ -204,6 +204,6 @@ WORKLOADS = {
         Workload("dgrad_f16_n32_56x56_c64_k128_3x3_s2", "dgrad", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=128, R=3, S=3, stride=(2, 2), pad=(1, 1),
                            groups=1),
-                 pool=-1, modes=("dp_sk",), reductions=("linear", "tree")),
+                 pool=-1, modes=("dp_sk", "auto"), reductions=("linear", "tree")),
     ]
 }
