@@ -699,6 +699,9 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
         // A chained launch (kp.pdl_chain bit 0, set by the caller) overlaps the previous kernel
         // only when nothing is zeroed for it and no timing event sits between the two.
         if (zero || tslot >= 0) kp.pdl_chain &= ~1;
+        // Stage-2 follows: it starts while the main kernel ends and waits for it on the device.
+        const bool stage2 = plan.reduction == SK_WORKSPACE && plan.shared_tiles > 0;
+        if (stage2 && tslot < 0) kp.pdl_chain |= 2;
         le = sk::launch_main(kp, v.op_kind, tc.cg, tc.tn, tc.st,
                              (zero && tslot < 0) || (kp.pdl_chain & 1) != 0, stream);
         if (tslot >= 0) cudaEventRecord(g_timing.used[tslot].second, stream);
@@ -718,6 +721,7 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
             s2.op_kind = v.op_kind;
             s2.rows = kp.conv.rows;
             s2.conv = kp.conv;
+            s2.after_main = tslot < 0 ? 1 : 0;
             le = sk::launch_stage2(s2, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "stage-2 launch"); break; }
             if (g_timing.on) ++g_timing.all_launches;

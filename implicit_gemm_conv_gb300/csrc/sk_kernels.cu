@@ -1973,6 +1973,7 @@ constexpr int kStage2Threads = 256;
 // the fragment-major order the fixup wrote it. A pair tile (CG = 2) is two such 128-row halves.
 template <int TN, int CG>
 __global__ void __launch_bounds__(kStage2Threads) sk_stage2_kernel(const __grid_constant__ Stage2Params P) {
+    if (P.after_main) grid_dependency_wait();   // the scratch is complete once the main kernel is
     const sk_plan_t& plan = P.plan;
     const int64_t t = blockIdx.x;
     int64_t first, n;
@@ -2103,28 +2104,33 @@ int launch_main(const KernelParams& p, int op, int cg, int tn, int st, bool afte
     return SK_DISPATCH(op, cg, tn, st, launch_main_t, p, after_zero, stream);
 }
 
+template <int TN, int CG>
+static int launch_stage2_t(const Stage2Params& p, dim3 grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kStage2Threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.after_main ? 1 : 0;
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, sk_stage2_kernel<TN, CG>, p));
+}
+
 int launch_stage2(const Stage2Params& p, cudaStream_t stream) {
     const int64_t tiles = n_shared_candidates(p.plan);
     if (tiles <= 0) return 0;
     const int cg = p.plan.tm == 2 * kTileM ? 2 : 1;
-    const int tn = p.plan.tn == 256 ? 256 : p.plan.tn == 64 ? 64 : 128;
+    const int tn = p.plan.tn == 256 ? 256 : p.plan.tn == 64 ? 64 : p.plan.tn == 192 ? 192 : 128;
     const unsigned slices = static_cast<unsigned>(cg * kTileM * tn / 4 / kStage2Threads);
     const dim3 grid(static_cast<unsigned>(tiles), slices);
-    if (tn == 64)
-        sk_stage2_kernel<64, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
-    else if (p.plan.tn == 192 && cg == 2)
-        sk_stage2_kernel<192, 2><<<dim3(static_cast<unsigned>(tiles), 256u * 192u / 4u / kStage2Threads),
-                                   dim3(kStage2Threads), 0, stream>>>(p);
-    else if (p.plan.tn == 192)
-        sk_stage2_kernel<192, 1><<<dim3(static_cast<unsigned>(tiles), 128u * 192u / 4u / kStage2Threads),
-                                   dim3(kStage2Threads), 0, stream>>>(p);
-    else if (cg == 2 && tn == 256)
-        sk_stage2_kernel<256, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
-    else if (cg == 2)
-        sk_stage2_kernel<128, 2><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
-    else
-        sk_stage2_kernel<128, 1><<<grid, dim3(kStage2Threads), 0, stream>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    if (tn == 64) return launch_stage2_t<64, 1>(p, grid, stream);
+    if (tn == 192) return cg == 2 ? launch_stage2_t<192, 2>(p, grid, stream)
+                                  : launch_stage2_t<192, 1>(p, grid, stream);
+    if (tn == 256) return launch_stage2_t<256, 2>(p, grid, stream);
+    return cg == 2 ? launch_stage2_t<128, 2>(p, grid, stream) : launch_stage2_t<128, 1>(p, grid, stream);
 }
 
 // Zeroes up to three 16-byte aligned ranges (flags + control block, scratch) and one strided

@@ -178,6 +178,9 @@ struct Stage2Params {
     const float* scratch;
     int32_t c_dtype;
     ConvGeom conv;         // shifted-row wgrad: where a tile row and column go in dW
+    // 1: launched to overlap the main kernel's tail (programmatic dependent launch); every thread
+    // waits for the main kernel's completion before its first access
+    int32_t after_main;
 };
 
 // Ranges a zeroing kernel clears ahead of a main kernel: up to three 16-byte aligned 1-D ranges
