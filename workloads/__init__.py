@@ -195,11 +195,11 @@ WORKLOADS = {
         Workload("fprop_f16_n32_56x56_c64_k64_3x3", "fprop", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
                            groups=1),
-                 pool=-1, modes=("dp_sk", "auto"), reductions=("linear", "tree")),
+                 pool=-1, modes=("dp_sk", "persistent", "auto"), reductions=("linear", "tree")),
         Workload("dgrad_f16_n32_56x56_c64_k64_3x3", "dgrad", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=64, R=3, S=3, stride=(1, 1), pad=(1, 1),
                            groups=1),
-                 pool=-1, modes=("dp_sk", "auto"), reductions=("linear", "tree")),
+                 pool=-1, modes=("dp_sk", "persistent", "auto"), reductions=("linear", "tree")),
         # A downsampling layer's data gradient: stride 2, four output phases.
         Workload("dgrad_f16_n32_56x56_c64_k128_3x3_s2", "dgrad", "f16", "f16", "u11",
                  conv=dict(N=32, H=56, W=56, C=64, K=128, R=3, S=3, stride=(2, 2), pad=(1, 1),
