@@ -370,10 +370,10 @@ int tile_cfg(const View& v, TileCfg& t) {
             // Few tiles over a long 16-bit reduction (the 512 x 512 x 65536 GEMM): each SM takes in
             // the operands of its share of the MMAs through its copy engine, at about 115 GB/s, so
             // the 256 x 256 pair tile's half bytes per FLOP matter most; one CTA per SM with a
-            // 6-stage ring keeps its copies in flight.
+            // 7-stage ring (224 KB) keeps its copies in flight.
             else if (v.op_kind == sk::kOpGemm16 && v.gemm_m > sk::kTileM && v.gemm_n > 128 &&
                      v.kred / 64 >= kAutoLongReductionSteps)
-                t = TileCfg{2, 256, 6};
+                t = TileCfg{2, 256, 7};
             return SK_OK;
         }
     }

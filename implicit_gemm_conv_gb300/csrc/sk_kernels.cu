@@ -2074,7 +2074,7 @@ static size_t smem_bytes_t() {
          ? ((op) == kOpWgradRow1 ? fn<kOpWgradRow1, 192, 2, 4>(__VA_ARGS__)                  \
             : (op) == kOpWgradRow2 ? fn<kOpWgradRow2, 192, 2, 3>(__VA_ARGS__)                \
             : (tn) == 256 ? ((op) == kOpFp8 ? fn<kOpFp8, 256, 2, 3>(__VA_ARGS__)             \
-                             : (st) == 6 ? fn<kOpGemm16, 256, 2, 6>(__VA_ARGS__)               \
+                             : (st) == 7 ? fn<kOpGemm16, 256, 2, 7>(__VA_ARGS__)               \
                                           : fn<kOpGemm16, 256, 2, 3>(__VA_ARGS__))            \
                         : ((op) == kOpFp8 ? fn<kOpFp8, 128, 2, 4>(__VA_ARGS__)                \
                            : (op) == kOpFp8Block ? fn<kOpFp8Block, 128, 2, 7>(__VA_ARGS__)    \

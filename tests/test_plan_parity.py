@@ -215,7 +215,7 @@ def test_pair_tile_setting():
     with sk.tile("auto"):   # 240 pair tiles: the pair; few pair tiles or 128 rows: one CTA per tile
         assert (sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tm,
                 sk.sk_plan(prob, "dp_sk", "linear", 74, 148).tn) == (256, 256)
-        # 4 pair tiles over 1024 K steps: the deep-ring pair (one CTA per SM, 6 stages)
+        # 4 pair tiles over 1024 K steps: the deep-ring pair (one CTA per SM, 7 stages)
         assert sk.sk_plan(gemm(512, 512, 65536, "bf16")[0], "dp_sk", "linear", 74, 148).tm == 256
         assert sk.sk_plan(gemm(512, 512, 4096, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
         assert sk.sk_plan(gemm(128, 8192, 4096, "bf16")[0], "dp_sk", "linear", 148, 148).tm == 128
