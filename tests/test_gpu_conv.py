@@ -396,10 +396,14 @@ def test_dgrad_strided_phases_finish_before_the_next_work(mode):
     dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
     dyd, wd = dy.to(DEV), w.to(DEV)
     dx = poisoned((N, H, W, C), TD[dt])
+    first = None
     for _ in range(20):
         dx.view(torch.uint8).fill_(0xFF)
         sk.sk_conv2d_dgrad_nhwc(dyd, wd, dx, stride, pad, groups, mode, "linear", 5)
         early = dx.clone()   # same stream, no synchronisation in between
         sk.sk_device_status()
         assert torch.equal(early.view(torch.uint8), dx.view(torch.uint8)), "a phase was still running"
+        if first is None:
+            first = early
+        assert torch.equal(first.view(torch.uint8), early.view(torch.uint8)), "result changed"
     check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what=f"strided dgrad {mode}, chained phases")
