@@ -1415,12 +1415,50 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
         me = pd.index;
     }
     if (me < 0) return;   // this CTA's part of the tile is its partial only
-    // One thread polls the tile's arrival counter until all n contributors have counted their
-    // partials (bounded); one word per tile keeps the polling off the flag table, which every
-    // folder of a tile would otherwise read whole on each round. The verdict goes to all epilogue
-    // threads through a barrier reduction, and each fences before its reads of the partials.
+    const int64_t stride = static_cast<int64_t>(CG) * kTileM * TN;   // floats between slots
+    const float* base = P.partials + (partial_slot(plan, pd.tile, pd.first, 0) * CG + half) *
+                                         static_cast<int64_t>(kTileM * TN);
+    const int64_t b = me * kF4 / nfold, e = (me + 1) * kF4 / nfold;
+    const int64_t cap = imax(1, static_cast<int64_t>(kBufBytes) / (16 * n));   // float4s per chunk
+    // A share that fits one chunk is gathered in arrival order: the lanes of the first epilogue
+    // warp poll the contributors' flags (each contributor's flag counts the partials it has
+    // published) and copy a contributor's slice as soon as its partial is out, so the copies
+    // overlap the wait for the last ones; the additions below still run in contributor order.
+    // Otherwise one thread polls the tile's arrival counter until all n contributors have counted
+    // their partials, and the slices follow chunk by chunk. Either way the verdict goes to all
+    // epilogue threads through a barrier reduction.
+    const bool early = e - b <= cap;
     bool arrived = true;
-    if (ethread == 0) {
+    if (early) {
+        if (ethread < 32) {
+            const uint32_t bytes = static_cast<uint32_t>((e - b) * 16);
+            if (ethread == 0) mbar_arrive_expect_tx(fold_bar, static_cast<uint32_t>(n) * bytes);
+            __syncwarp();
+            // this lane's contributors: j = lane, lane + 32, ... (a bit per pending one)
+            uint32_t pending = 0;
+            for (int64_t j = ethread, q = 0; j < n; j += 32, ++q) pending |= 1u << q;
+            uint64_t t0 = 0;
+            while (pending != 0) {
+                for (int64_t j = ethread, q = 0; j < n; j += 32, ++q) {
+                    if (!(pending & (1u << q))) continue;
+                    const int64_t c2 = pd.first + j;
+                    if (ld_acquire_gpu(P.flags + c2 * CG + half) < publication(plan, c2, pd.tile))
+                        continue;
+                    fence_proxy_async_global();   // the acquired partial is read by the async proxy
+                    bulk_copy_g2s(ring + static_cast<uint32_t>(j) * bytes, base + j * stride + b * 4,
+                                  bytes, fold_bar);
+                    pending &= ~(1u << q);
+                }
+                if (pending == 0) break;
+                if (t0 == 0) t0 = globaltimer_ns();
+                if (globaltimer_ns() - t0 > P.flag_timeout_ns) {
+                    arrived = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+    } else if (ethread == 0) {
         uint64_t t0 = 0;
         arrived = wait_flag(P.control + 1 + pd.tile * CG + half, static_cast<uint32_t>(n), t0,
                             P.flag_timeout_ns);
@@ -1434,11 +1472,6 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
     tile_coords(plan, pd.tile, g, mt, nt);
     const OutSpec o{P.c, P.ldc, P.c_dtype, OP, P.sa, P.sb, P.scale,
                     OP == kOpFp8 ? (P.sa != nullptr ? 1 : 2) : 0, &P.conv};
-    const int64_t stride = static_cast<int64_t>(CG) * kTileM * TN;   // floats between slots
-    const float* base = P.partials + (partial_slot(plan, pd.tile, pd.first, 0) * CG + half) *
-                                         static_cast<int64_t>(kTileM * TN);
-    const int64_t b = me * kF4 / nfold, e = (me + 1) * kF4 / nfold;
-    const int64_t cap = imax(1, static_cast<int64_t>(kBufBytes) / (16 * n));   // float4s per chunk
     const bool lin = plan.reduction == SK_LINEAR;
     uint8_t* ring_ptr = nullptr;
     asm volatile("cvta.shared.u64 %0, %1;" : "=l"(ring_ptr) : "l"(static_cast<uint64_t>(ring)));
@@ -1452,7 +1485,7 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
         // The chunk's slices of all n partials, slot-major, each one contiguous run of `bytes`:
         // one bulk copy per partial, issued by the lanes of the first epilogue warp and counted on
         // the fold barrier, whose single arrival (lane 0) expects them all.
-        if (ethread < 32) {
+        if (ethread < 32 && !early) {
             fence_proxy_async_global();   // the acquired partials are read by the async proxy
             if (ethread == 0) mbar_arrive_expect_tx(fold_bar, static_cast<uint32_t>(n) * bytes);
             __syncwarp();
