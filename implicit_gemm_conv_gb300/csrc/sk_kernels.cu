@@ -1505,8 +1505,18 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
             auto part = [&](int64_t j) { return sbuf[j * len + i]; };
             float4 v;
             if (lin) {
+                // The same additions in the same order; four slices are read ahead so that the
+                // shared-memory latency is not paid on every one.
                 v = part(0);
-                for (int64_t j = 1; j < n; ++j) v = add4(v, part(j));
+                int64_t j = 1;
+                for (; j + 4 <= n; j += 4) {
+                    const float4 x0 = part(j), x1 = part(j + 1), x2 = part(j + 2), x3 = part(j + 3);
+                    v = add4(v, x0);
+                    v = add4(v, x1);
+                    v = add4(v, x2);
+                    v = add4(v, x3);
+                }
+                for (; j < n; ++j) v = add4(v, part(j));
             } else {
                 // Tree: the pending block sums of the rounds form a binary counter. Contributor
                 // j's partial is added (on the right) to the block held at every level where j
