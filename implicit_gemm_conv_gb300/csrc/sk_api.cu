@@ -598,9 +598,12 @@ int timing_start(cudaStream_t s) {
 
 // ---- launch sequence ------------------------------------------------------------------------
 
+// part: 0 = the zeroing kernel (where the plan needs one), the main kernel and Stage-2; 1 = the
+// zeroing kernel alone; 2 = the main kernel and Stage-2 alone, the workspace's words having been
+// zeroed by an earlier part-1 call on the same stream.
 int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelParams& kp,
         void* out, size_t out_pitch_bytes, size_t out_rows, size_t out_row_bytes, void* ws,
-        size_t ws_bytes, cudaStream_t stream) {
+        size_t ws_bytes, cudaStream_t stream, int part = 0) {
     DevInfo dev;
     int rc = check_arch(dev);
     if (rc) return rc;
@@ -688,17 +691,20 @@ int run(const sk_problem& prob, int mode, int reduction, int ctas, sk::KernelPar
         }
         // Nothing to zero when no tile is shared and no ticket is drawn (the data-parallel plans):
         // the main kernel then runs alone, without overlapping what came before it.
-        const bool zero = plan.shared_tiles > 0 || kp.ticket || z.out != nullptr;
+        const bool need_zero = plan.shared_tiles > 0 || kp.ticket || z.out != nullptr;
+        const bool zero = need_zero && part == 0;
         int le = 0;
-        if (zero) {
+        if (need_zero && part != 2) {
             le = sk::launch_zero(z, stream);
             if (le != 0) { rc = cuda_fail(static_cast<cudaError_t>(le), "zeroing kernel launch"); break; }
             if (g_timing.on) ++g_timing.all_launches;
         }
+        if (part == 1) break;
         const int tslot = timing_start(stream);
         // A chained launch (kp.pdl_chain bit 0, set by the caller) overlaps the previous kernel
-        // only when nothing is zeroed for it and no timing event sits between the two.
-        if (zero || tslot >= 0) kp.pdl_chain &= ~1;
+        // only when nothing is zeroed just before it, no ticket is drawn (its prologue waits for
+        // the previous kernel) and no timing event sits between the two.
+        if (zero || kp.ticket || tslot >= 0) kp.pdl_chain &= ~1;
         // Stage-2 follows: it starts while the main kernel ends and waits for it on the device.
         const bool stage2 = plan.reduction == SK_WORKSPACE && plan.shared_tiles > 0;
         if (stage2 && tslot < 0) kp.pdl_chain |= 2;
@@ -863,14 +869,14 @@ int sk_plan_cta_work(const sk_plan_t* plan, int64_t cta, sk_segment_t* out, int 
 int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas, size_t* out) {
     if (!p || !out) return fail(SK_ERR_UNSUPPORTED, "NULL argument");
     if (p->op == SK_OP_DGRAD && (p->stride_h > 1 || p->stride_w > 1)) {
-        // The largest workspace of the phases, which run one after another on one stream, in
-        // the pages' view as their launches take it.
+        // The phases' workspaces side by side (the phases may run at the same time), in the
+        // pages' view as their launches take it.
         const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
         if (p->stride_h < 1 || p->stride_w < 1 || p->stride_h > 8 || p->stride_w > 8)
             return fail(SK_ERR_UNSUPPORTED, "stride must be in [1, 8]");
         std::vector<DgradPhase> phases;
         dgrad_phases(p->h, p->w, p->r, p->s, p->stride_h, p->stride_w, p->pad_h, p->pad_w, phases);
-        size_t most = 0;
+        size_t sum = 0;
         for (const DgradPhase& ph : phases) {
             if (!ph.live()) continue;
             sk_problem q = *p;
@@ -878,9 +884,9 @@ int sk_workspace_bytes(const sk_problem* p, int streamk, int reduction, int ctas
             sk_plan_t plan;
             const int rc = sk_plan(&q, streamk, reduction, ctas, 0, &plan);
             if (rc) return rc;
-            if (static_cast<size_t>(plan.ws_bytes) > most) most = static_cast<size_t>(plan.ws_bytes);
+            sum += static_cast<size_t>(sk::round_up(plan.ws_bytes, 256));
         }
-        *out = most;
+        *out = sum;
         return SK_OK;
     }
     sk_plan_t plan;
@@ -1337,7 +1343,8 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
     // One implicit GEMM over a traversal grid TH x TW of the activation AH x AW (channels AC).
     auto launch = [&](int64_t AH, int64_t AW, int64_t TH, int64_t TW, int tsh, int tsw, int tph,
                       int tpw, int Rt, int St, int r0, int s0, const sk::RowMap& rows,
-                      bool zeroed, int chain = 0) -> int {
+                      bool zeroed, int chain = 0, void* lws = nullptr, size_t lws_bytes = 0,
+                      int part = 0, bool own_slice = false) -> int {
         // The im2col kernel serves the pages' view: a dgrad phase problem that fits the shifted-row
         // view keeps the 128 x 128 tile (the automatic tile's choice for the pages' view).
         const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
@@ -1412,7 +1419,7 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         // A dgrad phase writes scattered rows of dx, zeroed beforehand when needed: no per-launch
         // zeroing of a row range (out_rows 0).
         return run(prob, streamk, reduction, ctas, kp, out, ldc * cs, zeroed ? 0 : pixels, ldc * cs,
-                   ws, ws_bytes, st);
+                   own_slice ? lws : ws, own_slice ? lws_bytes : ws_bytes, st, part);
     };
 
     // The shifted-row kernel over the activation (AH x AW, 64 channels) into the TH x TW output
@@ -1536,13 +1543,19 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(N * H * W * ldc * cs), st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dx)");
     }
-    // The phases write disjoint pixels of dx and read only dy and w, so a phase whose plan shares
-    // no tile (nothing zeroed, no workspace words) starts while the previous one is still running
-    // (a programmatic dependent launch that waits for nothing of it); the others follow in order.
+    // The phases write disjoint pixels of dx and read only dy and w. With a workspace of its own
+    // for every phase (side by side; the library allocates them when the caller passes none, and
+    // sk_workspace_bytes reports their sum), the zeroing kernels of all phases run first and then
+    // every phase's main kernel starts while the previous one runs (a programmatic dependent
+    // launch that waits for nothing of it). With one shared workspace (a caller's, holding the
+    // largest phase only) a phase whose plan shares no tile still overlaps the previous phase; the
+    // others follow it in order.
     std::vector<const DgradPhase*> live;
     for (const DgradPhase& ph : phases)
         if (ph.live()) live.push_back(&ph);
     std::vector<char> solo(live.size(), 0);
+    std::vector<size_t> wsz(live.size(), 0);
+    size_t total = 0;
     {
         const TileGuard pages_view(g_tile == SK_TILE_AUTO ? SK_TILE_128 : g_tile);
         for (size_t i = 0; i < live.size(); ++i) {
@@ -1555,11 +1568,11 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
             rc = sk_plan(&q, streamk, reduction, ctas, 0, &pl);
             if (rc) return rc;
             solo[i] = pl.shared_tiles == 0 ? 1 : 0;
+            wsz[i] = static_cast<size_t>(sk::round_up(pl.ws_bytes, 256));
+            total += wsz[i];
         }
     }
-    for (size_t i = 0; i < live.size(); ++i) {
-        const DgradPhase& ph = *live[i];
-        const int chain = (i > 0 && solo[i] ? 1 : 0) | (i + 1 < live.size() && solo[i + 1] ? 2 : 0);
+    auto phase_rows = [&](const DgradPhase& ph) {
         sk::RowMap rm;
         memset(&rm, 0, sizeof(rm));
         rm.on = 1;
@@ -1571,8 +1584,40 @@ int conv_fwd_like(int op, int in_dtype, int out_dtype, int64_t N, int64_t H, int
         rm.dsw = stride_w;
         rm.ah = ph.a;
         rm.aw = ph.b;
-        rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0, rm,
-                    true, chain);
+        return rm;
+    };
+    const bool side = ws == nullptr || ws_bytes >= total;
+    if (side) {
+        uint8_t* wbase = static_cast<uint8_t*>(ws);
+        if (ws == nullptr) {
+            cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&wbase), total, st);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+        }
+        size_t off = 0;
+        for (size_t i = 0; i < live.size() && rc == SK_OK; off += wsz[i], ++i) {
+            if (solo[i]) continue;
+            const DgradPhase& ph = *live[i];
+            rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0,
+                        phase_rows(ph), true, 0, wbase + off, wsz[i], 1, true);
+        }
+        off = 0;
+        for (size_t i = 0; i < live.size() && rc == SK_OK; off += wsz[i], ++i) {
+            const DgradPhase& ph = *live[i];
+            const int chain = (i > 0 ? 1 : 0) | (i + 1 < live.size() ? 2 : 0);
+            rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0,
+                        phase_rows(ph), true, chain, wbase + off, wsz[i], 2, true);
+        }
+        if (ws == nullptr) {
+            cudaError_t e = cudaFreeAsync(wbase, st);
+            if (e != cudaSuccess && rc == SK_OK) rc = cuda_fail(e, "cudaFreeAsync(workspace)");
+        }
+        return rc;
+    }
+    for (size_t i = 0; i < live.size(); ++i) {
+        const DgradPhase& ph = *live[i];
+        const int chain = (i > 0 && solo[i] ? 1 : 0) | (i + 1 < live.size() && solo[i + 1] ? 2 : 0);
+        rc = launch(Ho, Wo, ph.Hp, ph.Wp, 1, 1, ph.padh, ph.padw, ph.Rt, ph.St, ph.r0, ph.s0,
+                    phase_rows(ph), true, chain);
         if (rc) return rc;
     }
     return SK_OK;

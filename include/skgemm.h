@@ -234,7 +234,10 @@ int sk_conv2d_fprop_nhwc(int in_dtype, int y_dtype, int64_t N, int64_t H, int64_
  *   computed as a stride-1 convolution of dy with the flipped filter. With a stride above 1 it
  *   runs one such convolution per output phase (the dx pixels h = sh*i + a, w = sw*j + b): only
  *   the taps r = (a + ph) mod sh + sh*t reach them (likewise s), over an H/sh x W/sw grid;
- *   phases that no tap reaches are zero. sk_workspace_bytes covers the largest phase; sk_plan
+ *   phases that no tap reaches are zero. sk_workspace_bytes gives the phases' workspaces side
+ *   by side (each rounded up to 256 bytes): with that much (or ws == NULL, the library then
+ *   allocating it) the phases may run at the same time; a workspace that holds only the largest
+ *   phase also works, and the phases whose plans share tiles then run one after another. sk_plan
  *   has no single plan for a strided call and returns -2.
  *   Supported: strides 1..8, (K/groups) a multiple of 64, C/groups a multiple of 8, dilation 1,
  *   R, S <= 16, padding < filter size. The 128 x 128 tile; under SK_TILE_AUTO a stride-1 layer of

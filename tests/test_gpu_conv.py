@@ -407,3 +407,45 @@ def test_dgrad_strided_phases_finish_before_the_next_work(mode):
             first = early
         assert torch.equal(first.view(torch.uint8), early.view(torch.uint8)), "result changed"
     check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what=f"strided dgrad {mode}, chained phases")
+
+
+def test_dgrad_strided_workspace_of_the_largest_phase_only():
+    """A caller's workspace that holds only the largest phase's plan (smaller than
+    sk_workspace_bytes, which gives all phases side by side): the phases with shared tiles then run
+    one after another in it; the result matches the oracle and is bit-identical over 10 launches."""
+    from oracle import partition as P
+    N, H, W, C, K, R, S, stride, pad, groups, dt = STRIDED["s2_3x3_ragged"]
+    dy, w, ref = dgrad_case(N, H, W, C, K, R, S, pad, groups, dt, 7, stride)
+    prob = sk.make_problem("dgrad", ab_dtype=dt, c_dtype=dt, n=N, h=H, w=W, c=C, k=K, r=R, s=S,
+                           stride_h=stride[0], stride_w=stride[1], pad_h=pad[0], pad_w=pad[1],
+                           groups=groups)
+    most = 0
+    for a in range(stride[0]):
+        for b in range(stride[1]):
+            hp = len(range(a, H, stride[0]))
+            wp = len(range(b, W, stride[1]))
+            rt = len([r for r in range(R) if (a + pad[0] - r) % stride[0] == 0])
+            st = len([s for s in range(S) if (b + pad[1] - s) % stride[1] == 0])
+            if not (hp and wp and rt and st):
+                continue
+            plan = P.make_plan(tiles_m=-(-N * hp * wp // 128), tiles_n=-(-C // 128), groups=1,
+                               kred=rt * st * K, tm=128, tn=128, tk=64, pool=5, mode=P.DP_SK,
+                               reduction=P.LINEAR)
+            most = max(most, plan.ws_bytes)
+    full = sk.sk_workspace_bytes(prob, "dp_sk", "linear", 5)
+    assert most < full
+    ws = torch.empty(-(-most // 256) * 256, dtype=torch.uint8, device=DEV)
+    dyd, wd = dy.to(DEV), w.to(DEV)
+    dx = poisoned((N, H, W, C), TD[dt])
+    first = None
+    for _ in range(10):
+        ws.fill_(0xFF)
+        dx.view(torch.uint8).fill_(0xFF)
+        sk.sk_conv2d_dgrad_nhwc(dyd, wd, dx, stride, pad, groups, "dp_sk", "linear", 5, ws=ws)
+        sk.sk_device_status()
+        b = dx.view(torch.uint8).clone()
+        if first is None:
+            first = b
+            check_parity(dx.reshape(-1, C), ref, dt, R * S * K, what="strided dgrad, one phase's ws")
+        else:
+            assert torch.equal(first, b), "result changed between launches"
