@@ -123,6 +123,9 @@ __global__ void sk_flag_timeout_probe_kernel(uint64_t limit_ns) {
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;
+// The prologue of a one-CTA launch without a ticket, whose producer does not wait for it: the
+// barrier initialisation published to the other warps, and those warps' own prologue.
+constexpr uint32_t kPrologueBar = 3, kPrologueBar2 = 4;
 
 template <int OP, int TN, int CG, int ST>
 struct Cfg {
@@ -1892,6 +1895,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         asm volatile("" ::"r"(v));
     }
 
+    // One CTA without a ticket: the producer needs nothing of the prologue after the barriers'
+    // initialisation (not the TMEM allocation, the pad rows of the shifted-row wgrad or a ticket;
+    // its CTA id is the block index), so it starts its copies while the other warps finish it.
+    const bool early = CG == 1 && !P.ticket;
     uint32_t ticket = 0;
     if (threadIdx.x == 0) {
         if (P.pdl_chain & 2) grid_launch_dependents();   // the next launch of the call may start
@@ -1914,9 +1921,25 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         fence_mbarrier_init();
         ctl->abort = 0;
     }
+    if (early && warp == 0) {
+        // The arrival publishes the barriers and the sentinel to the other warps. The producer
+        // drains its own copies if it stops early (run_producer), and meets the others only at
+        // the CTA's last barrier.
+        named_bar_arrive(kPrologueBar, kThreads);
+        if (elect_one()) run_producer<OP, TN, CG, ST>(P, static_cast<int64_t>(blockIdx.x), ring, bars,
+                                                      ctl, 0u);
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+        return;
+    }
     // Barriers and the sentinel are in place (and, for a pair, both CTAs have started) before the
     // allocation writes the slot.
-    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (early) {
+        named_bar_sync(kPrologueBar, kThreads);
+    } else {
+        if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    }
     if (warp == 1) {
         tmem_alloc<CG>(ctl_addr + static_cast<uint32_t>(offsetof(SmemCtl, tmem_base)),
                        C::kTmemAlloc);
@@ -1932,7 +1955,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
                               (CG == 1 ? 1u : static_cast<uint32_t>(P.conv.stage_steps)) * 64u *
                                   C::kDyRowBytes;
         constexpr int kPadBytes = C::kDyPadRows * C::kDyRowBytes;
-        for (int i = static_cast<int>(threadIdx.x); i < C::kStages * kPadBytes / 16; i += kThreads) {
+        const int first = early ? 32 : 0;   // the producer warp is already copying
+        for (int i = static_cast<int>(threadIdx.x) - first; i < C::kStages * kPadBytes / 16;
+             i += kThreads - first) {
             const int st = i / (kPadBytes / 16), b = i - st * (kPadBytes / 16);
             st_shared_v4(ring + st * C::kStageBytes + pad0 + b * 16, 0u, 0u, 0u, 0u);
         }
@@ -1964,10 +1989,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         ctl->cta = static_cast<long long>(CG == 2 ? (blockIdx.x >> 1) : blockIdx.x);
     }
     tc_fence_before();
-    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (early) {
+        named_bar_sync(kPrologueBar2, kThreads - 32);
+    } else {
+        if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    }
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
-    const int64_t cta = ctl->cta;
+    const int64_t cta = early ? static_cast<int64_t>(blockIdx.x) : static_cast<int64_t>(ctl->cta);
     // Every thread reads the same slot, so the whole CTA takes this exit together. It is never
     // expected; it keeps a bad slot from ever reaching a TMEM access. A pair takes the verdict
     // of both its slots, so that both CTAs leave together.
@@ -1988,7 +2017,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
     if (bad) {
         // Never expected. Nothing has touched TMEM yet; the columns are still released before the
         // CTA leaves, so that a later CTA's allocation on this SM is not left waiting for them.
-        if (threadIdx.x == 0) record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
+        if (threadIdx.x == 32) {
+            record_error(kErrBounds, cta, -1, static_cast<long long>(tmem_base));
+            ctl->abort = 1;   // an early producer stops at its next wait and drains its copies
+        }
         tc_fence_before();
         if constexpr (CG == 2) cluster_sync(); else __syncthreads();
         if (warp == 1 && freeable) {
@@ -1998,7 +2030,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<OP, TN, CG, ST>::kMinBlocks)
         return;
     }
 
-    if (warp == 0) {
+    if (warp == 0) {   // not an early producer: that warp has left above
         if (elect_one()) run_producer<OP, TN, CG, ST>(P, cta, ring, bars, ctl, rank);
         __syncwarp();
     } else if (warp == 1) {

@@ -497,6 +497,11 @@ __device__ __forceinline__ void red_add_f32(float* p, float a) {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on a named barrier without waiting for it (its prior writes are then visible to the
+// threads that wait on the barrier).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Named barrier that also returns the AND (resp. OR) of `v` over the `nthreads` threads.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
     uint32_t r;
