@@ -516,6 +516,58 @@ __device__ void run_producer(const KernelParams& P, int64_t cta, uint32_t ring, 
         if constexpr (folds_groups_into_columns(OP) && !C::kFpRow) pixel_start(P.conv, mt, ps);
         const int64_t len = seg.k_end - seg.k_begin;
         const int64_t rot = segment_rotation(plan, dp, seg, tau);
+        if constexpr (C::kWgRow && CG == 1) {
+            // One K step per stage. The copies' coordinates advance step by step (image n, output
+            // row ho0), with no division and no per-step setup, so that the thread's own work
+            // between a stage's last copy and the next stage's first stays short against the
+            // copy engine's time per box (a copy instruction waits for the previous box).
+            const ConvGeom& cg = P.conv;
+            const uint32_t rps = static_cast<uint32_t>(cg.rows_per_step);
+            const uint32_t hp = static_cast<uint32_t>(cg.ho_pad);
+            const int32_t r0 = 2 * static_cast<int32_t>(mt);
+            const int32_t dy_c = static_cast<int32_t>(g) * cg.Kg, x_c = static_cast<int32_t>(g) * cg.Cg;
+            const RowLayout<CG, C::kPhases> lay(cg);
+            // k * rows_per_step < 2^31 (checked on the host)
+            const uint32_t kb = static_cast<uint32_t>(seg.k_begin);
+            const uint32_t ke = static_cast<uint32_t>(seg.k_end);
+            uint32_t kk = static_cast<uint32_t>(seg.k_begin + rot);
+            uint32_t n_img = (kk * rps) / hp;
+            uint32_t ho0 = kk * rps - n_img * hp;
+            for (int64_t j = 0; j < len; ++j) {
+                const uint32_t full = bars + stage * 8, empty = bars + (C::kStages + stage) * 8;
+                if (!mbar_wait(empty, phase ^ 1, P.mbar_timeout_ns) || ctl->abort) {
+                    record_error(kErrPipeline, cta, seg.tile, 0);
+                    ctl->abort = 1;
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_dst = ring + stage * C::kStageBytes;
+                mbar_arrive_expect_tx(full, stage_tx);
+                const int32_t h0 = static_cast<int32_t>(ho0), ni = static_cast<int32_t>(n_img);
+                tma_load_4d(a_dst + lay.dy_off, &P.tmap_b, full, dy_c, -cg.qmax, h0, ni);
+#pragma unroll
+                for (int phs = 0; phs < C::kPhases; ++phs)
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+                        if (r0 + jj < cg.R)
+                            tma_load_4d(a_dst + phs * lay.x_phase + jj * lay.x_lbo, &P.tmap_a, full,
+                                        x_c, phs - cg.pw, cg.sh * h0 + r0 + jj - cg.ph, ni);
+                ++issued;
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                if (++kk == ke) {   // the rotation wraps to the segment's start
+                    kk = kb;
+                    n_img = (kk * rps) / hp;
+                    ho0 = kk * rps - n_img * hp;
+                } else if ((ho0 += rps) == hp) {   // ho_pad is a multiple of rows_per_step
+                    ho0 = 0;
+                    ++n_img;
+                }
+            }
+            continue;
+        }
         for (int64_t j = 0; j < len; j += stage_step_count<OP, CG>(P.conv, seg, rot, j)) {
             int64_t k = seg.k_begin + rot + j;
             if (k >= seg.k_end) k -= len;
