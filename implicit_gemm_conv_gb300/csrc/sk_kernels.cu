@@ -1887,6 +1887,36 @@ __device__ void run_epilogue(const KernelParams& P, int64_t cta, uint32_t ring, 
         SegCursor ahead = cur;
         sk_segment_t next;
         const bool last = !seg_next(plan, cta, ahead, next);
+        if constexpr (C::kWgRow && CG == 1) {
+            if (seg.kind != SK_SEG_FULL && plan.reduction == SK_ATOMIC && !last) {
+                // A CTA whose range reaches into the next tile: the single accumulator goes to
+                // registers at once (192 columns a thread) and is released before this segment's
+                // additions, so that the next segment's MMAs start while they issue. (A CTA's last
+                // segment keeps the chunked additions of epilogue_segment, whose starting chunk
+                // differs from CTA to CTA: the contributors of a tile end together there. The
+                // same early release before a spread fold's publication gained nothing: that
+                // fold waits for the later segment's partial anyway.)
+                uint32_t r[TN / 32][32];
+#pragma unroll
+                for (int c = 0; c < TN / 32; ++c) tmem_ld_32x32b_x32(t_acc + c * 32, r[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+                if (e.row_ok) {
+#pragma unroll
+                    for (int c = 0; c < TN / 32; ++c) {
+                        const int64_t off = wgrow_col_offset(P.conv, P.ldc, c * 32);
+                        if (off < 0) continue;
+                        float* dst = static_cast<float*>(P.c) + e.out_row + off;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) red_add_f32(dst + i * P.ldc, as_f(r[c][i]));
+                    }
+                }
+                ++nseg;
+                continue;
+            }
+        }
         epilogue_segment<OP, TN, CG, ST>(P, cta, seg, e, t_acc, ethread, ring,
                                          bars + C::kBarFold * 8, last);
         note_shared(seg);
