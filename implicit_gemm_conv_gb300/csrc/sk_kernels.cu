@@ -1494,15 +1494,24 @@ __device__ void spread_fold(const KernelParams& P, int64_t cta, const PendingFol
             for (int64_t j = ethread, q = 0; j < n; j += 32, ++q) pending |= 1u << q;
             uint64_t t0 = 0;
             while (pending != 0) {
+                // The flags of this lane's pending contributors, read together (relaxed loads, not
+                // one acquire after another); one acquire fence then orders every partial seen out
+                // before the copies that read it.
+                uint32_t ready = 0;
                 for (int64_t j = ethread, q = 0; j < n; j += 32, ++q) {
                     if (!(pending & (1u << q))) continue;
                     const int64_t c2 = pd.first + j;
-                    if (ld_acquire_gpu(P.flags + c2 * CG + half) < publication(plan, c2, pd.tile))
-                        continue;
-                    fence_proxy_async_global();   // the acquired partial is read by the async proxy
-                    bulk_copy_g2s(ring + static_cast<uint32_t>(j) * bytes, base + j * stride + b * 4,
-                                  bytes, fold_bar);
-                    pending &= ~(1u << q);
+                    if (ld_relaxed_gpu(P.flags + c2 * CG + half) >= publication(plan, c2, pd.tile))
+                        ready |= 1u << q;
+                }
+                if (ready != 0) {
+                    fence_acq_rel_gpu();
+                    fence_proxy_async_global();   // the acquired partials are read by the async proxy
+                    for (int64_t j = ethread, q = 0; j < n; j += 32, ++q)
+                        if (ready & (1u << q))
+                            bulk_copy_g2s(ring + static_cast<uint32_t>(j) * bytes,
+                                          base + j * stride + b * 4, bytes, fold_bar);
+                    pending &= ~ready;
                 }
                 if (pending == 0) break;
                 if (t0 == 0) t0 = globaltimer_ns();
