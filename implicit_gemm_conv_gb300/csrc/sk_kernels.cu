@@ -1338,7 +1338,10 @@ __device__ void epilogue_segment(const KernelParams& P, int64_t cta, const sk_se
             if (ethread == 0) record_error(kErrBounds, cta, seg.tile, my_slot);
             return;
         }
+        // Rows outside the output (a tile's padding rows) are not stored: the folders add
+        // whatever their slots hold there, and those sums are never written out.
         for_each_chunk<kChunks>(t_acc, [&](int ch, float (&v)[32]) {
+            if (!e.row_ok) return;
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
                 __stcg(reinterpret_cast<float4*>(frag_ptr<TN>(own, ch * 32, i, e.row)),
